@@ -1,0 +1,179 @@
+"""fp64 CPU oracle for the attention forward pass -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
+arm of ``bench.py`` may import this package.  The product package never does,
+and the oracle imports nothing from the product.
+
+The arithmetic lives in ``attn_ref.c`` (plain C, double precision, OpenMP over
+(batch, head)); this module only compiles it with gcc and marshals numpy arrays.
+What each function computes, and the passage of the pages it follows, is stated
+in ``attn_ref.c``:
+
+* ``attn_dense``      full definition, S and P materialised per (batch, head)
+                      ("GPU 内核与 FlashAttention" §10, §11.1, §13.2)
+* ``attn_dense_rows`` the same definition for selected (b, h, i) rows
+* ``attn_varlen``     packed variable-length form, lse [B, H, max_seqlen_q]
+                      ("Flash Attention实现深度解析" §3.1)
+* ``attn_online``     the blockwise online recurrence ("GPU 内核与 FlashAttention"
+                      §11.3 and §14.1), used only to check that it is exact
+
+Inputs are bf16 bit patterns (``numpy.uint16``); outputs are float64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_ref.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile attn_ref.c into oracle/_build/liboracle.so (gcc, -O2, OpenMP)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
+        cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp",
+               "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        ci, cd = ctypes.c_int, ctypes.c_double
+        lib.oracle_attn_dense.argtypes = [u16p, u16p, u16p, ci, ci, ci, ci, ci, cd, f64p, f64p]
+        lib.oracle_attn_dense_rows.argtypes = [u16p, u16p, u16p, ci, ci, ci, ci, ci, cd,
+                                               ci, i64p, f64p, f64p]
+        lib.oracle_attn_varlen.argtypes = [u16p, u16p, u16p, i32p, i32p, ci, ci, ci, cd, ci,
+                                           f64p, f64p]
+        lib.oracle_attn_online.argtypes = [u16p, u16p, u16p, ci, ci, ci, ci, ci, cd, ci,
+                                           f64p, f64p]
+        for name in ("oracle_attn_dense", "oracle_attn_dense_rows", "oracle_attn_varlen",
+                     "oracle_attn_online", "oracle_num_threads"):
+            getattr(lib, name).restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [ci]
+        lib.oracle_set_num_threads.restype = None
+        _lib = lib
+        return lib
+
+
+def _u16(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("oracle inputs are bf16 bit patterns (numpy.uint16), got %s" % a.dtype)
+    return a
+
+
+def _ptr(a: np.ndarray, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle will use."""
+    return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    _load().oracle_set_num_threads(int(n))
+
+
+def _default_scale(d: int, scale):
+    return (1.0 / np.sqrt(d)) if scale is None else float(scale)
+
+
+def attn_dense(q, k, v, scale=None):
+    """q: [B, Nq, H, d], k/v: [B, Nk, H, d] (uint16 bf16 bits).
+
+    Returns (o [B, Nq, H, d] float64, lse [B, H, Nq] float64)."""
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    B, Nq, H, d = q.shape
+    Nk = k.shape[1]
+    if k.shape != (B, Nk, H, d) or v.shape != k.shape:
+        raise ValueError("shape mismatch")
+    o = np.zeros((B, Nq, H, d), np.float64)
+    lse = np.zeros((B, H, Nq), np.float64)
+    rc = _load().oracle_attn_dense(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+                                   _ptr(v, ctypes.c_uint16), B, Nq, Nk, H, d,
+                                   _default_scale(d, scale),
+                                   _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double))
+    if rc != 0:
+        raise MemoryError("oracle_attn_dense failed (%d)" % rc)
+    return o, lse
+
+
+def attn_dense_rows(q, k, v, rows, scale=None):
+    """Selected rows of the dense definition; rows: int array [n, 3] of (b, h, i).
+
+    Returns (o_rows [n, d], lse_rows [n])."""
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    B, Nq, H, d = q.shape
+    Nk = k.shape[1]
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    n = rows.shape[0]
+    o = np.zeros((n, d), np.float64)
+    lse = np.zeros((n,), np.float64)
+    rc = _load().oracle_attn_dense_rows(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+                                        _ptr(v, ctypes.c_uint16), B, Nq, Nk, H, d,
+                                        _default_scale(d, scale), n, _ptr(rows, ctypes.c_int64),
+                                        _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle_attn_dense_rows failed (%d)" % rc)
+    return o, lse
+
+
+def attn_varlen(q, k, v, cu_q, cu_k, max_seqlen_q, scale=None):
+    """Packed form: q [total_q, H, d], k/v [total_k, H, d], cu_* int32 [B+1].
+
+    Returns (o [total_q, H, d], lse [B, H, max_seqlen_q]); lse entries beyond a
+    sequence's length are NaN (never written)."""
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    cu_q = np.ascontiguousarray(cu_q, dtype=np.int32)
+    cu_k = np.ascontiguousarray(cu_k, dtype=np.int32)
+    _, H, d = q.shape
+    B = cu_q.shape[0] - 1
+    o = np.zeros(q.shape, np.float64)
+    lse = np.full((B, H, max_seqlen_q), np.nan, np.float64)
+    rc = _load().oracle_attn_varlen(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+                                    _ptr(v, ctypes.c_uint16), _ptr(cu_q, ctypes.c_int32),
+                                    _ptr(cu_k, ctypes.c_int32), B, H, d,
+                                    _default_scale(d, scale), int(max_seqlen_q),
+                                    _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle_attn_varlen failed (%d)" % rc)
+    return o, lse
+
+
+def attn_online(q, k, v, block, scale=None):
+    """Blockwise online recurrence with `block` keys per step (dense form)."""
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    B, Nq, H, d = q.shape
+    Nk = k.shape[1]
+    o = np.zeros((B, Nq, H, d), np.float64)
+    lse = np.zeros((B, H, Nq), np.float64)
+    rc = _load().oracle_attn_online(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+                                    _ptr(v, ctypes.c_uint16), B, Nq, Nk, H, d,
+                                    _default_scale(d, scale), int(block),
+                                    _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle_attn_online failed (%d)" % rc)
+    return o, lse

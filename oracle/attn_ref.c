@@ -1,0 +1,305 @@
+/*
+ * attn_ref.c -- plain fp64 CPU oracle for the attention forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file.  Its only users are the tests, the smoke check and the CPU
+ * baseline / reference arm of the benchmark.  It shares no code, header,
+ * table or helper with the CUDA path.
+ *
+ * Sources (page titles as printed on the pages):
+ *   [GKFA]  "GPU 内核与 FlashAttention" (hs-black, scaling-gpu-kernels)
+ *             §10   standard attention: S = Q K^T (times the scale), P = softmax(S), O = P V
+ *             §11.1 safe softmax: subtract the row maximum before exp
+ *             §11.2 merge of two partial (m, l) pairs
+ *             §11.3 online output recurrence (m, l, o-tilde), o = o-tilde / l
+ *             §13.2 and §14.1 the forward keeps only L = m + log l per row
+ *   [FMHA] "Flash Attention实现深度解析" (maplevalley) §3.1: the host entry
+ *             returns {out, softmax_lse} with lse shaped [batch, heads, max_seqlen_q]
+ *   [CH2]  "Flash Attention 2 Chapter2": tensors are [batch, seq, heads, d_head]
+ *             (the generate_qkv listing in the section on mapping tensors to mma)
+ *
+ * Definition computed here (all arithmetic in double, on the bf16 input values
+ * widened exactly):
+ *   s_ij  = scale * sum_c q_ic k_jc                      ([GKFA] §10)
+ *   m_i   = max_j s_ij                                   ([GKFA] §11.1)
+ *   p_ij  = exp(s_ij - m_i),  l_i = sum_j p_ij,  P_ij = p_ij / l_i
+ *   o_ic  = sum_j P_ij v_jc                              ([GKFA] §10)
+ *   LSE_i = m_i + ln(l_i)   (natural log, scaled-score units; [GKFA] §13.2)
+ * The full S row block of one (batch, head) is materialised, then turned into
+ * P in place, then multiplied by V: no blocking, no fusion.
+ *
+ * Rows that have no key at all (possible only in the variable-length form with
+ * an empty key sequence) have no softmax.  The pages are silent; this oracle
+ * returns o = 0 and LSE = -inf for them (log of an empty sum).
+ *
+ * oracle_attn_online() restates the blockwise recurrence of [GKFA] §11.3 with
+ * the deferred division of §14.1, again in double.  It exists only so tests can
+ * check the pages' claim that the recurrence is exact (it must agree with the
+ * full definition to rounding).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static double bf16_to_double(uint16_t h)
+{
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/*
+ * One head: nq query rows against nk key/value rows.
+ *   q row i  starts at q + i * q_rs     (d elements, contiguous)
+ *   k/v row j starts at k/v + j * kv_rs
+ *   o row i  starts at o + i * o_rs     (d doubles)
+ *   lse of row i at lse[i * lse_stride]
+ * Returns 0, or -1 when the S block cannot be allocated.
+ */
+static int head_attention(const uint16_t *q, size_t q_rs, int nq,
+                          const uint16_t *k, const uint16_t *v, size_t kv_rs, int nk,
+                          int d, double scale,
+                          double *o, size_t o_rs, double *lse, size_t lse_stride)
+{
+    if (nq <= 0)
+        return 0;
+    if (nk <= 0) {
+        for (int i = 0; i < nq; ++i) {
+            for (int c = 0; c < d; ++c)
+                o[(size_t)i * o_rs + c] = 0.0;
+            lse[(size_t)i * lse_stride] = -INFINITY;
+        }
+        return 0;
+    }
+    double *S = (double *)malloc((size_t)nq * (size_t)nk * sizeof(double));
+    if (!S)
+        return -1;
+
+    /* S = scale * Q K^T, materialised ([GKFA] §10). */
+    for (int i = 0; i < nq; ++i) {
+        const uint16_t *qi = q + (size_t)i * q_rs;
+        for (int j = 0; j < nk; ++j) {
+            const uint16_t *kj = k + (size_t)j * kv_rs;
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c)
+                acc += bf16_to_double(qi[c]) * bf16_to_double(kj[c]);
+            S[(size_t)i * nk + j] = scale * acc;
+        }
+    }
+
+    /* Safe softmax, row by row, three passes: max, exp and sum, divide
+       ([GKFA] §11.1).  P overwrites S. */
+    for (int i = 0; i < nq; ++i) {
+        double *row = S + (size_t)i * nk;
+        double m = row[0];
+        for (int j = 1; j < nk; ++j)
+            if (row[j] > m)
+                m = row[j];
+        double l = 0.0;
+        for (int j = 0; j < nk; ++j) {
+            row[j] = exp(row[j] - m);
+            l += row[j];
+        }
+        for (int j = 0; j < nk; ++j)
+            row[j] /= l;
+        lse[(size_t)i * lse_stride] = m + log(l); /* [GKFA] §13.2 */
+    }
+
+    /* O = P V ([GKFA] §10). */
+    for (int i = 0; i < nq; ++i) {
+        const double *prow = S + (size_t)i * nk;
+        double *oi = o + (size_t)i * o_rs;
+        for (int c = 0; c < d; ++c)
+            oi[c] = 0.0;
+        for (int j = 0; j < nk; ++j) {
+            const uint16_t *vj = v + (size_t)j * kv_rs;
+            const double p = prow[j];
+            for (int c = 0; c < d; ++c)
+                oi[c] += p * bf16_to_double(vj[c]);
+        }
+    }
+    free(S);
+    return 0;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/*
+ * Dense form.  q, o: [B, Nq, H, d]; k, v: [B, Nk, H, d]; lse: [B, H, Nq].
+ * Inputs are bf16 bit patterns; outputs are double.
+ * Parallel over (b, h) only.  Returns 0, or -1 on allocation failure.
+ */
+int oracle_attn_dense(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      int B, int Nq, int Nk, int H, int d, double scale,
+                      double *o, double *lse)
+{
+    int err = 0;
+    const size_t q_rs = (size_t)H * d, kv_rs = (size_t)H * d;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1) reduction(| : err)
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < H; ++h) {
+            const size_t qoff = (size_t)b * Nq * H * d + (size_t)h * d;
+            const size_t kvoff = (size_t)b * Nk * H * d + (size_t)h * d;
+            err |= head_attention(q + qoff, q_rs, Nq, k + kvoff, v + kvoff, kv_rs, Nk, d, scale,
+                                  o + qoff, q_rs, lse + ((size_t)b * H + h) * Nq, 1);
+        }
+    }
+    return err ? -1 : 0;
+}
+
+/*
+ * Selected rows of the dense form: rows[3*r .. 3*r+2] = (b, h, i).
+ * o_rows: [n_rows, d]; lse_rows: [n_rows].  Each row is computed with the
+ * same per-head routine as oracle_attn_dense (a one-row head).
+ */
+int oracle_attn_dense_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                           int B, int Nq, int Nk, int H, int d, double scale,
+                           int n_rows, const int64_t *rows, double *o_rows, double *lse_rows)
+{
+    int err = 0;
+    const size_t kv_rs = (size_t)H * d;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int r = 0; r < n_rows; ++r) {
+        const int64_t b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
+        if (b < 0 || b >= B || h < 0 || h >= H || i < 0 || i >= Nq) {
+            err |= 1;
+            continue;
+        }
+        const size_t qoff = (((size_t)b * Nq + i) * H + h) * d;
+        const size_t kvoff = (size_t)b * Nk * H * d + (size_t)h * d;
+        err |= head_attention(q + qoff, 0, 1, k + kvoff, v + kvoff, kv_rs, Nk, d, scale,
+                              o_rows + (size_t)r * d, 0, lse_rows + r, 1);
+    }
+    return err ? -1 : 0;
+}
+
+/*
+ * Variable-length packed form ([FMHA] §3.1).  Sequence b owns query rows
+ * [cu_q[b], cu_q[b+1]) and key rows [cu_k[b], cu_k[b+1]) of the packed
+ * tensors q, o: [total_q, H, d] and k, v: [total_k, H, d].  Each sequence
+ * attends only within itself.  lse: [B, H, max_seqlen_q]; entry
+ * (b, h, i) is written for i < len_q(b) only.
+ */
+int oracle_attn_varlen(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       const int32_t *cu_q, const int32_t *cu_k, int B, int H, int d,
+                       double scale, int max_seqlen_q, double *o, double *lse)
+{
+    int err = 0;
+    const size_t rs = (size_t)H * d;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1) reduction(| : err)
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < H; ++h) {
+            const int nq = cu_q[b + 1] - cu_q[b];
+            const int nk = cu_k[b + 1] - cu_k[b];
+            if (nq > max_seqlen_q) {
+                err |= 1;
+                continue;
+            }
+            const size_t qoff = (size_t)cu_q[b] * rs + (size_t)h * d;
+            const size_t kvoff = (size_t)cu_k[b] * rs + (size_t)h * d;
+            err |= head_attention(q + qoff, rs, nq, k + kvoff, v + kvoff, rs, nk, d, scale,
+                                  o + qoff, rs, lse + ((size_t)b * H + h) * max_seqlen_q, 1);
+        }
+    }
+    return err ? -1 : 0;
+}
+
+/*
+ * Blockwise online recurrence, dense form, in double ([GKFA] §11.3, §14.1).
+ * For each query row keep m (running max), l (running sum) and the
+ * unnormalised output o~.  For each block of `block` keys:
+ *   m'  = max(m, max_j s_j)
+ *   l   = e^(m - m') l  + sum_j e^(s_j - m')
+ *   o~  = e^(m - m') o~ + sum_j e^(s_j - m') v_j
+ *   m   = m'
+ * After the last block: o = o~ / l and LSE = m + ln l.
+ * Start values: m = -inf, l = 0, o~ = 0 (first correction factor e^-inf = 0).
+ */
+int oracle_attn_online(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       int B, int Nq, int Nk, int H, int d, double scale, int block,
+                       double *o, double *lse)
+{
+    if (block <= 0)
+        return -1;
+    int err = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1) reduction(| : err)
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < H; ++h) {
+            double *ot = (double *)malloc((size_t)d * sizeof(double));
+            double *s = (double *)malloc((size_t)block * sizeof(double));
+            if (!ot || !s) {
+                free(ot);
+                free(s);
+                err |= 1;
+                continue;
+            }
+            for (int i = 0; i < Nq; ++i) {
+                const uint16_t *qi = q + (((size_t)b * Nq + i) * H + h) * d;
+                double m = -INFINITY, l = 0.0;
+                for (int c = 0; c < d; ++c)
+                    ot[c] = 0.0;
+                for (int j0 = 0; j0 < Nk; j0 += block) {
+                    const int nb = (Nk - j0 < block) ? (Nk - j0) : block;
+                    double bmax = -INFINITY;
+                    for (int jj = 0; jj < nb; ++jj) {
+                        const uint16_t *kj = k + (((size_t)b * Nk + j0 + jj) * H + h) * d;
+                        double acc = 0.0;
+                        for (int c = 0; c < d; ++c)
+                            acc += bf16_to_double(qi[c]) * bf16_to_double(kj[c]);
+                        s[jj] = scale * acc;
+                        if (s[jj] > bmax)
+                            bmax = s[jj];
+                    }
+                    const double mn = (bmax > m) ? bmax : m;
+                    const double corr = exp(m - mn); /* 0 on the first block */
+                    l *= corr;
+                    for (int c = 0; c < d; ++c)
+                        ot[c] *= corr;
+                    for (int jj = 0; jj < nb; ++jj) {
+                        const double p = exp(s[jj] - mn);
+                        const uint16_t *vj = v + (((size_t)b * Nk + j0 + jj) * H + h) * d;
+                        l += p;
+                        for (int c = 0; c < d; ++c)
+                            ot[c] += p * bf16_to_double(vj[c]);
+                    }
+                    m = mn;
+                }
+                double *oi = o + (((size_t)b * Nq + i) * H + h) * d;
+                if (Nk <= 0) {
+                    for (int c = 0; c < d; ++c)
+                        oi[c] = 0.0;
+                    lse[((size_t)b * H + h) * Nq + i] = -INFINITY;
+                } else {
+                    for (int c = 0; c < d; ++c)
+                        oi[c] = ot[c] / l;
+                    lse[((size_t)b * H + h) * Nq + i] = m + log(l);
+                }
+            }
+            free(ot);
+            free(s);
+        }
+    }
+    return err ? -1 : 0;
+}
