@@ -1,1 +1,251 @@
-"""GB300-native FlashAttention-2 forward (placeholder; binding added with the C-ABI)."""
+"""GB300 (sm_103a) FlashAttention-2 forward.
+
+Thin Python binding over the C ABI declared in ``include/fa.h``: the functions
+named ``fa_*`` here take plain integers (device addresses) and sizes exactly
+like their C counterparts; ``forward`` / ``forward_qk`` add argument
+marshalling for torch tensors (shapes, allocation of the outputs, the current
+stream).  Every step of the computation runs in the CUDA kernels of
+``libfa_gb300.so``; there is no CPU path.  If the library has not been built
+(``python -m attention_forward_fa2_gb300.build``) any call raises.
+
+What is computed ("GPU 内核与 FlashAttention" §10, §11.3, §14.1):
+``O = softmax(scale * Q K^T) V`` per (batch, head), plus the fp32 natural-log
+log-sum-exp of every score row.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfa_gb300.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = -1
+FA_ERR_UNSUPPORTED = -2
+FA_ERR_ALIGN = -3
+FA_ERR_CUDA = -4
+FA_ERR_TIMEOUT = -5
+FA_ERR_NO_DEVICE = -6
+FA_ERR_BAD_SEQLENS = -7
+
+# Every symbol include/fa.h declares.
+EXPORTS = (
+    "fa_fwd", "fa_fwd_qk", "fa_check_status", "fa_strerror", "fa_last_cuda_error",
+    "fa_set_timeout_ns", "fa_set_config", "fa_get_config", "fa_autotune",
+    "fa_selftest_wait_timeout", "fa_version",
+)
+
+
+class FaError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        msg = "%s (FA code %d)" % (strerror(code) if _lib is not None else "error", code)
+        if code == FA_ERR_CUDA and _lib is not None:
+            msg += ", cudaError %d" % _lib.fa_last_cuda_error()
+        super().__init__((what + ": " if what else "") + msg)
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfa_gb300.so (raises if it is missing: there is no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libfa_gb300.so is not built (%s); run "
+                               "`python -m attention_forward_fa2_gb300.build`" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        vp, ci, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, vp, vp]
+        L.fa_fwd_qk.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp, vp, vp]
+        L.fa_check_status.argtypes = [vp, ctypes.POINTER(ci)]
+        L.fa_strerror.argtypes = [ci]
+        L.fa_strerror.restype = ctypes.c_char_p
+        L.fa_last_cuda_error.argtypes = []
+        L.fa_set_timeout_ns.argtypes = [ctypes.c_ulonglong]
+        L.fa_set_config.argtypes = [ctypes.c_char_p]
+        L.fa_get_config.argtypes = [ci, ci, ci, ctypes.c_char_p, ci]
+        L.fa_autotune.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, vp, vp]
+        L.fa_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, vp]
+        L.fa_version.argtypes = []
+        for name in EXPORTS:
+            if name != "fa_strerror":
+                getattr(L, name).restype = ci
+        _lib = L
+        return L
+
+
+# ------------------------------------------------------------ raw C-ABI calls
+def fa_fwd(q, k, v, o, lse, B, N, H, d, scale, cu_seqlens, stream) -> int:
+    return lib().fa_fwd(q, k, v, o, lse, B, N, H, d, scale, cu_seqlens, stream)
+
+
+def fa_fwd_qk(q, k, v, o, lse, B, Nq, Nk, H, d, scale, cu_q, cu_k, stream) -> int:
+    return lib().fa_fwd_qk(q, k, v, o, lse, B, Nq, Nk, H, d, scale, cu_q, cu_k, stream)
+
+
+def fa_check_status(stream=None):
+    info = (ctypes.c_int * 3)()
+    rc = lib().fa_check_status(stream, info)
+    return rc, tuple(info)
+
+
+def fa_autotune(q, k, v, o, lse, B, N, H, d, scale, cu_seqlens, stream) -> int:
+    return lib().fa_autotune(q, k, v, o, lse, B, N, H, d, scale, cu_seqlens, stream)
+
+
+def fa_selftest_wait_timeout(timeout_ns: int, stream=None) -> int:
+    return lib().fa_selftest_wait_timeout(int(timeout_ns), stream)
+
+
+def strerror(code: int) -> str:
+    return lib().fa_strerror(int(code)).decode()
+
+
+def version() -> int:
+    return lib().fa_version()
+
+
+def set_timeout_ns(ns: int) -> None:
+    lib().fa_set_timeout_ns(int(ns))
+
+
+def set_config(spec) -> None:
+    rc = lib().fa_set_config(spec.encode() if spec else None)
+    if rc != FA_OK:
+        raise FaError(rc, "set_config(%r)" % (spec,))
+
+
+def get_config(d: int, N: int, varlen: bool = False) -> str:
+    buf = ctypes.create_string_buffer(128)
+    rc = lib().fa_get_config(int(d), int(N), int(bool(varlen)), buf, 128)
+    if rc != FA_OK:
+        raise FaError(rc, "get_config")
+    return buf.value.decode()
+
+
+# ------------------------------------------------------ torch-tensor wrappers
+def _stream_handle(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check_tensor(name, t, dtype, ndim):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor (the library has no CPU path)" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError("%s must have %d dims, got %s" % (name, ndim, tuple(t.shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def forward_qk(q, k, v, scale=None, cu_seqlens_q=None, cu_seqlens_k=None,
+               max_seqlen_q=None, max_seqlen_k=None, out=None, lse=None, stream=None):
+    """Attention forward with separate query / key lengths.
+
+    Dense: q [B, Nq, H, d], k/v [B, Nk, H, d] (bf16, CUDA, contiguous).
+    Variable length: q [total_q, H, d], k/v [total_k, H, d], cu_seqlens_* int32
+    [B + 1] on the device, max_seqlen_* the longest query / key sequence.
+    Returns (o, lse): o like q (bf16), lse [B, H, Nq] fp32 (natural log).
+    """
+    import torch
+    varlen = cu_seqlens_q is not None or cu_seqlens_k is not None
+    if varlen:
+        if cu_seqlens_q is None or cu_seqlens_k is None or max_seqlen_q is None or max_seqlen_k is None:
+            raise ValueError("variable-length form needs cu_seqlens_q/k and max_seqlen_q/k")
+        for name, t in (("q", q), ("k", k), ("v", v)):
+            _check_tensor(name, t, torch.bfloat16, 3)
+        _check_tensor("cu_seqlens_q", cu_seqlens_q, torch.int32, 1)
+        _check_tensor("cu_seqlens_k", cu_seqlens_k, torch.int32, 1)
+        B = cu_seqlens_q.numel() - 1
+        if cu_seqlens_k.numel() != B + 1:
+            raise ValueError("cu_seqlens_q and cu_seqlens_k differ in length")
+        _, H, d = q.shape
+        if k.shape[1:] != (H, d) or v.shape != k.shape:
+            raise ValueError("k/v shape mismatch")
+        Nq, Nk = int(max_seqlen_q), int(max_seqlen_k)
+    else:
+        for name, t in (("q", q), ("k", k), ("v", v)):
+            _check_tensor(name, t, torch.bfloat16, 4)
+        B, Nq, H, d = q.shape
+        Nk = k.shape[1]
+        if k.shape != (B, Nk, H, d) or v.shape != k.shape:
+            raise ValueError("k/v shape mismatch")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check_tensor("out", out, torch.bfloat16, q.dim())
+        if out.shape != q.shape:
+            raise ValueError("out shape mismatch")
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    else:
+        _check_tensor("lse", lse, torch.float32, 3)
+        if tuple(lse.shape) != (B, H, Nq):
+            raise ValueError("lse must be [B, H, Nq]")
+    with torch.cuda.device(q.device):
+        rc = fa_fwd_qk(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                       B, Nq, Nk, H, d, float(scale),
+                       cu_seqlens_q.data_ptr() if varlen else None,
+                       cu_seqlens_k.data_ptr() if varlen else None,
+                       _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_qk")
+    return out, lse
+
+
+def forward(q, k, v, scale=None, cu_seqlens=None, max_seqlen=None, out=None, lse=None,
+            stream=None):
+    """Self-attention shapes (the C entry fa_fwd): dense q/k/v [B, N, H, d], or
+    packed [total, H, d] with one cu_seqlens for queries and keys."""
+    if cu_seqlens is not None:
+        if max_seqlen is None:
+            raise ValueError("max_seqlen is required with cu_seqlens")
+        return forward_qk(q, k, v, scale, cu_seqlens, cu_seqlens, max_seqlen, max_seqlen,
+                          out=out, lse=lse, stream=stream)
+    return forward_qk(q, k, v, scale, out=out, lse=lse, stream=stream)
+
+
+def check_status(stream=None):
+    """Synchronise and return (code, (block, warp, site)) of the first device error."""
+    import torch
+    with torch.cuda.device(torch.cuda.current_device()):
+        return fa_check_status(_stream_handle(stream))
+
+
+def autotune(q, k, v, scale=None, cu_seqlens=None, max_seqlen=None, stream=None):
+    """Time the candidate kernel configs on these tensors and keep the fastest
+    for their (d, N bucket, varlen) key.  Returns the chosen config spec."""
+    import torch
+    varlen = cu_seqlens is not None
+    if varlen:
+        B = cu_seqlens.numel() - 1
+        _, H, d = q.shape
+        N = int(max_seqlen)
+    else:
+        B, N, H, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    rc = fa_autotune(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                     B, N, H, d, float(scale), cu_seqlens.data_ptr() if varlen else None,
+                     _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_autotune")
+    return get_config(d, N, varlen)

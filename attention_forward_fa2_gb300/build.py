@@ -1,0 +1,90 @@
+"""Build the CUDA library in-tree: attention_forward_fa2_gb300/libfa_gb300.so.
+
+nvcc compiles each translation unit for sm_103a in parallel, then links a
+shared library with the C ABI of include/fa.h.  Usage:
+
+    python -m attention_forward_fa2_gb300.build [--force] [--verbose]
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import shutil
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD = os.path.join(PKG, "_build")
+LIB = os.path.join(PKG, "libfa_gb300.so")
+UNITS = ("fa_api.cu", "fa_fwd_d128.cu", "fa_fwd_d64.cu")
+HEADERS = ("ptx.cuh", "fa_fwd_kernel.cuh", "fa_launch.h")
+
+NVCC_FLAGS = [
+    "-gencode", "arch=compute_103a,code=sm_103a",
+    "-O3", "-lineinfo", "-std=c++17",
+    "-Xcompiler", "-fPIC",
+    "-Xptxas", "-v",
+]
+
+
+def nvcc() -> str:
+    path = shutil.which("nvcc")
+    if path:
+        return path
+    cand = "/usr/local/cuda/bin/nvcc"
+    if os.path.exists(cand):
+        return cand
+    raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libfa_gb300.so")
+
+
+def _newest_input() -> float:
+    files = [os.path.join(CSRC, f) for f in UNITS + HEADERS]
+    files.append(os.path.join(INCLUDE, "fa.h"))
+    files.append(os.path.abspath(__file__))
+    return max(os.path.getmtime(f) for f in files)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile (if stale) and return the path of the shared library."""
+    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
+        return LIB
+    os.makedirs(BUILD, exist_ok=True)
+    cc = nvcc()
+    procs = []
+    for unit in UNITS:
+        obj = os.path.join(BUILD, unit.replace(".cu", ".o"))
+        log = open(os.path.join(BUILD, unit.replace(".cu", ".ptxas.log")), "w")
+        cmd = [cc] + NVCC_FLAGS + ["-I", INCLUDE, "-I", CSRC, "-c", os.path.join(CSRC, unit), "-o", obj]
+        procs.append((unit, obj, log, subprocess.Popen(cmd, stdout=log, stderr=subprocess.STDOUT)))
+    failed = []
+    for unit, obj, log, proc in procs:
+        rc = proc.wait()
+        log.close()
+        if rc != 0:
+            failed.append(unit)
+        if verbose or rc != 0:
+            with open(log.name) as f:
+                sys.stderr.write(f.read())
+    if failed:
+        raise RuntimeError("nvcc failed for: %s" % ", ".join(failed))
+    tmp = LIB + ".tmp.%d" % os.getpid()
+    link = [cc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-o", tmp]
+    link += [obj for _, obj, _, _ in procs]
+    subprocess.run(link, check=True)
+    os.replace(tmp, LIB)
+    return LIB
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--force", action="store_true")
+    ap.add_argument("--verbose", action="store_true")
+    args = ap.parse_args(argv)
+    print(build(force=args.force, verbose=args.verbose))
+
+
+if __name__ == "__main__":
+    main()

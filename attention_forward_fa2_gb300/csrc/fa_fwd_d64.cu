@@ -1,0 +1,11 @@
+// Kernel instantiations for d_head = 64.
+#include "fa_launch.h"
+
+namespace fa {
+FA_DEFINE_LAUNCH(64, 2, false)
+FA_DEFINE_LAUNCH(64, 3, false)
+FA_DEFINE_LAUNCH(64, 4, false)
+FA_DEFINE_LAUNCH(64, 2, true)
+FA_DEFINE_LAUNCH(64, 3, true)
+FA_DEFINE_LAUNCH(64, 4, true)
+}  // namespace fa

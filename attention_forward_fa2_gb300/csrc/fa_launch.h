@@ -1,0 +1,42 @@
+// fa_launch.h -- host-side launch interface between the C-ABI layer and the
+// kernel translation units (one per head dimension, compiled in parallel).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+
+struct LaunchArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;
+  FwdParams p;
+  dim3 grid;
+  cudaStream_t stream;
+};
+
+// Key/value tile width used by every instantiation.
+constexpr int kBC = 128;
+
+// Dynamic shared memory one CTA of launch_fwd<D, STAGES, ...> needs.
+template <int D, int STAGES>
+constexpr int smem_bytes() {
+  return SmemLayout<D, kBC, STAGES>::kAlloc;
+}
+
+template <int D, int STAGES, bool VARLEN>
+cudaError_t launch_fwd(const LaunchArgs& a);
+
+// Defined in the translation unit that owns the kernel.
+#define FA_DEFINE_LAUNCH(D, STAGES, VARLEN)                                                   \
+  template <>                                                                                 \
+  cudaError_t launch_fwd<D, STAGES, VARLEN>(const LaunchArgs& a) {                            \
+    auto* kern = &fa_fwd_kernel<D, kBC, STAGES, VARLEN>;                                      \
+    constexpr int smem = SmemLayout<D, kBC, STAGES>::kAlloc;                                  \
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); \
+    if (e != cudaSuccess) return e;                                                           \
+    kern<<<a.grid, kThreads, smem, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);          \
+    return cudaGetLastError();                                                                \
+  }
+
+}  // namespace fa

@@ -1,0 +1,144 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) FlashAttention-2 forward library.
+ *
+ * The library computes, for bf16 tensors in [batch, seq, heads, d_head]
+ * layout (the layout of the input generator on "Flash Attention 2 Chapter2",
+ * section on mapping attention tensors to mma operands),
+ *
+ *     O[b,i,h,:]  = sum_j softmax_j(scale * q_i . k_j) * v_j        (bf16 out)
+ *     LSE[b,h,i]  = log sum_j exp(scale * q_i . k_j)                (fp32, natural log)
+ *
+ * "GPU 内核与 FlashAttention" §10 defines S, P and O; §11.3 the online softmax
+ * recurrence the kernel uses; §13.2 and §14.1 the per-row log-sum-exp kept by
+ * the forward pass.  "Flash Attention实现深度解析" §3.1 gives the host entry
+ * that returns {out, softmax_lse} with lse shaped [batch, heads, max_seqlen_q]
+ * and packed [total, heads, d_head] tensors for variable-length batches.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named q, k, v, o, lse, cu_seqlens* are DEVICE pointers owned by
+ *     the caller.  The library never allocates global memory per call and never
+ *     frees caller memory.  Tensor memory (TMEM) is allocated and released
+ *     inside each kernel.
+ *   - q, k, v, o must be 16-byte aligned and densely packed (no padding).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *     enqueue work and return; results are valid once the stream is
+ *     synchronised.  Errors detected on the device (timeouts, inconsistent
+ *     cu_seqlens) are reported by fa_check_status().
+ *   - Return value: FA_OK (0) or one of the negative FA_ERR_* codes.  Argument
+ *     errors are detected on the host before anything is enqueued.
+ *   - Not thread-safe with respect to fa_set_* / fa_autotune, which change
+ *     process-wide settings.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FA_OK 0
+#define FA_ERR_INVALID_ARG (-1)  /* null pointer, negative size, bad scale, B*H too large */
+#define FA_ERR_UNSUPPORTED (-2)  /* d_head not in {64, 128}, or no sm_103a device       */
+#define FA_ERR_ALIGN (-3)        /* a tensor pointer is not 16-byte aligned             */
+#define FA_ERR_CUDA (-4)         /* a CUDA call failed; fa_last_cuda_error() has it     */
+#define FA_ERR_TIMEOUT (-5)      /* a device-side wait gave up (fa_check_status)        */
+#define FA_ERR_NO_DEVICE (-6)    /* no CUDA device is visible                           */
+#define FA_ERR_BAD_SEQLENS (-7)  /* cu_seqlens inconsistent with the maximum lengths    */
+
+/*
+ * fa_fwd -- attention forward, self-attention shapes (Nq = Nk = N).
+ *
+ * Dense form (cu_seqlens == NULL):
+ *   q, k, v, o : bf16 [B, N, H, d], contiguous; element (b, n, h, c) at
+ *                ((b * N + n) * H + h) * d + c.
+ *   lse        : fp32 [B, H, N].
+ * Variable-length form (cu_seqlens != NULL):
+ *   cu_seqlens : int32 [B + 1] device array, cu[0] = 0, non-decreasing; sequence
+ *                b owns packed rows [cu[b], cu[b+1]) of q, k, v and o, each
+ *                [total, H, d] with total = cu[B].  Sequences attend only within
+ *                themselves.
+ *   N          : the maximum sequence length (every length must be <= N); it
+ *                bounds the launch grid and is the row stride of lse.
+ *   lse        : fp32 [B, H, N]; entries (b, h, i) with i >= len(b) are not written.
+ *   A sequence longer than N is reported as FA_ERR_BAD_SEQLENS by
+ *   fa_check_status(), and its CTAs write nothing.
+ * scale        : softmax scale, finite and > 0 (1/sqrt(d) is the usual value).
+ * d            : 64 or 128.
+ * B == 0 or N == 0 is a no-op that returns FA_OK.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int N, int H,
+           int d, float scale, const int* cu_seqlens, void* stream);
+
+/*
+ * fa_fwd_qk -- general form with separate query and key lengths (for example
+ * the 64-query by 4096-key slice of "Flash Attention 2 Chapter2", introduction).
+ *
+ * Dense form (both cu pointers NULL): q, o [B, Nq, H, d]; k, v [B, Nk, H, d];
+ *   lse [B, H, Nq].  Nk must be >= 1 when Nq >= 1.
+ * Variable-length form (both cu pointers non-NULL): q, o [total_q, H, d];
+ *   k, v [total_k, H, d]; Nq / Nk are the maximum query / key lengths.  A
+ *   sequence with no keys gets o = 0 and lse = -inf (log of an empty sum).
+ * Passing exactly one cu pointer is FA_ERR_INVALID_ARG.
+ */
+int fa_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Nq,
+              int Nk, int H, int d, float scale, const int* cu_seqlens_q,
+              const int* cu_seqlens_k, void* stream);
+
+/*
+ * fa_check_status -- synchronises `stream`, then returns and clears the first
+ * device-side error recorded since the last call (FA_OK if none).  When
+ * `info` is not NULL it receives {flat block index, warp, wait site} of that
+ * error (zeros if none).  Returns FA_ERR_CUDA if synchronisation fails.
+ */
+int fa_check_status(void* stream, int* info);
+
+/* Human-readable text for an FA_* code (static storage). */
+const char* fa_strerror(int code);
+
+/* The cudaError_t of the most recent FA_ERR_CUDA on this thread. */
+int fa_last_cuda_error(void);
+
+/*
+ * fa_set_timeout_ns -- limit for every device-side wait (mbarrier waits) in
+ * later launches.  On expiry the kernel records FA_ERR_TIMEOUT, drains its
+ * own copies and MMAs, releases tensor memory and exits.  Default 1e9 ns.
+ * ns == 0 restores the default.
+ */
+int fa_set_timeout_ns(unsigned long long ns);
+
+/*
+ * Kernel configuration ("Flash Attention 2 Chapter6", Kernel 7: the
+ * configuration space is searched per shape instead of fixed).  A config is
+ * a text spec "stages=<2|3|4>,threshold=<float>": the depth of the
+ * shared-memory key/value ring and the O-rescale threshold in log2 units
+ * (0 rescales whenever a row maximum grows).
+ *
+ * fa_set_config  -- force `spec` for every later call (NULL or "" clears it).
+ * fa_get_config  -- writes the spec that a call with (d, N, varlen) would use
+ *                   into buf (NUL-terminated, truncated to len); returns FA_OK.
+ * fa_autotune    -- times every candidate config on the caller's tensors (same
+ *                   arguments as fa_fwd), keeps the fastest for the key
+ *                   (d, N bucket, varlen) and leaves the outputs written by
+ *                   the winner.  Synchronises `stream`.
+ */
+int fa_set_config(const char* spec);
+int fa_get_config(int d, int N, int varlen, char* buf, int len);
+int fa_autotune(const void* q, const void* k, const void* v, void* o, float* lse, int B, int N,
+                int H, int d, float scale, const int* cu_seqlens, void* stream);
+
+/*
+ * fa_selftest_wait_timeout -- launches one small kernel whose only work is an
+ * mbarrier wait that nothing completes, bounded by `timeout_ns` (> 0, at most
+ * 10 s).  It exercises the same bounded-wait routine as the attention kernel;
+ * the expected outcome is FA_ERR_TIMEOUT from fa_check_status() with the
+ * device still usable.  Returns FA_OK when the launch was enqueued.
+ */
+int fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FA_GB300_H */

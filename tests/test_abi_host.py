@@ -1,0 +1,135 @@
+"""Host-side checks of the C-ABI library: it builds, loads, exports every symbol
+include/fa.h declares, and rejects bad arguments before touching a device.
+No call here launches GPU work."""
+import os
+import re
+
+import pytest
+import torch
+
+import attention_forward_fa2_gb300 as fa
+from attention_forward_fa2_gb300 import build as fabuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    fabuild.build()
+    return fa.lib()
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_exactly_the_binding_exports():
+    assert _declared() == sorted(fa.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+
+
+def test_version_and_strerror(L):
+    assert fa.version() == 100
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
+        assert fa.strerror(code) and fa.strerror(code) != "unknown error"
+    assert fa.strerror(-99) == "unknown error"
+
+
+def test_config_spec_roundtrip(L):
+    try:
+        fa.set_config("stages=3,threshold=0")
+        assert fa.get_config(128, 4096) == "stages=3,threshold=0"
+        fa.set_config("threshold=8")
+        assert fa.get_config(64, 512) == "stages=4,threshold=8"
+        for bad in ("stages=5", "stages=1", "threshold=-1", "foo=1", "stages", "threshold=nan"):
+            with pytest.raises(fa.FaError):
+                fa.set_config(bad)
+    finally:
+        fa.set_config(None)
+    assert fa.get_config(128, 4096) == "stages=4,threshold=8"
+
+
+def test_timeout_setter(L):
+    assert L.fa_set_timeout_ns(5_000_000) == 0
+    assert L.fa_set_timeout_ns(0) == 0  # back to the default
+
+
+# Fake, never-dereferenced addresses: validation fails before any CUDA call.
+A = 0x10000
+MIS = 0x10008  # 8-byte aligned only
+
+
+def _fwd(L, q=A, k=A, v=A, o=A, lse=A, B=1, N=128, H=1, d=128, scale=0.1, cu=None):
+    return L.fa_fwd(q, k, v, o, lse, B, N, H, d, scale, cu, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-0.5), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(B=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(N=-3), fa.FA_ERR_INVALID_ARG),
+    (dict(H=-2), fa.FA_ERR_INVALID_ARG),
+    (dict(q=0), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=0), fa.FA_ERR_INVALID_ARG),
+    (dict(q=MIS), fa.FA_ERR_ALIGN),
+    (dict(v=MIS), fa.FA_ERR_ALIGN),
+    (dict(o=MIS), fa.FA_ERR_ALIGN),
+    (dict(lse=A + 2), fa.FA_ERR_ALIGN),
+    (dict(H=70000), fa.FA_ERR_INVALID_ARG),
+    (dict(B=70000), fa.FA_ERR_INVALID_ARG),
+    (dict(B=40000, N=65536), fa.FA_ERR_INVALID_ARG),
+])
+def test_argument_errors(L, kw, code):
+    assert _fwd(L, **kw) == code
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(N=0), dict(H=0), dict(B=0, q=0, k=0, v=0, o=0, lse=0)])
+def test_empty_problems_are_noops(L, kw):
+    assert _fwd(L, **kw) == fa.FA_OK
+
+
+def test_qk_form_argument_errors(L):
+    # exactly one cu_seqlens pointer
+    assert L.fa_fwd_qk(A, A, A, A, A, 1, 8, 8, 1, 128, 0.1, A, None, None) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_fwd_qk(A, A, A, A, A, 1, 8, 8, 1, 128, 0.1, None, A, None) == fa.FA_ERR_INVALID_ARG
+    # dense with queries but no keys
+    assert L.fa_fwd_qk(A, A, A, A, A, 1, 8, 0, 1, 128, 0.1, None, None, None) == fa.FA_ERR_INVALID_ARG
+    # misaligned cu_seqlens
+    assert L.fa_fwd_qk(A, A, A, A, A, 1, 8, 8, 1, 128, 0.1, A + 2, A, None) == fa.FA_ERR_ALIGN
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a device")
+def test_valid_call_without_device_reports_no_device(L):
+    assert _fwd(L) == fa.FA_ERR_NO_DEVICE
+
+
+def test_selftest_argument_range(L):
+    assert L.fa_selftest_wait_timeout(0, None) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_selftest_wait_timeout(20_000_000_000, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_torch_wrapper_rejects_cpu_tensors(L):
+    q = torch.zeros(1, 8, 1, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        fa.forward(q, q, q)
+
+
+def test_product_package_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "attention_forward_fa2_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "attn_ref" not in text and "liboracle" not in text, f

@@ -1,0 +1,256 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Small cases compare every output element; the full-size workloads compare
+sampled rows that the oracle computes one by one, in the same launch
+configuration the benchmark times.  Bar: max|dO| <= 2e-2, max|dLSE| <= 1e-3.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attention_forward_fa2_gb300 as fa
+from attention_forward_fa2_gb300 import inputs as I
+from fa_testutil import (LSE_TOL, O_TOL, assert_close, bits, gpu_dense, gpu_varlen,
+                         sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from attention_forward_fa2_gb300 import build
+    build.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fa.set_config(None)
+    yield
+    fa.set_config(None)
+
+
+def _oracle_dense(oracle_mod, q, k, v, scale=None):
+    return oracle_mod.attn_dense(bits(q), bits(k), bits(v), scale=scale)
+
+
+# ----------------------------------------------------------- named workloads
+def test_tiny_full_parity(oracle_mod):
+    w = I.TINY
+    q, k, v, _, _ = I.make(w)
+    o, lse = gpu_dense(q, k, v)
+    o_ref, lse_ref = _oracle_dense(oracle_mod, q, k, v)
+    assert_close(o, lse, o_ref, lse_ref, "tiny")
+
+
+def test_slice_full_parity(oracle_mod):
+    w = I.SLICE
+    q, k, v, _, _ = I.make(w)
+    o, lse = gpu_dense(q, k, v)
+    o_ref, lse_ref = _oracle_dense(oracle_mod, q, k, v)
+    assert_close(o, lse, o_ref, lse_ref, "slice 64x4096")
+
+
+def _sampled_dense(oracle_mod, w, n_random=48):
+    q, k, v, _, _ = I.make(w)
+    o, lse = gpu_dense(q, k, v)
+    assert np.all(np.isfinite(lse))
+    rows = sample_rows(w.B, w.Nq, w.H, n_random=n_random, seed=w.seed)
+    o_ref, lse_ref = oracle_mod.attn_dense_rows(bits(q), bits(k), bits(v), rows)
+    b, h, i = rows[:, 0], rows[:, 1], rows[:, 2]
+    return assert_close(o[b, i, h, :], lse[b, h, i], o_ref, lse_ref, w.name)
+
+
+def test_page_workload_sampled(oracle_mod):
+    _sampled_dense(oracle_mod, I.PAGE, n_random=96)
+
+
+@pytest.mark.parametrize("w", I.SWEEP, ids=[w.name for w in I.SWEEP])
+def test_sweep_sampled(oracle_mod, w):
+    _sampled_dense(oracle_mod, w, n_random=24)
+
+
+def test_varlen_workload_sampled(oracle_mod):
+    w = I.VARLEN
+    q, k, v, cu_q, cu_k = I.make(w)
+    maxlen = max(w.lengths)
+    o, lse = gpu_varlen(q, k, v, cu_q, cu_k, maxlen, maxlen)
+    cu = cu_q.numpy()
+    rng = np.random.default_rng(7)
+    for bseq in range(w.B):
+        n = int(cu[bseq + 1] - cu[bseq])
+        qs = q[cu[bseq]:cu[bseq + 1]].unsqueeze(0)
+        ks = k[cu[bseq]:cu[bseq + 1]].unsqueeze(0)
+        vs = v[cu[bseq]:cu[bseq + 1]].unsqueeze(0)
+        idx = sorted({0, n - 1, min(127, n - 1), min(128, n - 1), int(rng.integers(n)), (n // 256) * 256 % n})
+        hs = [0, w.H - 1, int(rng.integers(w.H))]
+        rows = np.array([(0, h, i) for h in hs for i in idx], dtype=np.int64)
+        o_ref, lse_ref = oracle_mod.attn_dense_rows(bits(qs), bits(ks), bits(vs), rows)
+        og = np.stack([o[cu[bseq] + i, h] for (_, h, i) in rows])
+        lg = np.array([lse[bseq, h, i] for (_, h, i) in rows])
+        assert_close(og, lg, o_ref, lse_ref, "varlen seq %d (len %d)" % (bseq, n))
+
+
+# ----------------------------------------------------------------- edge cases
+@pytest.mark.parametrize("B,Nq,Nk,H,d", [
+    (1, 1, 1, 1, 128), (1, 1, 5, 1, 64), (2, 127, 129, 3, 128), (1, 128, 128, 2, 64),
+    (1, 129, 127, 1, 128), (1, 255, 300, 2, 128), (1, 256, 256, 1, 64), (1, 257, 1, 2, 128),
+    (3, 300, 513, 2, 64), (1, 64, 4096, 1, 64), (2, 513, 384, 1, 128), (1, 1000, 1000, 1, 128),
+])
+def test_ragged_shapes_full_parity(oracle_mod, B, Nq, Nk, H, d):
+    q, k, v = I.make_dense(B, Nq, Nk, H, d, seed=1000 + Nq + Nk + d)
+    o, lse = gpu_dense(q, k, v)
+    o_ref, lse_ref = _oracle_dense(oracle_mod, q, k, v)
+    assert_close(o, lse, o_ref, lse_ref, "ragged %s" % ((B, Nq, Nk, H, d),))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_varlen_ragged_full_parity(oracle_mod, d):
+    lens_q = [1, 127, 128, 129, 255, 256, 257, 300, 5, 700]
+    lens_k = [3, 130, 128, 1, 255, 600, 257, 300, 129, 64]
+    H = 3
+    q, k, v, cu_q, cu_k = I.make_varlen(lens_q, H, d, 77 + d, lengths_k=lens_k)
+    o, lse = gpu_varlen(q, k, v, cu_q, cu_k, max(lens_q), max(lens_k))
+    o_ref, lse_ref = oracle_mod.attn_varlen(bits(q), bits(k), bits(v), cu_q.numpy(), cu_k.numpy(),
+                                            max(lens_q))
+    valid = ~np.isnan(lse_ref)
+    assert_close(o, lse[valid], o_ref, lse_ref[valid], "varlen ragged d%d" % d)
+
+
+def test_varlen_empty_sequences(oracle_mod):
+    lens_q = [0, 3, 200, 0, 130]
+    lens_k = [4, 0, 131, 0, 300]
+    q, k, v, cu_q, cu_k = I.make_varlen(lens_q, 2, 128, 91, lengths_k=lens_k)
+    lse_init = torch.full((5, 2, 200), 123.0, device="cuda")
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    o, lse = fa.forward_qk(dq, dk, dv, None, cu_q.cuda(), cu_k.cuda(), 200, 300, lse=lse_init)
+    rc, info = fa.check_status()
+    assert rc == fa.FA_OK, info
+    o = o.double().cpu().numpy()
+    lse = lse.double().cpu().numpy()
+    o_ref, lse_ref = oracle_mod.attn_varlen(bits(q), bits(k), bits(v), cu_q.numpy(), cu_k.numpy(), 200)
+    valid = ~np.isnan(lse_ref)
+    fin = np.isfinite(lse_ref)
+    assert np.all(np.isneginf(lse[valid & ~fin]))       # sequence with no keys
+    assert np.all(o[0:3] == 0.0)                           # its O rows are zero
+    assert_close(o, lse[valid & fin], o_ref, lse_ref[valid & fin], "varlen empty")
+    assert np.all(lse[~valid] == 123.0)                    # rows past a length untouched
+
+
+def test_empty_problem_writes_nothing():
+    o = torch.full((2, 4, 1, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((2, 1, 4), 7.0, device="cuda")
+    z = torch.zeros((2, 0, 1, 128), dtype=torch.bfloat16, device="cuda")
+    rc = fa.fa_fwd(z.data_ptr(), z.data_ptr(), z.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                   2, 0, 1, 128, 0.1, None, torch.cuda.current_stream().cuda_stream)
+    assert rc == fa.FA_OK
+    torch.cuda.synchronize()
+    assert torch.all(o == 7.0) and torch.all(lse == 7.0)
+
+
+# ----------------------------------------------------- invariants on the GPU
+def test_zero_query_gives_mean_of_values():
+    B, N, H, d = 1, 300, 2, 128
+    _, k, v = I.make_dense(B, N, N, H, d, 5)
+    q = torch.zeros_like(k)
+    o, lse = gpu_dense(q, k, v)
+    mean = v.double().mean(dim=1).numpy()
+    for i in (0, 150, 299):
+        assert np.max(np.abs(o[:, i] - mean)) <= O_TOL
+    assert np.max(np.abs(lse - math.log(N))) <= LSE_TOL
+
+
+def test_identical_value_rows():
+    B, N, H, d = 1, 400, 1, 64
+    q, k, _ = I.make_dense(B, N, N, H, d, 6)
+    row = torch.linspace(-2, 2, d).to(torch.bfloat16)
+    v = row.expand(B, N, H, d).contiguous()
+    o, _ = gpu_dense(q, k, v)
+    assert np.max(np.abs(o - row.double().numpy())) <= O_TOL
+
+
+def test_key_value_permutation_invariance():
+    B, N, H, d = 1, 512, 2, 128
+    q, k, v = I.make_dense(B, N, N, H, d, 8)
+    perm = torch.from_numpy(np.random.default_rng(3).permutation(N))
+    o1, l1 = gpu_dense(q, k, v)
+    o2, l2 = gpu_dense(q, k[:, perm].contiguous(), v[:, perm].contiguous())
+    assert np.max(np.abs(o1 - o2)) <= O_TOL and np.max(np.abs(l1 - l2)) <= LSE_TOL
+
+
+def test_large_scores_stay_finite(oracle_mod):
+    """Scores of order 1e3: the online max keeps every exponent <= 0."""
+    B, N, H, d = 1, 256, 1, 128
+    q, k, v = I.make_dense(B, N, N, H, d, 9)
+    q = (q.float() * 8).to(torch.bfloat16)
+    o, lse = gpu_dense(q, k, v, scale=2.0)
+    o_ref, lse_ref = oracle_mod.attn_dense(bits(q), bits(k), bits(v), scale=2.0)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    assert np.max(np.abs(o - o_ref)) <= O_TOL
+    assert np.max(np.abs(lse - lse_ref) / np.maximum(1.0, np.abs(lse_ref))) <= LSE_TOL
+
+
+def test_deterministic():
+    q, k, v = I.make_dense(2, 700, 700, 2, 128, 10)
+    o1, l1 = gpu_dense(q, k, v)
+    o2, l2 = gpu_dense(q, k, v)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ------------------------------------------------------------ configurations
+@pytest.mark.parametrize("spec", ["stages=2,threshold=0", "stages=3,threshold=0",
+                                  "stages=4,threshold=0", "stages=2,threshold=8",
+                                  "stages=3,threshold=8", "stages=4,threshold=8"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_every_config(oracle_mod, spec, d):
+    fa.set_config(spec)
+    try:
+        q, k, v = I.make_dense(2, 333, 517, 2, d, 11 + d)
+        o, lse = gpu_dense(q, k, v)
+        o_ref, lse_ref = _oracle_dense(oracle_mod, q, k, v)
+        assert_close(o, lse, o_ref, lse_ref, spec)
+        lens = [129, 1, 384, 77]
+        q, k, v, cu_q, cu_k = I.make_varlen(lens, 2, d, 12 + d)
+        o, lse = gpu_varlen(q, k, v, cu_q, cu_k, 384, 384)
+        o_ref, lse_ref = oracle_mod.attn_varlen(bits(q), bits(k), bits(v), cu_q.numpy(), cu_k.numpy(), 384)
+        valid = ~np.isnan(lse_ref)
+        assert_close(o, lse[valid], o_ref, lse_ref[valid], spec + " varlen")
+    finally:
+        fa.set_config(None)
+
+
+def test_autotune_keeps_parity(oracle_mod):
+    q, k, v = I.make_dense(1, 1024, 1024, 4, 128, 13)
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    spec = fa.autotune(dq, dk, dv)
+    assert spec.startswith("stages=")
+    o, lse = gpu_dense(q, k, v)
+    o_ref, lse_ref = _oracle_dense(oracle_mod, q, k, v)
+    assert_close(o, lse, o_ref, lse_ref, "autotuned " + spec)
+
+
+# ------------------------------------------------------- failure detection
+def test_device_checked_seqlens_error():
+    """A sequence longer than the declared maximum is refused by the kernel's
+    own check (nothing is read or written for it) and reported."""
+    lens = [100, 300]
+    q, k, v, cu_q, cu_k = I.make_varlen(lens, 1, 128, 14)
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    o = torch.zeros_like(dq)
+    lse = torch.zeros((2, 1, 256), device="cuda")
+    rc = fa.fa_fwd(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                   2, 256, 1, 128, 0.1, cu_q.cuda().data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == fa.FA_OK
+    code, _ = fa.check_status()
+    assert code == fa.FA_ERR_BAD_SEQLENS
+    assert fa.check_status()[0] == fa.FA_OK  # cleared
+
+
+def test_wait_timeout_is_reported_and_device_stays_usable(oracle_mod):
+    rc = fa.fa_selftest_wait_timeout(20_000_000, torch.cuda.current_stream().cuda_stream)
+    assert rc == fa.FA_OK
+    code, info = fa.check_status()
+    assert code == fa.FA_ERR_TIMEOUT and info[2] == 99
+    q, k, v = I.make_dense(1, 200, 200, 1, 128, 15)
+    o, lse = gpu_dense(q, k, v)
+    o_ref, lse_ref = _oracle_dense(oracle_mod, q, k, v)
+    assert_close(o, lse, o_ref, lse_ref, "after timeout")
