@@ -48,6 +48,7 @@ struct DeviceState {
   bool init = false;
   bool supported = false;
   int* status = nullptr;  // device address of g_status on this device
+  int num_sms = 0;
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -77,6 +78,8 @@ int device_state(DeviceState** out) {
     if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
       return cuda_fail(e);
     st.supported = (major == 10 && minor == 3);
+    if ((e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e);
     if (st.supported) {
       void* p = nullptr;
       if ((e = cudaGetSymbolAddress(&p, g_status)) != cudaSuccess) return cuda_fail(e);
@@ -125,7 +128,7 @@ Config pick_config(int d, int N, int varlen) {
   if (g_forced) return g_forced_cfg;
   auto it = g_tuned.find(std::make_tuple(d, n_bucket(N), varlen));
   if (it != g_tuned.end()) return it->second;
-  return Config{d == 128 ? 4 : 4, 8.f};
+  return Config{d == 128 ? 2 : 3, 8.f};
 }
 
 bool parse_config(const char* spec, Config* out) {
@@ -157,13 +160,36 @@ bool parse_config(const char* spec, Config* out) {
   return true;
 }
 
+// Ring depth actually used: each slot holds one K tile and one V tile, so
+// d = 128 fits two slots next to the query tiles; d = 64 fits up to four.
+int effective_stages(int d, int stages) { return d == 128 ? 2 : stages; }
+
 template <int D, bool VARLEN>
-cudaError_t dispatch_stages(int stages, const fa::LaunchArgs& a) {
+cudaError_t dispatch_stages(int stages, const fa::LaunchArgs& a);
+
+template <>
+cudaError_t dispatch_stages<128, false>(int, const fa::LaunchArgs& a) {
+  return fa::launch_fwd<128, 2, false>(a);
+}
+template <>
+cudaError_t dispatch_stages<128, true>(int, const fa::LaunchArgs& a) {
+  return fa::launch_fwd<128, 2, true>(a);
+}
+template <bool VARLEN>
+cudaError_t dispatch_d64(int stages, const fa::LaunchArgs& a) {
   switch (stages) {
-    case 2: return fa::launch_fwd<D, 2, VARLEN>(a);
-    case 3: return fa::launch_fwd<D, 3, VARLEN>(a);
-    default: return fa::launch_fwd<D, 4, VARLEN>(a);
+    case 2: return fa::launch_fwd<64, 2, VARLEN>(a);
+    case 3: return fa::launch_fwd<64, 3, VARLEN>(a);
+    default: return fa::launch_fwd<64, 4, VARLEN>(a);
   }
+}
+template <>
+cudaError_t dispatch_stages<64, false>(int stages, const fa::LaunchArgs& a) {
+  return dispatch_d64<false>(stages, a);
+}
+template <>
+cudaError_t dispatch_stages<64, true>(int stages, const fa::LaunchArgs& a) {
+  return dispatch_d64<true>(stages, a);
 }
 
 struct Problem {
@@ -245,6 +271,9 @@ int run(const Problem& P, const Config& cfg) {
   p.Nk = P.Nk;
   p.H = P.H;
   p.num_mblocks = (P.Nq + fa::kBR * fa::kQT - 1) / (fa::kBR * fa::kQT);
+  const long long units = static_cast<long long>(P.B) * P.H * p.num_mblocks;
+  if (units > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  p.num_units = static_cast<int>(units);
   p.cu_q = P.cu_q;
   p.cu_k = P.cu_k;
   p.lse = P.lse;
@@ -257,7 +286,8 @@ int run(const Problem& P, const Config& cfg) {
     p.timeout_ns = g_timeout_ns;
   }
   p.status = st->status;
-  a.grid = dim3(static_cast<unsigned>(p.num_mblocks), static_cast<unsigned>(P.H), static_cast<unsigned>(P.B));
+  // Persistent grid: one CTA per SM (each walks units blockIdx.x + k * gridDim.x).
+  a.grid = dim3(static_cast<unsigned>(units < st->num_sms ? units : st->num_sms), 1, 1);
   a.stream = P.stream;
 
   cudaError_t e;
@@ -360,7 +390,8 @@ int fa_set_config(const char* spec) {
 int fa_get_config(int d, int N, int varlen, char* buf, int len) {
   if (!buf || len <= 0) return FA_ERR_INVALID_ARG;
   const Config c = pick_config(d, N, varlen ? 1 : 0);
-  std::snprintf(buf, static_cast<size_t>(len), "stages=%d,threshold=%g", c.stages, c.threshold);
+  std::snprintf(buf, static_cast<size_t>(len), "stages=%d,threshold=%g", effective_stages(d, c.stages),
+                c.threshold);
   return FA_OK;
 }
 
@@ -377,11 +408,15 @@ int fa_autotune(const void* q, const void* k, const void* v, void* o, float* lse
     cudaEventDestroy(e0);
     return cuda_fail(ce);
   }
-  const Config cands[] = {{2, 0.f}, {3, 0.f}, {4, 0.f}, {2, 8.f}, {3, 8.f}, {4, 8.f}};
-  Config best{4, 8.f};
+  const Config cands_d64[] = {{2, 0.f}, {3, 0.f}, {4, 0.f}, {2, 8.f}, {3, 8.f}, {4, 8.f}};
+  const Config cands_d128[] = {{2, 0.f}, {2, 8.f}};
+  const Config* cands = d == 128 ? cands_d128 : cands_d64;
+  const int n_cands = d == 128 ? 2 : 6;
+  Config best{d == 128 ? 2 : 3, 8.f};
   float best_ms = 1e30f;
   int result = FA_OK;
-  for (const Config& c : cands) {
+  for (int ci = 0; ci < n_cands; ++ci) {
+    const Config& c = cands[ci];
     int r = run(P, c);  // warm-up
     if (r != FA_OK) { result = r; break; }
     float ms_min = 1e30f;

@@ -1,4 +1,4 @@
-// Kernel instantiations for d_head = 64.
+// Kernel instantiations for d_head = 64 (2 to 4 K/V ring slots).
 #include "fa_launch.h"
 
 namespace fa {

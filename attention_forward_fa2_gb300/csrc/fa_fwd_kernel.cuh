@@ -9,12 +9,16 @@
 // end and only the log-sum-exp kept per row (§14.1).  The N x N score matrix
 // never reaches global memory.
 //
-// Work split (§14.2, loop order with the query block outermost): one CTA owns
-// two 128-row query tiles of one (b, h) and streams all key/value tiles of
-// that head.  Roles inside the CTA (§15.2-§15.4, re-expressed for tcgen05):
+// Work split (§14.2, loop order with the query block outermost): a work unit
+// is two 128-row query tiles of one (b, h) against all key/value tiles of that
+// head.  The kernel is persistent: each CTA walks the units blockIdx.x,
+// blockIdx.x + gridDim.x, ...; units are numbered with the query block fastest,
+// so the CTAs that run at the same time share the K/V of a few heads in L2.
+// Roles inside the CTA (§15.2-§15.4, re-expressed for tcgen05):
 //   warps 0-3   softmax warpgroup for query tile 0 (one thread per row)
 //   warps 4-7   softmax warpgroup for query tile 1
-//   warps 8-11  correction warpgroup: rescales O in TMEM, then the epilogue
+//   warps 8-11  correction/epilogue warpgroup: final correction of O by 1/l,
+//               bf16 conversion, TMA store -- overlapping the next unit
 //   warp 12     MMA issue (one thread) + TMEM allocation
 //   warp 13     TMA loads (one thread)
 //   warps 14-15 idle (they only complete the register hand-off warpgroup)
@@ -22,12 +26,22 @@
 //   S_t  = columns [t*BC, t*BC + BC)         fp32 scores of tile t
 //   P_t  = columns [t*BC + BC/2, t*BC + BC)  bf16 probabilities, packed in pairs
 //   O_t  = columns [2*BC + t*D, 2*BC + t*D + D)  fp32 output accumulator
+// Key/value ring: slot g holds K(j) and V(j-1), the two tiles step j of a unit
+// consumes (S(j) = Q K(j)^T and O += P(j-1) V(j-1)); one barrier fills it and
+// one MMA commit releases it.  The ring runs on across units.
 // Two query tiles alternate on the tensor core: while one softmax warpgroup
 // exponentiates its S, the tensor core runs the other tile's GEMMs
 // ("GPU 内核与 FlashAttention" §15.3 ping-pong).  Within a tile, the MMA for
 // P(j-1) V(j-1) is issued before S(j) = Q K(j)^T; tcgen05.mma operations from
 // one thread execute in issue order, so S(j) may overwrite the columns that
 // held P(j-1).
+//
+// Rescale of O when a row maximum grows ("Flash Attention 2 Chapter6",
+// scale_l_O): the reference maximum only moves when a block maximum exceeds it
+// by more than a threshold, so rescales are rare after the first blocks; the
+// softmax warp that owns the rows applies it in TMEM itself (its TMEM lane
+// quarter holds exactly its rows of O), after S(j) completed, which implies
+// that P(j-1) V(j-1) has completed.
 //
 // Scale folding ("Flash Attention 2 Chapter6", Kernel 6): p = 2^(s * c - m * c)
 // with c = scale * log2(e), one FFMA feeding the ex2 unit per score.
@@ -41,14 +55,14 @@
 namespace fa {
 
 constexpr int kBR = 128;       // query rows per tile (tcgen05 M)
-constexpr int kQT = 2;         // query tiles per CTA
+constexpr int kQT = 2;         // query tiles per work unit
 constexpr int kThreads = 512;  // 16 warps
 constexpr int kPanel = 64;     // bf16 columns per 128-byte swizzle row
 
 // Register split after setmaxnreg (must sum to 65536 over 512 threads).
 constexpr int kRegSoftmax = 176;
-constexpr int kRegCorrection = 96;
-constexpr int kRegOther = 64;
+constexpr int kRegCorrection = 80;
+constexpr int kRegOther = 80;
 static_assert(2 * 128 * kRegSoftmax + 128 * kRegCorrection + 128 * kRegOther <= 65536,
               "register split exceeds the launch allocation");
 
@@ -57,11 +71,10 @@ enum WaitSite : int {
   kSiteLoadKV = 1,
   kSiteMmaQ = 2,
   kSiteMmaK = 3,
-  kSiteMmaV = 4,
+  kSiteLoadQ = 4,
   kSiteMmaP = 5,
-  kSiteMmaO = 6,
+  kSiteMmaOEmpty = 6,
   kSiteSoftS = 7,
-  kSiteCorrAlpha = 8,
   kSiteCorrFinal = 9,
   kSiteTeardown = 10,
 };
@@ -69,6 +82,7 @@ enum WaitSite : int {
 struct FwdParams {
   int B, Nq, Nk, H;            // variable-length form: Nq / Nk are the maximum lengths
   int num_mblocks;             // ceil(Nq / (kBR * kQT))
+  int num_units;               // B * H * num_mblocks
   const int* cu_q;             // variable-length form: int32 [B + 1]
   const int* cu_k;
   float* lse;                  // [B, H, Nq] fp32
@@ -86,7 +100,7 @@ constexpr int kErrBadSeqlens = -7;
 
 __device__ __forceinline__ void record_error(int* status, int code, int site) {
   if (atomicCAS(status, 0, code) == 0) {
-    status[1] = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    status[1] = blockIdx.x;
     status[2] = threadIdx.x >> 5;
     status[3] = site;
   }
@@ -98,27 +112,32 @@ struct SmemLayout {
   static constexpr int kQPanelBytes = kBR * 128;
   static constexpr int kKVTileBytes = BC * D * 2;
   static constexpr int kKVPanelBytes = BC * 128;
+  static constexpr int kSlotBytes = 2 * kKVTileBytes;  // K(j) then V(j-1)
+  static constexpr int kStageWarpBytes = 32 * D * 2;   // 32 output rows per epilogue warp
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kOffQ + kQT * kQTileBytes;
-  static constexpr int kOffBar = kOffKV + STAGES * kKVTileBytes;
+  static constexpr int kOffStage = kOffKV + STAGES * kSlotBytes;
+  static constexpr int kOffBar = kOffStage + 4 * kStageWarpBytes;
   // barriers (8 bytes each)
   static constexpr int kBarQFull = 0;
-  static constexpr int kBarKVFull = 1;
+  static constexpr int kBarQEmpty = 1;
+  static constexpr int kBarKVFull = 2;
   static constexpr int kBarKVEmpty = kBarKVFull + STAGES;
   static constexpr int kBarSFull = kBarKVEmpty + STAGES;
   static constexpr int kBarPFull = kBarSFull + kQT;
-  static constexpr int kBarAlpha = kBarPFull + kQT;
-  static constexpr int kBarOReady = kBarAlpha + kQT;
-  static constexpr int kBarOFinal = kBarOReady + kQT;
-  static constexpr int kBarTeardown = kBarOFinal + kQT;
+  static constexpr int kBarLReady = kBarPFull + kQT;
+  static constexpr int kBarOFinal = kBarLReady + kQT;
+  static constexpr int kBarOEmpty = kBarOFinal + kQT;
+  static constexpr int kBarTeardown = kBarOEmpty + kQT;
   static constexpr int kNumBars = kBarTeardown + 1;
-  static constexpr int kOffAlpha = kOffBar + ((kNumBars * 8 + 15) / 16) * 16;
-  static constexpr int kOffInvL = kOffAlpha + kQT * kBR * 4;
+  static constexpr int kOffInvL = kOffBar + ((kNumBars * 8 + 15) / 16) * 16;
   static constexpr int kOffTmem = kOffInvL + kQT * kBR * 4;
   static constexpr int kOffAbort = kOffTmem + 16;
   static constexpr int kBytes = kOffAbort + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
-  static_assert(kOffKV % 1024 == 0 && kKVTileBytes % 1024 == 0, "swizzled tiles need 1 KiB alignment");
+  static_assert(kOffKV % 1024 == 0 && kKVTileBytes % 1024 == 0 && kOffStage % 1024 == 0 &&
+                    kStageWarpBytes % 1024 == 0,
+                "swizzled tiles need 1 KiB alignment");
   static_assert(kAlloc <= 232448, "shared memory budget exceeded");
 };
 
@@ -147,6 +166,58 @@ __device__ __forceinline__ RowWindow make_window(int seq_start, int seq_end, int
   return w;
 }
 
+// One work unit: query block mb (two 128-row tiles) of head h in batch b.
+struct Unit {
+  int b, h;
+  int q_start, q_end, k_start, k_end;  // row ranges of the sequence (packed rows if variable length)
+  int q_row0;                          // first query row of the unit
+  int nkv;                             // key/value tiles
+  int lse_base;                        // (b * H + h) * Nq
+  bool run;                            // the unit has query rows and keys
+  bool nokeys;                         // query rows but no keys (variable length only)
+  bool active[kQT];
+  RowWindow qwin[kQT];
+};
+
+// Every role decodes the same unit identically (pure function of u and params).
+template <int BC, bool VARLEN>
+__device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
+  Unit w;
+  const int mb = u % p.num_mblocks;
+  const int r = u / p.num_mblocks;
+  w.h = r % p.H;
+  w.b = r / p.H;
+  w.q_start = 0;
+  w.q_end = p.Nq;
+  w.k_start = 0;
+  w.k_end = p.Nk;
+  bool bad = false;
+  if constexpr (VARLEN) {
+    w.q_start = p.cu_q[w.b];
+    w.q_end = p.cu_q[w.b + 1];
+    w.k_start = p.cu_k[w.b];
+    w.k_end = p.cu_k[w.b + 1];
+    const int len_q = w.q_end - w.q_start, len_k = w.k_end - w.k_start;
+    bad = len_q < 0 || len_k < 0 || len_q > p.Nq || len_k > p.Nk || w.q_start < 0 || w.k_start < 0;
+  }
+  w.q_row0 = w.q_start + mb * (kBR * kQT);
+  w.nkv = bad ? 0 : (w.k_end - w.k_start + BC - 1) / BC;
+  w.lse_base = (w.b * p.H + w.h) * p.Nq;
+  const bool has_rows = !bad && w.q_row0 < w.q_end;
+  w.run = has_rows && w.nkv > 0;
+  w.nokeys = has_rows && w.nkv == 0;
+#pragma unroll
+  for (int t = 0; t < kQT; ++t) {
+    const int r0 = w.q_row0 + t * kBR;
+    w.active[t] = w.run && r0 < w.q_end;
+    w.qwin[t] = make_window<VARLEN>(w.q_start, w.q_end, r0, kBR);
+  }
+  if (bad && mb == 0 && w.h == 0) {
+    if ((threadIdx.x & 31) == 0 && threadIdx.x < 32) record_error(p.status, kErrBadSeqlens, 0);
+  }
+  return w;
+}
+
 template <int D, int BC, int STAGES, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -166,51 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int mb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-
-  // ------------------------------------------------ work unit and sequence
-  int q_start = 0, q_end = p.Nq, k_start = 0, k_end = p.Nk;
-  if constexpr (VARLEN) {
-    q_start = p.cu_q[b];
-    q_end = p.cu_q[b + 1];
-    k_start = p.cu_k[b];
-    k_end = p.cu_k[b + 1];
-    const int len_q = q_end - q_start, len_k = k_end - k_start;
-    if (len_q < 0 || len_k < 0 || len_q > p.Nq || len_k > p.Nk || q_start < 0 || k_start < 0) {
-      if (threadIdx.x == 0 && mb == 0 && h == 0) record_error(p.status, kErrBadSeqlens, 0);
-      return;
-    }
-  }
-  const int q_row0 = q_start + mb * (kBR * kQT);
-  if (q_row0 >= q_end) return;  // past the end of this sequence
-  const int nkv = (k_end - k_start + BC - 1) / BC;
-  const int lse_base = (b * p.H + h) * p.Nq;
-
-  if (nkv == 0) {
-    // No keys: o = 0 and LSE = -inf (log of an empty sum).
-    const int rows = min(kBR * kQT, q_end - q_row0);
-    const size_t rs = static_cast<size_t>(p.H) * D;
-    for (int e = threadIdx.x; e < rows * D; e += kThreads) {
-      const int r = e / D, c = e % D;
-      p.o[static_cast<size_t>(q_row0 + r) * rs + static_cast<size_t>(h) * D + c] = __float2bfloat16(0.f);
-    }
-    for (int r = threadIdx.x; r < rows; r += kThreads)
-      p.lse[lse_base + (q_row0 - q_start) + r] = -INFINITY;
-    return;
-  }
-
-  bool tile_active[kQT];
-  RowWindow qwin[kQT];
-#pragma unroll
-  for (int t = 0; t < kQT; ++t) {
-    const int r0 = q_row0 + t * kBR;
-    tile_active[t] = r0 < q_end;
-    qwin[t] = make_window<VARLEN>(q_start, q_end, r0, kBR);
-  }
 
   const uint32_t bar0 = base + L::kOffBar;
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
-  float* const s_alpha = reinterpret_cast<float*>(gbase + L::kOffAlpha);
   float* const s_invl = reinterpret_cast<float*>(gbase + L::kOffInvL);
   volatile uint32_t* const s_tmem = reinterpret_cast<volatile uint32_t*>(gbase + L::kOffTmem);
   volatile int* const s_abort = reinterpret_cast<volatile int*>(gbase + L::kOffAbort);
@@ -226,16 +255,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     *s_abort = 0;
     ptx::mbar_init(bar(L::kBarQFull), 1);
+    ptx::mbar_init(bar(L::kBarQEmpty), 1);
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(bar(L::kBarKVFull + s), 1);
       ptx::mbar_init(bar(L::kBarKVEmpty + s), 1);
     }
     for (int t = 0; t < kQT; ++t) {
       ptx::mbar_init(bar(L::kBarSFull + t), 1);
-      ptx::mbar_init(bar(L::kBarPFull + t), kBR);
-      ptx::mbar_init(bar(L::kBarAlpha + t), kBR);
-      ptx::mbar_init(bar(L::kBarOReady + t), kBR);
-      ptx::mbar_init(bar(L::kBarOFinal + t), 1);
+      ptx::mbar_init(bar(L::kBarPFull + t), kBR);   // P(j) written, O rescaled
+      ptx::mbar_init(bar(L::kBarLReady + t), kBR);  // final 1/l of every row
+      ptx::mbar_init(bar(L::kBarOFinal + t), 1);    // last P V of the unit done
+      ptx::mbar_init(bar(L::kBarOEmpty + t), kBR);  // epilogue finished reading O_t
     }
     ptx::mbar_init(bar(L::kBarTeardown), 1);
     ptx::fence_mbar_init();
@@ -253,133 +283,165 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::setmaxnreg_dec<kRegOther>();
     if (warp == 13 && lane == 0) {
       // =========================================================== TMA loads
-      uint32_t q_bytes = 0;
-#pragma unroll
-      for (int t = 0; t < kQT; ++t) q_bytes += tile_active[t] ? L::kQTileBytes : 0;
-      ptx::mbar_arrive_expect_tx(bar(L::kBarQFull), q_bytes);
-#pragma unroll
-      for (int t = 0; t < kQT; ++t) {
-        if (!tile_active[t]) continue;
-#pragma unroll
-        for (int pnl = 0; pnl < kDPanels; ++pnl) {
-          const uint32_t dst = base + L::kOffQ + t * L::kQTileBytes + pnl * L::kQPanelBytes;
-          if constexpr (VARLEN)
-            ptx::tma_load_3d(dst, &tm_q, bar(L::kBarQFull), pnl * kPanel, h, qwin[t].load_row);
-          else
-            ptx::tma_load_4d(dst, &tm_q, bar(L::kBarQFull), pnl * kPanel, h, qwin[t].load_row, b);
-        }
-      }
-      int issued = 0;  // ring positions handed to the TMA unit so far
+      uint32_t qcount = 0;  // units whose Q was loaded
+      uint32_t g = 0;       // ring slots handed to the TMA unit so far
       bool ok = true;
 #pragma unroll 1
-      for (int j = 0; j < nkv && ok; ++j) {
-        const RowWindow kw = make_window<VARLEN>(k_start, k_end, k_start + j * BC, BC);
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const Unit w = decode_unit<BC, VARLEN>(p, u);
+        if (!w.run) continue;
+        // Q of this unit, once the previous unit's S MMAs no longer read it.
+        if (!ptx::mbar_wait(bar(L::kBarQEmpty), (qcount & 1u) ^ 1u, s_abort, tmo)) {
+          record_error(p.status, kErrTimeout, kSiteLoadQ);
+          ok = false;
+          break;
+        }
+        uint32_t q_bytes = 0;
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          const int tpos = 2 * j + which;
-          const int slot = tpos % STAGES;
-          const uint32_t round = static_cast<uint32_t>(tpos / STAGES);
-          if (!ptx::mbar_wait(bar(L::kBarKVEmpty + slot), (round & 1u) ^ 1u, s_abort, tmo)) {
+        for (int t = 0; t < kQT; ++t) q_bytes += w.active[t] ? L::kQTileBytes : 0;
+        ptx::mbar_arrive_expect_tx(bar(L::kBarQFull), q_bytes);
+        ++qcount;
+#pragma unroll
+        for (int t = 0; t < kQT; ++t) {
+          if (!w.active[t]) continue;
+#pragma unroll
+          for (int pnl = 0; pnl < kDPanels; ++pnl) {
+            const uint32_t dst = base + L::kOffQ + t * L::kQTileBytes + pnl * L::kQPanelBytes;
+            if constexpr (VARLEN)
+              ptx::tma_load_3d(dst, &tm_q, bar(L::kBarQFull), pnl * kPanel, w.h, w.qwin[t].load_row);
+            else
+              ptx::tma_load_4d(dst, &tm_q, bar(L::kBarQFull), pnl * kPanel, w.h, w.qwin[t].load_row, w.b);
+          }
+        }
+#pragma unroll 1
+        for (int j = 0; j <= w.nkv; ++j) {
+          const uint32_t slot = g % STAGES;
+          if (!ptx::mbar_wait(bar(L::kBarKVEmpty + slot), ((g / STAGES) & 1u) ^ 1u, s_abort, tmo)) {
             record_error(p.status, kErrTimeout, kSiteLoadKV);
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(bar(L::kBarKVFull + slot), L::kKVTileBytes);
-          issued = tpos + 1;
-          const void* tm = which == 0 ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
+          const uint32_t bytes = (j < w.nkv ? L::kKVTileBytes : 0) + (j >= 1 ? L::kKVTileBytes : 0);
+          ptx::mbar_arrive_expect_tx(bar(L::kBarKVFull + slot), bytes);
+          ++g;
+          const uint32_t sbase = base + L::kOffKV + slot * L::kSlotBytes;
+          if (j < w.nkv) {
+            const RowWindow kw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + j * BC, BC);
 #pragma unroll
-          for (int pnl = 0; pnl < kDPanels; ++pnl) {
-            const uint32_t dst = base + L::kOffKV + slot * L::kKVTileBytes + pnl * L::kKVPanelBytes;
-            if constexpr (VARLEN)
-              ptx::tma_load_3d(dst, tm, bar(L::kBarKVFull + slot), pnl * kPanel, h, kw.load_row);
-            else
-              ptx::tma_load_4d(dst, tm, bar(L::kBarKVFull + slot), pnl * kPanel, h, kw.load_row, b);
+            for (int pnl = 0; pnl < kDPanels; ++pnl) {
+              const uint32_t dst = sbase + pnl * L::kKVPanelBytes;
+              if constexpr (VARLEN)
+                ptx::tma_load_3d(dst, &tm_k, bar(L::kBarKVFull + slot), pnl * kPanel, w.h, kw.load_row);
+              else
+                ptx::tma_load_4d(dst, &tm_k, bar(L::kBarKVFull + slot), pnl * kPanel, w.h, kw.load_row, w.b);
+            }
+          }
+          if (j >= 1) {
+            const RowWindow vw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + (j - 1) * BC, BC);
+#pragma unroll
+            for (int pnl = 0; pnl < kDPanels; ++pnl) {
+              const uint32_t dst = sbase + L::kKVTileBytes + pnl * L::kKVPanelBytes;
+              if constexpr (VARLEN)
+                ptx::tma_load_3d(dst, &tm_v, bar(L::kBarKVFull + slot), pnl * kPanel, w.h, vw.load_row);
+              else
+                ptx::tma_load_4d(dst, &tm_v, bar(L::kBarKVFull + slot), pnl * kPanel, w.h, vw.load_row, w.b);
+            }
           }
         }
       }
       // Teardown: never leave a TMA write to shared memory in flight.  Slot s
-      // last received ring position s + STAGES * (rounds - 1).
-      ptx::mbar_wait_drain(bar(L::kBarQFull), 0, tmo);
-      for (int s = 0; s < STAGES; ++s) {
-        if (issued > s) {
-          const int rounds = (issued - 1 - s) / STAGES + 1;
-          ptx::mbar_wait_drain(bar(L::kBarKVFull + s), static_cast<uint32_t>(rounds - 1) & 1u, tmo);
+      // last received ring index s + STAGES * (rounds - 1).
+      if (qcount > 0) ptx::mbar_wait_drain(bar(L::kBarQFull), (qcount - 1) & 1u, tmo);
+      for (uint32_t s = 0; s < STAGES; ++s) {
+        if (g > s) {
+          const uint32_t rounds = (g - 1 - s) / STAGES + 1;
+          ptx::mbar_wait_drain(bar(L::kBarKVFull + s), (rounds - 1) & 1u, tmo);
         }
       }
     } else if (warp == 12 && lane == 0) {
       // ========================================================== MMA issue
       constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(kBR, BC, 0, 0);
       constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(kBR, D, 0, 1);
-      bool ok = ptx::mbar_wait(bar(L::kBarQFull), 0, s_abort, tmo);
-      if (!ok) record_error(p.status, kErrTimeout, kSiteMmaQ);
-      ptx::tc_fence_after();
+      uint32_t qcount = 0, g = 0;
+      uint32_t pc[kQT] = {0, 0};  // P-full completions consumed, per tile
+      uint32_t uc[kQT] = {0, 0};  // units with the tile active, per tile
+      bool ok = true;
 #pragma unroll 1
-      for (int j = 0; j <= nkv && ok; ++j) {
-        const int posK = 2 * j, posV = 2 * (j - 1) + 1;
-        const int slotK = posK % STAGES, slotV = (posV + STAGES) % STAGES;
-        if (j < nkv) {
-          if (!ptx::mbar_wait(bar(L::kBarKVFull + slotK), static_cast<uint32_t>(posK / STAGES) & 1u, s_abort, tmo)) {
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const Unit w = decode_unit<BC, VARLEN>(p, u);
+        if (!w.run) continue;
+        if (!ptx::mbar_wait(bar(L::kBarQFull), qcount & 1u, s_abort, tmo)) {
+          record_error(p.status, kErrTimeout, kSiteMmaQ);
+          ok = false;
+          break;
+        }
+        ++qcount;
+        ptx::tc_fence_after();
+#pragma unroll 1
+        for (int j = 0; j <= w.nkv && ok; ++j) {
+          const uint32_t slot = g % STAGES;
+          if (!ptx::mbar_wait(bar(L::kBarKVFull + slot), (g / STAGES) & 1u, s_abort, tmo)) {
             record_error(p.status, kErrTimeout, kSiteMmaK);
             ok = false;
             break;
           }
-        }
-        if (j >= 1) {
-          if (!ptx::mbar_wait(bar(L::kBarKVFull + slotV), static_cast<uint32_t>(posV / STAGES) & 1u, s_abort, tmo)) {
-            record_error(p.status, kErrTimeout, kSiteMmaV);
-            ok = false;
-            break;
-          }
-        }
-        ptx::tc_fence_after();
+          ptx::tc_fence_after();
+          const uint32_t k_base = base + L::kOffKV + slot * L::kSlotBytes;
+          const uint32_t v_base = k_base + L::kKVTileBytes;
 #pragma unroll
-        for (int t = 0; t < kQT; ++t) {
-          if (!tile_active[t]) continue;
-          const uint32_t tS = tmem + static_cast<uint32_t>(t * BC);
-          const uint32_t tP = tS + BC / 2;
-          const uint32_t tO = tmem + static_cast<uint32_t>(2 * BC + t * D);
-          if (j >= 1) {
-            // O_t += P_t(j-1) V(j-1)
-            if (!ptx::mbar_wait(bar(L::kBarPFull + t), static_cast<uint32_t>(j - 1) & 1u, s_abort, tmo)) {
-              record_error(p.status, kErrTimeout, kSiteMmaP);
-              ok = false;
-              break;
-            }
-            if (j >= 2 && !ptx::mbar_wait(bar(L::kBarOReady + t), static_cast<uint32_t>(j - 2) & 1u, s_abort, tmo)) {
-              record_error(p.status, kErrTimeout, kSiteMmaO);
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
-            const uint32_t v_base = base + L::kOffKV + slotV * L::kKVTileBytes;
+          for (int t = 0; t < kQT; ++t) {
+            if (!w.active[t]) continue;
+            const uint32_t tS = tmem + static_cast<uint32_t>(t * BC);
+            const uint32_t tP = tS + BC / 2;
+            const uint32_t tO = tmem + static_cast<uint32_t>(2 * BC + t * D);
+            if (j >= 1) {
+              // O_t += P_t(j-1) V(j-1), once P is written and O rescaled.
+              if (!ptx::mbar_wait(bar(L::kBarPFull + t), pc[t] & 1u, s_abort, tmo)) {
+                record_error(p.status, kErrTimeout, kSiteMmaP);
+                ok = false;
+                break;
+              }
+              ++pc[t];
+              // The first P V of a unit overwrites O_t: the epilogue of the
+              // previous unit must have finished reading it.
+              if (j == 1 && !ptx::mbar_wait(bar(L::kBarOEmpty + t), (uc[t] & 1u) ^ 1u, s_abort, tmo)) {
+                record_error(p.status, kErrTimeout, kSiteMmaOEmpty);
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < BC / 16; ++kk) {
-              // V is MN-major: 16 keys = two 8-row swizzle atoms = 2048 bytes;
-              // the two 64-column halves of d sit one panel (BC * 128 bytes) apart.
-              const uint64_t bdesc = ptx::sw128_desc(v_base + kk * 2048, L::kKVPanelBytes, 1024);
-              ptx::mma_ts(tO, tP + kk * 8, bdesc, idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < BC / 16; ++kk) {
+                // V is MN-major: 16 keys = two 8-row swizzle atoms = 2048 bytes;
+                // the two 64-column halves of d sit one panel (BC * 128 bytes) apart.
+                const uint64_t bdesc = ptx::sw128_desc(v_base + kk * 2048, L::kKVPanelBytes, 1024);
+                ptx::mma_ts(tO, tP + kk * 8, bdesc, idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+              }
+              if (j == w.nkv) ptx::mma_commit(bar(L::kBarOFinal + t));
             }
-            if (j == nkv) ptx::mma_commit(bar(L::kBarOFinal + t));
-          }
-          if (j < nkv) {
-            // S_t = Q_t K(j)^T
-            const uint32_t q_base = base + L::kOffQ + t * L::kQTileBytes;
-            const uint32_t k_base = base + L::kOffKV + slotK * L::kKVTileBytes;
+            if (j < w.nkv) {
+              // S_t = Q_t K(j)^T
+              const uint32_t q_base = base + L::kOffQ + t * L::kQTileBytes;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              // K-major, 128-byte swizzle: 16 columns = 32 bytes inside a panel.
-              const uint32_t off_q = (kk / 4) * L::kQPanelBytes + (kk % 4) * 32;
-              const uint32_t off_k = (kk / 4) * L::kKVPanelBytes + (kk % 4) * 32;
-              const uint64_t adesc = ptx::sw128_desc(q_base + off_q, 16, 1024);
-              const uint64_t bdesc = ptx::sw128_desc(k_base + off_k, 16, 1024);
-              ptx::mma_ss(tS, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < D / 16; ++kk) {
+                // K-major, 128-byte swizzle: 16 columns = 32 bytes inside a panel.
+                const uint32_t off_q = (kk / 4) * L::kQPanelBytes + (kk % 4) * 32;
+                const uint32_t off_k = (kk / 4) * L::kKVPanelBytes + (kk % 4) * 32;
+                const uint64_t adesc = ptx::sw128_desc(q_base + off_q, 16, 1024);
+                const uint64_t bdesc = ptx::sw128_desc(k_base + off_k, 16, 1024);
+                ptx::mma_ss(tS, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+              }
+              ptx::mma_commit(bar(L::kBarSFull + t));
             }
-            ptx::mma_commit(bar(L::kBarSFull + t));
           }
+          if (!ok) break;
+          // Q of this unit is free once its last S MMAs complete.
+          if (j == w.nkv - 1) ptx::mma_commit(bar(L::kBarQEmpty));
+          ptx::mma_commit(bar(L::kBarKVEmpty + slot));  // K(j) and V(j-1) no longer needed
+          ++g;
         }
-        if (!ok) break;
-        if (j < nkv) ptx::mma_commit(bar(L::kBarKVEmpty + slotK));
-        if (j >= 1) ptx::mma_commit(bar(L::kBarKVEmpty + slotV));
+#pragma unroll
+        for (int t = 0; t < kQT; ++t) uc[t] += w.active[t] ? 1u : 0u;
       }
       // Teardown: all MMAs must be complete before TMEM is released.
       ptx::mma_commit(bar(L::kBarTeardown));
@@ -390,189 +452,224 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ softmax
     const int t = warp >> 2;
     const int row = ((warp & 3) << 5) + lane;
-    const RowWindow qw = t == 0 ? qwin[0] : qwin[1];  // no dynamic indexing of local arrays
-    const bool active = t == 0 ? tile_active[0] : tile_active[1];
-    if (active) {
-      const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
-      const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(t * BC);
-      const uint32_t tP = tS + BC / 2;
-      const float c2 = p.scale_log2;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
+    const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(t * BC);
+    const uint32_t tP = tS + BC / 2;
+    const float c2 = p.scale_log2;
+    uint32_t sc = 0;  // S-full completions consumed
+    bool ok = true;
+#pragma unroll 1
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      const Unit w = decode_unit<BC, VARLEN>(p, u);
+      const bool active = t == 0 ? w.active[0] : w.active[1];
+      if (!active) continue;
+      const RowWindow qw = t == 0 ? w.qwin[0] : w.qwin[1];
       float m_ref = -INFINITY;
       float l = 0.f;
-      bool ok = true;
 #pragma unroll 1
-      for (int j = 0; j < nkv; ++j) {
-        if (!ptx::mbar_wait_warp(bar(L::kBarSFull + t), static_cast<uint32_t>(j) & 1u, s_abort, tmo)) {
+      for (int j = 0; j < w.nkv; ++j) {
+        if (!ptx::mbar_wait_warp(bar(L::kBarSFull + t), sc & 1u, s_abort, tmo)) {
           record_error(p.status, kErrTimeout, kSiteSoftS);
           ok = false;
           break;
         }
+        ++sc;
         ptx::tc_fence_after();
         uint32_t sr[BC];
 #pragma unroll
-        for (int c = 0; c < BC / 32; ++c)
-          ptx::tmem_ld32(tS + c * 32, &sr[c * 32]);
+        for (int c = 0; c < BC / 32; ++c) ptx::tmem_ld32(tS + c * 32, &sr[c * 32]);
         ptx::tmem_wait_ld();
         float s[BC];
 #pragma unroll
         for (int c = 0; c < BC; ++c) s[c] = __uint_as_float(sr[c]);
-        const RowWindow kw = make_window<VARLEN>(k_start, k_end, k_start + j * BC, BC);
-        if (kw.lo != 0 || kw.hi != BC) {
+        if (j == w.nkv - 1 || VARLEN) {
+          // Keys outside [lo, hi) of this tile: past the end, or (variable
+          // length) before the sequence start / already seen by the previous tile.
+          const RowWindow kw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + j * BC, BC);
+          if (kw.lo != 0 || kw.hi != BC) {
 #pragma unroll
-          for (int c = 0; c < BC; ++c)
-            if (c < kw.lo || c >= kw.hi) s[c] = -INFINITY;
+            for (int c = 0; c < BC; ++c)
+              if (c < kw.lo || c >= kw.hi) s[c] = -INFINITY;
+          }
         }
-        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+        // Row max: four independent chains of three-input maxima.
+        float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-        for (int c = 4; c < BC; c += 4) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
-          mx2 = fmaxf(mx2, s[c + 2]);
-          mx3 = fmaxf(mx3, s[c + 3]);
+        for (int c = 4; c < BC; c += 8) {
+          mx[0] = ptx::fmax3(mx[0], s[c], s[c + 1]);
+          mx[1] = ptx::fmax3(mx[1], s[c + 2], s[c + 3]);
+          if (c + 4 < BC) {
+            mx[2] = ptx::fmax3(mx[2], s[c + 4], s[c + 5]);
+            mx[3] = ptx::fmax3(mx[3], s[c + 6], s[c + 7]);
+          }
         }
-        const float bm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+        const float bm = fmaxf(ptx::fmax3(mx[0], mx[1], mx[2]), mx[3]);
         // Move the reference max only when the block max exceeds it by more
         // than the threshold (log2 units): the merge identity of §11.2 holds
         // for any common reference value, so results stay exact.
         float m_new = m_ref;
         if (bm > m_ref && (m_ref == -INFINITY || (bm - m_ref) * c2 > p.rescale_threshold)) m_new = bm;
         const float alpha = (m_new == m_ref) ? 1.f : ptx::ex2((m_ref - m_new) * c2);
-        if (j >= 1) {
-          s_alpha[t * kBR + row] = alpha;
-          ptx::mbar_arrive(bar(L::kBarAlpha + t));
-        }
         m_ref = m_new;
         const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref * c2;
-        float sum0 = 0.f, sum1 = 0.f;
-        uint32_t pk[BC / 2];
+        // p = 2^(s*c2 - m*c2): one packed FFMA per two scores, then ex2 each;
+        // row sums in four packed accumulators; P stored in 16-column chunks.
+        const uint64_t c2x2 = ptx::f2_pack(c2, c2);
+        const uint64_t negx2 = ptx::f2_pack(neg, neg);
+        uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int c = 0; c < BC; c += 2) {
-          const float e0 = ptx::ex2(fmaf(s[c], c2, neg));
-          const float e1 = ptx::ex2(fmaf(s[c + 1], c2, neg));
-          sum0 += e0;
-          sum1 += e1;
-          pk[c / 2] = ptx::pack_bf16x2(e0, e1);
-        }
-        l = l * alpha + (sum0 + sum1);
+        for (int c0 = 0; c0 < BC; c0 += 32) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < BC / 2; c += 16) ptx::tmem_st16(tP + c, &pk[c]);
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(L::kBarPFull + t));
-      }
-      if (ok) {
-        // Final message for the epilogue: 1 / l, and the row's log-sum-exp.
-        const bool has = l > 0.f;
-        s_invl[t * kBR + row] = has ? 1.f / l : 0.f;
-        const int r_in_seq = qw.load_row - q_start + row;
-        if (row >= qw.lo && row < qw.hi) {
-          const float lse = has ? (m_ref * p.scale + log2f(l) * 0.69314718055994530942f) : -INFINITY;
-          p.lse[lse_base + r_in_seq] = lse;
+          for (int c = c0; c < c0 + 32; c += 2) {
+            float x0, x1;
+            ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[c], s[c + 1]), c2x2, negx2), x0, x1);
+            const float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1);
+            const uint64_t e01 = ptx::f2_pack(e0, e1);
+            acc[(c >> 1) & 3] = ptx::f2_add(acc[(c >> 1) & 3], e01);
+            pk[(c - c0) / 2] = ptx::pack_bf16x2(e0, e1);
+          }
+          ptx::tmem_st16(tP + c0 / 2, pk);
         }
-        ptx::mbar_arrive(bar(L::kBarAlpha + t));
-      }
-    }
-  } else {
-    ptx::setmaxnreg_dec<kRegCorrection>();
-    // ============================================================= correction
-    const int wq = warp & 3;
-    const int row = (wq << 5) + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(wq << 5) << 16;
-    bool ok = true;
-#pragma unroll 1
-    for (int j = 1; j < nkv && ok; ++j) {
-#pragma unroll
-      for (int t = 0; t < kQT; ++t) {
-        if (!tile_active[t]) continue;
-        if (!ptx::mbar_wait_warp(bar(L::kBarAlpha + t), static_cast<uint32_t>(j - 1) & 1u, s_abort, tmo)) {
-          record_error(p.status, kErrTimeout, kSiteCorrAlpha);
-          ok = false;
-          break;
-        }
-        const float a = s_alpha[t * kBR + row];
-        if (__any_sync(0xffffffffu, a != 1.f)) {
-          ptx::tc_fence_after();
+        float a0, a1, a2, a3, a4, a5, a6, a7;
+        ptx::f2_unpack(acc[0], a0, a1);
+        ptx::f2_unpack(acc[1], a2, a3);
+        ptx::f2_unpack(acc[2], a4, a5);
+        ptx::f2_unpack(acc[3], a6, a7);
+        l = l * alpha + (((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)));
+        if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // Correction of the unnormalised output: O_t rows of this warp hold
+          // the sum over steps < j referenced to the old maximum.  Done after
+          // the exponentials (the scores are dead by then); it only has to
+          // land before P(j) is published.
           const uint32_t tO = tmem + lane_off + static_cast<uint32_t>(2 * BC + t * D);
+          const uint64_t ax2 = ptx::f2_pack(alpha, alpha);
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t r[32];
             ptx::tmem_ld32(tO + c * 32, r);
             ptx::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * a);
+            for (int e = 0; e < 32; e += 2) {
+              float x0, x1;
+              ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), ax2), x0, x1);
+              r[e] = __float_as_uint(x0);
+              r[e + 1] = __float_as_uint(x1);
+            }
             ptx::tmem_st32(tO + c * 32, r);
           }
-          ptx::tmem_wait_st();
         }
+        ptx::tmem_wait_st();  // P stores (and any O rescale) have landed
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(L::kBarOReady + t));
+        ptx::mbar_arrive(bar(L::kBarPFull + t));
       }
+      if (!ok) break;
+      // Final message for the epilogue: 1 / l, and the row's log-sum-exp.
+      const bool has = l > 0.f;
+      s_invl[t * kBR + row] = has ? 1.f / l : 0.f;
+      if (row >= qw.lo && row < qw.hi) {
+        const float lse = has ? (m_ref * p.scale + log2f(l) * 0.69314718055994530942f) : -INFINITY;
+        p.lse[w.lse_base + (qw.load_row - w.q_start + row)] = lse;
+      }
+      ptx::mbar_arrive(bar(L::kBarLReady + t));
     }
-    // ============================================================== epilogue
-    bool stored = false;
-#pragma unroll
-    for (int t = 0; t < kQT; ++t) {
-      if (!ok || !tile_active[t]) continue;
-      if (!ptx::mbar_wait_warp(bar(L::kBarAlpha + t), static_cast<uint32_t>(nkv - 1) & 1u, s_abort, tmo) ||
-          !ptx::mbar_wait_warp(bar(L::kBarOFinal + t), 0, s_abort, tmo)) {
-        record_error(p.status, kErrTimeout, kSiteCorrFinal);
-        ok = false;
-        break;
+  } else {
+    ptx::setmaxnreg_dec<kRegCorrection>();
+    // ================================================= correction + epilogue
+    const int wq = warp & 3;
+    const int row = (wq << 5) + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq << 5) << 16;
+    // This warp's 32 output rows are staged here for the TMA store.
+    const uint32_t stage = base + L::kOffStage + wq * L::kStageWarpBytes;
+    uint32_t uc[kQT] = {0, 0};
+    bool pending = false;  // a TMA store from the staging area may still be reading it
+    bool ok = true;
+#pragma unroll 1
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      const Unit w = decode_unit<BC, VARLEN>(p, u);
+      if (w.nokeys) {
+        // No keys: o = 0 and LSE = -inf (log of an empty sum).
+        const int rows = min(kBR * kQT, w.q_end - w.q_row0);
+        const size_t rs = static_cast<size_t>(p.H) * D;
+        for (int e = threadIdx.x - 256; e < rows * D; e += 128) {
+          const int r = e / D, c = e % D;
+          p.o[static_cast<size_t>(w.q_row0 + r) * rs + static_cast<size_t>(w.h) * D + c] = __float2bfloat16(0.f);
+        }
+        for (int r = threadIdx.x - 256; r < rows; r += 128)
+          p.lse[w.lse_base + (w.q_row0 - w.q_start) + r] = -INFINITY;
+        continue;
       }
-      ptx::tc_fence_after();
-      const float inv_l = s_invl[t * kBR + row];
-      const uint32_t tO = tmem + lane_off + static_cast<uint32_t>(2 * BC + t * D);
-      const RowWindow& qw = qwin[t];
-      const bool warp_full = (wq << 5) >= qw.lo;  // every row of this warp is valid
-      const bool use_tma = !VARLEN || warp_full;
-      const bool row_ok = row >= qw.lo && row < qw.hi;
-      // The query tile's shared memory is free once its last S MMA is done,
-      // which the O-final commit guarantees; reuse it as the staging buffer.
-      const uint32_t stage = base + L::kOffQ + t * L::kQTileBytes;
-      // Row pointer for the direct-store path (only formed for valid rows).
-      __nv_bfloat16* const grow =
-          row_ok ? p.o + (static_cast<size_t>(qw.load_row + row) * p.H + h) * D : p.o;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        ptx::tmem_ld32(tO + c * 32, r);
-        ptx::tmem_wait_ld();
-        uint32_t w[16];
+      for (int t = 0; t < kQT; ++t) {
+        if (!w.active[t]) continue;
+        if (!ptx::mbar_wait_warp(bar(L::kBarLReady + t), uc[t] & 1u, s_abort, tmo) ||
+            !ptx::mbar_wait_warp(bar(L::kBarOFinal + t), uc[t] & 1u, s_abort, tmo)) {
+          record_error(p.status, kErrTimeout, kSiteCorrFinal);
+          ok = false;
+          break;
+        }
+        ++uc[t];
+        ptx::tc_fence_after();
+        const float inv_l = s_invl[t * kBR + row];
+        const uint32_t tO = tmem + lane_off + static_cast<uint32_t>(2 * BC + t * D);
+        const RowWindow qw = w.qwin[t];
+        const bool warp_full = (wq << 5) >= qw.lo;  // every row of this warp is valid
+        const bool use_tma = !VARLEN || warp_full;
+        const bool row_ok = row >= qw.lo && row < qw.hi;
+        // Row pointer for the direct-store path (only formed for valid rows).
+        __nv_bfloat16* const grow =
+            row_ok ? p.o + (static_cast<size_t>(qw.load_row + row) * p.H + w.h) * D : p.o;
+        if (use_tma && pending) {
+          // The previous store from this warp's staging area must have read it.
+          if (lane == 0) ptx::bulk_wait_group_read_0();
+          __syncwarp();
+          pending = false;
+        }
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          w[e] = ptx::pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          ptx::tmem_ld32(tO + c * 32, r);
+          ptx::tmem_wait_ld();
+          uint32_t wv[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            wv[e] = ptx::pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
+          if (use_tma) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              // 16-byte chunk (4c + q4) of the row: panel / chunk in panel, swizzled.
+              const int c16 = 4 * c + q4;
+              const int pnl = c16 / 8, chunk = c16 % 8;
+              const uint32_t addr = stage + pnl * 4096 + lane * 128 + ((chunk ^ (lane & 7)) << 4);
+              ptx::st_shared_v4(addr, wv[4 * q4], wv[4 * q4 + 1], wv[4 * q4 + 2], wv[4 * q4 + 3]);
+            }
+          } else if (row_ok) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              ptx::st_global_v4(grow + c * 32 + q4 * 8, wv[4 * q4], wv[4 * q4 + 1], wv[4 * q4 + 2], wv[4 * q4 + 3]);
+          }
+        }
+        // O_t has been read: the next unit's first P V may overwrite it.
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::kBarOEmpty + t));
         if (use_tma) {
-          const int pnl = (c * 32) / kPanel;
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int chunk = ((c * 32) % kPanel) / 8 + q4;
-            const uint32_t addr = stage + pnl * L::kQPanelBytes + row * 128 + ((chunk ^ (row & 7)) << 4);
-            ptx::st_shared_v4(addr, w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+            for (int pnl = 0; pnl < kDPanels; ++pnl) {
+              if constexpr (VARLEN)
+                ptx::tma_store_3d(&tm_o, stage + pnl * 4096, pnl * kPanel, w.h, qw.load_row + (wq << 5));
+              else
+                ptx::tma_store_4d(&tm_o, stage + pnl * 4096, pnl * kPanel, w.h, qw.load_row + (wq << 5), w.b);
+            }
+            ptx::bulk_commit_group();
           }
-        } else if (row_ok) {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            ptx::st_global_v4(grow + c * 32 + q4 * 8, w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
-        }
-      }
-      if (use_tma) {
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-#pragma unroll
-          for (int pnl = 0; pnl < kDPanels; ++pnl) {
-            const uint32_t src = stage + pnl * L::kQPanelBytes + (wq << 5) * 128;
-            if constexpr (VARLEN)
-              ptx::tma_store_3d(&tm_o, src, pnl * kPanel, h, qw.load_row + (wq << 5));
-            else
-              ptx::tma_store_4d(&tm_o, src, pnl * kPanel, h, qw.load_row + (wq << 5), b);
-          }
-          ptx::bulk_commit_group();
-          stored = true;
+          pending = true;
         }
       }
     }
-    if (lane == 0 && stored) ptx::bulk_wait_group_read_0();
+    if (lane == 0 && pending) ptx::bulk_wait_group_read_0();
   }
 
   // ---------------------------------------------------------------- teardown

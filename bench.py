@@ -1,0 +1,418 @@
+"""Benchmark of the GB300 FlashAttention-2 forward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload page|tiny|slice|varlen|sweep_d128_n8192|...]
+
+One step is one forward pass (one kernel launch) over the whole batch of the
+workload: by default the page workload B16 N4096 H16 d128, bf16 inputs in
+[batch, seq, heads, d_head] layout drawn N(0,1) from a fixed seed.  Inputs
+(805 MB) and the output (268 MB) are larger than L2, so no flush is needed
+between steps.
+
+value      TFLOP/s = 4*B*H*N^2*d / (device time per step), inputs resident in HBM,
+           summed over ranks (each rank runs its own replica of the workload;
+           the forward has no exchange step, so scaling is weak).
+e2e        the same metric through the public call with host buffers: each step
+           copies q, k, v from pinned host memory, runs the forward and copies
+           O and LSE back, all inside the timed region.
+roofline   the kernel's achieved TFLOP/s (algorithmic FLOPs / launch time,
+           CUDA events on the launch stream) against the measured bf16 peak.
+cpu_baseline  the fp64 CPU oracle (test infrastructure) timed on a bounded
+           sample of the same workload on this host's cores (rank 0, N=1).
+
+--impl reference times that oracle as the reference arm (the pages ship no
+implementation; the oracle is the reference), printing the same JSON line.
+Rank 0 prints one JSON line on stdout.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s (bf16, B16 N4096 H16 d128) and % of GB300 bf16 peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = ("attention_forward_fa2_gb300/csrc/fa_fwd_kernel.cuh",
+                  "attention_forward_fa2_gb300/csrc/ptx.cuh")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(workload: str):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
+    the current kernel source for this workload."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = t.get(workload)
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return entry.get("bytes_per_launch")
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu):
+        self.gpu = gpu  # nvidia-smi -i accepts an index or a UUID
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        loaded = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# -------------------------------------------------------------- distributed
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if n_gpus > 1 and world != n_gpus:
+        raise SystemExit("--gpus %d needs torchrun with %d processes (WORLD_SIZE=%d)" % (n_gpus, n_gpus, world))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, local, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------- oracle timing
+class OracleSample:
+    """A bounded sample of workload `w` for the fp64 oracle: one batch,
+    min(threads, H) heads, the full key length, and as many query rows as fit
+    `budget_s` seconds on `threads` host threads (calibrated once)."""
+
+    def __init__(self, w, budget_s: float, threads: int):
+        import oracle
+        from attention_forward_fa2_gb300 import inputs as I
+        self.oracle = oracle
+        oracle.set_num_threads(threads)
+        self.threads = threads
+        H = max(1, min(threads, w.H))
+        Nk = max(w.lengths) if w.varlen else w.Nk
+        d = w.d
+        q, k, v = I.make_dense(1, 8, Nk, H, d, seed=w.seed + 1000)
+        self.kb, self.vb = I.bf16_bits(k), I.bf16_bits(v)
+        t0 = time.perf_counter()
+        oracle.attn_dense(I.bf16_bits(q), self.kb, self.vb)
+        t_cal = max(time.perf_counter() - t0, 1e-4)
+        nq_max = max(w.lengths) if w.varlen else w.Nq
+        nq = int(max(1, min(nq_max, 8 * budget_s / t_cal)))
+        q, _, _ = I.make_dense(1, nq, 1, H, d, seed=w.seed + 2000)
+        self.qb = I.bf16_bits(q)
+        self.flops = 4.0 * H * nq * Nk * d
+        self.desc = ("fp64 oracle (S and P materialised) on 1 batch x %d heads x %d queries x %d keys, "
+                     "d=%d, a bounded sample of the %s workload; %d threads" % (H, nq, Nk, d, w.name, threads))
+
+    def run(self) -> float:
+        t0 = time.perf_counter()
+        self.oracle.attn_dense(self.qb, self.kb, self.vb)
+        return time.perf_counter() - t0
+
+
+# --------------------------------------------------------------------- arms
+def run_reference(args, w):
+    rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return 0
+    cores = host_cores()
+    budget = max(0.5, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
+    sample = OracleSample(w, budget, cores)
+    for _ in range(args.warmup):
+        sample.run()
+    times = [sample.run() for _ in range(args.steps)]
+    total = sum(times)
+    value = sample.flops * len(times) / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), generated on the host)", "config": workload_config(w, None),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample.desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, kernel_cfg):
+    cfg = {"workload": "%s: %s" % (w.name, w.note or ""), "B": w.B, "H": w.H, "d": w.d,
+           "layout": "[batch, seq, heads, d_head] bf16", "causal": False,
+           "l2": "inputs and output larger than L2 (no flush needed)",
+           "parallelism": "replicas (one full workload per GPU, no collective)"}
+    if w.varlen:
+        cfg["sequences"] = len(w.lengths)
+        cfg["total_tokens"] = sum(w.lengths)
+        cfg["max_seqlen"] = max(w.lengths)
+    else:
+        cfg["Nq"] = w.Nq
+        cfg["Nk"] = w.Nk
+    if kernel_cfg:
+        cfg["kernel_config"] = kernel_cfg
+    return cfg
+
+
+def run_ours(args, w):
+    import torch
+    import attention_forward_fa2_gb300 as fa
+    from attention_forward_fa2_gb300 import build as fabuild
+    from attention_forward_fa2_gb300 import inputs as I
+
+    rank, local, world = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    fabuild.build()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+
+    q, k, v, cu_q, cu_k = I.make(w)
+    maxlen = max(w.lengths) if w.varlen else None
+    dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
+    dcu = cu_q.to(dev) if w.varlen else None
+    o = torch.empty_like(dq)
+    Nq = maxlen if w.varlen else w.Nq
+    lse = torch.empty((w.B, w.H, Nq), dtype=torch.float32, device=dev)
+
+    def step():
+        if w.varlen:
+            fa.forward(dq, dk, dv, cu_seqlens=dcu, max_seqlen=maxlen, out=o, lse=lse)
+        else:
+            fa.forward_qk(dq, dk, dv, out=o, lse=lse)
+
+    if args.autotune:
+        if w.varlen:
+            fa.autotune(dq, dk, dv, cu_seqlens=dcu, max_seqlen=maxlen)
+        else:
+            fa.autotune(dq, dk, dv)
+    kernel_cfg = fa.get_config(w.d, maxlen if w.varlen else w.Nk, w.varlen)
+
+    # ---------------------------------------------------------- device timing
+    for _ in range(args.warmup):
+        step()
+    rc, info = fa.check_status()
+    if rc != fa.FA_OK:
+        raise SystemExit("device error during warm-up: %s %s" % (fa.strerror(rc), info))
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    sampler = ClockSampler("GPU-%s" % uuid if uuid is not None else str(local))
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    rc, info = fa.check_status()
+    if rc != fa.FA_OK:
+        raise SystemExit("device error in the timed region: %s %s" % (fa.strerror(rc), info))
+    ms_max = max_over_ranks(ms, world)
+    flops = w.flops()
+    value = world * flops / (ms_max * 1e-3) / 1e12
+    kernel_tflops = flops / (ms * 1e-3) / 1e12  # one launch per step, this rank
+
+    # -------------------------------------------------------- end to end
+    e2e_steps = max(3, min(args.steps, 20))
+    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    hcu = cu_q.pin_memory() if w.varlen else None
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        if w.varlen:
+            dcu.copy_(hcu, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in (q, k, v)) + (cu_q.numel() * 4 if w.varlen else 0)
+    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+    rc, info = fa.check_status()
+    if rc != fa.FA_OK:
+        raise SystemExit("device error in the e2e region: %s %s" % (fa.strerror(rc), info))
+
+    if rank != 0:
+        return 0
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    traffic = load_traffic(w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), generated on the host)",
+        "config": workload_config(w, kernel_cfg),
+        "pct_of_peak": 100.0 * kernel_tflops / peak,
+        "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": UNIT,
+                     "frac": kernel_tflops / peak, "traffic": traffic,
+                     "peak_source": "%s bf16 dense burst (MEASURED_PEAKS.json)" % src
+                     if src == "measured" else "fallback 1.9 PFLOP/s bf16",
+                     "kernel": "fa_fwd_kernel<%d,128,*>" % w.d,
+                     "algorithmic_flops_per_launch": flops},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        cores = host_cores()
+        sample = OracleSample(w, args.cpu_seconds, cores)
+        dt = sample.run()
+        line["cpu_baseline"] = {"value": sample.flops / dt / 1e12, "unit": UNIT, "cores": cores,
+                                "kind": "oracle", "sample": sample.desc, "seconds": dt}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    from attention_forward_fa2_gb300 import inputs as I
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="page", choices=sorted(I.WORKLOADS))
+    ap.add_argument("--autotune", action="store_true", help="tune the kernel config first")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    w = I.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -109,9 +109,10 @@ int fa_set_timeout_ns(unsigned long long ns);
 /*
  * Kernel configuration ("Flash Attention 2 Chapter6", Kernel 7: the
  * configuration space is searched per shape instead of fixed).  A config is
- * a text spec "stages=<2|3|4>,threshold=<float>": the depth of the
- * shared-memory key/value ring and the O-rescale threshold in log2 units
- * (0 rescales whenever a row maximum grows).
+ * a text spec "stages=<2|3|4>,threshold=<float>": the number of slots of the
+ * shared-memory key/value ring (each slot holds one K tile and one V tile;
+ * d = 128 always uses 2, the most that fit) and the O-rescale threshold in
+ * log2 units (0 rescales whenever a row maximum grows).
  *
  * fa_set_config  -- force `spec` for every later call (NULL or "" clears it).
  * fa_get_config  -- writes the spec that a call with (d, N, varlen) would use

@@ -45,7 +45,8 @@ def test_version_and_strerror(L):
 def test_config_spec_roundtrip(L):
     try:
         fa.set_config("stages=3,threshold=0")
-        assert fa.get_config(128, 4096) == "stages=3,threshold=0"
+        assert fa.get_config(64, 4096) == "stages=3,threshold=0"
+        assert fa.get_config(128, 4096) == "stages=2,threshold=0"  # d=128 fits two slots
         fa.set_config("threshold=8")
         assert fa.get_config(64, 512) == "stages=4,threshold=8"
         for bad in ("stages=5", "stages=1", "threshold=-1", "foo=1", "stages", "threshold=nan"):
@@ -53,7 +54,8 @@ def test_config_spec_roundtrip(L):
                 fa.set_config(bad)
     finally:
         fa.set_config(None)
-    assert fa.get_config(128, 4096) == "stages=4,threshold=8"
+    assert fa.get_config(128, 4096) == "stages=2,threshold=8"
+    assert fa.get_config(64, 4096) == "stages=3,threshold=8"
 
 
 def test_timeout_setter(L):
