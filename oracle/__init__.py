@@ -10,7 +10,8 @@ What each function computes, and the passage of the pages it follows, is stated
 in ``attn_ref.c``:
 
 * ``attn_dense``      full definition, S and P materialised per (batch, head)
-                      ("GPU 内核与 FlashAttention" §10, §11.1, §13.2)
+                      ("GPU 内核与 FlashAttention" §10, §11.1, §13.2); optional causal
+                      mask (§14.4, bottom-right aligned) and grouped K/V heads (§14.2)
 * ``attn_dense_rows`` the same definition for selected (b, h, i) rows
 * ``attn_varlen``     packed variable-length form, lse [B, H, max_seqlen_q]
                       ("Flash Attention实现深度解析" §3.1)
@@ -61,11 +62,12 @@ def _load():
         i32p = ctypes.POINTER(ctypes.c_int32)
         i64p = ctypes.POINTER(ctypes.c_int64)
         ci, cd = ctypes.c_int, ctypes.c_double
-        lib.oracle_attn_dense.argtypes = [u16p, u16p, u16p, ci, ci, ci, ci, ci, cd, f64p, f64p]
-        lib.oracle_attn_dense_rows.argtypes = [u16p, u16p, u16p, ci, ci, ci, ci, ci, cd,
+        lib.oracle_attn_dense.argtypes = [u16p, u16p, u16p, ci, ci, ci, ci, ci, ci, cd, ci,
+                                          f64p, f64p]
+        lib.oracle_attn_dense_rows.argtypes = [u16p, u16p, u16p, ci, ci, ci, ci, ci, ci, cd, ci,
                                                ci, i64p, f64p, f64p]
-        lib.oracle_attn_varlen.argtypes = [u16p, u16p, u16p, i32p, i32p, ci, ci, ci, cd, ci,
-                                           f64p, f64p]
+        lib.oracle_attn_varlen.argtypes = [u16p, u16p, u16p, i32p, i32p, ci, ci, ci, ci, cd, ci,
+                                           ci, f64p, f64p]
         lib.oracle_attn_online.argtypes = [u16p, u16p, u16p, ci, ci, ci, ci, ci, cd, ci,
                                            f64p, f64p]
         for name in ("oracle_attn_dense", "oracle_attn_dense_rows", "oracle_attn_varlen",
@@ -101,48 +103,49 @@ def _default_scale(d: int, scale):
     return (1.0 / np.sqrt(d)) if scale is None else float(scale)
 
 
-def attn_dense(q, k, v, scale=None):
-    """q: [B, Nq, H, d], k/v: [B, Nk, H, d] (uint16 bf16 bits).
+def attn_dense(q, k, v, scale=None, causal=False):
+    """q: [B, Nq, H, d], k/v: [B, Nk, Hk, d] (uint16 bf16 bits), H a multiple of Hk.
 
     Returns (o [B, Nq, H, d] float64, lse [B, H, Nq] float64)."""
     q, k, v = _u16(q), _u16(k), _u16(v)
     B, Nq, H, d = q.shape
-    Nk = k.shape[1]
-    if k.shape != (B, Nk, H, d) or v.shape != k.shape:
+    Nk, Hk = k.shape[1], k.shape[2]
+    if k.shape != (B, Nk, Hk, d) or v.shape != k.shape or H % Hk:
         raise ValueError("shape mismatch")
     o = np.zeros((B, Nq, H, d), np.float64)
     lse = np.zeros((B, H, Nq), np.float64)
     rc = _load().oracle_attn_dense(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
-                                   _ptr(v, ctypes.c_uint16), B, Nq, Nk, H, d,
-                                   _default_scale(d, scale),
+                                   _ptr(v, ctypes.c_uint16), B, Nq, Nk, H, Hk, d,
+                                   _default_scale(d, scale), int(bool(causal)),
                                    _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double))
     if rc != 0:
         raise MemoryError("oracle_attn_dense failed (%d)" % rc)
     return o, lse
 
 
-def attn_dense_rows(q, k, v, rows, scale=None):
+def attn_dense_rows(q, k, v, rows, scale=None, causal=False):
     """Selected rows of the dense definition; rows: int array [n, 3] of (b, h, i).
 
     Returns (o_rows [n, d], lse_rows [n])."""
     q, k, v = _u16(q), _u16(k), _u16(v)
     B, Nq, H, d = q.shape
-    Nk = k.shape[1]
+    Nk, Hk = k.shape[1], k.shape[2]
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
     n = rows.shape[0]
     o = np.zeros((n, d), np.float64)
     lse = np.zeros((n,), np.float64)
     rc = _load().oracle_attn_dense_rows(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
-                                        _ptr(v, ctypes.c_uint16), B, Nq, Nk, H, d,
-                                        _default_scale(d, scale), n, _ptr(rows, ctypes.c_int64),
+                                        _ptr(v, ctypes.c_uint16), B, Nq, Nk, H, Hk, d,
+                                        _default_scale(d, scale), int(bool(causal)), n,
+                                        _ptr(rows, ctypes.c_int64),
                                         _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double))
     if rc != 0:
         raise ValueError("oracle_attn_dense_rows failed (%d)" % rc)
     return o, lse
 
 
-def attn_varlen(q, k, v, cu_q, cu_k, max_seqlen_q, scale=None):
-    """Packed form: q [total_q, H, d], k/v [total_k, H, d], cu_* int32 [B+1].
+def attn_varlen(q, k, v, cu_q, cu_k, max_seqlen_q, scale=None, causal=False):
+    """Packed form: q [total_q, H, d], k/v [total_k, Hk, d], cu_* int32 [B+1].
 
     Returns (o [total_q, H, d], lse [B, H, max_seqlen_q]); lse entries beyond a
     sequence's length are NaN (never written)."""
@@ -150,13 +153,15 @@ def attn_varlen(q, k, v, cu_q, cu_k, max_seqlen_q, scale=None):
     cu_q = np.ascontiguousarray(cu_q, dtype=np.int32)
     cu_k = np.ascontiguousarray(cu_k, dtype=np.int32)
     _, H, d = q.shape
+    Hk = k.shape[1]
     B = cu_q.shape[0] - 1
     o = np.zeros(q.shape, np.float64)
     lse = np.full((B, H, max_seqlen_q), np.nan, np.float64)
     rc = _load().oracle_attn_varlen(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
                                     _ptr(v, ctypes.c_uint16), _ptr(cu_q, ctypes.c_int32),
-                                    _ptr(cu_k, ctypes.c_int32), B, H, d,
-                                    _default_scale(d, scale), int(max_seqlen_q),
+                                    _ptr(cu_k, ctypes.c_int32), B, H, Hk, d,
+                                    _default_scale(d, scale), int(bool(causal)),
+                                    int(max_seqlen_q),
                                     _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double))
     if rc != 0:
         raise ValueError("oracle_attn_varlen failed (%d)" % rc)

@@ -28,9 +28,17 @@
  * The full S row block of one (batch, head) is materialised, then turned into
  * P in place, then multiplied by V: no blocking, no fusion.
  *
- * Rows that have no key at all (possible only in the variable-length form with
- * an empty key sequence) have no softmax.  The pages are silent; this oracle
- * returns o = 0 and LSE = -inf for them (log of an empty sum).
+ * Rows that have no key at all (an empty key sequence, or a causal row that
+ * sees no key) have no softmax.  The pages are silent; this oracle returns
+ * o = 0 and LSE = -inf for them (log of an empty sum).
+ *
+ * Causal masking ([GKFA] §14.4): scores with key index j > i are -inf.  When
+ * the query and key lengths differ the pages are silent; this oracle aligns
+ * the mask bottom-right, i.e. query i sees keys j <= i + (Nk - Nq), which is
+ * j <= i for equal lengths.
+ *
+ * Grouped key/value heads ([GKFA] §14.2, MQA/GQA): with Hk key/value heads and
+ * H = G * Hk query heads, query head h reads key/value head h / G.
  *
  * oracle_attn_online() restates the blockwise recurrence of [GKFA] §11.3 with
  * the deferred division of §14.1, again in double.  It exists only so tests can
@@ -63,7 +71,7 @@ static double bf16_to_double(uint16_t h)
  */
 static int head_attention(const uint16_t *q, size_t q_rs, int nq,
                           const uint16_t *k, const uint16_t *v, size_t kv_rs, int nk,
-                          int d, double scale,
+                          int d, double scale, int causal, long row0, long offset,
                           double *o, size_t o_rs, double *lse, size_t lse_stride)
 {
     if (nq <= 0)
@@ -80,10 +88,16 @@ static int head_attention(const uint16_t *q, size_t q_rs, int nq,
     if (!S)
         return -1;
 
-    /* S = scale * Q K^T, materialised ([GKFA] §10). */
+    /* S = scale * Q K^T, materialised ([GKFA] §10).  Under the causal mask,
+       row i (absolute index row0 + i) sees keys j <= row0 + i + offset only;
+       the others are -inf ([GKFA] §14.4). */
     for (int i = 0; i < nq; ++i) {
         const uint16_t *qi = q + (size_t)i * q_rs;
         for (int j = 0; j < nk; ++j) {
+            if (causal && (long)j > row0 + i + offset) {
+                S[(size_t)i * nk + j] = -INFINITY;
+                continue;
+            }
             const uint16_t *kj = k + (size_t)j * kv_rs;
             double acc = 0.0;
             for (int c = 0; c < d; ++c)
@@ -93,13 +107,20 @@ static int head_attention(const uint16_t *q, size_t q_rs, int nq,
     }
 
     /* Safe softmax, row by row, three passes: max, exp and sum, divide
-       ([GKFA] §11.1).  P overwrites S. */
+       ([GKFA] §11.1).  P overwrites S.  A row whose scores are all -inf has
+       no softmax: o = 0, LSE = -inf. */
     for (int i = 0; i < nq; ++i) {
         double *row = S + (size_t)i * nk;
         double m = row[0];
         for (int j = 1; j < nk; ++j)
             if (row[j] > m)
                 m = row[j];
+        if (m == -INFINITY) {
+            for (int j = 0; j < nk; ++j)
+                row[j] = 0.0;
+            lse[(size_t)i * lse_stride] = -INFINITY;
+            continue;
+        }
         double l = 0.0;
         for (int j = 0; j < nk; ++j) {
             row[j] = exp(row[j] - m);
@@ -147,22 +168,26 @@ void oracle_set_num_threads(int n)
 }
 
 /*
- * Dense form.  q, o: [B, Nq, H, d]; k, v: [B, Nk, H, d]; lse: [B, H, Nq].
+ * Dense form.  q, o: [B, Nq, H, d]; k, v: [B, Nk, Hk, d]; lse: [B, H, Nq].
  * Inputs are bf16 bit patterns; outputs are double.
  * Parallel over (b, h) only.  Returns 0, or -1 on allocation failure.
  */
 int oracle_attn_dense(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                      int B, int Nq, int Nk, int H, int d, double scale,
+                      int B, int Nq, int Nk, int H, int Hk, int d, double scale, int causal,
                       double *o, double *lse)
 {
+    if (Hk <= 0 || H % Hk != 0)
+        return -1;
     int err = 0;
-    const size_t q_rs = (size_t)H * d, kv_rs = (size_t)H * d;
+    const int G = H / Hk;
+    const size_t q_rs = (size_t)H * d, kv_rs = (size_t)Hk * d;
 #pragma omp parallel for collapse(2) schedule(dynamic, 1) reduction(| : err)
     for (int b = 0; b < B; ++b) {
         for (int h = 0; h < H; ++h) {
             const size_t qoff = (size_t)b * Nq * H * d + (size_t)h * d;
-            const size_t kvoff = (size_t)b * Nk * H * d + (size_t)h * d;
+            const size_t kvoff = (size_t)b * Nk * Hk * d + (size_t)(h / G) * d;
             err |= head_attention(q + qoff, q_rs, Nq, k + kvoff, v + kvoff, kv_rs, Nk, d, scale,
+                                  causal, 0, (long)Nk - Nq,
                                   o + qoff, q_rs, lse + ((size_t)b * H + h) * Nq, 1);
         }
     }
@@ -175,11 +200,14 @@ int oracle_attn_dense(const uint16_t *q, const uint16_t *k, const uint16_t *v,
  * same per-head routine as oracle_attn_dense (a one-row head).
  */
 int oracle_attn_dense_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                           int B, int Nq, int Nk, int H, int d, double scale,
+                           int B, int Nq, int Nk, int H, int Hk, int d, double scale, int causal,
                            int n_rows, const int64_t *rows, double *o_rows, double *lse_rows)
 {
+    if (Hk <= 0 || H % Hk != 0)
+        return -1;
     int err = 0;
-    const size_t kv_rs = (size_t)H * d;
+    const int G = H / Hk;
+    const size_t kv_rs = (size_t)Hk * d;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
     for (int r = 0; r < n_rows; ++r) {
         const int64_t b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
@@ -188,8 +216,9 @@ int oracle_attn_dense_rows(const uint16_t *q, const uint16_t *k, const uint16_t 
             continue;
         }
         const size_t qoff = (((size_t)b * Nq + i) * H + h) * d;
-        const size_t kvoff = (size_t)b * Nk * H * d + (size_t)h * d;
+        const size_t kvoff = (size_t)b * Nk * Hk * d + (size_t)(h / G) * d;
         err |= head_attention(q + qoff, 0, 1, k + kvoff, v + kvoff, kv_rs, Nk, d, scale,
+                              causal, (long)i, (long)Nk - Nq,
                               o_rows + (size_t)r * d, 0, lse_rows + r, 1);
     }
     return err ? -1 : 0;
@@ -198,16 +227,19 @@ int oracle_attn_dense_rows(const uint16_t *q, const uint16_t *k, const uint16_t 
 /*
  * Variable-length packed form ([FMHA] §3.1).  Sequence b owns query rows
  * [cu_q[b], cu_q[b+1]) and key rows [cu_k[b], cu_k[b+1]) of the packed
- * tensors q, o: [total_q, H, d] and k, v: [total_k, H, d].  Each sequence
+ * tensors q, o: [total_q, H, d] and k, v: [total_k, Hk, d].  Each sequence
  * attends only within itself.  lse: [B, H, max_seqlen_q]; entry
  * (b, h, i) is written for i < len_q(b) only.
  */
 int oracle_attn_varlen(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                       const int32_t *cu_q, const int32_t *cu_k, int B, int H, int d,
-                       double scale, int max_seqlen_q, double *o, double *lse)
+                       const int32_t *cu_q, const int32_t *cu_k, int B, int H, int Hk, int d,
+                       double scale, int causal, int max_seqlen_q, double *o, double *lse)
 {
+    if (Hk <= 0 || H % Hk != 0)
+        return -1;
     int err = 0;
-    const size_t rs = (size_t)H * d;
+    const int G = H / Hk;
+    const size_t rs = (size_t)H * d, kv_rs = (size_t)Hk * d;
 #pragma omp parallel for collapse(2) schedule(dynamic, 1) reduction(| : err)
     for (int b = 0; b < B; ++b) {
         for (int h = 0; h < H; ++h) {
@@ -218,8 +250,9 @@ int oracle_attn_varlen(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                 continue;
             }
             const size_t qoff = (size_t)cu_q[b] * rs + (size_t)h * d;
-            const size_t kvoff = (size_t)cu_k[b] * rs + (size_t)h * d;
-            err |= head_attention(q + qoff, rs, nq, k + kvoff, v + kvoff, rs, nk, d, scale,
+            const size_t kvoff = (size_t)cu_k[b] * kv_rs + (size_t)(h / G) * d;
+            err |= head_attention(q + qoff, rs, nq, k + kvoff, v + kvoff, kv_rs, nk, d, scale,
+                                  causal, 0, (long)nk - nq,
                                   o + qoff, rs, lse + ((size_t)b * H + h) * max_seqlen_q, 1);
         }
     }

@@ -304,3 +304,108 @@ def test_varlen_empty_keys_convention(oracle_mod):
     assert np.all(o[:2] == 0.0)
     assert np.all(np.isneginf(lse[0, :, :2]))
     assert np.all(np.isfinite(o[2:]))
+
+
+# ------------------------------------------------------- causal and GQA
+def _brute_causal(qf, kf, vf, scale, Hk):
+    """Plain softmax over the visible keys j <= i + (Nk - Nq) (no max shift,
+    math.fsum); rows that see no key give o = 0, lse = -inf."""
+    B, Nq, H, d = qf.shape
+    Nk = kf.shape[1]
+    G = H // Hk
+    o = np.zeros((B, Nq, H, d))
+    lse = np.zeros((B, H, Nq))
+    for b in range(B):
+        for h in range(H):
+            for i in range(Nq):
+                vis = [j for j in range(Nk) if j <= i + Nk - Nq]
+                if not vis:
+                    lse[b, h, i] = -math.inf
+                    continue
+                e = [math.exp(scale * math.fsum(qf[b, i, h, c] * kf[b, j, h // G, c] for c in range(d)))
+                     for j in vis]
+                den = math.fsum(e)
+                lse[b, h, i] = math.log(den)
+                for c in range(d):
+                    o[b, i, h, c] = math.fsum(e[n] * vf[b, j, h // G, c] for n, j in enumerate(vis)) / den
+    return o, lse
+
+
+@pytest.mark.parametrize("B,Nq,Nk,H,Hk,d", [(1, 5, 5, 2, 2, 4), (2, 3, 7, 4, 2, 3),
+                                             (1, 6, 4, 3, 1, 4), (1, 4, 4, 4, 1, 2)])
+def test_causal_and_grouped_heads_brute_force(oracle_mod, B, Nq, Nk, H, Hk, d):
+    g = torch.Generator().manual_seed(60 + Nq + Nk + Hk)
+    q = I.randn_bf16((B, Nq, H, d), g)
+    k = I.randn_bf16((B, Nk, Hk, d), g)
+    v = I.randn_bf16((B, Nk, Hk, d), g)
+    qb, kb, vb = I.bf16_bits(q), I.bf16_bits(k), I.bf16_bits(v)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = oracle_mod.attn_dense(qb, kb, vb, causal=True)
+    o_bf, lse_bf = _brute_causal(_f(qb), _f(kb), _f(vb), scale, Hk)
+    np.testing.assert_allclose(o, o_bf, rtol=0, atol=1e-13)
+    fin = np.isfinite(lse_bf)
+    np.testing.assert_allclose(lse[fin], lse_bf[fin], rtol=0, atol=1e-13)
+    assert np.all(np.isneginf(lse[~fin]))
+    if Hk == H:
+        o_nc, _ = oracle_mod.attn_dense(qb, kb, vb, causal=False)
+        o_bf_nc, _ = _brute_plain(_f(qb), _f(kb), _f(vb), scale)
+        np.testing.assert_allclose(o_nc, o_bf_nc, rtol=0, atol=1e-13)
+
+
+def test_causal_row_is_prefix_attention(oracle_mod):
+    """With equal lengths, causal row i is plain attention of q_i over the first
+    i + 1 keys ("GPU 内核与 FlashAttention" §14.4): compare with the unmasked
+    definition evaluated on the truncated key set."""
+    B, N, H, d = 1, 40, 2, 16
+    qb, kb, vb = _rand_dense(B, N, N, H, d, 61)
+    o, lse = oracle_mod.attn_dense(qb, kb, vb, causal=True)
+    for i in (0, 1, 17, 39):
+        op, lp = oracle_mod.attn_dense(qb[:, i:i + 1].copy(), kb[:, :i + 1].copy(), vb[:, :i + 1].copy())
+        np.testing.assert_allclose(o[:, i], op[:, 0], rtol=0, atol=1e-14)
+        np.testing.assert_allclose(lse[:, :, i], lp[:, :, 0], rtol=0, atol=1e-14)
+
+
+def test_causal_first_row_sees_one_key(oracle_mod):
+    B, N, H, d = 2, 9, 3, 8
+    qb, kb, vb = _rand_dense(B, N, N, H, d, 62)
+    o, lse = oracle_mod.attn_dense(qb, kb, vb, causal=True)
+    np.testing.assert_array_equal(o[:, 0], _f(vb)[:, 0])
+    s0 = np.einsum("bhc,bhc->bh", _f(qb)[:, 0], _f(kb)[:, 0]) / math.sqrt(d)
+    np.testing.assert_allclose(lse[:, :, 0], s0, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_heads_equal_repeated_heads(oracle_mod, causal):
+    """Query head h reads key/value head h / G: identical to plain multi-head
+    attention on K, V with every head repeated G times."""
+    B, Nq, Nk, H, Hk, d = 2, 33, 47, 6, 2, 16
+    g = torch.Generator().manual_seed(63)
+    q = I.bf16_bits(I.randn_bf16((B, Nq, H, d), g))
+    k = I.bf16_bits(I.randn_bf16((B, Nk, Hk, d), g))
+    v = I.bf16_bits(I.randn_bf16((B, Nk, Hk, d), g))
+    o, lse = oracle_mod.attn_dense(q, k, v, causal=causal)
+    G = H // Hk
+    o2, lse2 = oracle_mod.attn_dense(q, np.repeat(k, G, axis=2), np.repeat(v, G, axis=2), causal=causal)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, lse2)
+
+
+def test_causal_rows_and_varlen_match_dense(oracle_mod):
+    B, Nq, Nk, H, Hk, d = 2, 30, 45, 4, 2, 8
+    g = torch.Generator().manual_seed(64)
+    q = I.bf16_bits(I.randn_bf16((B, Nq, H, d), g))
+    k = I.bf16_bits(I.randn_bf16((B, Nk, Hk, d), g))
+    v = I.bf16_bits(I.randn_bf16((B, Nk, Hk, d), g))
+    o, lse = oracle_mod.attn_dense(q, k, v, causal=True)
+    rows = np.array([[0, 0, 0], [1, 3, 29], [0, 2, 11], [1, 1, 7]])
+    orow, lrow = oracle_mod.attn_dense_rows(q, k, v, rows, causal=True)
+    for r, (b, h, i) in enumerate(rows):
+        np.testing.assert_array_equal(orow[r], o[b, i, h])
+        assert lrow[r] == lse[b, h, i]
+    # the same batch as a packed variable-length batch of two equal sequences
+    cu_q = np.array([0, Nq, 2 * Nq], np.int32)
+    cu_k = np.array([0, Nk, 2 * Nk], np.int32)
+    ov, lv = oracle_mod.attn_varlen(q.reshape(B * Nq, H, d), k.reshape(B * Nk, Hk, d),
+                                    v.reshape(B * Nk, Hk, d), cu_q, cu_k, Nq, causal=True)
+    np.testing.assert_array_equal(ov.reshape(o.shape), o)
+    np.testing.assert_array_equal(lv, lse)
