@@ -31,9 +31,11 @@ FA_ERR_TIMEOUT = -5
 FA_ERR_NO_DEVICE = -6
 FA_ERR_BAD_SEQLENS = -7
 
+FA_FLAG_CAUSAL = 1
+
 # Every symbol include/fa.h declares.
 EXPORTS = (
-    "fa_fwd", "fa_fwd_qk", "fa_check_status", "fa_strerror", "fa_last_cuda_error",
+    "fa_fwd", "fa_fwd_qk", "fa_fwd_ex", "fa_check_status", "fa_strerror", "fa_last_cuda_error",
     "fa_set_timeout_ns", "fa_set_config", "fa_get_config", "fa_autotune",
     "fa_selftest_wait_timeout", "fa_version",
 )
@@ -65,6 +67,7 @@ def lib() -> ctypes.CDLL:
         vp, ci, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, vp, vp]
         L.fa_fwd_qk.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp, vp, vp]
+        L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, vp, vp, ci, vp]
         L.fa_check_status.argtypes = [vp, ctypes.POINTER(ci)]
         L.fa_strerror.argtypes = [ci]
         L.fa_strerror.restype = ctypes.c_char_p
@@ -89,6 +92,10 @@ def fa_fwd(q, k, v, o, lse, B, N, H, d, scale, cu_seqlens, stream) -> int:
 
 def fa_fwd_qk(q, k, v, o, lse, B, Nq, Nk, H, d, scale, cu_q, cu_k, stream) -> int:
     return lib().fa_fwd_qk(q, k, v, o, lse, B, Nq, Nk, H, d, scale, cu_q, cu_k, stream)
+
+
+def fa_fwd_ex(q, k, v, o, lse, B, Nq, Nk, H, Hk, d, scale, cu_q, cu_k, flags, stream) -> int:
+    return lib().fa_fwd_ex(q, k, v, o, lse, B, Nq, Nk, H, Hk, d, scale, cu_q, cu_k, flags, stream)
 
 
 def fa_check_status(stream=None):
@@ -153,12 +160,15 @@ def _check_tensor(name, t, dtype, ndim):
 
 
 def forward_qk(q, k, v, scale=None, cu_seqlens_q=None, cu_seqlens_k=None,
-               max_seqlen_q=None, max_seqlen_k=None, out=None, lse=None, stream=None):
+               max_seqlen_q=None, max_seqlen_k=None, out=None, lse=None, stream=None,
+               causal=False):
     """Attention forward with separate query / key lengths.
 
-    Dense: q [B, Nq, H, d], k/v [B, Nk, H, d] (bf16, CUDA, contiguous).
-    Variable length: q [total_q, H, d], k/v [total_k, H, d], cu_seqlens_* int32
+    Dense: q [B, Nq, H, d], k/v [B, Nk, Hk, d] (bf16, CUDA, contiguous), H a
+    multiple of Hk (grouped key/value heads).
+    Variable length: q [total_q, H, d], k/v [total_k, Hk, d], cu_seqlens_* int32
     [B + 1] on the device, max_seqlen_* the longest query / key sequence.
+    causal: mask keys j > i + (Nk - Nq) (bottom-right aligned).
     Returns (o, lse): o like q (bf16), lse [B, H, Nq] fp32 (natural log).
     """
     import torch
@@ -174,16 +184,19 @@ def forward_qk(q, k, v, scale=None, cu_seqlens_q=None, cu_seqlens_k=None,
         if cu_seqlens_k.numel() != B + 1:
             raise ValueError("cu_seqlens_q and cu_seqlens_k differ in length")
         _, H, d = q.shape
-        if k.shape[1:] != (H, d) or v.shape != k.shape:
+        Hk = k.shape[1]
+        if k.shape[2] != d or v.shape != k.shape:
             raise ValueError("k/v shape mismatch")
         Nq, Nk = int(max_seqlen_q), int(max_seqlen_k)
     else:
         for name, t in (("q", q), ("k", k), ("v", v)):
             _check_tensor(name, t, torch.bfloat16, 4)
         B, Nq, H, d = q.shape
-        Nk = k.shape[1]
-        if k.shape != (B, Nk, H, d) or v.shape != k.shape:
+        Nk, Hk = k.shape[1], k.shape[2]
+        if k.shape != (B, Nk, Hk, d) or v.shape != k.shape:
             raise ValueError("k/v shape mismatch")
+    if Hk == 0 or H % Hk:
+        raise ValueError("query heads (%d) must be a multiple of key/value heads (%d)" % (H, Hk))
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
@@ -199,26 +212,26 @@ def forward_qk(q, k, v, scale=None, cu_seqlens_q=None, cu_seqlens_k=None,
         if tuple(lse.shape) != (B, H, Nq):
             raise ValueError("lse must be [B, H, Nq]")
     with torch.cuda.device(q.device):
-        rc = fa_fwd_qk(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                       B, Nq, Nk, H, d, float(scale),
+        rc = fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                       B, Nq, Nk, H, Hk, d, float(scale),
                        cu_seqlens_q.data_ptr() if varlen else None,
                        cu_seqlens_k.data_ptr() if varlen else None,
-                       _stream_handle(stream))
+                       FA_FLAG_CAUSAL if causal else 0, _stream_handle(stream))
     if rc != FA_OK:
-        raise FaError(rc, "fa_fwd_qk")
+        raise FaError(rc, "fa_fwd_ex")
     return out, lse
 
 
 def forward(q, k, v, scale=None, cu_seqlens=None, max_seqlen=None, out=None, lse=None,
-            stream=None):
+            stream=None, causal=False):
     """Self-attention shapes (the C entry fa_fwd): dense q/k/v [B, N, H, d], or
     packed [total, H, d] with one cu_seqlens for queries and keys."""
     if cu_seqlens is not None:
         if max_seqlen is None:
             raise ValueError("max_seqlen is required with cu_seqlens")
         return forward_qk(q, k, v, scale, cu_seqlens, cu_seqlens, max_seqlen, max_seqlen,
-                          out=out, lse=lse, stream=stream)
-    return forward_qk(q, k, v, scale, out=out, lse=lse, stream=stream)
+                          out=out, lse=lse, stream=stream, causal=causal)
+    return forward_qk(q, k, v, scale, out=out, lse=lse, stream=stream, causal=causal)
 
 
 def check_status(stream=None):

@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfa_gb300.so")
-UNITS = ("fa_api.cu", "fa_fwd_d128.cu", "fa_fwd_d64.cu")
+UNITS = ("fa_api.cu", "fa_fwd_d128.cu", "fa_fwd_d128_causal.cu", "fa_fwd_d64.cu",
+         "fa_fwd_d64_causal.cu")
 HEADERS = ("ptx.cuh", "fa_fwd_kernel.cuh", "fa_launch.h")
 
 NVCC_FLAGS = [

@@ -164,47 +164,37 @@ bool parse_config(const char* spec, Config* out) {
 // d = 128 fits two slots next to the query tiles; d = 64 fits up to four.
 int effective_stages(int d, int stages) { return d == 128 ? 2 : stages; }
 
-template <int D, bool VARLEN>
-cudaError_t dispatch_stages(int stages, const fa::LaunchArgs& a);
-
-template <>
-cudaError_t dispatch_stages<128, false>(int, const fa::LaunchArgs& a) {
-  return fa::launch_fwd<128, 2, false>(a);
-}
-template <>
-cudaError_t dispatch_stages<128, true>(int, const fa::LaunchArgs& a) {
-  return fa::launch_fwd<128, 2, true>(a);
-}
-template <bool VARLEN>
+template <bool VARLEN, bool CAUSAL>
 cudaError_t dispatch_d64(int stages, const fa::LaunchArgs& a) {
   switch (stages) {
-    case 2: return fa::launch_fwd<64, 2, VARLEN>(a);
-    case 3: return fa::launch_fwd<64, 3, VARLEN>(a);
-    default: return fa::launch_fwd<64, 4, VARLEN>(a);
+    case 2: return fa::launch_fwd<64, 2, VARLEN, CAUSAL>(a);
+    case 3: return fa::launch_fwd<64, 3, VARLEN, CAUSAL>(a);
+    default: return fa::launch_fwd<64, 4, VARLEN, CAUSAL>(a);
   }
 }
-template <>
-cudaError_t dispatch_stages<64, false>(int stages, const fa::LaunchArgs& a) {
-  return dispatch_d64<false>(stages, a);
-}
-template <>
-cudaError_t dispatch_stages<64, true>(int stages, const fa::LaunchArgs& a) {
-  return dispatch_d64<true>(stages, a);
+
+template <bool VARLEN, bool CAUSAL>
+cudaError_t dispatch(int d, int stages, const fa::LaunchArgs& a) {
+  if (d == 128) return fa::launch_fwd<128, 2, VARLEN, CAUSAL>(a);
+  return dispatch_d64<VARLEN, CAUSAL>(stages, a);
 }
 
 struct Problem {
   const void *q, *k, *v;
   void* o;
   float* lse;
-  int B, Nq, Nk, H, d;
+  int B, Nq, Nk, H, Hk, d;
   float scale;
   const int *cu_q, *cu_k;
+  int flags;
   cudaStream_t stream;
 };
 
 // Validates a problem; returns FA_OK, a negative error, or 1 for "nothing to do".
 int validate(const Problem& P) {
-  if (P.B < 0 || P.Nq < 0 || P.Nk < 0 || P.H < 0) return FA_ERR_INVALID_ARG;
+  if (P.B < 0 || P.Nq < 0 || P.Nk < 0 || P.H < 0 || P.Hk < 0) return FA_ERR_INVALID_ARG;
+  if ((P.flags & ~FA_FLAG_CAUSAL) != 0) return FA_ERR_INVALID_ARG;
+  if (P.H > 0 && (P.Hk == 0 || P.H % P.Hk != 0)) return FA_ERR_INVALID_ARG;
   if (!(std::isfinite(P.scale) && P.scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (P.d != 64 && P.d != 128) return FA_ERR_UNSUPPORTED;
   const bool varlen = P.cu_q != nullptr;
@@ -240,8 +230,8 @@ int run(const Problem& P, const Config& cfg) {
   if (!varlen) {
     cuuint64_t dq[4] = {(cuuint64_t)D, (cuuint64_t)P.H, (cuuint64_t)P.Nq, (cuuint64_t)P.B};
     cuuint64_t sq[3] = {D * esz, (cuuint64_t)P.H * D * esz, (cuuint64_t)P.Nq * P.H * D * esz};
-    cuuint64_t dk[4] = {(cuuint64_t)D, (cuuint64_t)P.H, (cuuint64_t)P.Nk, (cuuint64_t)P.B};
-    cuuint64_t sk[3] = {D * esz, (cuuint64_t)P.H * D * esz, (cuuint64_t)P.Nk * P.H * D * esz};
+    cuuint64_t dk[4] = {(cuuint64_t)D, (cuuint64_t)P.Hk, (cuuint64_t)P.Nk, (cuuint64_t)P.B};
+    cuuint64_t sk[3] = {D * esz, (cuuint64_t)P.Hk * D * esz, (cuuint64_t)P.Nk * P.Hk * D * esz};
     cuuint32_t box_q[4] = {64, 1, (cuuint32_t)fa::kBR, 1};
     cuuint32_t box_k[4] = {64, 1, (cuuint32_t)fa::kBC, 1};
     cuuint32_t box_o[4] = {64, 1, 32, 1};
@@ -254,15 +244,16 @@ int run(const Problem& P, const Config& cfg) {
     // Packed rows: the row extent is an upper bound (every length <= the
     // maximum); the kernel never addresses rows at or past a sequence's end.
     cuuint64_t dq[3] = {(cuuint64_t)D, (cuuint64_t)P.H, (cuuint64_t)P.B * P.Nq};
-    cuuint64_t dk[3] = {(cuuint64_t)D, (cuuint64_t)P.H, (cuuint64_t)(P.B * (long long)P.Nk > 0 ? P.B * (long long)P.Nk : 1)};
+    cuuint64_t dk[3] = {(cuuint64_t)D, (cuuint64_t)P.Hk, (cuuint64_t)(P.B * (long long)P.Nk > 0 ? P.B * (long long)P.Nk : 1)};
     cuuint64_t sr[2] = {D * esz, (cuuint64_t)P.H * D * esz};
+    cuuint64_t srk[2] = {D * esz, (cuuint64_t)P.Hk * D * esz};
     cuuint32_t box_q[3] = {64, 1, (cuuint32_t)fa::kBR};
     cuuint32_t box_k[3] = {64, 1, (cuuint32_t)fa::kBC};
     cuuint32_t box_o[3] = {64, 1, 32};
     int e;
     if ((e = encode(&a.tm_q, P.q, 3, dq, sr, box_q)) != FA_OK) return e;
-    if ((e = encode(&a.tm_k, P.k, 3, dk, sr, box_k)) != FA_OK) return e;
-    if ((e = encode(&a.tm_v, P.v, 3, dk, sr, box_k)) != FA_OK) return e;
+    if ((e = encode(&a.tm_k, P.k, 3, dk, srk, box_k)) != FA_OK) return e;
+    if ((e = encode(&a.tm_v, P.v, 3, dk, srk, box_k)) != FA_OK) return e;
     if ((e = encode(&a.tm_o, P.o, 3, dq, sr, box_o)) != FA_OK) return e;
   }
   fa::FwdParams& p = a.p;
@@ -270,10 +261,14 @@ int run(const Problem& P, const Config& cfg) {
   p.Nq = P.Nq;
   p.Nk = P.Nk;
   p.H = P.H;
+  p.group = P.H / P.Hk;
+  p.causal = (P.flags & FA_FLAG_CAUSAL) ? 1 : 0;
   p.num_mblocks = (P.Nq + fa::kBR * fa::kQT - 1) / (fa::kBR * fa::kQT);
   const long long units = static_cast<long long>(P.B) * P.H * p.num_mblocks;
   if (units > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   p.num_units = static_cast<int>(units);
+  p.units_per_item = p.causal ? 2 : 1;
+  p.num_items = static_cast<int>((units + p.units_per_item - 1) / p.units_per_item);
   p.cu_q = P.cu_q;
   p.cu_k = P.cu_k;
   p.lse = P.lse;
@@ -286,15 +281,15 @@ int run(const Problem& P, const Config& cfg) {
     p.timeout_ns = g_timeout_ns;
   }
   p.status = st->status;
-  // Persistent grid: one CTA per SM (each walks units blockIdx.x + k * gridDim.x).
-  a.grid = dim3(static_cast<unsigned>(units < st->num_sms ? units : st->num_sms), 1, 1);
+  // Persistent grid: one CTA per SM (each walks items blockIdx.x + k * gridDim.x).
+  a.grid = dim3(static_cast<unsigned>(p.num_items < st->num_sms ? p.num_items : st->num_sms), 1, 1);
   a.stream = P.stream;
 
   cudaError_t e;
-  if (D == 128)
-    e = varlen ? dispatch_stages<128, true>(cfg.stages, a) : dispatch_stages<128, false>(cfg.stages, a);
+  if (p.causal)
+    e = varlen ? dispatch<true, true>(D, cfg.stages, a) : dispatch<false, true>(D, cfg.stages, a);
   else
-    e = varlen ? dispatch_stages<64, true>(cfg.stages, a) : dispatch_stages<64, false>(cfg.stages, a);
+    e = varlen ? dispatch<true, false>(D, cfg.stages, a) : dispatch<false, false>(D, cfg.stages, a);
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;
 }
@@ -320,12 +315,18 @@ __global__ void wait_timeout_kernel(unsigned long long timeout_ns, int* status) 
 
 extern "C" {
 
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Nq,
+              int Nk, int H, int Hk, int d, float scale, const int* cu_seqlens_q,
+              const int* cu_seqlens_k, int flags, void* stream) {
+  Problem P{q, k, v, o, lse, B, Nq, Nk, H, Hk, d, scale, cu_seqlens_q, cu_seqlens_k, flags,
+            static_cast<cudaStream_t>(stream)};
+  return run(P, pick_config(d, Nk, cu_seqlens_q != nullptr));
+}
+
 int fa_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Nq,
               int Nk, int H, int d, float scale, const int* cu_seqlens_q,
               const int* cu_seqlens_k, void* stream) {
-  Problem P{q, k, v, o, lse, B, Nq, Nk, H, d, scale, cu_seqlens_q, cu_seqlens_k,
-            static_cast<cudaStream_t>(stream)};
-  return run(P, pick_config(d, Nk, cu_seqlens_q != nullptr));
+  return fa_fwd_ex(q, k, v, o, lse, B, Nq, Nk, H, H, d, scale, cu_seqlens_q, cu_seqlens_k, 0, stream);
 }
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int N, int H,
@@ -397,7 +398,7 @@ int fa_get_config(int d, int N, int varlen, char* buf, int len) {
 
 int fa_autotune(const void* q, const void* k, const void* v, void* o, float* lse, int B, int N,
                 int H, int d, float scale, const int* cu_seqlens, void* stream) {
-  Problem P{q, k, v, o, lse, B, N, N, H, d, scale, cu_seqlens, cu_seqlens,
+  Problem P{q, k, v, o, lse, B, N, N, H, H, d, scale, cu_seqlens, cu_seqlens, 0,
             static_cast<cudaStream_t>(stream)};
   const int rc = validate(P);
   if (rc != FA_OK) return rc == 1 ? FA_OK : rc;

@@ -1,0 +1,7 @@
+// Kernel instantiations for d_head = 128 with the causal mask.
+#include "fa_launch.h"
+
+namespace fa {
+FA_DEFINE_LAUNCH(128, 2, false, true)
+FA_DEFINE_LAUNCH(128, 2, true, true)
+}  // namespace fa

@@ -43,6 +43,14 @@
 // quarter holds exactly its rows of O), after S(j) completed, which implies
 // that P(j-1) V(j-1) has completed.
 //
+// Causal masking ("GPU 内核与 FlashAttention" §14.4): key tiles entirely above
+// the diagonal are skipped (each query tile runs only the key tiles its rows
+// can see), only tiles that cross the diagonal are masked element-wise, and the
+// heaviest query blocks are scheduled first.  With different query and key
+// lengths the mask is aligned bottom-right: query i sees keys j <= i + Nk - Nq.
+// Grouped key/value heads (§14.2, MQA/GQA): query head h reads key/value head
+// h / G; K and V are never replicated in memory.
+//
 // Scale folding ("Flash Attention 2 Chapter6", Kernel 6): p = 2^(s * c - m * c)
 // with c = scale * log2(e), one FFMA feeding the ex2 unit per score.
 #pragma once
@@ -59,12 +67,16 @@ constexpr int kQT = 2;         // query tiles per work unit
 constexpr int kThreads = 512;  // 16 warps
 constexpr int kPanel = 64;     // bf16 columns per 128-byte swizzle row
 
-// Register split after setmaxnreg (must sum to 65536 over 512 threads).
-constexpr int kRegSoftmax = 176;
-constexpr int kRegCorrection = 80;
-constexpr int kRegOther = 80;
-static_assert(2 * 128 * kRegSoftmax + 128 * kRegCorrection + 128 * kRegOther <= 65536,
-              "register split exceeds the launch allocation");
+// Register split after setmaxnreg (must sum to 65536 over 512 threads); the
+// variable-length form needs a little more in the softmax warps (window masks).
+template <bool VARLEN>
+struct RegSplit {
+  static constexpr int kSoftmax = VARLEN ? 184 : 176;
+  static constexpr int kCorrection = VARLEN ? 72 : 80;
+  static constexpr int kOther = VARLEN ? 72 : 80;
+  static_assert(2 * 128 * kSoftmax + 128 * kCorrection + 128 * kOther <= 65536,
+                "register split exceeds the launch allocation");
+};
 
 // Where a wait gave up (recorded with FA_ERR_TIMEOUT).
 enum WaitSite : int {
@@ -81,8 +93,12 @@ enum WaitSite : int {
 
 struct FwdParams {
   int B, Nq, Nk, H;            // variable-length form: Nq / Nk are the maximum lengths
+  int group;                   // query heads per key/value head (H / Hk)
+  int causal;                  // 1: causal mask, bottom-right aligned
   int num_mblocks;             // ceil(Nq / (kBR * kQT))
   int num_units;               // B * H * num_mblocks
+  int units_per_item;          // units a CTA takes at a time (2 when causal: a balanced pair)
+  int num_items;               // ceil(num_units / units_per_item)
   const int* cu_q;             // variable-length form: int32 [B + 1]
   const int* cu_k;
   float* lse;                  // [B, H, Nq] fp32
@@ -168,25 +184,36 @@ __device__ __forceinline__ RowWindow make_window(int seq_start, int seq_end, int
 
 // One work unit: query block mb (two 128-row tiles) of head h in batch b.
 struct Unit {
-  int b, h;
+  int b, h, hk;                        // batch, query head, key/value head
   int q_start, q_end, k_start, k_end;  // row ranges of the sequence (packed rows if variable length)
   int q_row0;                          // first query row of the unit
-  int nkv;                             // key/value tiles
+  int off;                             // causal: query i sees keys j <= i + off
+  int nkv;                             // key/value steps of the unit (max over its tiles)
   int lse_base;                        // (b * H + h) * Nq
-  bool run;                            // the unit has query rows and keys
-  bool nokeys;                         // query rows but no keys (variable length only)
-  bool active[kQT];
+  bool run;                            // some tile of the unit has rows and visible keys
+  bool nokeys;                         // query rows but no keys at all (variable length only)
+  bool active[kQT];                    // tile t has rows and runs nt[t] > 0 key steps
+  bool zero[kQT];                      // tile t has rows but sees no key: o = 0, LSE = -inf
+  int nt[kQT];                         // key/value tiles tile t needs
   RowWindow qwin[kQT];
 };
 
 // Every role decodes the same unit identically (pure function of u and params).
-template <int BC, bool VARLEN>
+template <int BC, bool VARLEN, bool CAUSAL>
 __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   Unit w;
-  const int mb = u % p.num_mblocks;
+  int mb = u % p.num_mblocks;
+  if constexpr (CAUSAL) {
+    // Zigzag order within a head: last, first, second last, second, ... so that
+    // the two units of an item (the heaviest left with the lightest left) carry
+    // the same work and the persistent round-robin stays balanced.
+    const int pi = mb >> 1;
+    mb = (mb & 1) ? pi : p.num_mblocks - 1 - pi;
+  }
   const int r = u / p.num_mblocks;
   w.h = r % p.H;
   w.b = r / p.H;
+  w.hk = w.h / p.group;
   w.q_start = 0;
   w.q_end = p.Nq;
   w.k_start = 0;
@@ -201,24 +228,45 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
     bad = len_q < 0 || len_k < 0 || len_q > p.Nq || len_k > p.Nk || w.q_start < 0 || w.k_start < 0;
   }
   w.q_row0 = w.q_start + mb * (kBR * kQT);
-  w.nkv = bad ? 0 : (w.k_end - w.k_start + BC - 1) / BC;
+  w.off = (w.k_end - w.k_start) - (w.q_end - w.q_start);
+  const int nkv_all = bad ? 0 : (w.k_end - w.k_start + BC - 1) / BC;
   w.lse_base = (w.b * p.H + w.h) * p.Nq;
   const bool has_rows = !bad && w.q_row0 < w.q_end;
-  w.run = has_rows && w.nkv > 0;
-  w.nokeys = has_rows && w.nkv == 0;
+  w.nkv = 0;
 #pragma unroll
   for (int t = 0; t < kQT; ++t) {
     const int r0 = w.q_row0 + t * kBR;
-    w.active[t] = w.run && r0 < w.q_end;
     w.qwin[t] = make_window<VARLEN>(w.q_start, w.q_end, r0, kBR);
+    const bool rows = has_rows && r0 < w.q_end;
+    int n = nkv_all;
+    if (CAUSAL && rows) {
+      // Last valid row of the tile, in sequence coordinates, and the last key it sees.
+      const int i_last = w.qwin[t].load_row - w.q_start + w.qwin[t].hi - 1;
+      const int key_last = i_last + w.off;
+      n = key_last < 0 ? 0 : min(nkv_all, key_last / BC + 1);
+    }
+    w.nt[t] = rows ? n : 0;
+    w.active[t] = rows && n > 0;
+    w.zero[t] = rows && n == 0 && nkv_all > 0;
+    w.nkv = max(w.nkv, w.nt[t]);
   }
+  w.run = w.active[0] || w.active[1];
+  w.nokeys = has_rows && nkv_all == 0;
   if (bad && mb == 0 && w.h == 0) {
     if ((threadIdx.x & 31) == 0 && threadIdx.x < 32) record_error(p.status, kErrBadSeqlens, 0);
   }
   return w;
 }
 
-template <int D, int BC, int STAGES, bool VARLEN>
+// Persistent walk over the work units of this CTA: items blockIdx.x,
+// blockIdx.x + gridDim.x, ...; each item is units_per_item consecutive units.
+// Every role runs the same walk, so all roles see the same unit sequence.
+#define FA_FOR_EACH_UNIT(u)                                                          \
+  for (int it_ = blockIdx.x; it_ < p.num_items && ok; it_ += gridDim.x)               \
+    for (int sub_ = 0, u = it_ * p.units_per_item;                                     \
+         sub_ < p.units_per_item && u < p.num_units && ok; ++sub_, ++u)
+
+template <int D, int BC, int STAGES, bool VARLEN, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -280,15 +328,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *s_tmem;
 
   if (warp >= 12) {
-    ptx::setmaxnreg_dec<kRegOther>();
+    ptx::setmaxnreg_dec<RegSplit<VARLEN>::kOther>();
     if (warp == 13 && lane == 0) {
       // =========================================================== TMA loads
       uint32_t qcount = 0;  // units whose Q was loaded
       uint32_t g = 0;       // ring slots handed to the TMA unit so far
       bool ok = true;
 #pragma unroll 1
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-        const Unit w = decode_unit<BC, VARLEN>(p, u);
+      FA_FOR_EACH_UNIT(u) {
+        const Unit w = decode_unit<BC, VARLEN, CAUSAL>(p, u);
         if (!w.run) continue;
         // Q of this unit, once the previous unit's S MMAs no longer read it.
         if (!ptx::mbar_wait(bar(L::kBarQEmpty), (qcount & 1u) ^ 1u, s_abort, tmo)) {
@@ -331,9 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int pnl = 0; pnl < kDPanels; ++pnl) {
               const uint32_t dst = sbase + pnl * L::kKVPanelBytes;
               if constexpr (VARLEN)
-                ptx::tma_load_3d(dst, &tm_k, bar(L::kBarKVFull + slot), pnl * kPanel, w.h, kw.load_row);
+                ptx::tma_load_3d(dst, &tm_k, bar(L::kBarKVFull + slot), pnl * kPanel, w.hk, kw.load_row);
               else
-                ptx::tma_load_4d(dst, &tm_k, bar(L::kBarKVFull + slot), pnl * kPanel, w.h, kw.load_row, w.b);
+                ptx::tma_load_4d(dst, &tm_k, bar(L::kBarKVFull + slot), pnl * kPanel, w.hk, kw.load_row, w.b);
             }
           }
           if (j >= 1) {
@@ -342,9 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int pnl = 0; pnl < kDPanels; ++pnl) {
               const uint32_t dst = sbase + L::kKVTileBytes + pnl * L::kKVPanelBytes;
               if constexpr (VARLEN)
-                ptx::tma_load_3d(dst, &tm_v, bar(L::kBarKVFull + slot), pnl * kPanel, w.h, vw.load_row);
+                ptx::tma_load_3d(dst, &tm_v, bar(L::kBarKVFull + slot), pnl * kPanel, w.hk, vw.load_row);
               else
-                ptx::tma_load_4d(dst, &tm_v, bar(L::kBarKVFull + slot), pnl * kPanel, w.h, vw.load_row, w.b);
+                ptx::tma_load_4d(dst, &tm_v, bar(L::kBarKVFull + slot), pnl * kPanel, w.hk, vw.load_row, w.b);
             }
           }
         }
@@ -367,8 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t uc[kQT] = {0, 0};  // units with the tile active, per tile
       bool ok = true;
 #pragma unroll 1
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-        const Unit w = decode_unit<BC, VARLEN>(p, u);
+      FA_FOR_EACH_UNIT(u) {
+        const Unit w = decode_unit<BC, VARLEN, CAUSAL>(p, u);
         if (!w.run) continue;
         if (!ptx::mbar_wait(bar(L::kBarQFull), qcount & 1u, s_abort, tmo)) {
           record_error(p.status, kErrTimeout, kSiteMmaQ);
@@ -391,10 +439,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int t = 0; t < kQT; ++t) {
             if (!w.active[t]) continue;
+            const int nt = t == 0 ? w.nt[0] : w.nt[1];
             const uint32_t tS = tmem + static_cast<uint32_t>(t * BC);
             const uint32_t tP = tS + BC / 2;
             const uint32_t tO = tmem + static_cast<uint32_t>(2 * BC + t * D);
-            if (j >= 1) {
+            if (j >= 1 && j <= nt) {
               // O_t += P_t(j-1) V(j-1), once P is written and O rescaled.
               if (!ptx::mbar_wait(bar(L::kBarPFull + t), pc[t] & 1u, s_abort, tmo)) {
                 record_error(p.status, kErrTimeout, kSiteMmaP);
@@ -417,9 +466,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t bdesc = ptx::sw128_desc(v_base + kk * 2048, L::kKVPanelBytes, 1024);
                 ptx::mma_ts(tO, tP + kk * 8, bdesc, idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
               }
-              if (j == w.nkv) ptx::mma_commit(bar(L::kBarOFinal + t));
+              if (j == nt) ptx::mma_commit(bar(L::kBarOFinal + t));
             }
-            if (j < w.nkv) {
+            if (j < nt) {
               // S_t = Q_t K(j)^T
               const uint32_t q_base = base + L::kOffQ + t * L::kQTileBytes;
 #pragma unroll
@@ -448,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ptx::mbar_wait_drain(bar(L::kBarTeardown), 0, tmo)) record_error(p.status, kErrTimeout, kSiteTeardown);
     }
   } else if (warp < 8) {
-    ptx::setmaxnreg_inc<kRegSoftmax>();
+    ptx::setmaxnreg_inc<RegSplit<VARLEN>::kSoftmax>();
     // ================================================================ softmax
     const int t = warp >> 2;
     const int row = ((warp & 3) << 5) + lane;
@@ -459,15 +508,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t sc = 0;  // S-full completions consumed
     bool ok = true;
 #pragma unroll 1
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-      const Unit w = decode_unit<BC, VARLEN>(p, u);
+    FA_FOR_EACH_UNIT(u) {
+      const Unit w = decode_unit<BC, VARLEN, CAUSAL>(p, u);
       const bool active = t == 0 ? w.active[0] : w.active[1];
       if (!active) continue;
       const RowWindow qw = t == 0 ? w.qwin[0] : w.qwin[1];
+      const int nt = t == 0 ? w.nt[0] : w.nt[1];
+      // Causal: this row sees sequence keys <= i_row + off.
+      const int key_lim = (qw.load_row - w.q_start + row) + w.off;
+      const int first_row_lim = (qw.load_row - w.q_start + qw.lo) + w.off;
+      // Only the last key tile (ragged end, shifted variable-length window) and,
+      // when causal, the tiles from the first one crossing the diagonal need masks.
+      const int nkv_all = (w.k_end - w.k_start + BC - 1) / BC;
+      int j_mask = nkv_all - 1;
+      if constexpr (CAUSAL) j_mask = min(j_mask, first_row_lim + 1 < 0 ? 0 : (first_row_lim + 1) / BC);
       float m_ref = -INFINITY;
       float l = 0.f;
 #pragma unroll 1
-      for (int j = 0; j < w.nkv; ++j) {
+      for (int j = 0; j < nt; ++j) {
         if (!ptx::mbar_wait_warp(bar(L::kBarSFull + t), sc & 1u, s_abort, tmo)) {
           record_error(p.status, kErrTimeout, kSiteSoftS);
           ok = false;
@@ -482,14 +540,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         float s[BC];
 #pragma unroll
         for (int c = 0; c < BC; ++c) s[c] = __uint_as_float(sr[c]);
-        if (j == w.nkv - 1 || VARLEN) {
-          // Keys outside [lo, hi) of this tile: past the end, or (variable
-          // length) before the sequence start / already seen by the previous tile.
+        if (j >= j_mask) {
           const RowWindow kw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + j * BC, BC);
           if (kw.lo != 0 || kw.hi != BC) {
+            // Keys outside [lo, hi) of this tile: past the end, or (variable
+            // length) before the sequence start / already seen by the previous tile.
 #pragma unroll
             for (int c = 0; c < BC; ++c)
               if (c < kw.lo || c >= kw.hi) s[c] = -INFINITY;
+          }
+          const int kbase = kw.load_row - w.k_start;  // sequence index of column 0
+          if (CAUSAL && kbase + BC - 1 > first_row_lim) {
+            // The tile crosses the diagonal: mask keys above this row's limit.
+            const int lim = key_lim - kbase;
+#pragma unroll
+            for (int c = 0; c < BC; ++c)
+              if (c > lim) s[c] = -INFINITY;
           }
         }
         // Row max: four independent chains of three-input maxima.
@@ -574,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_arrive(bar(L::kBarLReady + t));
     }
   } else {
-    ptx::setmaxnreg_dec<kRegCorrection>();
+    ptx::setmaxnreg_dec<RegSplit<VARLEN>::kCorrection>();
     // ================================================= correction + epilogue
     const int wq = warp & 3;
     const int row = (wq << 5) + lane;
@@ -585,8 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool pending = false;  // a TMA store from the staging area may still be reading it
     bool ok = true;
 #pragma unroll 1
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-      const Unit w = decode_unit<BC, VARLEN>(p, u);
+    FA_FOR_EACH_UNIT(u) {
+      const Unit w = decode_unit<BC, VARLEN, CAUSAL>(p, u);
       if (w.nokeys) {
         // No keys: o = 0 and LSE = -inf (log of an empty sum).
         const int rows = min(kBR * kQT, w.q_end - w.q_row0);
@@ -601,6 +667,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int t = 0; t < kQT; ++t) {
+        if (w.zero[t]) {
+          // Causal rows that see no key: o = 0 and LSE = -inf.
+          const RowWindow zw = w.qwin[t];
+          const size_t rs = static_cast<size_t>(p.H) * D;
+          for (int e = threadIdx.x - 256; e < kBR * D; e += 128) {
+            const int r = e / D, c = e % D;
+            if (r >= zw.lo && r < zw.hi)
+              p.o[static_cast<size_t>(zw.load_row + r) * rs + static_cast<size_t>(w.h) * D + c] = __float2bfloat16(0.f);
+          }
+          for (int r = threadIdx.x - 256; r < kBR; r += 128)
+            if (r >= zw.lo && r < zw.hi) p.lse[w.lse_base + (zw.load_row - w.q_start + r)] = -INFINITY;
+        }
         if (!w.active[t]) continue;
         if (!ptx::mbar_wait_warp(bar(L::kBarLReady + t), uc[t] & 1u, s_abort, tmo) ||
             !ptx::mbar_wait_warp(bar(L::kBarOFinal + t), uc[t] & 1u, s_abort, tmo)) {

@@ -24,14 +24,14 @@ constexpr int smem_bytes() {
   return SmemLayout<D, kBC, STAGES>::kAlloc;
 }
 
-template <int D, int STAGES, bool VARLEN>
+template <int D, int STAGES, bool VARLEN, bool CAUSAL>
 cudaError_t launch_fwd(const LaunchArgs& a);
 
 // Defined in the translation unit that owns the kernel.
-#define FA_DEFINE_LAUNCH(D, STAGES, VARLEN)                                                   \
+#define FA_DEFINE_LAUNCH(D, STAGES, VARLEN, CAUSAL)                                           \
   template <>                                                                                 \
-  cudaError_t launch_fwd<D, STAGES, VARLEN>(const LaunchArgs& a) {                            \
-    auto* kern = &fa_fwd_kernel<D, kBC, STAGES, VARLEN>;                                      \
+  cudaError_t launch_fwd<D, STAGES, VARLEN, CAUSAL>(const LaunchArgs& a) {                    \
+    auto* kern = &fa_fwd_kernel<D, kBC, STAGES, VARLEN, CAUSAL>;                              \
     constexpr int smem = SmemLayout<D, kBC, STAGES>::kAlloc;                                  \
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); \
     if (e != cudaSuccess) return e;                                                           \

@@ -41,12 +41,18 @@ class Workload:
     def varlen(self) -> bool:
         return self.lengths is not None
 
-    def flops(self) -> float:
+    def flops(self, causal: bool = False) -> float:
         """Matmul FLOPs, 4 * B * H * Nq * Nk * d ("GPU 内核与 FlashAttention" §10);
-        variable-length: sum over sequences of 4 * H * len^2 * d."""
+        variable-length: sum over sequences of 4 * H * len^2 * d.  Causal: only the
+        visible (query, key) pairs count, query i seeing keys j <= i + Nk - Nq."""
+        def pairs(nq, nk):
+            if not causal:
+                return nq * nk
+            off = nk - nq
+            return sum(min(nk, max(0, i + off + 1)) for i in range(nq))
         if self.varlen:
-            return float(sum(4 * self.H * n * n * self.d for n in self.lengths))
-        return 4.0 * self.B * self.H * self.Nq * self.Nk * self.d
+            return float(sum(4 * self.H * pairs(n, n) * self.d for n in self.lengths))
+        return 4.0 * self.B * self.H * pairs(self.Nq, self.Nk) * self.d
 
     def hbm_bytes(self) -> float:
         """Algorithmic HBM bytes: Q, K, V read once, O written once (bf16), LSE

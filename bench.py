@@ -244,9 +244,9 @@ def run_reference(args, w):
     return 0
 
 
-def workload_config(w, kernel_cfg):
+def workload_config(w, kernel_cfg, causal=False):
     cfg = {"workload": "%s: %s" % (w.name, w.note or ""), "B": w.B, "H": w.H, "d": w.d,
-           "layout": "[batch, seq, heads, d_head] bf16", "causal": False,
+           "layout": "[batch, seq, heads, d_head] bf16", "causal": bool(causal),
            "l2": "inputs and output larger than L2 (no flush needed)",
            "parallelism": "replicas (one full workload per GPU, no collective)"}
     if w.varlen:
@@ -283,9 +283,9 @@ def run_ours(args, w):
 
     def step():
         if w.varlen:
-            fa.forward(dq, dk, dv, cu_seqlens=dcu, max_seqlen=maxlen, out=o, lse=lse)
+            fa.forward(dq, dk, dv, cu_seqlens=dcu, max_seqlen=maxlen, out=o, lse=lse, causal=args.causal)
         else:
-            fa.forward_qk(dq, dk, dv, out=o, lse=lse)
+            fa.forward_qk(dq, dk, dv, out=o, lse=lse, causal=args.causal)
 
     if args.autotune:
         if w.varlen:
@@ -319,7 +319,7 @@ def run_ours(args, w):
     if rc != fa.FA_OK:
         raise SystemExit("device error in the timed region: %s %s" % (fa.strerror(rc), info))
     ms_max = max_over_ranks(ms, world)
-    flops = w.flops()
+    flops = w.flops(causal=args.causal)
     value = world * flops / (ms_max * 1e-3) / 1e12
     kernel_tflops = flops / (ms * 1e-3) / 1e12  # one launch per step, this rank
 
@@ -367,7 +367,7 @@ def run_ours(args, w):
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1), generated on the host)",
-        "config": workload_config(w, kernel_cfg),
+        "config": workload_config(w, kernel_cfg, args.causal),
         "pct_of_peak": 100.0 * kernel_tflops / peak,
         "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": UNIT,
                      "frac": kernel_tflops / peak, "traffic": traffic,
@@ -403,6 +403,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="page", choices=sorted(I.WORKLOADS))
     ap.add_argument("--autotune", action="store_true", help="tune the kernel config first")
+    ap.add_argument("--causal", action="store_true",
+                    help="causal mask (FLOPs count the visible query/key pairs only)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

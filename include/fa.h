@@ -85,6 +85,25 @@ int fa_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse, 
               const int* cu_seqlens_k, void* stream);
 
 /*
+ * fa_fwd_ex -- the general entry: fa_fwd_qk plus grouped key/value heads and
+ * flags.
+ *   Hk    : key/value heads; H must be a multiple of Hk.  Query head h reads
+ *           key/value head h / (H / Hk) ("GPU 内核与 FlashAttention" §14.2,
+ *           MQA / GQA).  k and v are [B, Nk, Hk, d] (dense) or
+ *           [total_k, Hk, d] (variable length); q, o and lse are as in fa_fwd_qk.
+ *   flags : 0, or FA_FLAG_CAUSAL for the causal mask of §14.4, aligned
+ *           bottom-right when the lengths differ: query i sees keys
+ *           j <= i + (Nk - Nq) (per sequence in the variable-length form).
+ *           Key tiles above the diagonal are skipped.  Rows that see no key
+ *           get o = 0 and lse = -inf.
+ * Unknown flag bits, Hk <= 0 or H % Hk != 0 give FA_ERR_INVALID_ARG.
+ */
+#define FA_FLAG_CAUSAL 1
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Nq,
+              int Nk, int H, int Hk, int d, float scale, const int* cu_seqlens_q,
+              const int* cu_seqlens_k, int flags, void* stream);
+
+/*
  * fa_check_status -- synchronises `stream`, then returns and clears the first
  * device-side error recorded since the last call (FA_OK if none).  When
  * `info` is not NULL it receives {flat block index, warp, wait site} of that

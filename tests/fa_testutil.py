@@ -11,18 +11,18 @@ O_TOL = 2e-2
 LSE_TOL = 1e-3
 
 
-def gpu_dense(q, k, v, scale=None):
-    """CPU bf16 q [B,Nq,H,d], k/v [B,Nk,H,d] -> (o float64 [B,Nq,H,d], lse float64 [B,H,Nq])."""
+def gpu_dense(q, k, v, scale=None, causal=False):
+    """CPU bf16 q [B,Nq,H,d], k/v [B,Nk,Hk,d] -> (o float64 [B,Nq,H,d], lse float64 [B,H,Nq])."""
     dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
-    o, lse = fa.forward_qk(dq, dk, dv, scale)
+    o, lse = fa.forward_qk(dq, dk, dv, scale, causal=causal)
     rc, info = fa.check_status()
     assert rc == fa.FA_OK, (fa.strerror(rc), info)
     return o.to(torch.float64).cpu().numpy(), lse.to(torch.float64).cpu().numpy()
 
 
-def gpu_varlen(q, k, v, cu_q, cu_k, max_q, max_k, scale=None):
+def gpu_varlen(q, k, v, cu_q, cu_k, max_q, max_k, scale=None, causal=False):
     dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
-    o, lse = fa.forward_qk(dq, dk, dv, scale, cu_q.cuda(), cu_k.cuda(), max_q, max_k)
+    o, lse = fa.forward_qk(dq, dk, dv, scale, cu_q.cuda(), cu_k.cuda(), max_q, max_k, causal=causal)
     rc, info = fa.check_status()
     assert rc == fa.FA_OK, (fa.strerror(rc), info)
     return o.to(torch.float64).cpu().numpy(), lse.to(torch.float64).cpu().numpy()
@@ -36,6 +36,11 @@ def max_errs(o, lse, o_ref, lse_ref):
 
 
 def assert_close(o, lse, o_ref, lse_ref, what=""):
+    # Rows that see no key: LSE must be -inf on both sides (compared separately).
+    lse, lse_ref = np.asarray(lse), np.asarray(lse_ref)
+    empty = np.isneginf(lse_ref)
+    assert np.array_equal(np.isneginf(lse), empty), "%s: rows without keys differ" % what
+    lse, lse_ref = np.where(empty, 0.0, lse), np.where(empty, 0.0, lse_ref)
     eo, el = max_errs(o, lse, o_ref, lse_ref)
     assert eo <= O_TOL and el <= LSE_TOL, "%s: max|dO|=%.3g (tol %g) max|dLSE|=%.3g (tol %g)" % (
         what, eo, O_TOL, el, LSE_TOL)

@@ -135,3 +135,14 @@ def test_product_package_never_touches_the_oracle():
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "attn_ref" not in text and "liboracle" not in text, f
+
+
+def test_ex_form_argument_errors(L):
+    ex = L.fa_fwd_ex
+    # H not a multiple of Hk, Hk = 0, unknown flag bits
+    assert ex(A, A, A, A, A, 1, 8, 8, 6, 4, 128, 0.1, None, None, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert ex(A, A, A, A, A, 1, 8, 8, 4, 0, 128, 0.1, None, None, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert ex(A, A, A, A, A, 1, 8, 8, 4, 2, 128, 0.1, None, None, 4, None) == fa.FA_ERR_INVALID_ARG
+    assert ex(A, A, A, A, A, 1, 8, 8, 4, -1, 128, 0.1, None, None, 0, None) == fa.FA_ERR_INVALID_ARG
+    # empty problems stay no-ops with the causal flag
+    assert ex(A, A, A, A, A, 0, 8, 8, 4, 2, 128, 0.1, None, None, fa.FA_FLAG_CAUSAL, None) == fa.FA_OK

@@ -254,3 +254,71 @@ def test_wait_timeout_is_reported_and_device_stays_usable(oracle_mod):
     o, lse = gpu_dense(q, k, v)
     o_ref, lse_ref = _oracle_dense(oracle_mod, q, k, v)
     assert_close(o, lse, o_ref, lse_ref, "after timeout")
+
+
+# ------------------------------------------------- causal and grouped heads
+def _make_gqa(B, Nq, Nk, H, Hk, d, seed):
+    g = torch.Generator().manual_seed(seed)
+    return (I.randn_bf16((B, Nq, H, d), g), I.randn_bf16((B, Nk, Hk, d), g),
+            I.randn_bf16((B, Nk, Hk, d), g))
+
+
+@pytest.mark.parametrize("B,Nq,Nk,H,Hk,d", [
+    (1, 256, 256, 2, 2, 128), (2, 300, 300, 2, 1, 128), (1, 129, 513, 2, 2, 64),
+    (1, 513, 129, 2, 2, 128), (1, 1000, 1000, 4, 2, 128), (1, 1, 1, 1, 1, 128),
+    (1, 64, 4096, 1, 1, 128), (2, 700, 700, 3, 3, 64), (1, 384, 256, 2, 1, 64),
+])
+def test_causal_full_parity(oracle_mod, B, Nq, Nk, H, Hk, d):
+    q, k, v = _make_gqa(B, Nq, Nk, H, Hk, d, 2000 + Nq + Nk + d)
+    o, lse = gpu_dense(q, k, v, causal=True)
+    o_ref, lse_ref = oracle_mod.attn_dense(bits(q), bits(k), bits(v), causal=True)
+    assert_close(o, lse, o_ref, lse_ref, "causal %s" % ((B, Nq, Nk, H, Hk, d),))
+
+
+@pytest.mark.parametrize("H,Hk,d", [(8, 1, 128), (8, 2, 128), (8, 4, 64), (6, 3, 128)])
+def test_grouped_heads_full_parity(oracle_mod, H, Hk, d):
+    q, k, v = _make_gqa(2, 300, 517, H, Hk, d, 3000 + H + Hk + d)
+    o, lse = gpu_dense(q, k, v)
+    o_ref, lse_ref = oracle_mod.attn_dense(bits(q), bits(k), bits(v))
+    assert_close(o, lse, o_ref, lse_ref, "gqa H%d Hk%d d%d" % (H, Hk, d))
+
+
+@pytest.mark.parametrize("Hk", [3, 1])
+def test_causal_varlen_full_parity(oracle_mod, Hk):
+    lens_q = [1, 127, 128, 129, 300, 256, 40, 700]
+    lens_k = [1, 130, 128, 100, 300, 600, 260, 700]
+    H, d = 3, 128
+    cu_q = torch.tensor([0] + list(np.cumsum(lens_q)), dtype=torch.int32)
+    cu_k = torch.tensor([0] + list(np.cumsum(lens_k)), dtype=torch.int32)
+    g = torch.Generator().manual_seed(70 + Hk)
+    q = I.randn_bf16((int(cu_q[-1]), H, d), g)
+    k = I.randn_bf16((int(cu_k[-1]), Hk, d), g)
+    v = I.randn_bf16((int(cu_k[-1]), Hk, d), g)
+    o, lse = gpu_varlen(q, k, v, cu_q, cu_k, max(lens_q), max(lens_k), causal=True)
+    o_ref, lse_ref = oracle_mod.attn_varlen(bits(q), bits(k), bits(v), cu_q.numpy(), cu_k.numpy(),
+                                            max(lens_q), causal=True)
+    valid = ~np.isnan(lse_ref)
+    assert_close(o, lse[valid], o_ref, lse_ref[valid], "causal varlen Hk%d" % Hk)
+
+
+def test_causal_page_workload_sampled(oracle_mod):
+    w = I.PAGE
+    q, k, v, _, _ = I.make(w)
+    o, lse = gpu_dense(q, k, v, causal=True)
+    rows = sample_rows(w.B, w.Nq, w.H, n_random=64, seed=77)
+    o_ref, lse_ref = oracle_mod.attn_dense_rows(bits(q), bits(k), bits(v), rows, causal=True)
+    b, h, i = rows[:, 0], rows[:, 1], rows[:, 2]
+    assert_close(o[b, i, h, :], lse[b, h, i], o_ref, lse_ref, "causal page")
+
+
+@pytest.mark.parametrize("spec", ["stages=2,threshold=0", "stages=4,threshold=8"])
+def test_causal_gqa_configs(oracle_mod, spec):
+    fa.set_config(spec)
+    try:
+        for d in (64, 128):
+            q, k, v = _make_gqa(1, 400, 333, 4, 2, d, 80 + d)
+            o, lse = gpu_dense(q, k, v, causal=True)
+            o_ref, lse_ref = oracle_mod.attn_dense(bits(q), bits(k), bits(v), causal=True)
+            assert_close(o, lse, o_ref, lse_ref, spec + " d%d" % d)
+    finally:
+        fa.set_config(None)
