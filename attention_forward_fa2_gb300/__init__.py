@@ -37,7 +37,8 @@ FA_FLAG_CAUSAL = 1
 EXPORTS = (
     "fa_fwd", "fa_fwd_qk", "fa_fwd_ex", "fa_check_status", "fa_strerror", "fa_last_cuda_error",
     "fa_set_timeout_ns", "fa_set_config", "fa_get_config", "fa_autotune",
-    "fa_selftest_wait_timeout", "fa_version",
+    "fa_selftest_wait_timeout", "fa_version", "fa_splitkv_num_splits",
+    "fa_splitkv_workspace_bytes", "fa_fwd_splitkv",
 )
 
 
@@ -78,9 +79,14 @@ def lib() -> ctypes.CDLL:
         L.fa_autotune.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, vp, vp]
         L.fa_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, vp]
         L.fa_version.argtypes = []
+        L.fa_splitkv_num_splits.argtypes = [ci, ci, ci, ci, ci, ci]
+        L.fa_splitkv_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
+        L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp,
+                                     ctypes.c_ulonglong, vp]
         for name in EXPORTS:
             if name != "fa_strerror":
                 getattr(L, name).restype = ci
+        L.fa_splitkv_workspace_bytes.restype = ctypes.c_longlong
         _lib = L
         return L
 
@@ -96,6 +102,26 @@ def fa_fwd_qk(q, k, v, o, lse, B, Nq, Nk, H, d, scale, cu_q, cu_k, stream) -> in
 
 def fa_fwd_ex(q, k, v, o, lse, B, Nq, Nk, H, Hk, d, scale, cu_q, cu_k, flags, stream) -> int:
     return lib().fa_fwd_ex(q, k, v, o, lse, B, Nq, Nk, H, Hk, d, scale, cu_q, cu_k, flags, stream)
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, B, Nq, Nk, H, Hk, d, scale, flags, num_splits, workspace,
+                   workspace_bytes, stream) -> int:
+    return lib().fa_fwd_splitkv(q, k, v, o, lse, B, Nq, Nk, H, Hk, d, scale, flags, num_splits,
+                                workspace, workspace_bytes, stream)
+
+
+def splitkv_num_splits(B, Nq, Nk, H, d, requested=0) -> int:
+    n = lib().fa_splitkv_num_splits(B, Nq, Nk, H, d, int(requested))
+    if n < 0:
+        raise FaError(n, "fa_splitkv_num_splits")
+    return n
+
+
+def splitkv_workspace_bytes(B, Nq, H, d, num_splits) -> int:
+    n = lib().fa_splitkv_workspace_bytes(B, Nq, H, d, int(num_splits))
+    if n < 0:
+        raise FaError(int(n), "fa_splitkv_workspace_bytes")
+    return int(n)
 
 
 def fa_check_status(stream=None):
@@ -262,3 +288,38 @@ def autotune(q, k, v, scale=None, cu_seqlens=None, max_seqlen=None, stream=None)
     if rc != FA_OK:
         raise FaError(rc, "fa_autotune")
     return get_config(d, N, varlen)
+
+
+def forward_splitkv(q, k, v, scale=None, causal=False, num_splits=None, workspace=None, out=None,
+                    lse=None, stream=None):
+    """Key-split form for short query sets (dense q [B, Nq, H, d], k/v
+    [B, Nk, Hk, d]).  num_splits None / 0 lets the library choose; workspace is
+    a CUDA tensor of at least splitkv_workspace_bytes(...) bytes (allocated here
+    through torch when None).  Returns (o, lse) like forward_qk."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_tensor(name, t, torch.bfloat16, 4)
+    B, Nq, H, d = q.shape
+    Nk, Hk = k.shape[1], k.shape[2]
+    if k.shape != (B, Nk, Hk, d) or v.shape != k.shape:
+        raise ValueError("k/v shape mismatch")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    with torch.cuda.device(q.device):
+        splits = splitkv_num_splits(B, Nq, Nk, H, d, num_splits or 0)
+        need = splitkv_workspace_bytes(B, Nq, H, d, splits)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        elif not workspace.is_cuda:
+            raise ValueError("workspace must be a CUDA tensor")
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+        rc = fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                            B, Nq, Nk, H, Hk, d, float(scale), FA_FLAG_CAUSAL if causal else 0,
+                            splits, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                            _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_splitkv")
+    return out, lse

@@ -15,6 +15,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <string>
@@ -215,16 +216,11 @@ int validate(const Problem& P) {
   return FA_OK;
 }
 
-int run(const Problem& P, const Config& cfg) {
-  const int rc = validate(P);
-  if (rc != FA_OK) return rc == 1 ? FA_OK : rc;
-  DeviceState* st = nullptr;
-  const int drc = device_state(&st);
-  if (drc != FA_OK) return drc;
+// Encodes the tensor maps and fills the kernel parameters shared by every
+// form (grid left to the caller).  Expects a validated, non-empty problem.
+int prepare(const Problem& P, const Config& cfg, DeviceState* st, fa::LaunchArgs& a) {
   const bool varlen = P.cu_q != nullptr;
   const int D = P.d;
-
-  fa::LaunchArgs a;
   std::memset(&a, 0, sizeof(a));
   const cuuint64_t esz = 2;
   if (!varlen) {
@@ -281,15 +277,100 @@ int run(const Problem& P, const Config& cfg) {
     p.timeout_ns = g_timeout_ns;
   }
   p.status = st->status;
+  p.num_splits = 1;
+  p.split_tiles = 0;
+  a.stream = P.stream;
+  return FA_OK;
+}
+
+int run(const Problem& P, const Config& cfg) {
+  const int rc = validate(P);
+  if (rc != FA_OK) return rc == 1 ? FA_OK : rc;
+  DeviceState* st = nullptr;
+  const int drc = device_state(&st);
+  if (drc != FA_OK) return drc;
+  const bool varlen = P.cu_q != nullptr;
+  const int D = P.d;
+  fa::LaunchArgs a;
+  const int prc = prepare(P, cfg, st, a);
+  if (prc != FA_OK) return prc;
+  fa::FwdParams& p = a.p;
   // Persistent grid: one CTA per SM (each walks items blockIdx.x + k * gridDim.x).
   a.grid = dim3(static_cast<unsigned>(p.num_items < st->num_sms ? p.num_items : st->num_sms), 1, 1);
-  a.stream = P.stream;
 
   cudaError_t e;
   if (p.causal)
     e = varlen ? dispatch<true, true>(D, cfg.stages, a) : dispatch<false, true>(D, cfg.stages, a);
   else
     e = varlen ? dispatch<true, false>(D, cfg.stages, a) : dispatch<false, false>(D, cfg.stages, a);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
+constexpr int kMaxSplits = 128;
+
+// Key tiles per split for a requested number of splits (<= 0: choose one).
+// Chooses enough splits to give every SM a unit, at least two key tiles per
+// split, at most kMaxSplits.
+int split_tiles_for(int B, int Nq, int Nk, int H, int num_sms, int requested) {
+  const int nkv = (Nk + fa::kBC - 1) / fa::kBC;
+  if (nkv <= 0) return 1;
+  int splits = requested;
+  if (splits <= 0) {
+    const long long units = static_cast<long long>(B) * H * ((Nq + fa::kBR * fa::kQT - 1) / (fa::kBR * fa::kQT));
+    splits = units >= num_sms ? 1 : static_cast<int>(num_sms / units);
+    splits = std::min(splits, (nkv + 1) / 2);
+  }
+  splits = std::max(1, std::min(std::min(splits, nkv), kMaxSplits));
+  return (nkv + splits - 1) / splits;
+}
+
+int splits_for_tiles(int Nk, int tiles) {
+  const int nkv = (Nk + fa::kBC - 1) / fa::kBC;
+  return nkv <= 0 ? 1 : (nkv + tiles - 1) / tiles;
+}
+
+size_t split_workspace_bytes(int B, int Nq, int H, int d, int splits) {
+  const size_t rows = static_cast<size_t>(B) * H * Nq;
+  return static_cast<size_t>(splits) * rows * (static_cast<size_t>(d) + 1) * sizeof(float);
+}
+
+// The key-split form: partial results into ws (fp32, [S, rows, d] then
+// [S, rows]), then the combine kernel.  Dense tensors only.
+int run_split(const Problem& P, const Config& cfg, int requested_splits, void* ws, size_t ws_bytes) {
+  if (P.cu_q != nullptr || P.cu_k != nullptr) return FA_ERR_INVALID_ARG;
+  const int rc = validate(P);
+  if (rc != FA_OK) return rc == 1 ? FA_OK : rc;
+  DeviceState* st = nullptr;
+  const int drc = device_state(&st);
+  if (drc != FA_OK) return drc;
+  const int tiles = split_tiles_for(P.B, P.Nq, P.Nk, P.H, st->num_sms, requested_splits);
+  const int splits = splits_for_tiles(P.Nk, tiles);
+  const size_t need = split_workspace_bytes(P.B, P.Nq, P.H, P.d, splits);
+  if (ws == nullptr || ws_bytes < need || !aligned16(ws)) return FA_ERR_INVALID_ARG;
+  fa::LaunchArgs a;
+  const int prc = prepare(P, cfg, st, a);
+  if (prc != FA_OK) return prc;
+  fa::FwdParams& p = a.p;
+  const long long units = static_cast<long long>(p.num_units) * splits;
+  if (units > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  p.num_splits = splits;
+  p.split_tiles = tiles;
+  p.num_units = static_cast<int>(units);
+  p.units_per_item = 1;
+  p.num_items = p.num_units;
+  const size_t rows = static_cast<size_t>(P.B) * P.H * P.Nq;
+  p.ws_o = static_cast<float*>(ws);
+  p.ws_lse = p.ws_o + static_cast<size_t>(splits) * rows * P.d;
+  a.grid = dim3(static_cast<unsigned>(p.num_items < st->num_sms ? p.num_items : st->num_sms), 1, 1);
+  cudaError_t e;
+  if (P.d == 128)
+    e = p.causal ? fa::launch_fwd_split<128, 2, true>(a) : fa::launch_fwd_split<128, 2, false>(a);
+  else
+    e = p.causal ? fa::launch_fwd_split<64, 3, true>(a) : fa::launch_fwd_split<64, 3, false>(a);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = fa::launch_combine(P.d, p.ws_o, p.ws_lse, splits, static_cast<long long>(rows), P.H, P.Nq,
+                         static_cast<__nv_bfloat16*>(P.o), P.lse, P.stream);
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;
 }
@@ -459,6 +540,28 @@ int fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;
+}
+
+int fa_splitkv_num_splits(int B, int Nq, int Nk, int H, int d, int requested) {
+  if (B < 0 || Nq < 0 || Nk < 0 || H < 0 || (d != 64 && d != 128)) return FA_ERR_INVALID_ARG;
+  DeviceState* st = nullptr;
+  const int drc = device_state(&st);
+  if (drc != FA_OK) return drc;
+  return splits_for_tiles(Nk, split_tiles_for(B, Nq, Nk, H, st->num_sms, requested));
+}
+
+long long fa_splitkv_workspace_bytes(int B, int Nq, int H, int d, int num_splits) {
+  if (B < 0 || Nq < 0 || H < 0 || (d != 64 && d != 128) || num_splits < 1 || num_splits > kMaxSplits)
+    return FA_ERR_INVALID_ARG;
+  return static_cast<long long>(split_workspace_bytes(B, Nq, H, d, num_splits));
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Nq,
+                   int Nk, int H, int Hk, int d, float scale, int flags, int num_splits,
+                   void* workspace, unsigned long long workspace_bytes, void* stream) {
+  Problem P{q, k, v, o, lse, B, Nq, Nk, H, Hk, d, scale, nullptr, nullptr, flags,
+            static_cast<cudaStream_t>(stream)};
+  return run_split(P, pick_config(d, Nk, 0), num_splits, workspace, static_cast<size_t>(workspace_bytes));
 }
 
 int fa_version(void) { return 100; }

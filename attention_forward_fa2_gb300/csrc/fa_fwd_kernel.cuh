@@ -51,6 +51,11 @@
 // Grouped key/value heads (§14.2, MQA/GQA): query head h reads key/value head
 // h / G; K and V are never replicated in memory.
 //
+// Split keys (SPLIT): for short query sets a unit covers only a range of key
+// tiles; its normalised fp32 output and log-sum-exp go to a workspace, and a
+// second kernel merges the splits with the two-block merge of §11.2
+// (LSE = log sum_s e^LSE_s, O = sum_s e^(LSE_s - LSE) O_s), which is exact.
+//
 // Scale folding ("Flash Attention 2 Chapter6", Kernel 6): p = 2^(s * c - m * c)
 // with c = scale * log2(e), one FFMA feeding the ex2 unit per score.
 #pragma once
@@ -99,6 +104,10 @@ struct FwdParams {
   int num_units;               // B * H * num_mblocks
   int units_per_item;          // units a CTA takes at a time (2 when causal: a balanced pair)
   int num_items;               // ceil(num_units / units_per_item)
+  int num_splits;              // key splits per query block (1 unless split)
+  int split_tiles;             // key tiles per split
+  float* ws_o;                 // split: [num_splits, B, H, Nq, D] fp32 partial outputs
+  float* ws_lse;               // split: [num_splits, B, H, Nq] fp32 partial log-sum-exp
   const int* cu_q;             // variable-length form: int32 [B + 1]
   const int* cu_k;
   float* lse;                  // [B, H, Nq] fp32
@@ -189,6 +198,9 @@ struct Unit {
   int q_row0;                          // first query row of the unit
   int off;                             // causal: query i sees keys j <= i + off
   int nkv;                             // key/value steps of the unit (max over its tiles)
+  int j0;                              // first key tile of the unit (split)
+  int split;                           // split index
+  int nkv_all;                         // key tiles of the whole sequence
   int lse_base;                        // (b * H + h) * Nq
   bool run;                            // some tile of the unit has rows and visible keys
   bool nokeys;                         // query rows but no keys at all (variable length only)
@@ -199,9 +211,14 @@ struct Unit {
 };
 
 // Every role decodes the same unit identically (pure function of u and params).
-template <int BC, bool VARLEN, bool CAUSAL>
+template <int BC, bool VARLEN, bool CAUSAL, bool SPLIT>
 __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   Unit w;
+  w.split = 0;
+  if constexpr (SPLIT) {
+    w.split = u % p.num_splits;
+    u /= p.num_splits;
+  }
   int mb = u % p.num_mblocks;
   if constexpr (CAUSAL) {
     // Zigzag order within a head: last, first, second last, second, ... so that
@@ -230,6 +247,9 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   w.q_row0 = w.q_start + mb * (kBR * kQT);
   w.off = (w.k_end - w.k_start) - (w.q_end - w.q_start);
   const int nkv_all = bad ? 0 : (w.k_end - w.k_start + BC - 1) / BC;
+  w.nkv_all = nkv_all;
+  w.j0 = SPLIT ? w.split * p.split_tiles : 0;
+  const int nkv_here = SPLIT ? max(0, min(p.split_tiles, nkv_all - w.j0)) : nkv_all;
   w.lse_base = (w.b * p.H + w.h) * p.Nq;
   const bool has_rows = !bad && w.q_row0 < w.q_end;
   w.nkv = 0;
@@ -238,20 +258,21 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
     const int r0 = w.q_row0 + t * kBR;
     w.qwin[t] = make_window<VARLEN>(w.q_start, w.q_end, r0, kBR);
     const bool rows = has_rows && r0 < w.q_end;
-    int n = nkv_all;
+    int n = nkv_here;
     if (CAUSAL && rows) {
       // Last valid row of the tile, in sequence coordinates, and the last key it sees.
       const int i_last = w.qwin[t].load_row - w.q_start + w.qwin[t].hi - 1;
       const int key_last = i_last + w.off;
-      n = key_last < 0 ? 0 : min(nkv_all, key_last / BC + 1);
+      n = key_last < 0 ? 0 : min(nkv_here, key_last / BC + 1 - w.j0);
+      n = max(n, 0);
     }
     w.nt[t] = rows ? n : 0;
     w.active[t] = rows && n > 0;
-    w.zero[t] = rows && n == 0 && nkv_all > 0;
+    w.zero[t] = rows && n == 0 && (nkv_all > 0 || SPLIT);
     w.nkv = max(w.nkv, w.nt[t]);
   }
   w.run = w.active[0] || w.active[1];
-  w.nokeys = has_rows && nkv_all == 0;
+  w.nokeys = has_rows && nkv_all == 0 && !SPLIT;
   if (bad && mb == 0 && w.h == 0) {
     if ((threadIdx.x & 31) == 0 && threadIdx.x < 32) record_error(p.status, kErrBadSeqlens, 0);
   }
@@ -266,7 +287,7 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
     for (int sub_ = 0, u = it_ * p.units_per_item;                                     \
          sub_ < p.units_per_item && u < p.num_units && ok; ++sub_, ++u)
 
-template <int D, int BC, int STAGES, bool VARLEN, bool CAUSAL>
+template <int D, int BC, int STAGES, bool VARLEN, bool CAUSAL, bool SPLIT = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -336,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
 #pragma unroll 1
       FA_FOR_EACH_UNIT(u) {
-        const Unit w = decode_unit<BC, VARLEN, CAUSAL>(p, u);
+        const Unit w = decode_unit<BC, VARLEN, CAUSAL, SPLIT>(p, u);
         if (!w.run) continue;
         // Q of this unit, once the previous unit's S MMAs no longer read it.
         if (!ptx::mbar_wait(bar(L::kBarQEmpty), (qcount & 1u) ^ 1u, s_abort, tmo)) {
@@ -374,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++g;
           const uint32_t sbase = base + L::kOffKV + slot * L::kSlotBytes;
           if (j < w.nkv) {
-            const RowWindow kw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + j * BC, BC);
+            const RowWindow kw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + (w.j0 + j) * BC, BC);
 #pragma unroll
             for (int pnl = 0; pnl < kDPanels; ++pnl) {
               const uint32_t dst = sbase + pnl * L::kKVPanelBytes;
@@ -385,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (j >= 1) {
-            const RowWindow vw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + (j - 1) * BC, BC);
+            const RowWindow vw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + (w.j0 + j - 1) * BC, BC);
 #pragma unroll
             for (int pnl = 0; pnl < kDPanels; ++pnl) {
               const uint32_t dst = sbase + L::kKVTileBytes + pnl * L::kKVPanelBytes;
@@ -416,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
 #pragma unroll 1
       FA_FOR_EACH_UNIT(u) {
-        const Unit w = decode_unit<BC, VARLEN, CAUSAL>(p, u);
+        const Unit w = decode_unit<BC, VARLEN, CAUSAL, SPLIT>(p, u);
         if (!w.run) continue;
         if (!ptx::mbar_wait(bar(L::kBarQFull), qcount & 1u, s_abort, tmo)) {
           record_error(p.status, kErrTimeout, kSiteMmaQ);
@@ -509,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
 #pragma unroll 1
     FA_FOR_EACH_UNIT(u) {
-      const Unit w = decode_unit<BC, VARLEN, CAUSAL>(p, u);
+      const Unit w = decode_unit<BC, VARLEN, CAUSAL, SPLIT>(p, u);
       const bool active = t == 0 ? w.active[0] : w.active[1];
       if (!active) continue;
       const RowWindow qw = t == 0 ? w.qwin[0] : w.qwin[1];
@@ -519,8 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int first_row_lim = (qw.load_row - w.q_start + qw.lo) + w.off;
       // Only the last key tile (ragged end, shifted variable-length window) and,
       // when causal, the tiles from the first one crossing the diagonal need masks.
-      const int nkv_all = (w.k_end - w.k_start + BC - 1) / BC;
-      int j_mask = nkv_all - 1;
+      int j_mask = w.nkv_all - 1;
       if constexpr (CAUSAL) j_mask = min(j_mask, first_row_lim + 1 < 0 ? 0 : (first_row_lim + 1) / BC);
       float m_ref = -INFINITY;
       float l = 0.f;
@@ -540,8 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float s[BC];
 #pragma unroll
         for (int c = 0; c < BC; ++c) s[c] = __uint_as_float(sr[c]);
-        if (j >= j_mask) {
-          const RowWindow kw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + j * BC, BC);
+        if (w.j0 + j >= j_mask) {
+          const RowWindow kw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + (w.j0 + j) * BC, BC);
           if (kw.lo != 0 || kw.hi != BC) {
             // Keys outside [lo, hi) of this tile: past the end, or (variable
             // length) before the sequence start / already seen by the previous tile.
@@ -635,7 +655,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_invl[t * kBR + row] = has ? 1.f / l : 0.f;
       if (row >= qw.lo && row < qw.hi) {
         const float lse = has ? (m_ref * p.scale + log2f(l) * 0.69314718055994530942f) : -INFINITY;
-        p.lse[w.lse_base + (qw.load_row - w.q_start + row)] = lse;
+        const int i_seq = qw.load_row - w.q_start + row;
+        if constexpr (SPLIT)
+          p.ws_lse[static_cast<size_t>(w.split) * p.B * p.H * p.Nq + w.lse_base + i_seq] = lse;
+        else
+          p.lse[w.lse_base + i_seq] = lse;
       }
       ptx::mbar_arrive(bar(L::kBarLReady + t));
     }
@@ -652,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
 #pragma unroll 1
     FA_FOR_EACH_UNIT(u) {
-      const Unit w = decode_unit<BC, VARLEN, CAUSAL>(p, u);
+      const Unit w = decode_unit<BC, VARLEN, CAUSAL, SPLIT>(p, u);
       if (w.nokeys) {
         // No keys: o = 0 and LSE = -inf (log of an empty sum).
         const int rows = min(kBR * kQT, w.q_end - w.q_row0);
@@ -667,7 +691,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int t = 0; t < kQT; ++t) {
-        if (w.zero[t]) {
+        if (SPLIT && w.zero[t]) {
+          // No visible key in this split: partial o = 0, partial LSE = -inf.
+          const RowWindow zw = w.qwin[t];
+          const size_t sbase = static_cast<size_t>(w.split) * p.B * p.H * p.Nq + w.lse_base;
+          for (int e = threadIdx.x - 256; e < kBR * D; e += 128) {
+            const int r = e / D, c = e % D;
+            if (r >= zw.lo && r < zw.hi)
+              p.ws_o[(sbase + (zw.load_row - w.q_start + r)) * D + c] = 0.f;
+          }
+          for (int r = threadIdx.x - 256; r < kBR; r += 128)
+            if (r >= zw.lo && r < zw.hi) p.ws_lse[sbase + (zw.load_row - w.q_start + r)] = -INFINITY;
+        } else if (w.zero[t]) {
           // Causal rows that see no key: o = 0 and LSE = -inf.
           const RowWindow zw = w.qwin[t];
           const size_t rs = static_cast<size_t>(p.H) * D;
@@ -692,11 +727,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_off + static_cast<uint32_t>(2 * BC + t * D);
         const RowWindow qw = w.qwin[t];
         const bool warp_full = (wq << 5) >= qw.lo;  // every row of this warp is valid
-        const bool use_tma = !VARLEN || warp_full;
+        const bool use_tma = !SPLIT && (!VARLEN || warp_full);
         const bool row_ok = row >= qw.lo && row < qw.hi;
         // Row pointer for the direct-store path (only formed for valid rows).
         __nv_bfloat16* const grow =
             row_ok ? p.o + (static_cast<size_t>(qw.load_row + row) * p.H + w.h) * D : p.o;
+        float* const srow =
+            SPLIT && row_ok ? p.ws_o + (static_cast<size_t>(w.split) * p.B * p.H * p.Nq + w.lse_base +
+                                        (qw.load_row - w.q_start + row)) * D
+                            : nullptr;
         if (use_tma && pending) {
           // The previous store from this warp's staging area must have read it.
           if (lane == 0) ptx::bulk_wait_group_read_0();
@@ -708,6 +747,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t r[32];
           ptx::tmem_ld32(tO + c * 32, r);
           ptx::tmem_wait_ld();
+          if constexpr (SPLIT) {
+            // Partial output of this key split, normalised by its own l, in fp32.
+            if (row_ok) {
+#pragma unroll
+              for (int q4 = 0; q4 < 8; ++q4)
+                ptx::st_global_v4(srow + c * 32 + q4 * 4,
+                                  __float_as_uint(__uint_as_float(r[4 * q4]) * inv_l),
+                                  __float_as_uint(__uint_as_float(r[4 * q4 + 1]) * inv_l),
+                                  __float_as_uint(__uint_as_float(r[4 * q4 + 2]) * inv_l),
+                                  __float_as_uint(__uint_as_float(r[4 * q4 + 3]) * inv_l));
+            }
+            continue;
+          }
           uint32_t wv[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)

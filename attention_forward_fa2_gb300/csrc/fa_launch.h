@@ -39,4 +39,23 @@ cudaError_t launch_fwd(const LaunchArgs& a);
     return cudaGetLastError();                                                                \
   }
 
+// Key-split form (dense tensors only): the unit also carries a key split.
+template <int D, int STAGES, bool CAUSAL>
+cudaError_t launch_fwd_split(const LaunchArgs& a);
+
+#define FA_DEFINE_LAUNCH_SPLIT(D, STAGES, CAUSAL)                                              \
+  template <>                                                                                 \
+  cudaError_t launch_fwd_split<D, STAGES, CAUSAL>(const LaunchArgs& a) {                      \
+    auto* kern = &fa_fwd_kernel<D, kBC, STAGES, false, CAUSAL, true>;                         \
+    constexpr int smem = SmemLayout<D, kBC, STAGES>::kAlloc;                                  \
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); \
+    if (e != cudaSuccess) return e;                                                           \
+    kern<<<a.grid, kThreads, smem, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);          \
+    return cudaGetLastError();                                                                \
+  }
+
+// Merge of the key splits (fa_combine.cuh); D in {64, 128}.
+cudaError_t launch_combine(int D, const float* ws_o, const float* ws_lse, int S, long long rows, int H,
+                           int Nq, __nv_bfloat16* o, float* lse, cudaStream_t stream);
+
 }  // namespace fa

@@ -282,11 +282,20 @@ def run_ours(args, w):
     lse = torch.empty((w.B, w.H, Nq), dtype=torch.float32, device=dev)
 
     def step():
-        if w.varlen:
+        if args.split:
+            fa.forward_splitkv(dq, dk, dv, out=o, lse=lse, causal=args.causal, workspace=ws)
+        elif w.varlen:
             fa.forward(dq, dk, dv, cu_seqlens=dcu, max_seqlen=maxlen, out=o, lse=lse, causal=args.causal)
         else:
             fa.forward_qk(dq, dk, dv, out=o, lse=lse, causal=args.causal)
 
+    ws = None
+    if args.split:
+        if w.varlen:
+            raise SystemExit("--split takes dense workloads only")
+        n_split = fa.splitkv_num_splits(w.B, w.Nq, w.Nk, w.H, w.d)
+        ws = torch.empty(fa.splitkv_workspace_bytes(w.B, w.Nq, w.H, w.d, n_split), dtype=torch.uint8,
+                         device=dev)
     if args.autotune:
         if w.varlen:
             fa.autotune(dq, dk, dv, cu_seqlens=dcu, max_seqlen=maxlen)
@@ -378,7 +387,7 @@ def run_ours(args, w):
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "steps": e2e_steps},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if args.split else 1),
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -403,6 +412,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="page", choices=sorted(I.WORKLOADS))
     ap.add_argument("--autotune", action="store_true", help="tune the kernel config first")
+    ap.add_argument("--split", action="store_true",
+                    help="key-split form (short query sets); launches also count the merge kernel")
     ap.add_argument("--causal", action="store_true",
                     help="causal mask (FLOPs count the visible query/key pairs only)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle sample budget")

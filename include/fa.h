@@ -104,6 +104,39 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
               const int* cu_seqlens_k, int flags, void* stream);
 
 /*
+ * Key-split form for short query sets (dense tensors; for example the
+ * 64-query x 4096-key slice of "Flash Attention 2 Chapter2", introduction).
+ * The key range of every (batch, head, 256-row query block) is cut into
+ * num_splits contiguous ranges that run on different SMs; each writes its
+ * normalised fp32 output and log-sum-exp to `workspace`, and a second kernel
+ * merges them exactly ("GPU 内核与 FlashAttention" §11.2: LSE = log sum_s
+ * e^LSE_s, O = sum_s e^(LSE_s - LSE) O_s).
+ *
+ * fa_splitkv_num_splits      -- splits a call with these sizes would use for
+ *                               `requested` (<= 0: chosen to give every SM a
+ *                               unit, at least two key tiles per split; capped
+ *                               at 128 and at the number of 128-key tiles).
+ *                               Needs the current device; returns the count or
+ *                               a negative FA_ERR_* code.
+ * fa_splitkv_workspace_bytes -- bytes of workspace for num_splits splits:
+ *                               num_splits * B * H * Nq * (d + 1) * 4; negative
+ *                               FA_ERR_* code on bad arguments.
+ * fa_fwd_splitkv             -- arguments as fa_fwd_ex (dense only, no
+ *                               cu_seqlens), plus num_splits (<= 0: choose) and
+ *                               a caller-owned DEVICE workspace, 16-byte aligned,
+ *                               of at least fa_splitkv_workspace_bytes(...,
+ *                               fa_splitkv_num_splits(...)) bytes; a smaller or
+ *                               misaligned workspace gives FA_ERR_INVALID_ARG.
+ *                               The workspace is fully rewritten by every call;
+ *                               calls that share one must not overlap on the GPU.
+ */
+int fa_splitkv_num_splits(int B, int Nq, int Nk, int H, int d, int requested);
+long long fa_splitkv_workspace_bytes(int B, int Nq, int H, int d, int num_splits);
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Nq,
+                   int Nk, int H, int Hk, int d, float scale, int flags, int num_splits,
+                   void* workspace, unsigned long long workspace_bytes, void* stream);
+
+/*
  * fa_check_status -- synchronises `stream`, then returns and clears the first
  * device-side error recorded since the last call (FA_OK if none).  When
  * `info` is not NULL it receives {flat block index, warp, wait site} of that

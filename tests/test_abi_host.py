@@ -146,3 +146,13 @@ def test_ex_form_argument_errors(L):
     assert ex(A, A, A, A, A, 1, 8, 8, 4, -1, 128, 0.1, None, None, 0, None) == fa.FA_ERR_INVALID_ARG
     # empty problems stay no-ops with the causal flag
     assert ex(A, A, A, A, A, 0, 8, 8, 4, 2, 128, 0.1, None, None, fa.FA_FLAG_CAUSAL, None) == fa.FA_OK
+
+
+def test_splitkv_workspace_arithmetic(L):
+    assert L.fa_splitkv_workspace_bytes(1, 64, 1, 128, 16) == 16 * 64 * 129 * 4
+    assert L.fa_splitkv_workspace_bytes(2, 300, 4, 64, 3) == 3 * 2 * 4 * 300 * 65 * 4
+    assert L.fa_splitkv_workspace_bytes(1, 64, 1, 96, 4) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_splitkv_workspace_bytes(1, 64, 1, 128, 0) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_splitkv_workspace_bytes(1, 64, 1, 128, 129) == fa.FA_ERR_INVALID_ARG
+    # variable-length tensors are not accepted by the key-split form
+    assert L.fa_splitkv_num_splits(1, 64, 4096, 1, 96, 0) == fa.FA_ERR_INVALID_ARG

@@ -322,3 +322,57 @@ def test_causal_gqa_configs(oracle_mod, spec):
             assert_close(o, lse, o_ref, lse_ref, spec + " d%d" % d)
     finally:
         fa.set_config(None)
+
+
+# ------------------------------------------------------------ key-split form
+def _gpu_split(q, k, v, causal=False, num_splits=None):
+    o, lse = fa.forward_splitkv(q.cuda(), k.cuda(), v.cuda(), causal=causal, num_splits=num_splits)
+    rc, info = fa.check_status()
+    assert rc == fa.FA_OK, (fa.strerror(rc), info)
+    return o.double().cpu().numpy(), lse.double().cpu().numpy()
+
+
+def test_splitkv_slice_full_parity(oracle_mod):
+    w = I.SLICE
+    q, k, v, _, _ = I.make(w)
+    assert fa.splitkv_num_splits(w.B, w.Nq, w.Nk, w.H, w.d) > 1
+    o, lse = _gpu_split(q, k, v)
+    o_ref, lse_ref = oracle_mod.attn_dense(bits(q), bits(k), bits(v))
+    assert_close(o, lse, o_ref, lse_ref, "split slice")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 5, 16, 32])
+@pytest.mark.parametrize("causal", [False, True])
+def test_splitkv_counts(oracle_mod, splits, causal):
+    q, k, v = _make_gqa(1, 64, 4096, 2, 1, 128, 90 + splits)
+    o, lse = _gpu_split(q, k, v, causal=causal, num_splits=splits)
+    o_ref, lse_ref = oracle_mod.attn_dense(bits(q), bits(k), bits(v), causal=causal)
+    assert_close(o, lse, o_ref, lse_ref, "split %d causal %s" % (splits, causal))
+
+
+@pytest.mark.parametrize("B,Nq,Nk,H,Hk,d,causal", [
+    (2, 300, 1000, 4, 2, 64, False), (1, 257, 999, 3, 3, 128, True), (1, 1, 129, 1, 1, 128, False),
+    (3, 100, 2048, 2, 1, 64, True), (1, 513, 384, 2, 2, 128, True),
+])
+def test_splitkv_shapes(oracle_mod, B, Nq, Nk, H, Hk, d, causal):
+    q, k, v = _make_gqa(B, Nq, Nk, H, Hk, d, 95 + Nq + Nk)
+    o, lse = _gpu_split(q, k, v, causal=causal)
+    o_ref, lse_ref = oracle_mod.attn_dense(bits(q), bits(k), bits(v), causal=causal)
+    assert_close(o, lse, o_ref, lse_ref, "split %s" % ((B, Nq, Nk, H, Hk, d, causal),))
+
+
+def test_splitkv_rejects_small_or_misaligned_workspace():
+    q, k, v = _make_gqa(1, 64, 1024, 1, 1, 128, 99)
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    o = torch.empty_like(dq)
+    lse = torch.empty((1, 1, 64), device="cuda")
+    n = fa.splitkv_num_splits(1, 64, 1024, 1, 128, 4)
+    need = fa.splitkv_workspace_bytes(1, 64, 1, 128, n)
+    ws = torch.empty(need + 64, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    args = (dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), o.data_ptr(), lse.data_ptr(), 1, 64, 1024, 1, 1,
+            128, 0.1, 0, 4)
+    assert fa.fa_fwd_splitkv(*args, ws.data_ptr(), need - 4, s) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_splitkv(*args, ws.data_ptr() + 8, need, s) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_splitkv(*args, ws.data_ptr(), need, s) == fa.FA_OK
+    assert fa.check_status()[0] == fa.FA_OK
