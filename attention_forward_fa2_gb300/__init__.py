@@ -30,6 +30,7 @@ FA_ERR_CUDA = -4
 FA_ERR_TIMEOUT = -5
 FA_ERR_NO_DEVICE = -6
 FA_ERR_BAD_SEQLENS = -7
+FA_ERR_SCRATCH_LIMIT = -8
 
 FA_FLAG_CAUSAL = 1
 
@@ -38,7 +39,7 @@ EXPORTS = (
     "fa_fwd", "fa_fwd_qk", "fa_fwd_ex", "fa_check_status", "fa_strerror", "fa_last_cuda_error",
     "fa_set_timeout_ns", "fa_set_config", "fa_get_config", "fa_autotune",
     "fa_selftest_wait_timeout", "fa_version", "fa_splitkv_num_splits",
-    "fa_splitkv_workspace_bytes", "fa_fwd_splitkv",
+    "fa_splitkv_workspace_bytes", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc",
 )
 
 
@@ -83,6 +84,7 @@ def lib() -> ctypes.CDLL:
         L.fa_splitkv_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
         L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp,
                                      ctypes.c_ulonglong, vp]
+        L.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
         for name in EXPORTS:
             if name != "fa_strerror":
                 getattr(L, name).restype = ci
@@ -108,6 +110,13 @@ def fa_fwd_splitkv(q, k, v, o, lse, B, Nq, Nk, H, Hk, d, scale, flags, num_split
                    workspace_bytes, stream) -> int:
     return lib().fa_fwd_splitkv(q, k, v, o, lse, B, Nq, Nk, H, Hk, d, scale, flags, num_splits,
                                 workspace, workspace_bytes, stream)
+
+
+def fa_fwd_splitkv_noalloc(q, k, v, o, lse, B, Nq, Nk, H, Hk, d, scale, flags, num_splits,
+                           stream) -> int:
+    """Key-split forward using the library's fixed scratch (no allocation)."""
+    return lib().fa_fwd_splitkv_noalloc(q, k, v, o, lse, B, Nq, Nk, H, Hk, d, scale, flags,
+                                        num_splits, stream)
 
 
 def splitkv_num_splits(B, Nq, Nk, H, d, requested=0) -> int:

@@ -443,6 +443,7 @@ const char* fa_strerror(int code) {
     case FA_ERR_TIMEOUT: return "device-side wait timed out";
     case FA_ERR_NO_DEVICE: return "no CUDA device";
     case FA_ERR_BAD_SEQLENS: return "cu_seqlens inconsistent with the maximum sequence length";
+    case FA_ERR_SCRATCH_LIMIT: return "problem needs more than the library's fixed 16 MiB scratch";
     default: return "unknown error";
   }
 }

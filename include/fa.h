@@ -44,6 +44,7 @@ extern "C" {
 #define FA_ERR_TIMEOUT (-5)      /* a device-side wait gave up (fa_check_status)        */
 #define FA_ERR_NO_DEVICE (-6)    /* no CUDA device is visible                           */
 #define FA_ERR_BAD_SEQLENS (-7)  /* cu_seqlens inconsistent with the maximum lengths    */
+#define FA_ERR_SCRATCH_LIMIT (-8) /* problem needs more than the fixed 16 MiB scratch   */
 
 /*
  * fa_fwd -- attention forward, self-attention shapes (Nq = Nk = N).
@@ -135,6 +136,29 @@ long long fa_splitkv_workspace_bytes(int B, int Nq, int H, int d, int num_splits
 int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Nq,
                    int Nk, int H, int Hk, int d, float scale, int flags, int num_splits,
                    void* workspace, unsigned long long workspace_bytes, void* stream);
+
+/*
+ * fa_fwd_splitkv_noalloc -- the key-split forward (fa_fwd_splitkv) for callers
+ * that cannot allocate device memory when attention runs: runtimes that reserve
+ * all device memory up front and forbid later allocations, real-time paths
+ * where an allocation's latency or failure is not acceptable, or C callers
+ * with no memory pool of their own.  The pages have no counterpart; this is a
+ * deployment variant of the same computation.
+ *   Arguments as fa_fwd_splitkv without the workspace: the caller passes only
+ *   inputs and outputs (device pointers), and nothing is allocated.
+ *   Scratch: a fixed 16 MiB array inside the library, held on every GPU that
+ *   loads the library until the process exits.  A problem needing more
+ *   (B * H * Nq * splits * (d + 1) * 4 bytes, splits from
+ *   fa_splitkv_num_splits) returns FA_ERR_SCRATCH_LIMIT and launches nothing.
+ *   The first call on a device looks up the array's device address (a one-time
+ *   set-up per device); make that first call before any stream capture.
+ *   All calls on a device share the array: calls that overlap on the GPU (other
+ *   streams or host threads) race and must be serialised by the caller.  No
+ *   part of the array needs clearing: each call writes every entry it reads.
+ */
+int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                           int Nq, int Nk, int H, int Hk, int d, float scale, int flags,
+                           int num_splits, void* stream);
 
 /*
  * fa_check_status -- synchronises `stream`, then returns and clears the first
