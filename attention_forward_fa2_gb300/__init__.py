@@ -174,6 +174,25 @@ def get_config(d: int, N: int, varlen: bool = False) -> str:
 
 
 # ------------------------------------------------------ torch-tensor wrappers
+class _NoDeviceSwitch:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+
+_NO_SWITCH = _NoDeviceSwitch()
+
+
+def _on_device(device):
+    """Make `device` current for the call (no-op when it already is)."""
+    import torch
+    if device.index is None or device.index == torch.cuda.current_device():
+        return _NO_SWITCH
+    return torch.cuda.device(device)
+
+
 def _stream_handle(stream):
     import torch
     s = torch.cuda.current_stream() if stream is None else stream
@@ -246,7 +265,7 @@ def forward_qk(q, k, v, scale=None, cu_seqlens_q=None, cu_seqlens_k=None,
         _check_tensor("lse", lse, torch.float32, 3)
         if tuple(lse.shape) != (B, H, Nq):
             raise ValueError("lse must be [B, H, Nq]")
-    with torch.cuda.device(q.device):
+    with _on_device(q.device):
         rc = fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                        B, Nq, Nk, H, Hk, d, float(scale),
                        cu_seqlens_q.data_ptr() if varlen else None,

@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {
@@ -17,6 +19,20 @@ struct LaunchArgs {
 
 // Key/value tile width used by every instantiation.
 constexpr int kBC = 128;
+
+// Raises a kernel's dynamic shared-memory limit once per device (the
+// attribute persists; setting it on every launch costs host time).
+// `done` is one bit per device ordinal < 64, owned by the calling kernel.
+inline cudaError_t set_smem_once(const void* kern, int smem, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // Dynamic shared memory one CTA of launch_fwd<D, STAGES, ...> needs.
 template <int D, int STAGES>
@@ -33,7 +49,8 @@ cudaError_t launch_fwd(const LaunchArgs& a);
   cudaError_t launch_fwd<D, STAGES, VARLEN, CAUSAL>(const LaunchArgs& a) {                    \
     auto* kern = &fa_fwd_kernel<D, kBC, STAGES, VARLEN, CAUSAL>;                              \
     constexpr int smem = SmemLayout<D, kBC, STAGES>::kAlloc;                                  \
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); \
+    static std::atomic<unsigned long long> done{0};                                          \
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem, done);          \
     if (e != cudaSuccess) return e;                                                           \
     kern<<<a.grid, kThreads, smem, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);          \
     return cudaGetLastError();                                                                \
@@ -48,7 +65,8 @@ cudaError_t launch_fwd_split(const LaunchArgs& a);
   cudaError_t launch_fwd_split<D, STAGES, CAUSAL>(const LaunchArgs& a) {                      \
     auto* kern = &fa_fwd_kernel<D, kBC, STAGES, false, CAUSAL, true>;                         \
     constexpr int smem = SmemLayout<D, kBC, STAGES>::kAlloc;                                  \
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); \
+    static std::atomic<unsigned long long> done{0};                                          \
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem, done);          \
     if (e != cudaSuccess) return e;                                                           \
     kern<<<a.grid, kThreads, smem, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);          \
     return cudaGetLastError();                                                                \

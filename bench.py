@@ -261,6 +261,13 @@ def workload_config(w, kernel_cfg, causal=False):
     return cfg
 
 
+def add_mode(cfg, args):
+    cfg["launch"] = "cuda graph replay" if args.graph else "stream launches"
+    if args.split:
+        cfg["form"] = "key-split (fa_fwd_splitkv)"
+    return cfg
+
+
 def run_ours(args, w):
     import torch
     import attention_forward_fa2_gb300 as fa
@@ -306,6 +313,19 @@ def run_ours(args, w):
     # ---------------------------------------------------------- device timing
     for _ in range(args.warmup):
         step()
+    graph = None
+    if args.graph:
+        # Replay the timed launches from a CUDA graph: removes host launch
+        # overhead, which dominates for problems of a few microseconds.
+        torch.cuda.synchronize(dev)
+        gs = torch.cuda.Stream(device=dev)
+        gs.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(gs):
+            with torch.cuda.graph(graph, stream=gs):
+                for _ in range(args.steps):
+                    step()
+        torch.cuda.synchronize(dev)
     rc, info = fa.check_status()
     if rc != fa.FA_OK:
         raise SystemExit("device error during warm-up: %s %s" % (fa.strerror(rc), info))
@@ -317,8 +337,11 @@ def run_ours(args, w):
     barrier(world)
     torch.cuda.synchronize(dev)
     e0.record(stream)
-    for _ in range(args.steps):
-        step()
+    if graph is not None:
+        graph.replay()
+    else:
+        for _ in range(args.steps):
+            step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -376,7 +399,7 @@ def run_ours(args, w):
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1), generated on the host)",
-        "config": workload_config(w, kernel_cfg, args.causal),
+        "config": add_mode(workload_config(w, kernel_cfg, args.causal), args),
         "pct_of_peak": 100.0 * kernel_tflops / peak,
         "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": UNIT,
                      "frac": kernel_tflops / peak, "traffic": traffic,
@@ -412,6 +435,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="page", choices=sorted(I.WORKLOADS))
     ap.add_argument("--autotune", action="store_true", help="tune the kernel config first")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay the timed launches from a CUDA graph (small problems)")
     ap.add_argument("--split", action="store_true",
                     help="key-split form (short query sets); launches also count the merge kernel")
     ap.add_argument("--causal", action="store_true",
