@@ -37,12 +37,17 @@ thread_local int t_last_cuda_error = 0;
 std::mutex g_mu;
 unsigned long long g_timeout_ns = 1000000000ull;
 
+// Tile configuration ("Flash Attention 2 Chapter6", Kernel 7 searches B_r, B_c
+// and the pipeline depth per shape).
 struct Config {
-  int stages;
-  float threshold;
+  int bc;           // B_c: keys per K/V tile, 64 or 128
+  int qtiles;       // query tiles of 128 rows per work unit: B_r = 128 * qtiles
+  int stages;       // K/V ring slots
+  float threshold;  // O-rescale threshold, log2 units
 };
+constexpr Config kSpecBase{128, 2, 4, 8.f};  // fields a spec leaves out
 bool g_forced = false;
-Config g_forced_cfg{4, 8.f};
+Config g_forced_cfg = kSpecBase;
 std::map<std::tuple<int, int, int>, Config> g_tuned;  // (d, N bucket, varlen) -> config
 
 struct DeviceState {
@@ -129,11 +134,11 @@ Config pick_config(int d, int N, int varlen) {
   if (g_forced) return g_forced_cfg;
   auto it = g_tuned.find(std::make_tuple(d, n_bucket(N), varlen));
   if (it != g_tuned.end()) return it->second;
-  return Config{d == 128 ? 2 : 3, 8.f};
+  return Config{128, 2, d == 128 ? 2 : 3, 8.f};
 }
 
 bool parse_config(const char* spec, Config* out) {
-  Config c{4, 8.f};
+  Config c = kSpecBase;
   std::string s(spec);
   size_t pos = 0;
   while (pos < s.size()) {
@@ -146,8 +151,16 @@ bool parse_config(const char* spec, Config* out) {
     char* e = nullptr;
     if (key == "stages") {
       long v = std::strtol(val.c_str(), &e, 10);
-      if (*e || v < 2 || v > 4) return false;
+      if (val.empty() || *e || v < 2 || v > 4) return false;
       c.stages = static_cast<int>(v);
+    } else if (key == "bc") {
+      long v = std::strtol(val.c_str(), &e, 10);
+      if (val.empty() || *e || (v != 64 && v != 128)) return false;
+      c.bc = static_cast<int>(v);
+    } else if (key == "br") {
+      long v = std::strtol(val.c_str(), &e, 10);
+      if (val.empty() || *e || (v != 128 && v != 256)) return false;
+      c.qtiles = static_cast<int>(v / 128);
     } else if (key == "threshold") {
       double v = std::strtod(val.c_str(), &e);
       if (*e || !std::isfinite(v) || v < 0 || v > 64) return false;
@@ -161,23 +174,38 @@ bool parse_config(const char* spec, Config* out) {
   return true;
 }
 
-// Ring depth actually used: each slot holds one K tile and one V tile, so
-// d = 128 fits two slots next to the query tiles; d = 64 fits up to four.
-int effective_stages(int d, int stages) { return d == 128 ? 2 : stages; }
+// The config a call actually runs.  Each ring slot holds one K tile and one V
+// tile: with d = 128 and 128-key tiles only two slots fit next to the query
+// tiles.  The causal kernels are built with 128-key tiles only.
+Config resolve(Config c, int d, bool causal) {
+  if (causal) c.bc = 128;
+  if (d == 128 && c.bc == 128) c.stages = 2;
+  return c;
+}
 
-template <bool VARLEN, bool CAUSAL>
-cudaError_t dispatch_d64(int stages, const fa::LaunchArgs& a) {
+template <int D, int BC, bool VARLEN, bool CAUSAL>
+cudaError_t dispatch_stages(int stages, const fa::LaunchArgs& a) {
   switch (stages) {
-    case 2: return fa::launch_fwd<64, 2, VARLEN, CAUSAL>(a);
-    case 3: return fa::launch_fwd<64, 3, VARLEN, CAUSAL>(a);
-    default: return fa::launch_fwd<64, 4, VARLEN, CAUSAL>(a);
+    case 2: return fa::launch_fwd<D, BC, 2, VARLEN, CAUSAL>(a);
+    case 3: return fa::launch_fwd<D, BC, 3, VARLEN, CAUSAL>(a);
+    default: return fa::launch_fwd<D, BC, 4, VARLEN, CAUSAL>(a);
   }
 }
 
+// Expects a resolved config.
 template <bool VARLEN, bool CAUSAL>
-cudaError_t dispatch(int d, int stages, const fa::LaunchArgs& a) {
-  if (d == 128) return fa::launch_fwd<128, 2, VARLEN, CAUSAL>(a);
-  return dispatch_d64<VARLEN, CAUSAL>(stages, a);
+cudaError_t dispatch(int d, const Config& c, const fa::LaunchArgs& a) {
+  if constexpr (CAUSAL) {
+    if (d == 128) return fa::launch_fwd<128, 128, 2, VARLEN, true>(a);
+    return dispatch_stages<64, 128, VARLEN, true>(c.stages, a);
+  } else {
+    if (d == 128) {
+      if (c.bc == 128) return fa::launch_fwd<128, 128, 2, VARLEN, false>(a);
+      return dispatch_stages<128, 64, VARLEN, false>(c.stages, a);
+    }
+    if (c.bc == 128) return dispatch_stages<64, 128, VARLEN, false>(c.stages, a);
+    return dispatch_stages<64, 64, VARLEN, false>(c.stages, a);
+  }
 }
 
 struct Problem {
@@ -217,7 +245,8 @@ int validate(const Problem& P) {
 }
 
 // Encodes the tensor maps and fills the kernel parameters shared by every
-// form (grid left to the caller).  Expects a validated, non-empty problem.
+// form (grid left to the caller).  Expects a validated, non-empty problem and
+// a resolved config.
 int prepare(const Problem& P, const Config& cfg, DeviceState* st, fa::LaunchArgs& a) {
   const bool varlen = P.cu_q != nullptr;
   const int D = P.d;
@@ -229,7 +258,7 @@ int prepare(const Problem& P, const Config& cfg, DeviceState* st, fa::LaunchArgs
     cuuint64_t dk[4] = {(cuuint64_t)D, (cuuint64_t)P.Hk, (cuuint64_t)P.Nk, (cuuint64_t)P.B};
     cuuint64_t sk[3] = {D * esz, (cuuint64_t)P.Hk * D * esz, (cuuint64_t)P.Nk * P.Hk * D * esz};
     cuuint32_t box_q[4] = {64, 1, (cuuint32_t)fa::kBR, 1};
-    cuuint32_t box_k[4] = {64, 1, (cuuint32_t)fa::kBC, 1};
+    cuuint32_t box_k[4] = {64, 1, (cuuint32_t)cfg.bc, 1};
     cuuint32_t box_o[4] = {64, 1, 32, 1};
     int e;
     if ((e = encode(&a.tm_q, P.q, 4, dq, sq, box_q)) != FA_OK) return e;
@@ -244,7 +273,7 @@ int prepare(const Problem& P, const Config& cfg, DeviceState* st, fa::LaunchArgs
     cuuint64_t sr[2] = {D * esz, (cuuint64_t)P.H * D * esz};
     cuuint64_t srk[2] = {D * esz, (cuuint64_t)P.Hk * D * esz};
     cuuint32_t box_q[3] = {64, 1, (cuuint32_t)fa::kBR};
-    cuuint32_t box_k[3] = {64, 1, (cuuint32_t)fa::kBC};
+    cuuint32_t box_k[3] = {64, 1, (cuuint32_t)cfg.bc};
     cuuint32_t box_o[3] = {64, 1, 32};
     int e;
     if ((e = encode(&a.tm_q, P.q, 3, dq, sr, box_q)) != FA_OK) return e;
@@ -259,7 +288,8 @@ int prepare(const Problem& P, const Config& cfg, DeviceState* st, fa::LaunchArgs
   p.H = P.H;
   p.group = P.H / P.Hk;
   p.causal = (P.flags & FA_FLAG_CAUSAL) ? 1 : 0;
-  p.num_mblocks = (P.Nq + fa::kBR * fa::kQT - 1) / (fa::kBR * fa::kQT);
+  p.qtiles = cfg.qtiles;
+  p.num_mblocks = (P.Nq + fa::kBR * cfg.qtiles - 1) / (fa::kBR * cfg.qtiles);
   const long long units = static_cast<long long>(P.B) * P.H * p.num_mblocks;
   if (units > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   p.num_units = static_cast<int>(units);
@@ -283,7 +313,7 @@ int prepare(const Problem& P, const Config& cfg, DeviceState* st, fa::LaunchArgs
   return FA_OK;
 }
 
-int run(const Problem& P, const Config& cfg) {
+int run(const Problem& P, const Config& cfg_in) {
   const int rc = validate(P);
   if (rc != FA_OK) return rc == 1 ? FA_OK : rc;
   DeviceState* st = nullptr;
@@ -291,6 +321,7 @@ int run(const Problem& P, const Config& cfg) {
   if (drc != FA_OK) return drc;
   const bool varlen = P.cu_q != nullptr;
   const int D = P.d;
+  const Config cfg = resolve(cfg_in, D, (P.flags & FA_FLAG_CAUSAL) != 0);
   fa::LaunchArgs a;
   const int prc = prepare(P, cfg, st, a);
   if (prc != FA_OK) return prc;
@@ -300,9 +331,9 @@ int run(const Problem& P, const Config& cfg) {
 
   cudaError_t e;
   if (p.causal)
-    e = varlen ? dispatch<true, true>(D, cfg.stages, a) : dispatch<false, true>(D, cfg.stages, a);
+    e = varlen ? dispatch<true, true>(D, cfg, a) : dispatch<false, true>(D, cfg, a);
   else
-    e = varlen ? dispatch<true, false>(D, cfg.stages, a) : dispatch<false, false>(D, cfg.stages, a);
+    e = varlen ? dispatch<true, false>(D, cfg, a) : dispatch<false, false>(D, cfg, a);
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;
 }
@@ -348,8 +379,11 @@ int run_split(const Problem& P, const Config& cfg, int requested_splits, void* w
   const int splits = splits_for_tiles(P.Nk, tiles);
   const size_t need = split_workspace_bytes(P.B, P.Nq, P.H, P.d, splits);
   if (ws == nullptr || ws_bytes < need || !aligned16(ws)) return FA_ERR_INVALID_ARG;
+  // The split kernels use 128-key tiles and 256-row units (the split count
+  // above assumes both); only the rescale threshold follows the config.
+  Config scfg{128, 2, P.d == 128 ? 2 : 3, cfg.threshold};
   fa::LaunchArgs a;
-  const int prc = prepare(P, cfg, st, a);
+  const int prc = prepare(P, scfg, st, a);
   if (prc != FA_OK) return prc;
   fa::FwdParams& p = a.p;
   const long long units = static_cast<long long>(p.num_units) * splits;
@@ -472,9 +506,9 @@ int fa_set_config(const char* spec) {
 
 int fa_get_config(int d, int N, int varlen, char* buf, int len) {
   if (!buf || len <= 0) return FA_ERR_INVALID_ARG;
-  const Config c = pick_config(d, N, varlen ? 1 : 0);
-  std::snprintf(buf, static_cast<size_t>(len), "stages=%d,threshold=%g", effective_stages(d, c.stages),
-                c.threshold);
+  const Config c = resolve(pick_config(d, N, varlen ? 1 : 0), d, false);
+  std::snprintf(buf, static_cast<size_t>(len), "br=%d,bc=%d,stages=%d,threshold=%g", 128 * c.qtiles, c.bc,
+                c.stages, c.threshold);
   return FA_OK;
 }
 
@@ -491,11 +525,18 @@ int fa_autotune(const void* q, const void* k, const void* v, void* o, float* lse
     cudaEventDestroy(e0);
     return cuda_fail(ce);
   }
-  const Config cands_d64[] = {{2, 0.f}, {3, 0.f}, {4, 0.f}, {2, 8.f}, {3, 8.f}, {4, 8.f}};
-  const Config cands_d128[] = {{2, 0.f}, {2, 8.f}};
-  const Config* cands = d == 128 ? cands_d128 : cands_d64;
-  const int n_cands = d == 128 ? 2 : 6;
-  Config best{d == 128 ? 2 : 3, 8.f};
+  // The search space: B_r in {256, 128}, B_c in {128, 64}, every ring depth
+  // that fits, rescale threshold 8 or 0 (rescale whenever the max grows).
+  // Configs that do not fit shared memory or tensor memory are never built.
+  Config cands[48];
+  int n_cands = 0;
+  for (int qt = 2; qt >= 1; --qt)
+    for (int bc = 128; bc >= 64; bc /= 2)
+      for (int st = 2; st <= 4; ++st) {
+        if (d == 128 && bc == 128 && st > 2) continue;
+        for (float th : {8.f, 0.f}) cands[n_cands++] = Config{bc, qt, st, th};
+      }
+  Config best = pick_config(d, N, cu_seqlens ? 1 : 0);
   float best_ms = 1e30f;
   int result = FA_OK;
   for (int ci = 0; ci < n_cands; ++ci) {

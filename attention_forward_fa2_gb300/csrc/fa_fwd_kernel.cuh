@@ -11,7 +11,8 @@
 //
 // Work split (§14.2, loop order with the query block outermost): a work unit
 // is two 128-row query tiles of one (b, h) against all key/value tiles of that
-// head.  The kernel is persistent: each CTA walks the units blockIdx.x,
+// head (B_r = 256; with qtiles = 1 a unit is one tile, B_r = 128, and the
+// second softmax warpgroup idles).  The kernel is persistent: each CTA walks the units blockIdx.x,
 // blockIdx.x + gridDim.x, ...; units are numbered with the query block fastest,
 // so the CTAs that run at the same time share the K/V of a few heads in L2.
 // Roles inside the CTA (§15.2-§15.4, re-expressed for tcgen05):
@@ -100,7 +101,8 @@ struct FwdParams {
   int B, Nq, Nk, H;            // variable-length form: Nq / Nk are the maximum lengths
   int group;                   // query heads per key/value head (H / Hk)
   int causal;                  // 1: causal mask, bottom-right aligned
-  int num_mblocks;             // ceil(Nq / (kBR * kQT))
+  int qtiles;                  // query tiles per unit: 1 (B_r = 128) or 2 (B_r = 256)
+  int num_mblocks;             // ceil(Nq / (kBR * qtiles))
   int num_units;               // B * H * num_mblocks
   int units_per_item;          // units a CTA takes at a time (2 when causal: a balanced pair)
   int num_items;               // ceil(num_units / units_per_item)
@@ -244,7 +246,7 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
     const int len_q = w.q_end - w.q_start, len_k = w.k_end - w.k_start;
     bad = len_q < 0 || len_k < 0 || len_q > p.Nq || len_k > p.Nk || w.q_start < 0 || w.k_start < 0;
   }
-  w.q_row0 = w.q_start + mb * (kBR * kQT);
+  w.q_row0 = w.q_start + mb * (kBR * p.qtiles);
   w.off = (w.k_end - w.k_start) - (w.q_end - w.q_start);
   const int nkv_all = bad ? 0 : (w.k_end - w.k_start + BC - 1) / BC;
   w.nkv_all = nkv_all;
@@ -257,7 +259,7 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   for (int t = 0; t < kQT; ++t) {
     const int r0 = w.q_row0 + t * kBR;
     w.qwin[t] = make_window<VARLEN>(w.q_start, w.q_end, r0, kBR);
-    const bool rows = has_rows && r0 < w.q_end;
+    const bool rows = has_rows && t < p.qtiles && r0 < w.q_end;
     int n = nkv_here;
     if (CAUSAL && rows) {
       // Last valid row of the tile, in sequence coordinates, and the last key it sees.
@@ -679,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Unit w = decode_unit<BC, VARLEN, CAUSAL, SPLIT>(p, u);
       if (w.nokeys) {
         // No keys: o = 0 and LSE = -inf (log of an empty sum).
-        const int rows = min(kBR * kQT, w.q_end - w.q_row0);
+        const int rows = min(kBR * p.qtiles, w.q_end - w.q_row0);
         const size_t rs = static_cast<size_t>(p.H) * D;
         for (int e = threadIdx.x - 256; e < rows * D; e += 128) {
           const int r = e / D, c = e % D;

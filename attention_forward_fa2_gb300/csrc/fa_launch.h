@@ -17,7 +17,7 @@ struct LaunchArgs {
   cudaStream_t stream;
 };
 
-// Key/value tile width used by every instantiation.
+// Key/value tile width of the key-split form and of the default config.
 constexpr int kBC = 128;
 
 // Raises a kernel's dynamic shared-memory limit once per device (the
@@ -34,21 +34,15 @@ inline cudaError_t set_smem_once(const void* kern, int smem, std::atomic<unsigne
   return e;
 }
 
-// Dynamic shared memory one CTA of launch_fwd<D, STAGES, ...> needs.
-template <int D, int STAGES>
-constexpr int smem_bytes() {
-  return SmemLayout<D, kBC, STAGES>::kAlloc;
-}
-
-template <int D, int STAGES, bool VARLEN, bool CAUSAL>
+template <int D, int BC, int STAGES, bool VARLEN, bool CAUSAL>
 cudaError_t launch_fwd(const LaunchArgs& a);
 
 // Defined in the translation unit that owns the kernel.
-#define FA_DEFINE_LAUNCH(D, STAGES, VARLEN, CAUSAL)                                           \
+#define FA_DEFINE_LAUNCH(D, BC, STAGES, VARLEN, CAUSAL)                                       \
   template <>                                                                                 \
-  cudaError_t launch_fwd<D, STAGES, VARLEN, CAUSAL>(const LaunchArgs& a) {                    \
-    auto* kern = &fa_fwd_kernel<D, kBC, STAGES, VARLEN, CAUSAL>;                              \
-    constexpr int smem = SmemLayout<D, kBC, STAGES>::kAlloc;                                  \
+  cudaError_t launch_fwd<D, BC, STAGES, VARLEN, CAUSAL>(const LaunchArgs& a) {                \
+    auto* kern = &fa_fwd_kernel<D, BC, STAGES, VARLEN, CAUSAL>;                               \
+    constexpr int smem = SmemLayout<D, BC, STAGES>::kAlloc;                                   \
     static std::atomic<unsigned long long> done{0};                                          \
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem, done);          \
     if (e != cudaSuccess) return e;                                                           \

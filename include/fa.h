@@ -185,10 +185,17 @@ int fa_set_timeout_ns(unsigned long long ns);
 /*
  * Kernel configuration ("Flash Attention 2 Chapter6", Kernel 7: the
  * configuration space is searched per shape instead of fixed).  A config is
- * a text spec "stages=<2|3|4>,threshold=<float>": the number of slots of the
- * shared-memory key/value ring (each slot holds one K tile and one V tile;
- * d = 128 always uses 2, the most that fit) and the O-rescale threshold in
- * log2 units (0 rescales whenever a row maximum grows).
+ * a text spec of comma-separated key=value items, any subset of
+ *   br=<128|256>      query rows per work unit (B_r: one or two 128-row tiles)
+ *   bc=<64|128>       keys per K/V tile (B_c)
+ *   stages=<2|3|4>    slots of the shared-memory K/V ring (each holds one K
+ *                     and one V tile; d = 128 with bc = 128 always uses 2,
+ *                     the most that fit)
+ *   threshold=<float> O-rescale threshold in log2 units, 0..64 (0 rescales
+ *                     whenever a row maximum grows)
+ * Items left out take br=256, bc=128, stages=4, threshold=8.  Causal calls
+ * always use bc=128.  fa_get_config reports all four items as
+ * "br=..,bc=..,stages=..,threshold=..".
  *
  * fa_set_config  -- force `spec` for every later call (NULL or "" clears it).
  * fa_get_config  -- writes the spec that a call with (d, N, varlen) would use

@@ -197,9 +197,11 @@ def test_deterministic():
 
 
 # ------------------------------------------------------------ configurations
-@pytest.mark.parametrize("spec", ["stages=2,threshold=0", "stages=3,threshold=0",
-                                  "stages=4,threshold=0", "stages=2,threshold=8",
-                                  "stages=3,threshold=8", "stages=4,threshold=8"])
+CONFIG_SPACE = ["br=%d,bc=%d,stages=%d,threshold=%d" % (br, bc, st, th)
+                for br in (256, 128) for bc in (128, 64) for st in (2, 3, 4) for th in (0, 8)]
+
+
+@pytest.mark.parametrize("spec", CONFIG_SPACE)
 @pytest.mark.parametrize("d", [64, 128])
 def test_every_config(oracle_mod, spec, d):
     fa.set_config(spec)
@@ -222,7 +224,7 @@ def test_autotune_keeps_parity(oracle_mod):
     q, k, v = I.make_dense(1, 1024, 1024, 4, 128, 13)
     dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
     spec = fa.autotune(dq, dk, dv)
-    assert spec.startswith("stages=")
+    assert spec.startswith("br=")
     o, lse = gpu_dense(q, k, v)
     o_ref, lse_ref = _oracle_dense(oracle_mod, q, k, v)
     assert_close(o, lse, o_ref, lse_ref, "autotuned " + spec)
@@ -311,7 +313,8 @@ def test_causal_page_workload_sampled(oracle_mod):
     assert_close(o[b, i, h, :], lse[b, h, i], o_ref, lse_ref, "causal page")
 
 
-@pytest.mark.parametrize("spec", ["stages=2,threshold=0", "stages=4,threshold=8"])
+@pytest.mark.parametrize("spec", ["stages=2,threshold=0", "stages=4,threshold=8",
+                                  "br=128,bc=64,stages=3,threshold=8"])
 def test_causal_gqa_configs(oracle_mod, spec):
     fa.set_config(spec)
     try:
