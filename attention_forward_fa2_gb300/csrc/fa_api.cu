@@ -44,8 +44,9 @@ struct Config {
   int qtiles;       // query tiles of 128 rows per work unit: B_r = 128 * qtiles
   int stages;       // K/V ring slots
   float threshold;  // O-rescale threshold, log2 units
+  int quad;         // 1: row max / sum over the four threads of a quad (warp shuffles)
 };
-constexpr Config kSpecBase{128, 2, 4, 8.f};  // fields a spec leaves out
+constexpr Config kSpecBase{128, 2, 4, 8.f, 0};  // fields a spec leaves out
 bool g_forced = false;
 Config g_forced_cfg = kSpecBase;
 std::map<std::tuple<int, int, int>, Config> g_tuned;  // (d, N bucket, varlen) -> config
@@ -134,7 +135,7 @@ Config pick_config(int d, int N, int varlen) {
   if (g_forced) return g_forced_cfg;
   auto it = g_tuned.find(std::make_tuple(d, n_bucket(N), varlen));
   if (it != g_tuned.end()) return it->second;
-  return Config{128, 2, d == 128 ? 2 : 3, 8.f};
+  return Config{128, 2, d == 128 ? 2 : 3, 8.f, 0};
 }
 
 bool parse_config(const char* spec, Config* out) {
@@ -161,6 +162,13 @@ bool parse_config(const char* spec, Config* out) {
       long v = std::strtol(val.c_str(), &e, 10);
       if (val.empty() || *e || (v != 128 && v != 256)) return false;
       c.qtiles = static_cast<int>(v / 128);
+    } else if (key == "reduce") {
+      if (val == "thread")
+        c.quad = 0;
+      else if (val == "quad")
+        c.quad = 1;
+      else
+        return false;
     } else if (key == "threshold") {
       double v = std::strtod(val.c_str(), &e);
       if (*e || !std::isfinite(v) || v < 0 || v > 64) return false;
@@ -177,9 +185,13 @@ bool parse_config(const char* spec, Config* out) {
 // The config a call actually runs.  Each ring slot holds one K tile and one V
 // tile: with d = 128 and 128-key tiles only two slots fit next to the query
 // tiles.  The causal kernels are built with 128-key tiles only.
+// The quad-shuffle form is built for 128-key tiles without mask, with the
+// default ring depth only.
 Config resolve(Config c, int d, bool causal) {
   if (causal) c.bc = 128;
+  if (causal || c.bc != 128) c.quad = 0;
   if (d == 128 && c.bc == 128) c.stages = 2;
+  if (c.quad && d == 64) c.stages = 3;
   return c;
 }
 
@@ -199,6 +211,10 @@ cudaError_t dispatch(int d, const Config& c, const fa::LaunchArgs& a) {
     if (d == 128) return fa::launch_fwd<128, 128, 2, VARLEN, true>(a);
     return dispatch_stages<64, 128, VARLEN, true>(c.stages, a);
   } else {
+    if (c.quad) {
+      if (d == 128) return fa::launch_fwd<128, 128, 2, VARLEN, false, true>(a);
+      return fa::launch_fwd<64, 128, 3, VARLEN, false, true>(a);
+    }
     if (d == 128) {
       if (c.bc == 128) return fa::launch_fwd<128, 128, 2, VARLEN, false>(a);
       return dispatch_stages<128, 64, VARLEN, false>(c.stages, a);
@@ -381,7 +397,7 @@ int run_split(const Problem& P, const Config& cfg, int requested_splits, void* w
   if (ws == nullptr || ws_bytes < need || !aligned16(ws)) return FA_ERR_INVALID_ARG;
   // The split kernels use 128-key tiles and 256-row units (the split count
   // above assumes both); only the rescale threshold follows the config.
-  Config scfg{128, 2, P.d == 128 ? 2 : 3, cfg.threshold};
+  Config scfg{128, 2, P.d == 128 ? 2 : 3, cfg.threshold, 0};
   fa::LaunchArgs a;
   const int prc = prepare(P, scfg, st, a);
   if (prc != FA_OK) return prc;
@@ -507,8 +523,8 @@ int fa_set_config(const char* spec) {
 int fa_get_config(int d, int N, int varlen, char* buf, int len) {
   if (!buf || len <= 0) return FA_ERR_INVALID_ARG;
   const Config c = resolve(pick_config(d, N, varlen ? 1 : 0), d, false);
-  std::snprintf(buf, static_cast<size_t>(len), "br=%d,bc=%d,stages=%d,threshold=%g", 128 * c.qtiles, c.bc,
-                c.stages, c.threshold);
+  std::snprintf(buf, static_cast<size_t>(len), "br=%d,bc=%d,stages=%d,threshold=%g,reduce=%s",
+                128 * c.qtiles, c.bc, c.stages, c.threshold, c.quad ? "quad" : "thread");
   return FA_OK;
 }
 
@@ -526,16 +542,19 @@ int fa_autotune(const void* q, const void* k, const void* v, void* o, float* lse
     return cuda_fail(ce);
   }
   // The search space: B_r in {256, 128}, B_c in {128, 64}, every ring depth
-  // that fits, rescale threshold 8 or 0 (rescale whenever the max grows).
+  // that fits, rescale threshold 8 or 0 (rescale whenever the max grows), and
+  // the row reduction (one thread per row, or a quad of threads with warp
+  // shuffles; the latter built for 128-key tiles at the default depth).
   // Configs that do not fit shared memory or tensor memory are never built.
-  Config cands[48];
+  Config cands[52];
   int n_cands = 0;
   for (int qt = 2; qt >= 1; --qt)
     for (int bc = 128; bc >= 64; bc /= 2)
       for (int st = 2; st <= 4; ++st) {
         if (d == 128 && bc == 128 && st > 2) continue;
-        for (float th : {8.f, 0.f}) cands[n_cands++] = Config{bc, qt, st, th};
+        for (float th : {8.f, 0.f}) cands[n_cands++] = Config{bc, qt, st, th, 0};
       }
+  for (float th : {8.f, 0.f}) cands[n_cands++] = Config{128, 2, d == 128 ? 2 : 3, th, 1};
   Config best = pick_config(d, N, cu_seqlens ? 1 : 0);
   float best_ms = 1e30f;
   int result = FA_OK;

@@ -289,7 +289,7 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
     for (int sub_ = 0, u = it_ * p.units_per_item;                                     \
          sub_ < p.units_per_item && u < p.num_units && ok; ++sub_, ++u)
 
-template <int D, int BC, int STAGES, bool VARLEN, bool CAUSAL, bool SPLIT = false>
+template <int D, int BC, int STAGES, bool VARLEN, bool CAUSAL, bool SPLIT = false, bool QUAD = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -298,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(BC == 64 || BC == 128, "key tile");
   static_assert(2 * BC + 2 * D <= 512, "TMEM columns");
+  static_assert(!QUAD || (BC == 128 && !CAUSAL && !SPLIT), "quad reduction: 128-key tiles, no mask or split");
   constexpr int kTmemCols = 512;
   constexpr int kDPanels = D / kPanel;
 
@@ -544,124 +545,266 @@ __global__ void __launch_bounds__(kThreads, 1)
       // when causal, the tiles from the first one crossing the diagonal need masks.
       int j_mask = w.nkv_all - 1;
       if constexpr (CAUSAL) j_mask = min(j_mask, first_row_lim + 1 < 0 ? 0 : (first_row_lim + 1) / BC);
-      float m_ref = -INFINITY;
-      float l = 0.f;
+      if constexpr (QUAD) {
+        // Row max and row sum reduced with warp shuffles: the 16-lane TMEM
+        // shapes spread each row over the four threads of a quad.  Thread
+        // (qr, qc) = (lane / 4, lane % 4) owns rows 8r + qr (r = 0..3) of the
+        // warp's 32 rows and, of each 8-column group g, columns 8g + 2qc and
+        // 8g + 2qc + 1 (32 of the 128 columns of every row).
+        const int qr = lane >> 2, qc = lane & 3;
+        const uint32_t tSw = tmem + lane_off + static_cast<uint32_t>(t * BC);
+        const uint32_t tPw = tSw + BC / 2;
+        const uint32_t tOw = tmem + lane_off + static_cast<uint32_t>(2 * BC + t * D);
+        float m_q[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float l_q[4] = {0.f, 0.f, 0.f, 0.f};  // this thread's share of each row sum
 #pragma unroll 1
-      for (int j = 0; j < nt; ++j) {
-        if (!ptx::mbar_wait_warp(bar(L::kBarSFull + t), sc & 1u, s_abort, tmo)) {
-          record_error(p.status, kErrTimeout, kSiteSoftS);
-          ok = false;
-          break;
-        }
-        ++sc;
-        ptx::tc_fence_after();
-        uint32_t sr[BC];
-#pragma unroll
-        for (int c = 0; c < BC / 32; ++c) ptx::tmem_ld32(tS + c * 32, &sr[c * 32]);
-        ptx::tmem_wait_ld();
-        float s[BC];
-#pragma unroll
-        for (int c = 0; c < BC; ++c) s[c] = __uint_as_float(sr[c]);
-        if (w.j0 + j >= j_mask) {
-          const RowWindow kw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + (w.j0 + j) * BC, BC);
-          if (kw.lo != 0 || kw.hi != BC) {
-            // Keys outside [lo, hi) of this tile: past the end, or (variable
-            // length) before the sequence start / already seen by the previous tile.
-#pragma unroll
-            for (int c = 0; c < BC; ++c)
-              if (c < kw.lo || c >= kw.hi) s[c] = -INFINITY;
+        for (int j = 0; j < nt; ++j) {
+          if (!ptx::mbar_wait_warp(bar(L::kBarSFull + t), sc & 1u, s_abort, tmo)) {
+            record_error(p.status, kErrTimeout, kSiteSoftS);
+            ok = false;
+            break;
           }
-          const int kbase = kw.load_row - w.k_start;  // sequence index of column 0
-          if (CAUSAL && kbase + BC - 1 > first_row_lim) {
-            // The tile crosses the diagonal: mask keys above this row's limit.
-            const int lim = key_lim - kbase;
+          ++sc;
+          ptx::tc_fence_after();
+          uint32_t raw[4][32];
 #pragma unroll
-            for (int c = 0; c < BC; ++c)
-              if (c > lim) s[c] = -INFINITY;
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch)
+              ptx::tmem_ld16x256_x8(tSw + (static_cast<uint32_t>(16 * h) << 16) + ch * 64, raw[2 * h + ch]);
+          ptx::tmem_wait_ld();
+          // s[r][k]: row 8r + qr, column 8 * (k / 2) + 2 * qc + k % 2.
+          float s[4][32];
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+              for (int g = 0; g < 8; ++g) {
+                const int k = 2 * (8 * ch + g);
+                s[2 * h][k] = __uint_as_float(raw[2 * h + ch][4 * g]);
+                s[2 * h][k + 1] = __uint_as_float(raw[2 * h + ch][4 * g + 1]);
+                s[2 * h + 1][k] = __uint_as_float(raw[2 * h + ch][4 * g + 2]);
+                s[2 * h + 1][k + 1] = __uint_as_float(raw[2 * h + ch][4 * g + 3]);
+              }
+          if (w.j0 + j >= j_mask) {
+            const RowWindow kw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + (w.j0 + j) * BC, BC);
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+              for (int k = 0; k < 32; ++k) {
+                const int col = 8 * (k >> 1) + 2 * qc + (k & 1);
+                if (col < kw.lo || col >= kw.hi) s[r][k] = -INFINITY;
+              }
           }
-        }
-        // Row max: four independent chains of three-input maxima.
-        float mx[4] = {s[0], s[1], s[2], s[3]};
+          float alpha[4];
 #pragma unroll
-        for (int c = 4; c < BC; c += 8) {
-          mx[0] = ptx::fmax3(mx[0], s[c], s[c + 1]);
-          mx[1] = ptx::fmax3(mx[1], s[c + 2], s[c + 3]);
-          if (c + 4 < BC) {
-            mx[2] = ptx::fmax3(mx[2], s[c + 4], s[c + 5]);
-            mx[3] = ptx::fmax3(mx[3], s[c + 6], s[c + 7]);
-          }
-        }
-        const float bm = fmaxf(ptx::fmax3(mx[0], mx[1], mx[2]), mx[3]);
-        // Move the reference max only when the block max exceeds it by more
-        // than the threshold (log2 units): the merge identity of §11.2 holds
-        // for any common reference value, so results stay exact.
-        float m_new = m_ref;
-        if (bm > m_ref && (m_ref == -INFINITY || (bm - m_ref) * c2 > p.rescale_threshold)) m_new = bm;
-        const float alpha = (m_new == m_ref) ? 1.f : ptx::ex2((m_ref - m_new) * c2);
-        m_ref = m_new;
-        const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref * c2;
-        // p = 2^(s*c2 - m*c2): one packed FFMA per two scores, then ex2 each;
-        // row sums in four packed accumulators; P stored in 16-column chunks.
-        const uint64_t c2x2 = ptx::f2_pack(c2, c2);
-        const uint64_t negx2 = ptx::f2_pack(neg, neg);
-        uint64_t acc[4] = {0, 0, 0, 0};
+          for (int r = 0; r < 4; ++r) {
+            float mx0 = ptx::fmax3(s[r][0], s[r][1], s[r][2]);
+            float mx1 = ptx::fmax3(s[r][3], s[r][4], s[r][5]);
 #pragma unroll
-        for (int c0 = 0; c0 < BC; c0 += 32) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int c = c0; c < c0 + 32; c += 2) {
-            float x0, x1;
-            ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[c], s[c + 1]), c2x2, negx2), x0, x1);
-            const float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1);
-            const uint64_t e01 = ptx::f2_pack(e0, e1);
-            acc[(c >> 1) & 3] = ptx::f2_add(acc[(c >> 1) & 3], e01);
-            pk[(c - c0) / 2] = ptx::pack_bf16x2(e0, e1);
-          }
-          ptx::tmem_st16(tP + c0 / 2, pk);
-        }
-        float a0, a1, a2, a3, a4, a5, a6, a7;
-        ptx::f2_unpack(acc[0], a0, a1);
-        ptx::f2_unpack(acc[1], a2, a3);
-        ptx::f2_unpack(acc[2], a4, a5);
-        ptx::f2_unpack(acc[3], a6, a7);
-        l = l * alpha + (((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)));
-        if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          // Correction of the unnormalised output: O_t rows of this warp hold
-          // the sum over steps < j referenced to the old maximum.  Done after
-          // the exponentials (the scores are dead by then); it only has to
-          // land before P(j) is published.
-          const uint32_t tO = tmem + lane_off + static_cast<uint32_t>(2 * BC + t * D);
-          const uint64_t ax2 = ptx::f2_pack(alpha, alpha);
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            ptx::tmem_ld32(tO + c * 32, r);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              float x0, x1;
-              ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), ax2), x0, x1);
-              r[e] = __float_as_uint(x0);
-              r[e + 1] = __float_as_uint(x1);
+            for (int k = 6; k < 30; k += 4) {
+              mx0 = ptx::fmax3(mx0, s[r][k], s[r][k + 1]);
+              mx1 = ptx::fmax3(mx1, s[r][k + 2], s[r][k + 3]);
             }
-            ptx::tmem_st32(tO + c * 32, r);
+            float bm = ptx::fmax3(mx0, mx1, fmaxf(s[r][30], s[r][31]));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+            float m_new = m_q[r];
+            if (bm > m_q[r] && (m_q[r] == -INFINITY || (bm - m_q[r]) * c2 > p.rescale_threshold)) m_new = bm;
+            alpha[r] = (m_new == m_q[r]) ? 1.f : ptx::ex2((m_q[r] - m_new) * c2);
+            m_q[r] = m_new;
+          }
+          const uint64_t c2x2 = ptx::f2_pack(c2, c2);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+              const int r = 2 * h + rr;
+              const float neg = (m_q[r] == -INFINITY) ? 0.f : -m_q[r] * c2;
+              const uint64_t negx2 = ptx::f2_pack(neg, neg);
+              uint64_t acc[2] = {0, 0};
+#pragma unroll
+              for (int g = 0; g < 16; ++g) {
+                float x0, x1;
+                ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[r][2 * g], s[r][2 * g + 1]), c2x2, negx2), x0, x1);
+                const float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1);
+                acc[g & 1] = ptx::f2_add(acc[g & 1], ptx::f2_pack(e0, e1));
+                pk[2 * g + rr] = ptx::pack_bf16x2(e0, e1);
+              }
+              float a0, a1, a2, a3;
+              ptx::f2_unpack(acc[0], a0, a1);
+              ptx::f2_unpack(acc[1], a2, a3);
+              l_q[r] = l_q[r] * alpha[r] + ((a0 + a1) + (a2 + a3));
+            }
+            ptx::tmem_st16x128_x16(tPw + (static_cast<uint32_t>(16 * h) << 16), pk);
+          }
+          const bool any_rescale = alpha[0] != 1.f || alpha[1] != 1.f || alpha[2] != 1.f || alpha[3] != 1.f;
+          if (j >= 1 && __any_sync(0xffffffffu, any_rescale)) {
+            // Same correction as the one-row-per-thread form, in the quad layout.
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int ch = 0; ch < D / 64; ++ch) {
+                uint32_t r[32];
+                const uint32_t a = tOw + (static_cast<uint32_t>(16 * h) << 16) + ch * 64;
+                ptx::tmem_ld16x256_x8(a, r);
+                ptx::tmem_wait_ld();
+                const uint64_t ax = ptx::f2_pack(alpha[2 * h], alpha[2 * h]);
+                const uint64_t bx = ptx::f2_pack(alpha[2 * h + 1], alpha[2 * h + 1]);
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                  float x0, x1, y0, y1;
+                  ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1])), ax), x0, x1);
+                  ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])), bx), y0, y1);
+                  r[4 * g] = __float_as_uint(x0);
+                  r[4 * g + 1] = __float_as_uint(x1);
+                  r[4 * g + 2] = __float_as_uint(y0);
+                  r[4 * g + 3] = __float_as_uint(y1);
+                }
+                ptx::tmem_st16x256_x8(a, r);
+              }
+          }
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(L::kBarPFull + t));
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          float l = l_q[r] + __shfl_xor_sync(0xffffffffu, l_q[r], 1);
+          l += __shfl_xor_sync(0xffffffffu, l, 2);
+          const int row_r = ((warp & 3) << 5) + 8 * r + qr;
+          if (qc == 0) {
+            const bool has = l > 0.f;
+            s_invl[t * kBR + row_r] = has ? 1.f / l : 0.f;
+            if (row_r >= qw.lo && row_r < qw.hi) {
+              const float lse = has ? (m_q[r] * p.scale + log2f(l) * 0.69314718055994530942f) : -INFINITY;
+              p.lse[w.lse_base + (qw.load_row - w.q_start + row_r)] = lse;
+            }
           }
         }
-        ptx::tmem_wait_st();  // P stores (and any O rescale) have landed
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(L::kBarPFull + t));
-      }
-      if (!ok) break;
-      // Final message for the epilogue: 1 / l, and the row's log-sum-exp.
-      const bool has = l > 0.f;
-      s_invl[t * kBR + row] = has ? 1.f / l : 0.f;
-      if (row >= qw.lo && row < qw.hi) {
-        const float lse = has ? (m_ref * p.scale + log2f(l) * 0.69314718055994530942f) : -INFINITY;
-        const int i_seq = qw.load_row - w.q_start + row;
-        if constexpr (SPLIT)
-          p.ws_lse[static_cast<size_t>(w.split) * p.B * p.H * p.Nq + w.lse_base + i_seq] = lse;
-        else
-          p.lse[w.lse_base + i_seq] = lse;
+      } else {
+        float m_ref = -INFINITY;
+        float l = 0.f;
+  #pragma unroll 1
+        for (int j = 0; j < nt; ++j) {
+          if (!ptx::mbar_wait_warp(bar(L::kBarSFull + t), sc & 1u, s_abort, tmo)) {
+            record_error(p.status, kErrTimeout, kSiteSoftS);
+            ok = false;
+            break;
+          }
+          ++sc;
+          ptx::tc_fence_after();
+          uint32_t sr[BC];
+  #pragma unroll
+          for (int c = 0; c < BC / 32; ++c) ptx::tmem_ld32(tS + c * 32, &sr[c * 32]);
+          ptx::tmem_wait_ld();
+          float s[BC];
+  #pragma unroll
+          for (int c = 0; c < BC; ++c) s[c] = __uint_as_float(sr[c]);
+          if (w.j0 + j >= j_mask) {
+            const RowWindow kw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + (w.j0 + j) * BC, BC);
+            if (kw.lo != 0 || kw.hi != BC) {
+              // Keys outside [lo, hi) of this tile: past the end, or (variable
+              // length) before the sequence start / already seen by the previous tile.
+  #pragma unroll
+              for (int c = 0; c < BC; ++c)
+                if (c < kw.lo || c >= kw.hi) s[c] = -INFINITY;
+            }
+            const int kbase = kw.load_row - w.k_start;  // sequence index of column 0
+            if (CAUSAL && kbase + BC - 1 > first_row_lim) {
+              // The tile crosses the diagonal: mask keys above this row's limit.
+              const int lim = key_lim - kbase;
+  #pragma unroll
+              for (int c = 0; c < BC; ++c)
+                if (c > lim) s[c] = -INFINITY;
+            }
+          }
+          // Row max: four independent chains of three-input maxima.
+          float mx[4] = {s[0], s[1], s[2], s[3]};
+  #pragma unroll
+          for (int c = 4; c < BC; c += 8) {
+            mx[0] = ptx::fmax3(mx[0], s[c], s[c + 1]);
+            mx[1] = ptx::fmax3(mx[1], s[c + 2], s[c + 3]);
+            if (c + 4 < BC) {
+              mx[2] = ptx::fmax3(mx[2], s[c + 4], s[c + 5]);
+              mx[3] = ptx::fmax3(mx[3], s[c + 6], s[c + 7]);
+            }
+          }
+          const float bm = fmaxf(ptx::fmax3(mx[0], mx[1], mx[2]), mx[3]);
+          // Move the reference max only when the block max exceeds it by more
+          // than the threshold (log2 units): the merge identity of §11.2 holds
+          // for any common reference value, so results stay exact.
+          float m_new = m_ref;
+          if (bm > m_ref && (m_ref == -INFINITY || (bm - m_ref) * c2 > p.rescale_threshold)) m_new = bm;
+          const float alpha = (m_new == m_ref) ? 1.f : ptx::ex2((m_ref - m_new) * c2);
+          m_ref = m_new;
+          const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref * c2;
+          // p = 2^(s*c2 - m*c2): one packed FFMA per two scores, then ex2 each;
+          // row sums in four packed accumulators; P stored in 16-column chunks.
+          const uint64_t c2x2 = ptx::f2_pack(c2, c2);
+          const uint64_t negx2 = ptx::f2_pack(neg, neg);
+          uint64_t acc[4] = {0, 0, 0, 0};
+  #pragma unroll
+          for (int c0 = 0; c0 < BC; c0 += 32) {
+            uint32_t pk[16];
+  #pragma unroll
+            for (int c = c0; c < c0 + 32; c += 2) {
+              float x0, x1;
+              ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[c], s[c + 1]), c2x2, negx2), x0, x1);
+              const float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1);
+              const uint64_t e01 = ptx::f2_pack(e0, e1);
+              acc[(c >> 1) & 3] = ptx::f2_add(acc[(c >> 1) & 3], e01);
+              pk[(c - c0) / 2] = ptx::pack_bf16x2(e0, e1);
+            }
+            ptx::tmem_st16(tP + c0 / 2, pk);
+          }
+          float a0, a1, a2, a3, a4, a5, a6, a7;
+          ptx::f2_unpack(acc[0], a0, a1);
+          ptx::f2_unpack(acc[1], a2, a3);
+          ptx::f2_unpack(acc[2], a4, a5);
+          ptx::f2_unpack(acc[3], a6, a7);
+          l = l * alpha + (((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)));
+          if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            // Correction of the unnormalised output: O_t rows of this warp hold
+            // the sum over steps < j referenced to the old maximum.  Done after
+            // the exponentials (the scores are dead by then); it only has to
+            // land before P(j) is published.
+            const uint32_t tO = tmem + lane_off + static_cast<uint32_t>(2 * BC + t * D);
+            const uint64_t ax2 = ptx::f2_pack(alpha, alpha);
+  #pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t r[32];
+              ptx::tmem_ld32(tO + c * 32, r);
+              ptx::tmem_wait_ld();
+  #pragma unroll
+              for (int e = 0; e < 32; e += 2) {
+                float x0, x1;
+                ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), ax2), x0, x1);
+                r[e] = __float_as_uint(x0);
+                r[e + 1] = __float_as_uint(x1);
+              }
+              ptx::tmem_st32(tO + c * 32, r);
+            }
+          }
+          ptx::tmem_wait_st();  // P stores (and any O rescale) have landed
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(L::kBarPFull + t));
+        }
+        if (!ok) break;
+        // Final message for the epilogue: 1 / l, and the row's log-sum-exp.
+        const bool has = l > 0.f;
+        s_invl[t * kBR + row] = has ? 1.f / l : 0.f;
+        if (row >= qw.lo && row < qw.hi) {
+          const float lse = has ? (m_ref * p.scale + log2f(l) * 0.69314718055994530942f) : -INFINITY;
+          const int i_seq = qw.load_row - w.q_start + row;
+          if constexpr (SPLIT)
+            p.ws_lse[static_cast<size_t>(w.split) * p.B * p.H * p.Nq + w.lse_base + i_seq] = lse;
+          else
+            p.lse[w.lse_base + i_seq] = lse;
+        }
       }
       ptx::mbar_arrive(bar(L::kBarLReady + t));
     }

@@ -34,7 +34,7 @@ inline cudaError_t set_smem_once(const void* kern, int smem, std::atomic<unsigne
   return e;
 }
 
-template <int D, int BC, int STAGES, bool VARLEN, bool CAUSAL>
+template <int D, int BC, int STAGES, bool VARLEN, bool CAUSAL, bool QUAD = false>
 cudaError_t launch_fwd(const LaunchArgs& a);
 
 // Defined in the translation unit that owns the kernel.
@@ -43,6 +43,19 @@ cudaError_t launch_fwd(const LaunchArgs& a);
   cudaError_t launch_fwd<D, BC, STAGES, VARLEN, CAUSAL>(const LaunchArgs& a) {                \
     auto* kern = &fa_fwd_kernel<D, BC, STAGES, VARLEN, CAUSAL>;                               \
     constexpr int smem = SmemLayout<D, BC, STAGES>::kAlloc;                                   \
+    static std::atomic<unsigned long long> done{0};                                          \
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem, done);          \
+    if (e != cudaSuccess) return e;                                                           \
+    kern<<<a.grid, kThreads, smem, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);          \
+    return cudaGetLastError();                                                                \
+  }
+
+// The quad-shuffle softmax form (128-key tiles, no mask).
+#define FA_DEFINE_LAUNCH_QUAD(D, STAGES, VARLEN)                                              \
+  template <>                                                                                 \
+  cudaError_t launch_fwd<D, 128, STAGES, VARLEN, false, true>(const LaunchArgs& a) {          \
+    auto* kern = &fa_fwd_kernel<D, 128, STAGES, VARLEN, false, false, true>;                  \
+    constexpr int smem = SmemLayout<D, 128, STAGES>::kAlloc;                                  \
     static std::atomic<unsigned long long> done{0};                                          \
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem, done);          \
     if (e != cudaSuccess) return e;                                                           \

@@ -45,21 +45,27 @@ def test_version_and_strerror(L):
 def test_config_spec_roundtrip(L):
     try:
         fa.set_config("stages=3,threshold=0")
-        assert fa.get_config(64, 4096) == "br=256,bc=128,stages=3,threshold=0"
-        assert fa.get_config(128, 4096) == "br=256,bc=128,stages=2,threshold=0"  # two slots fit
+        assert fa.get_config(64, 4096) == "br=256,bc=128,stages=3,threshold=0,reduce=thread"
+        assert fa.get_config(128, 4096) == "br=256,bc=128,stages=2,threshold=0,reduce=thread"  # two slots fit
         fa.set_config("threshold=8")
-        assert fa.get_config(64, 512) == "br=256,bc=128,stages=4,threshold=8"
+        assert fa.get_config(64, 512) == "br=256,bc=128,stages=4,threshold=8,reduce=thread"
         fa.set_config("br=128,bc=64,stages=4")
-        assert fa.get_config(128, 4096) == "br=128,bc=64,stages=4,threshold=8"
-        assert fa.get_config(64, 100, True) == "br=128,bc=64,stages=4,threshold=8"
+        assert fa.get_config(128, 4096) == "br=128,bc=64,stages=4,threshold=8,reduce=thread"
+        assert fa.get_config(64, 100, True) == "br=128,bc=64,stages=4,threshold=8,reduce=thread"
+        fa.set_config("reduce=quad,stages=2")
+        assert fa.get_config(128, 4096) == "br=256,bc=128,stages=2,threshold=8,reduce=quad"
+        assert fa.get_config(64, 4096) == "br=256,bc=128,stages=3,threshold=8,reduce=quad"
+        fa.set_config("reduce=quad,bc=64")  # built for 128-key tiles only
+        assert fa.get_config(64, 4096) == "br=256,bc=64,stages=4,threshold=8,reduce=thread"
         for bad in ("stages=5", "stages=1", "threshold=-1", "foo=1", "stages", "threshold=nan",
-                    "bc=32", "bc=256", "br=64", "br=512", "stages=", "bc=", "br=1e3"):
+                    "bc=32", "bc=256", "br=64", "br=512", "stages=", "bc=", "br=1e3",
+                    "reduce=warp", "reduce="):
             with pytest.raises(fa.FaError):
                 fa.set_config(bad)
     finally:
         fa.set_config(None)
-    assert fa.get_config(128, 4096) == "br=256,bc=128,stages=2,threshold=8"
-    assert fa.get_config(64, 4096) == "br=256,bc=128,stages=3,threshold=8"
+    assert fa.get_config(128, 4096) == "br=256,bc=128,stages=2,threshold=8,reduce=thread"
+    assert fa.get_config(64, 4096) == "br=256,bc=128,stages=3,threshold=8,reduce=thread"
 
 
 def test_timeout_setter(L):

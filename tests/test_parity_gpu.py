@@ -199,6 +199,7 @@ def test_deterministic():
 # ------------------------------------------------------------ configurations
 CONFIG_SPACE = ["br=%d,bc=%d,stages=%d,threshold=%d" % (br, bc, st, th)
                 for br in (256, 128) for bc in (128, 64) for st in (2, 3, 4) for th in (0, 8)]
+CONFIG_SPACE += ["reduce=quad,threshold=0", "reduce=quad,threshold=8"]
 
 
 @pytest.mark.parametrize("spec", CONFIG_SPACE)
