@@ -17,6 +17,8 @@ in ``attn_ref.c``:
                       ("Flash Attention实现深度解析" §3.1)
 * ``attn_online``     the blockwise online recurrence ("GPU 内核与 FlashAttention"
                       §11.3 and §14.1), used only to check that it is exact
+* ``attn_bwd_dense``  the backward pass (§13.1): dQ, dK, dV and D_i from the full
+                      materialised P, with the causal mask and grouped heads
 
 Inputs are bf16 bit patterns (``numpy.uint16``); outputs are float64.
 """
@@ -70,8 +72,10 @@ def _load():
                                            ci, f64p, f64p]
         lib.oracle_attn_online.argtypes = [u16p, u16p, u16p, ci, ci, ci, ci, ci, cd, ci,
                                            f64p, f64p]
+        lib.oracle_attn_bwd_dense.argtypes = [u16p, u16p, u16p, u16p, ci, ci, ci, ci, ci, ci, cd,
+                                              ci, f64p, f64p, f64p, f64p]
         for name in ("oracle_attn_dense", "oracle_attn_dense_rows", "oracle_attn_varlen",
-                     "oracle_attn_online", "oracle_num_threads"):
+                     "oracle_attn_online", "oracle_attn_bwd_dense", "oracle_num_threads"):
             getattr(lib, name).restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ci]
         lib.oracle_set_num_threads.restype = None
@@ -182,3 +186,28 @@ def attn_online(q, k, v, block, scale=None):
     if rc != 0:
         raise ValueError("oracle_attn_online failed (%d)" % rc)
     return o, lse
+
+
+def attn_bwd_dense(q, k, v, dout, scale=None, causal=False):
+    """Backward pass.  q, dout: [B, Nq, H, d]; k, v: [B, Nk, Hk, d] (uint16 bf16 bits).
+
+    Returns (dq [B, Nq, H, d], dk [B, Nk, Hk, d], dv [B, Nk, Hk, d], delta [B, H, Nq]),
+    all float64; delta[b, h, i] = D_i = sum_j P_ij dP_ij."""
+    q, k, v, dout = _u16(q), _u16(k), _u16(v), _u16(dout)
+    B, Nq, H, d = q.shape
+    Nk, Hk = k.shape[1], k.shape[2]
+    if k.shape != (B, Nk, Hk, d) or v.shape != k.shape or dout.shape != q.shape or H % Hk:
+        raise ValueError("shape mismatch")
+    dq = np.zeros((B, Nq, H, d), np.float64)
+    dk = np.zeros((B, Nk, Hk, d), np.float64)
+    dv = np.zeros((B, Nk, Hk, d), np.float64)
+    delta = np.zeros((B, H, Nq), np.float64)
+    rc = _load().oracle_attn_bwd_dense(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+                                       _ptr(v, ctypes.c_uint16), _ptr(dout, ctypes.c_uint16),
+                                       B, Nq, Nk, H, Hk, d, _default_scale(d, scale),
+                                       int(bool(causal)), _ptr(dq, ctypes.c_double),
+                                       _ptr(dk, ctypes.c_double), _ptr(dv, ctypes.c_double),
+                                       _ptr(delta, ctypes.c_double))
+    if rc != 0:
+        raise MemoryError("oracle_attn_bwd_dense failed (%d)" % rc)
+    return dq, dk, dv, delta

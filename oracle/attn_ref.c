@@ -1,5 +1,5 @@
 /*
- * attn_ref.c -- plain fp64 CPU oracle for the attention forward pass.
+ * attn_ref.c -- plain fp64 CPU oracle for the attention forward and backward passes.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
  * load this file.  Its only users are the tests, the smoke check and the CPU
@@ -39,6 +39,17 @@
  *
  * Grouped key/value heads ([GKFA] §14.2, MQA/GQA): with Hk key/value heads and
  * H = G * Hk query heads, query head h reads key/value head h / G.
+ *
+ * Backward pass ([GKFA] §13.1), oracle_attn_bwd_dense(): for a loss phi with
+ * dO = d phi / d O given, and P the full softmax above (materialised),
+ *   dV = P^T dO
+ *   dP = dO V^T                       (dP_ij = do_i . v_j)
+ *   D_i = sum_j P_ij dP_ij            (the definition; §13.1 shows D_i = do_i . o_i)
+ *   dS = P o (dP - D)                 (softmax Jacobian, row by row)
+ *   dQ = scale * dS K,  dK = scale * dS^T Q
+ * The factor scale appears because S = scale * Q K^T.  With grouped heads the
+ * key/value gradients of the G query heads that share a K/V head are summed
+ * ([GKFA] §14.2).  Rows that see no key have P = 0 and contribute nothing.
  *
  * oracle_attn_online() restates the blockwise recurrence of [GKFA] §11.3 with
  * the deferred division of §14.1, again in double.  It exists only so tests can
@@ -146,6 +157,144 @@ static int head_attention(const uint16_t *q, size_t q_rs, int nq,
     }
     free(S);
     return 0;
+}
+
+/*
+ * Backward of one head (definitions in the header comment).  q/do rows i at
+ * q + i*q_rs and dout + i*q_rs; k/v rows j at k + j*kv_rs.  dq row i is
+ * written at dq + i*q_rs; dk/dv row j is ADDED at dk/dv + j*kv_rs (doubles),
+ * so query heads sharing a key/value head accumulate.  delta[i*delta_stride]
+ * receives D_i.  Returns 0, or -1 when P cannot be allocated.
+ */
+static int head_attention_bwd(const uint16_t *q, const uint16_t *dout, size_t q_rs, int nq,
+                              const uint16_t *k, const uint16_t *v, size_t kv_rs, int nk,
+                              int d, double scale, int causal, long offset,
+                              double *dq, double *dk, double *dv, double *delta,
+                              size_t delta_stride)
+{
+    if (nq <= 0)
+        return 0;
+    double *P = (double *)malloc((size_t)nq * (size_t)(nk > 0 ? nk : 1) * sizeof(double));
+    double *dP = (double *)malloc((size_t)nq * (size_t)(nk > 0 ? nk : 1) * sizeof(double));
+    if (!P || !dP) {
+        free(P);
+        free(dP);
+        return -1;
+    }
+    /* P: the forward's softmax, materialised (S = scale Q K^T, causal -inf,
+       safe softmax, rows with no visible key all zero). */
+    for (int i = 0; i < nq; ++i) {
+        double *row = P + (size_t)i * nk;
+        double m = -INFINITY;
+        for (int j = 0; j < nk; ++j) {
+            if (causal && (long)j > i + offset) {
+                row[j] = -INFINITY;
+                continue;
+            }
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c)
+                acc += bf16_to_double(q[(size_t)i * q_rs + c]) * bf16_to_double(k[(size_t)j * kv_rs + c]);
+            row[j] = scale * acc;
+            if (row[j] > m)
+                m = row[j];
+        }
+        double l = 0.0;
+        for (int j = 0; j < nk; ++j) {
+            row[j] = (m == -INFINITY) ? 0.0 : exp(row[j] - m);
+            l += row[j];
+        }
+        for (int j = 0; j < nk; ++j)
+            row[j] = (l > 0.0) ? row[j] / l : 0.0;
+    }
+    /* dV += P^T dO. */
+    for (int j = 0; j < nk; ++j) {
+        double *dvj = dv + (size_t)j * kv_rs;
+        for (int i = 0; i < nq; ++i) {
+            const double pij = P[(size_t)i * nk + j];
+            if (pij == 0.0)
+                continue;
+            for (int c = 0; c < d; ++c)
+                dvj[c] += pij * bf16_to_double(dout[(size_t)i * q_rs + c]);
+        }
+    }
+    /* dP = dO V^T; D_i = sum_j P_ij dP_ij; dS = P o (dP - D), stored over dP. */
+    for (int i = 0; i < nq; ++i) {
+        double Di = 0.0;
+        for (int j = 0; j < nk; ++j) {
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c)
+                acc += bf16_to_double(dout[(size_t)i * q_rs + c]) * bf16_to_double(v[(size_t)j * kv_rs + c]);
+            dP[(size_t)i * nk + j] = acc;
+            Di += P[(size_t)i * nk + j] * acc;
+        }
+        delta[(size_t)i * delta_stride] = Di;
+        for (int j = 0; j < nk; ++j)
+            dP[(size_t)i * nk + j] = P[(size_t)i * nk + j] * (dP[(size_t)i * nk + j] - Di);
+    }
+    /* dQ = scale dS K;  dK += scale dS^T Q. */
+    for (int i = 0; i < nq; ++i) {
+        double *dqi = dq + (size_t)i * q_rs;
+        for (int c = 0; c < d; ++c)
+            dqi[c] = 0.0;
+        for (int j = 0; j < nk; ++j) {
+            const double ds = dP[(size_t)i * nk + j];
+            if (ds == 0.0)
+                continue;
+            for (int c = 0; c < d; ++c)
+                dqi[c] += scale * ds * bf16_to_double(k[(size_t)j * kv_rs + c]);
+        }
+    }
+    for (int j = 0; j < nk; ++j) {
+        double *dkj = dk + (size_t)j * kv_rs;
+        for (int i = 0; i < nq; ++i) {
+            const double ds = dP[(size_t)i * nk + j];
+            if (ds == 0.0)
+                continue;
+            for (int c = 0; c < d; ++c)
+                dkj[c] += scale * ds * bf16_to_double(q[(size_t)i * q_rs + c]);
+        }
+    }
+    free(P);
+    free(dP);
+    return 0;
+}
+
+/*
+ * Dense backward.  q, dout, dq: [B, Nq, H, d]; k, v, dk, dv: [B, Nk, Hk, d];
+ * delta: [B, H, Nq] (D_i).  Inputs are bf16 bit patterns, outputs double.
+ * Parallel over (b, key/value head); the G query heads of a group run in
+ * order inside one task, so their dK/dV sums need no atomics.
+ */
+int oracle_attn_bwd_dense(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          const uint16_t *dout, int B, int Nq, int Nk, int H, int Hk, int d,
+                          double scale, int causal, double *dq, double *dk, double *dv,
+                          double *delta)
+{
+    if (Hk <= 0 || H % Hk != 0)
+        return -1;
+    int err = 0;
+    const int G = H / Hk;
+    const size_t q_rs = (size_t)H * d, kv_rs = (size_t)Hk * d;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1) reduction(| : err)
+    for (int b = 0; b < B; ++b) {
+        for (int hk = 0; hk < Hk; ++hk) {
+            const size_t kvoff = (size_t)b * Nk * Hk * d + (size_t)hk * d;
+            for (int j = 0; j < Nk; ++j)
+                for (int c = 0; c < d; ++c) {
+                    dk[kvoff + (size_t)j * kv_rs + c] = 0.0;
+                    dv[kvoff + (size_t)j * kv_rs + c] = 0.0;
+                }
+            for (int g = 0; g < G; ++g) {
+                const int h = hk * G + g;
+                const size_t qoff = (size_t)b * Nq * H * d + (size_t)h * d;
+                err |= head_attention_bwd(q + qoff, dout + qoff, q_rs, Nq, k + kvoff, v + kvoff,
+                                          kv_rs, Nk, d, scale, causal, (long)Nk - Nq, dq + qoff,
+                                          dk + kvoff, dv + kvoff,
+                                          delta + ((size_t)b * H + h) * Nq, 1);
+            }
+        }
+    }
+    return err ? -1 : 0;
 }
 
 int oracle_num_threads(void)
