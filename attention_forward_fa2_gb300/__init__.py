@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) FlashAttention-2 forward.
+"""GB300 (sm_103a) FlashAttention-2 forward (and backward).
 
 Thin Python binding over the C ABI declared in ``include/fa.h``: the functions
 named ``fa_*`` here take plain integers (device addresses) and sizes exactly
@@ -10,7 +10,8 @@ stream).  Every step of the computation runs in the CUDA kernels of
 
 What is computed ("GPU 内核与 FlashAttention" §10, §11.3, §14.1):
 ``O = softmax(scale * Q K^T) V`` per (batch, head), plus the fp32 natural-log
-log-sum-exp of every score row.
+log-sum-exp of every score row; ``backward`` gives dQ, dK, dV from dO, O and the
+log-sum-exp (§13).
 """
 from __future__ import annotations
 
@@ -40,6 +41,7 @@ EXPORTS = (
     "fa_set_timeout_ns", "fa_set_config", "fa_get_config", "fa_autotune",
     "fa_selftest_wait_timeout", "fa_version", "fa_splitkv_num_splits",
     "fa_splitkv_workspace_bytes", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc",
+    "fa_bwd_workspace_bytes", "fa_bwd",
 )
 
 
@@ -85,10 +87,14 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp,
                                      ctypes.c_ulonglong, vp]
         L.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
+        L.fa_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci]
+        L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp,
+                             ctypes.c_longlong, vp]
         for name in EXPORTS:
             if name != "fa_strerror":
                 getattr(L, name).restype = ci
         L.fa_splitkv_workspace_bytes.restype = ctypes.c_longlong
+        L.fa_bwd_workspace_bytes.restype = ctypes.c_longlong
         _lib = L
         return L
 
@@ -130,6 +136,19 @@ def splitkv_workspace_bytes(B, Nq, H, d, num_splits) -> int:
     n = lib().fa_splitkv_workspace_bytes(B, Nq, H, d, int(num_splits))
     if n < 0:
         raise FaError(int(n), "fa_splitkv_workspace_bytes")
+    return int(n)
+
+
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Nq, Nk, H, Hk, d, scale, flags, workspace,
+           workspace_bytes, stream) -> int:
+    return lib().fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Nq, Nk, H, Hk, d, scale, flags,
+                        workspace, workspace_bytes, stream)
+
+
+def bwd_workspace_bytes(B, Nq, H, d) -> int:
+    n = lib().fa_bwd_workspace_bytes(B, Nq, H, d)
+    if n < 0:
+        raise FaError(int(n), "fa_bwd_workspace_bytes")
     return int(n)
 
 
@@ -351,3 +370,39 @@ def forward_splitkv(q, k, v, scale=None, causal=False, num_splits=None, workspac
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_splitkv")
     return out, lse
+
+
+def backward(q, k, v, o, lse, dout, scale=None, causal=False, workspace=None, dq=None, dk=None,
+             dv=None, stream=None):
+    """Gradients (dq, dk, dv) of O = softmax(scale q k^T) v given dout = dL/dO.
+
+    q, o, dout: [B, Nq, H, d] bf16; k, v: [B, Nk, Hk, d] bf16 (H a multiple of
+    Hk); lse: [B, H, Nq] fp32 from the forward with the same causal flag;
+    contiguous CUDA tensors on one device, d = 128.  workspace: optional uint8
+    tensor of at least bwd_workspace_bytes(B, Nq, H, d) bytes."""
+    import torch
+    B, Nq, H, d = q.shape
+    Nk, Hk = k.shape[1], k.shape[2]
+    for t in (q, k, v, o, dout):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v, o, dout must be contiguous bf16 CUDA tensors")
+    if o.shape != q.shape or dout.shape != q.shape or v.shape != k.shape or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("shape mismatch")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [B, H, Nq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = bwd_workspace_bytes(B, Nq, H, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    with _on_device(q.device):
+        rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                    lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Nq, Nk, H, Hk, d,
+                    float(scale), FA_FLAG_CAUSAL if causal else 0, workspace.data_ptr(),
+                    workspace.numel(), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd")
+    return dq, dk, dv

@@ -108,14 +108,15 @@ int device_state(DeviceState** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Tiled bf16 tensor map with 128-byte swizzle.  dims/strides are innermost
-// first; strides are in bytes for dims 1..rank-1.
+// Tiled tensor map (bf16 with 128-byte swizzle unless told otherwise).
+// dims/strides are innermost first; strides are in bytes for dims 1..rank-1.
 int encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
-           const cuuint64_t* strides, const cuuint32_t* box) {
+           const cuuint64_t* strides, const cuuint32_t* box,
+           CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+           CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
-                        const_cast<void*>(ptr), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = g_encode(m, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     t_last_cuda_error = static_cast<int>(r);
@@ -425,6 +426,119 @@ int run_split(const Problem& P, const Config& cfg, int requested_splits, void* w
   return FA_OK;
 }
 
+// ---------------------------------------------------------------- backward
+int bwd_nq_pad(int Nq) { return (Nq + fa::kBwdBQ - 1) / fa::kBwdBQ * fa::kBwdBQ; }
+
+// Workspace: dq_acc fp32 [B, H, nq_pad, d], then lse2 and delta fp32 [B, H, nq_pad].
+size_t bwd_workspace_bytes(int B, int Nq, int H, int d) {
+  const size_t rows = static_cast<size_t>(B) * H * bwd_nq_pad(Nq);
+  return rows * (static_cast<size_t>(d) + 2) * sizeof(float);
+}
+
+struct BwdProblem {
+  const void *q, *k, *v, *o, *dout;
+  const float* lse;
+  void *dq, *dk, *dv;
+  int B, Nq, Nk, H, Hk, d;
+  float scale;
+  int flags;
+  void* ws;
+  long long ws_bytes;
+  cudaStream_t stream;
+};
+
+int run_bwd(const BwdProblem& P) {
+  if (P.B < 0 || P.Nq < 0 || P.Nk < 0 || P.H < 0 || P.Hk < 0) return FA_ERR_INVALID_ARG;
+  if ((P.flags & ~FA_FLAG_CAUSAL) != 0) return FA_ERR_INVALID_ARG;
+  if (P.H > 0 && (P.Hk == 0 || P.H % P.Hk != 0)) return FA_ERR_INVALID_ARG;
+  if (!(std::isfinite(P.scale) && P.scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (P.d != 128) return FA_ERR_UNSUPPORTED;
+  if (P.B == 0 || P.H == 0) return FA_OK;
+  if (P.Nk == 0) return P.Nq == 0 ? FA_OK : FA_ERR_INVALID_ARG;  // as the forward: queries need keys
+  if (!P.k || !P.v || !P.dk || !P.dv || !P.ws) return FA_ERR_INVALID_ARG;
+  if (P.Nq > 0 && (!P.q || !P.o || !P.dout || !P.lse || !P.dq)) return FA_ERR_INVALID_ARG;
+  for (const void* ptr : {P.q, P.k, P.v, P.o, P.dout, static_cast<const void*>(P.dq), static_cast<const void*>(P.dk),
+                          static_cast<const void*>(P.dv), static_cast<const void*>(P.ws)})
+    if (ptr && !aligned16(ptr)) return FA_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(P.lse) & 3u) != 0) return FA_ERR_ALIGN;
+  if (P.H > 65535 || P.B > 65535) return FA_ERR_INVALID_ARG;
+  const long long rows_pad = static_cast<long long>(P.B) * P.H * bwd_nq_pad(P.Nq);
+  if (rows_pad > 0x7fffffffLL || static_cast<long long>(P.B) * P.Nk > 0x7fffffffLL ||
+      static_cast<long long>(P.B) * P.Nq > 0x7fffffffLL)
+    return FA_ERR_INVALID_ARG;
+  if (P.ws_bytes < 0 || static_cast<size_t>(P.ws_bytes) < bwd_workspace_bytes(P.B, P.Nq, P.H, P.d))
+    return FA_ERR_INVALID_ARG;
+  DeviceState* st = nullptr;
+  const int drc = device_state(&st);
+  if (drc != FA_OK) return drc;
+
+  const int D = P.d;
+  const cuuint64_t esz = 2;
+  fa::BwdLaunchArgs a;
+  std::memset(&a, 0, sizeof(a));
+  fa::BwdParams& p = a.p;
+  p.B = P.B;
+  p.Nq = P.Nq;
+  p.Nk = P.Nk;
+  p.H = P.H;
+  p.Hk = P.Hk;
+  p.group = P.H / P.Hk;
+  p.causal = (P.flags & FA_FLAG_CAUSAL) ? 1 : 0;
+  p.nq_pad = bwd_nq_pad(P.Nq);
+  p.num_qb = p.nq_pad / fa::kBwdBQ;
+  p.num_kb = (P.Nk + fa::kBwdBK - 1) / fa::kBwdBK;
+  const long long units = static_cast<long long>(P.B) * P.Hk * p.num_kb;
+  if (units > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  p.num_units = static_cast<int>(units);
+  p.units_per_item = p.causal ? 2 : 1;
+  p.num_items = (p.num_units + p.units_per_item - 1) / p.units_per_item;
+  p.o = static_cast<const __nv_bfloat16*>(P.o);
+  p.dout = static_cast<const __nv_bfloat16*>(P.dout);
+  p.lse = P.lse;
+  p.dq_acc = static_cast<float*>(P.ws);
+  p.lse2 = p.dq_acc + static_cast<size_t>(rows_pad) * D;
+  p.delta = p.lse2 + rows_pad;
+  p.dq = static_cast<__nv_bfloat16*>(P.dq);
+  p.dk = static_cast<__nv_bfloat16*>(P.dk);
+  p.dv = static_cast<__nv_bfloat16*>(P.dv);
+  p.scale = P.scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(P.scale) * 1.4426950408889634);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    p.timeout_ns = g_timeout_ns;
+  }
+  p.status = st->status;
+
+  // Query-side maps: at least one row even when Nq = 0 (the kernel then loads
+  // nothing; the map only has to be valid).
+  const void* qptr = P.Nq > 0 ? P.q : P.k;
+  const void* doptr = P.Nq > 0 ? P.dout : P.k;
+  const int nq_map = P.Nq > 0 ? P.Nq : 1;
+  const int hq_map = P.Nq > 0 ? P.H : P.Hk;
+  cuuint64_t dq4[4] = {(cuuint64_t)D, (cuuint64_t)hq_map, (cuuint64_t)nq_map, (cuuint64_t)P.B};
+  cuuint64_t sq4[3] = {D * esz, (cuuint64_t)hq_map * D * esz, (cuuint64_t)nq_map * hq_map * D * esz};
+  cuuint64_t dk4[4] = {(cuuint64_t)D, (cuuint64_t)P.Hk, (cuuint64_t)P.Nk, (cuuint64_t)P.B};
+  cuuint64_t sk4[3] = {D * esz, (cuuint64_t)P.Hk * D * esz, (cuuint64_t)P.Nk * P.Hk * D * esz};
+  cuuint32_t box_q[4] = {64, 1, (cuuint32_t)fa::kBwdBQ, 1};
+  cuuint32_t box_k[4] = {64, 1, (cuuint32_t)fa::kBwdBK, 1};
+  cuuint64_t dacc[2] = {(cuuint64_t)D, (cuuint64_t)(rows_pad > 0 ? rows_pad : 1)};
+  cuuint64_t sacc[1] = {(cuuint64_t)D * 4};
+  cuuint32_t box_acc[2] = {32, (cuuint32_t)fa::kBwdBQ};
+  int e;
+  if ((e = encode(&a.tm_q, qptr, 4, dq4, sq4, box_q)) != FA_OK) return e;
+  if ((e = encode(&a.tm_do, doptr, 4, dq4, sq4, box_q)) != FA_OK) return e;
+  if ((e = encode(&a.tm_k, P.k, 4, dk4, sk4, box_k)) != FA_OK) return e;
+  if ((e = encode(&a.tm_v, P.v, 4, dk4, sk4, box_k)) != FA_OK) return e;
+  if ((e = encode(&a.tm_dq, P.ws, 2, dacc, sacc, box_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                  CU_TENSOR_MAP_SWIZZLE_NONE)) != FA_OK)
+    return e;
+  a.grid = dim3(static_cast<unsigned>(p.num_items < st->num_sms ? p.num_items : st->num_sms), 1, 1);
+  a.stream = P.stream;
+  const cudaError_t ce = p.causal ? fa::launch_bwd<128, true>(a) : fa::launch_bwd<128, false>(a);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  return FA_OK;
+}
+
 __global__ void wait_timeout_kernel(unsigned long long timeout_ns, int* status) {
   __shared__ __align__(8) unsigned long long bar;
   __shared__ int abort_flag;
@@ -601,6 +715,20 @@ int fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;
+}
+
+long long fa_bwd_workspace_bytes(int B, int Nq, int H, int d) {
+  if (B < 0 || Nq < 0 || H < 0) return FA_ERR_INVALID_ARG;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  return static_cast<long long>(bwd_workspace_bytes(B, Nq, H, d));
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+           void* dq, void* dk, void* dv, int B, int Nq, int Nk, int H, int Hk, int d, float scale, int flags,
+           void* workspace, long long workspace_bytes, void* stream) {
+  BwdProblem P{q, k, v, o, dout, lse, dq, dk, dv, B, Nq, Nk, H, Hk, d, scale, flags, workspace,
+               workspace_bytes, static_cast<cudaStream_t>(stream)};
+  return run_bwd(P);
 }
 
 int fa_splitkv_num_splits(int B, int Nq, int Nk, int H, int d, int requested) {

@@ -1,0 +1,641 @@
+// fa_bwd_kernel.cuh -- FlashAttention-2 backward pass for sm_103a (GB300).
+//
+// What it computes ("GPU 内核与 FlashAttention" §13): given the forward's
+// inputs, its output O and per-row log-sum-exp L, and dO = d(loss)/dO,
+//     P   = exp(scale * Q K^T - L)        (recomputed, never stored)
+//     dV  = P^T dO
+//     dP  = dO V^T
+//     D_i = do_i . o_i                    (§13.1: equals sum_j P_ij dP_ij)
+//     dS  = P o (dP - D)
+//     dQ  = scale * dS K,   dK = scale * dS^T Q
+// following the blockwise order of §13.2 (FA2's Algorithm 2): a preprocessing
+// kernel computes D (and clears the dQ accumulator), then the main kernel runs
+// with the key/value block outermost -- each work unit owns one block of 128
+// keys of one (batch, key/value head), keeps dK and dV on chip for the whole
+// unit, loops over every query block of every query head that reads this
+// key/value head (grouped heads are summed here, §14.2), and adds its share
+// of dQ into an fp32 accumulator in global memory (§14.3: dQ is the one
+// shared write; here the add is a TMA reduce-add performed at L2 instead of
+// per-element atomics).  A last kernel scales the accumulator into bf16 dQ.
+//
+// Main kernel, per step (one block of 64 queries of one head):
+//   S^T  = K Q^T        M=128 keys, N=64 queries, K=d     tensor memory S[g%2]
+//   dP^T = V dO^T       M=128 keys, N=64                  tensor memory dP
+//   P^T  = 2^(S^T * scale * log2 e - L * log2 e)           softmax warps, bf16 over S
+//   dS^T = P^T o (dP^T - D)                                bf16 over dP, and to
+//                                                          shared memory
+//   dV  += P^T dO       M=128 keys, N=d, K=64              P^T from tensor memory
+//   dK  += dS^T Q       M=128 keys, N=d, K=64              dS^T from tensor memory
+//   dQ^T = K^T dS^T     M=d, N=64 queries, K=128 keys      both from shared memory
+// Computing dQ transposed keeps every MMA at M = 128 and makes each TMEM lane a
+// feature index, so the drain warps write whole 128-byte rows of the fp32
+// accumulator.  Keys are TMEM lanes in the other products: one thread owns
+// one key row and half of the 64 query columns of a step.
+// Tensor memory (512 columns): S0 [0,64) S1 [64,128) dP [128,192)
+// dQ^T [192,256) dV [256,384) dK [384,512).  S is double-buffered, so the
+// next step's S = K Q^T runs while the softmax warps work on this step.
+// Softmax warpgroup c reads columns [32c, 32c + 32) of S and dP and writes
+// its 16 packed bf16 words (P^T, dS^T) over the first 16 of those columns --
+// columns no other warp reads -- so the K = 64 operand of the dV and dK
+// MMAs sits at word offsets 0, 8 (queries 0-31) and 32, 40 (queries 32-63).
+//
+// Roles (512 threads):
+//   warps 0-7   softmax: P, dS (warps 0-3 query columns 0-31, 4-7 columns 32-63)
+//   warps 8-11  dQ drain (TMEM -> shared -> TMA reduce-add) and the dK/dV epilogue
+//   warp 12     MMA issue (one thread) + TMEM allocation
+//   warp 13     TMA loads (one thread)
+//   warps 14-15 idle
+// Every wait is bounded (ptx.cuh mbar_wait); on a timeout the kernel records
+// the site, stops every role, drains its own copies and MMAs and frees TMEM.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "fa_fwd_kernel.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+
+constexpr int kBwdBK = 128;  // keys per work unit (M of the key-row products)
+constexpr int kBwdBQ = 64;   // queries per step
+
+struct BwdParams {
+  int B, Nq, Nk, H, Hk, group;
+  int causal;           // bottom-right aligned: query i sees keys j <= i + Nk - Nq
+  int nq_pad;           // Nq rounded up to kBwdBQ (row stride of lse2 / delta / dq_acc)
+  int num_qb;           // query blocks per head
+  int num_kb;           // key blocks per head
+  int num_units;        // B * Hk * num_kb
+  int units_per_item;   // 2 when causal (a balanced pair of key blocks)
+  int num_items;
+  const __nv_bfloat16* o;     // [B, Nq, H, d]  (preprocessing)
+  const __nv_bfloat16* dout;  // [B, Nq, H, d]  (preprocessing)
+  const float* lse;           // [B, H, Nq] natural log, from the forward
+  float* lse2;                // [B, H, nq_pad]  L * log2(e); +inf where no gradient flows
+  float* delta;               // [B, H, nq_pad]  D_i
+  float* dq_acc;              // [B, H, nq_pad, d] fp32
+  __nv_bfloat16* dq;          // [B, Nq, H, d]
+  __nv_bfloat16* dk;          // [B, Nk, Hk, d]
+  __nv_bfloat16* dv;          // [B, Nk, Hk, d]
+  float scale;
+  float scale_log2;           // scale * log2(e)
+  unsigned long long timeout_ns;
+  int* status;
+};
+
+// ------------------------------------------------------------ preprocessing
+// One warp per (b, h, i < nq_pad): D_i = sum_c do_ic o_ic in fp32, lse2_i,
+// and a zeroed row of the dQ accumulator.  Padding rows (i >= Nq) and rows
+// without keys (L = -inf) get lse2 = +inf, so their P is exactly 0.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdParams p) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const long long rows = static_cast<long long>(p.B) * p.H * p.nq_pad;
+  if (row >= rows) return;
+  const int i = static_cast<int>(row % p.nq_pad);
+  const long long bh = row / p.nq_pad;
+  const int h = static_cast<int>(bh % p.H);
+  const int b = static_cast<int>(bh / p.H);
+  constexpr int kPer = D / 32;  // elements per lane
+  float acc = 0.f;
+  float l2 = INFINITY;
+  if (i < p.Nq) {
+    const size_t off = ((static_cast<size_t>(b) * p.Nq + i) * p.H + h) * D + lane * kPer;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+      acc += __bfloat162float(p.dout[off + e]) * __bfloat162float(p.o[off + e]);
+    const float L = p.lse[static_cast<size_t>(bh) * p.Nq + i];
+    if (L > -INFINITY) l2 = L * 1.44269504088896340736f;
+  }
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+  if (lane == 0) {
+    p.delta[row] = acc;
+    p.lse2[row] = l2;
+  }
+  float* const dst = p.dq_acc + static_cast<size_t>(row) * D + lane * kPer;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) dst[e] = 0.f;
+}
+
+// dq[b, i, h, :] = bf16(scale * dq_acc[b, h, i, :]); one warp per row.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdParams p) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const long long rows = static_cast<long long>(p.B) * p.H * p.Nq;
+  if (row >= rows) return;
+  const int i = static_cast<int>(row % p.Nq);
+  const long long bh = row / p.Nq;
+  const int h = static_cast<int>(bh % p.H);
+  const int b = static_cast<int>(bh / p.H);
+  constexpr int kPer = D / 32;
+  const float* src = p.dq_acc + (static_cast<size_t>(bh) * p.nq_pad + i) * D + lane * kPer;
+  __nv_bfloat16* dst = p.dq + ((static_cast<size_t>(b) * p.Nq + i) * p.H + h) * D + lane * kPer;
+#pragma unroll
+  for (int e = 0; e < kPer; e += 2) {
+    const float x0 = src[e] * p.scale, x1 = src[e + 1] * p.scale;
+    *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(x0, x1);
+  }
+}
+
+// ---------------------------------------------------------------- main kernel
+template <int D, int STAGES>
+struct BwdSmem {
+  static constexpr int kKVBytes = kBwdBK * D * 2;        // one K or V block
+  static constexpr int kKVPanel = kBwdBK * 128;          // 64 features x 128 rows
+  static constexpr int kQBytes = kBwdBQ * D * 2;         // one Q or dO block
+  static constexpr int kQPanel = kBwdBQ * 128;
+  static constexpr int kSlotBytes = 2 * kQBytes;         // Q then dO
+  static constexpr int kDSBytes = kBwdBK * kBwdBQ * 2;   // dS^T, keys x queries
+  static constexpr int kDQWarpBytes = kBwdBQ * 32 * 4;   // 64 queries x 32 features fp32
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kKVBytes;
+  static constexpr int kOffQ = kOffV + kKVBytes;
+  static constexpr int kOffDS = kOffQ + STAGES * kSlotBytes;
+  static constexpr int kOffDQ = kOffDS + kDSBytes;
+  static constexpr int kOffLD = kOffDQ + 4 * kDQWarpBytes;  // per slot: lse2[64], delta[64]
+  static constexpr int kLDBytes = 2 * kBwdBQ * 4;
+  static constexpr int kOffBar = kOffLD + STAGES * kLDBytes;
+  static constexpr int kBarKVFull = 0;
+  static constexpr int kBarKVEmpty = 1;
+  static constexpr int kBarQFull = 2;
+  static constexpr int kBarQEmpty = kBarQFull + STAGES;
+  static constexpr int kBarSFull = kBarQEmpty + STAGES;  // two
+  static constexpr int kBarDPFull = kBarSFull + 2;
+  static constexpr int kBarPFull = kBarDPFull + 1;
+  static constexpr int kBarDSFull = kBarPFull + 1;
+  static constexpr int kBarDQFull = kBarDSFull + 1;
+  static constexpr int kBarDQEmpty = kBarDQFull + 1;
+  static constexpr int kBarAccFull = kBarDQEmpty + 1;
+  static constexpr int kBarAccEmpty = kBarAccFull + 1;
+  static constexpr int kBarTeardown = kBarAccEmpty + 1;
+  static constexpr int kNumBars = kBarTeardown + 1;
+  static constexpr int kOffTmem = kOffBar + ((kNumBars * 8 + 15) / 16) * 16;
+  static constexpr int kOffAbort = kOffTmem + 16;
+  static constexpr int kBytes = kOffAbort + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kOffV % 1024 == 0 && kOffQ % 1024 == 0 && kOffDS % 1024 == 0 && kOffDQ % 1024 == 0,
+                "swizzled tiles need 1 KiB alignment");
+  static_assert(kAlloc <= 232448, "shared memory budget exceeded");
+};
+
+// One work unit: key block kb of key/value head hk in batch b, and the query
+// blocks [qb0, num_qb) of each of the group's query heads.
+struct BwdUnit {
+  int b, hk, kb;
+  int qb0;     // first query block that sees any key of this block
+  int nqb;     // query blocks per head
+  int nsteps;  // group * nqb
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ BwdUnit bwd_decode(const BwdParams& p, int u) {
+  BwdUnit w;
+  int kb = u % p.num_kb;
+  if constexpr (CAUSAL) {
+    // Heaviest key blocks (the first ones: every query sees them) paired with
+    // the lightest, as consecutive units of one item.
+    const int pi = kb >> 1;
+    kb = (kb & 1) ? p.num_kb - 1 - pi : pi;
+  }
+  const int r = u / p.num_kb;
+  w.kb = kb;
+  w.hk = r % p.Hk;
+  w.b = r / p.Hk;
+  w.qb0 = 0;
+  if constexpr (CAUSAL) {
+    // Query i sees key j iff j <= i + off: the first query of interest is
+    // kb * 128 - off (never past the last query: every key j < Nk is seen by
+    // query Nq - 1).
+    const int first = kb * kBwdBK - (p.Nk - p.Nq);
+    w.qb0 = first <= 0 ? 0 : first / kBwdBQ;
+  }
+  w.nqb = p.num_qb - w.qb0;
+  w.nsteps = w.nqb > 0 ? p.group * w.nqb : 0;
+  return w;
+}
+
+#define FA_BWD_FOR_EACH_UNIT(u)                                                      \
+  for (int it_ = blockIdx.x; it_ < p.num_items && ok; it_ += gridDim.x)               \
+    for (int sub_ = 0, u = it_ * p.units_per_item;                                     \
+         sub_ < p.units_per_item && u < p.num_units && ok; ++sub_, ++u)
+
+// Wait-site identifiers recorded with a timeout.
+enum BwdSite : int {
+  kBSiteLoadKV = 101, kBSiteLoadQ = 102, kBSiteMmaKV = 103, kBSiteMmaQ = 104, kBSiteMmaP = 105,
+  kBSiteMmaDS = 106, kBSiteMmaDQ = 107, kBSiteMmaAcc = 108, kBSiteSoftS = 109, kBSiteSoftDP = 110,
+  kBSiteSoftDQ = 111, kBSiteSoftQ = 112, kBSiteDrainDQ = 113, kBSiteDrainAcc = 114, kBSiteTeardown = 115
+};
+
+template <int D, int STAGES, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+  static_assert(D == 128, "backward kernel: d = 128");
+  using L = BwdSmem<D, STAGES>;
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 192, kColDV = 256, kColDK = 384;
+  constexpr int kDPanels = D / 64;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw_base);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t bar0 = base + L::kOffBar;
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  volatile uint32_t* const s_tmem = reinterpret_cast<volatile uint32_t*>(gbase + L::kOffTmem);
+  volatile int* const s_abort = reinterpret_cast<volatile int*>(gbase + L::kOffAbort);
+  const float* const s_ld = reinterpret_cast<const float*>(gbase + L::kOffLD);
+  const uint64_t tmo = p.timeout_ns;
+
+  if (warp == 13 && lane == 0) {
+    ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+    ptx::prefetch_tmap(&tm_do);
+    ptx::prefetch_tmap(&tm_dq);
+  }
+  if (threadIdx.x == 0) {
+    *s_abort = 0;
+    ptx::mbar_init(bar(L::kBarKVFull), 1);
+    ptx::mbar_init(bar(L::kBarKVEmpty), 1);
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(bar(L::kBarQFull + s), 1);
+      ptx::mbar_init(bar(L::kBarQEmpty + s), 1);
+    }
+    ptx::mbar_init(bar(L::kBarSFull), 1);
+    ptx::mbar_init(bar(L::kBarSFull + 1), 1);
+    ptx::mbar_init(bar(L::kBarDPFull), 1);
+    ptx::mbar_init(bar(L::kBarPFull), 256);
+    ptx::mbar_init(bar(L::kBarDSFull), 256);
+    ptx::mbar_init(bar(L::kBarDQFull), 1);
+    ptx::mbar_init(bar(L::kBarDQEmpty), 128);
+    ptx::mbar_init(bar(L::kBarAccFull), 1);
+    ptx::mbar_init(bar(L::kBarAccEmpty), 128);
+    ptx::mbar_init(bar(L::kBarTeardown), 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 12) {
+    ptx::tmem_alloc(ptx::smem_u32(const_cast<uint32_t*>(s_tmem)), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const int off = p.Nk - p.Nq;
+
+  if (warp >= 12) {
+    if (warp == 13 && lane == 0) {
+      // ============================================================ TMA loads
+      uint32_t g = 0, uc = 0;
+      bool ok = true;
+#pragma unroll 1
+      FA_BWD_FOR_EACH_UNIT(u) {
+        const BwdUnit w = bwd_decode<CAUSAL>(p, u);
+        if (w.nsteps == 0) continue;
+        if (uc > 0 && !ptx::mbar_wait(bar(L::kBarKVEmpty), (uc - 1) & 1u, s_abort, tmo)) {
+          record_error(p.status, kErrTimeout, kBSiteLoadKV);
+          ok = false;
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(bar(L::kBarKVFull), 2 * L::kKVBytes);
+#pragma unroll
+        for (int pn = 0; pn < kDPanels; ++pn) {
+          ptx::tma_load_4d(base + L::kOffK + pn * L::kKVPanel, &tm_k, bar(L::kBarKVFull), pn * 64, w.hk,
+                           w.kb * kBwdBK, w.b);
+          ptx::tma_load_4d(base + L::kOffV + pn * L::kKVPanel, &tm_v, bar(L::kBarKVFull), pn * 64, w.hk,
+                           w.kb * kBwdBK, w.b);
+        }
+        ++uc;
+#pragma unroll 1
+        for (int i = 0; i < w.nsteps && ok; ++i, ++g) {
+          const uint32_t slot = g % STAGES;
+          if (g >= STAGES && !ptx::mbar_wait(bar(L::kBarQEmpty + slot), ((g / STAGES) - 1) & 1u, s_abort, tmo)) {
+            record_error(p.status, kErrTimeout, kBSiteLoadQ);
+            ok = false;
+            break;
+          }
+          const int h = w.hk * p.group + i / w.nqb;
+          const int qb = w.qb0 + i % w.nqb;
+          const uint32_t fb = bar(L::kBarQFull + slot);
+          ptx::mbar_arrive_expect_tx(fb, L::kSlotBytes + L::kLDBytes);
+          const uint32_t sq = base + L::kOffQ + slot * L::kSlotBytes;
+#pragma unroll
+          for (int pn = 0; pn < kDPanels; ++pn) {
+            ptx::tma_load_4d(sq + pn * L::kQPanel, &tm_q, fb, pn * 64, h, qb * kBwdBQ, w.b);
+            ptx::tma_load_4d(sq + L::kQBytes + pn * L::kQPanel, &tm_do, fb, pn * 64, h, qb * kBwdBQ, w.b);
+          }
+          const size_t ro = (static_cast<size_t>(w.b) * p.H + h) * p.nq_pad + static_cast<size_t>(qb) * kBwdBQ;
+          const uint32_t sld = base + L::kOffLD + slot * L::kLDBytes;
+          ptx::bulk_load(sld, p.lse2 + ro, kBwdBQ * 4, fb);
+          ptx::bulk_load(sld + kBwdBQ * 4, p.delta + ro, kBwdBQ * 4, fb);
+        }
+      }
+      // Drain: every issued copy must land before the CTA exits.
+      if (uc > 0) ptx::mbar_wait_drain(bar(L::kBarKVFull), (uc - 1) & 1u, tmo);
+      for (uint32_t s = 0; s < STAGES; ++s) {
+        if (g > s) {
+          const uint32_t rounds = (g - 1 - s) / STAGES + 1;
+          ptx::mbar_wait_drain(bar(L::kBarQFull + s), (rounds - 1) & 1u, tmo);
+        }
+      }
+    } else if (warp == 12 && lane == 0) {
+      // ============================================================ MMA issue
+      constexpr uint32_t id_s = ptx::idesc_bf16_f32(128, kBwdBQ, 0, 0);   // K Q^T, V dO^T
+      constexpr uint32_t id_acc = ptx::idesc_bf16_f32(128, D, 0, 1);      // P^T dO, dS^T Q
+      constexpr uint32_t id_dq = ptx::idesc_bf16_f32(D, kBwdBQ, 1, 1);    // K^T dS^T
+      uint32_t g = 0, uc = 0;
+      bool ok = true;
+      auto wait = [&](uint32_t b, uint32_t par, int site) -> bool {
+        if (ptx::mbar_wait(b, par, s_abort, tmo)) return true;
+        record_error(p.status, kErrTimeout, site);
+        ok = false;
+        return false;
+      };
+      // S^T(step) = K Q^T into S[step % 2].
+      auto issue_s = [&](uint32_t step) {
+        const uint32_t sq = base + L::kOffQ + (step % STAGES) * L::kSlotBytes;
+        const uint32_t dS = tmem + kColS + (step & 1u) * kBwdBQ;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t oa = (kk / 4) * L::kKVPanel + (kk % 4) * 32;
+          const uint32_t ob = (kk / 4) * L::kQPanel + (kk % 4) * 32;
+          ptx::mma_ss(dS, ptx::sw128_desc(base + L::kOffK + oa, 16, 1024), ptx::sw128_desc(sq + ob, 16, 1024),
+                      id_s, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(bar(L::kBarSFull + (step & 1u)));
+      };
+#pragma unroll 1
+      FA_BWD_FOR_EACH_UNIT(u) {
+        const BwdUnit w = bwd_decode<CAUSAL>(p, u);
+        if (w.nsteps == 0) continue;
+        if (!wait(bar(L::kBarKVFull), uc & 1u, kBSiteMmaKV)) break;
+        ptx::tc_fence_after();
+        if (!wait(bar(L::kBarQFull + g % STAGES), (g / STAGES) & 1u, kBSiteMmaQ)) break;
+        ptx::tc_fence_after();
+        issue_s(g);
+#pragma unroll 1
+        for (int i = 0; i < w.nsteps && ok; ++i, ++g) {
+          const uint32_t slot = g % STAGES;
+          const uint32_t sq = base + L::kOffQ + slot * L::kSlotBytes;
+          const uint32_t sdo = sq + L::kQBytes;
+          // dP^T = V dO^T (the previous step's dK, which read dS^T from these
+          // columns, was issued before and runs first).
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t oa = (kk / 4) * L::kKVPanel + (kk % 4) * 32;
+            const uint32_t ob = (kk / 4) * L::kQPanel + (kk % 4) * 32;
+            ptx::mma_ss(tmem + kColDP, ptx::sw128_desc(base + L::kOffV + oa, 16, 1024),
+                        ptx::sw128_desc(sdo + ob, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(bar(L::kBarDPFull));
+          // dV += P^T dO once the softmax warps have written P^T.
+          if (!wait(bar(L::kBarPFull), g & 1u, kBSiteMmaP)) break;
+          if (i == 0 && uc > 0 && !wait(bar(L::kBarAccEmpty), (uc - 1) & 1u, kBSiteMmaAcc)) break;
+          ptx::tc_fence_after();
+          const uint32_t tP = tmem + kColS + (g & 1u) * kBwdBQ;
+#pragma unroll
+          for (int kk = 0; kk < kBwdBQ / 16; ++kk)
+            ptx::mma_ts(tmem + kColDV, tP + (kk >> 1) * 32 + (kk & 1) * 8,
+                        ptx::sw128_desc(sdo + kk * 2048, L::kQPanel, 1024), id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+          // Next step's S into the other buffer (its P^T was read by the
+          // previous dV, issued earlier).  Issued only after P(g) is in, so
+          // the P-full barrier cannot run two phases ahead of this thread.
+          if (i + 1 < w.nsteps) {
+            if (!wait(bar(L::kBarQFull + (g + 1) % STAGES), ((g + 1) / STAGES) & 1u, kBSiteMmaQ)) break;
+            ptx::tc_fence_after();
+            issue_s(g + 1);
+          }
+          // dK += dS^T Q and dQ^T = K^T dS^T once dS^T is written.
+          if (!wait(bar(L::kBarDSFull), g & 1u, kBSiteMmaDS)) break;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBwdBQ / 16; ++kk)
+            ptx::mma_ts(tmem + kColDK, tmem + kColDP + (kk >> 1) * 32 + (kk & 1) * 8,
+                        ptx::sw128_desc(sq + kk * 2048, L::kQPanel, 1024), id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+          if (g > 0 && !wait(bar(L::kBarDQEmpty), (g - 1) & 1u, kBSiteMmaDQ)) break;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBwdBK / 16; ++kk)
+            ptx::mma_ss(tmem + kColDQ, ptx::sw128_desc(base + L::kOffK + kk * 2048, L::kKVPanel, 1024),
+                        ptx::sw128_desc(base + L::kOffDS + kk * 2048, L::kDSBytes, 1024), id_dq, kk > 0 ? 1u : 0u);
+          ptx::mma_commit(bar(L::kBarDQFull));
+          ptx::mma_commit(bar(L::kBarQEmpty + slot));
+        }
+        if (!ok) break;
+        ptx::mma_commit(bar(L::kBarAccFull));
+        ptx::mma_commit(bar(L::kBarKVEmpty));
+        ++uc;
+      }
+      ptx::mma_commit(bar(L::kBarTeardown));
+      if (!ptx::mbar_wait_drain(bar(L::kBarTeardown), 0, tmo)) record_error(p.status, kErrTimeout, kBSiteTeardown);
+    }
+  } else if (warp < 8) {
+    // ================================================================ softmax
+    const int c = warp >> 2;                    // query columns [32c, 32c + 32)
+    const int r = ((warp & 3) << 5) + lane;     // key row of the block
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
+    const float c2 = p.scale_log2;
+    uint32_t g = 0;
+    bool ok = true;
+#pragma unroll 1
+    FA_BWD_FOR_EACH_UNIT(u) {
+      const BwdUnit w = bwd_decode<CAUSAL>(p, u);
+      if (w.nsteps == 0) continue;
+      const int kj = w.kb * kBwdBK + r;  // this thread's key
+      const bool key_ok = kj < p.Nk;
+#pragma unroll 1
+      for (int i = 0; i < w.nsteps && ok; ++i, ++g) {
+        const uint32_t slot = g % STAGES;
+        const int qb = w.qb0 + i % w.nqb;
+        if (!ptx::mbar_wait_warp(bar(L::kBarSFull + (g & 1u)), (g >> 1) & 1u, s_abort, tmo) ||
+            !ptx::mbar_wait_warp(bar(L::kBarQFull + slot), (g / STAGES) & 1u, s_abort, tmo)) {
+          record_error(p.status, kErrTimeout, kBSiteSoftS);
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        uint32_t sr[32];
+        ptx::tmem_ld32(tmem + lane_off + kColS + (g & 1u) * kBwdBQ + c * 32, sr);
+        ptx::tmem_wait_ld();
+        const float* lse2 = s_ld + slot * (L::kLDBytes / 4) + c * 32;
+        const float* dlt = lse2 + kBwdBQ;
+        // Keys past Nk, and (causal) keys after a query's limit, get P = 0.
+        const int q0 = qb * kBwdBQ + c * 32;
+        const int lim = CAUSAL ? kj - off - q0 : -1;  // column k is masked when k < lim
+        float pr[32];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          float x0, x1;
+          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])),
+                                     ptx::f2_pack(c2, c2), ptx::f2_pack(-lse2[k], -lse2[k + 1])),
+                         x0, x1);
+          pr[k] = ptx::ex2(x0);
+          pr[k + 1] = ptx::ex2(x1);
+        }
+        if (!key_ok) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) pr[k] = 0.f;
+        } else if (CAUSAL && lim > 0) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (k < lim) pr[k] = 0.f;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) pk[k] = ptx::pack_bf16x2(pr[2 * k], pr[2 * k + 1]);
+        ptx::tmem_st16(tmem + lane_off + kColS + (g & 1u) * kBwdBQ + c * 32, pk);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::kBarPFull));
+        // dS^T = P^T o (dP^T - D)
+        if (!ptx::mbar_wait_warp(bar(L::kBarDPFull), g & 1u, s_abort, tmo)) {
+          record_error(p.status, kErrTimeout, kBSiteSoftDP);
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        uint32_t dr[32];
+        ptx::tmem_ld32(tmem + lane_off + kColDP + c * 32, dr);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float d0 = pr[2 * k] * (__uint_as_float(dr[2 * k]) - dlt[2 * k]);
+          const float d1 = pr[2 * k + 1] * (__uint_as_float(dr[2 * k + 1]) - dlt[2 * k + 1]);
+          pk[k] = ptx::pack_bf16x2(d0, d1);
+        }
+        ptx::tmem_st16(tmem + lane_off + kColDP + c * 32, pk);
+        // The same bf16 dS^T row into shared memory (B operand of dQ^T):
+        // 128 keys x 64 queries, 128-byte rows, 128-byte swizzle.  The
+        // previous step's dQ^T MMA must have read the buffer.
+        if (g > 0 && !ptx::mbar_wait_warp(bar(L::kBarDQFull), (g - 1) & 1u, s_abort, tmo)) {
+          record_error(p.status, kErrTimeout, kBSiteSoftDQ);
+          ok = false;
+          break;
+        }
+        const uint32_t row_addr = base + L::kOffDS + r * 128;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int chunk = 4 * c + q4;
+          ptx::st_shared_v4(row_addr + ((chunk ^ (r & 7)) << 4), pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2],
+                            pk[4 * q4 + 3]);
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::kBarDSFull));
+      }
+    }
+  } else {
+    // ======================================== dQ drain and the dK / dV epilogue
+    const int wq = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(wq << 5) << 16;
+    const uint32_t stage = base + L::kOffDQ + wq * L::kDQWarpBytes;
+    uint32_t g = 0, uc = 0;
+    bool pending = false;
+    bool ok = true;
+#pragma unroll 1
+    FA_BWD_FOR_EACH_UNIT(u) {
+      const BwdUnit w = bwd_decode<CAUSAL>(p, u);
+      const int kj = w.kb * kBwdBK + (wq << 5) + lane;
+      const size_t krow = ((static_cast<size_t>(w.b) * p.Nk + kj) * p.Hk + w.hk) * D;
+      if (w.nsteps == 0) {
+        // No query sees these keys: dK = dV = 0.
+        if (kj < p.Nk) {
+          for (int e = 0; e < D; e += 8) {
+            ptx::st_global_v4(p.dk + krow + e, 0u, 0u, 0u, 0u);
+            ptx::st_global_v4(p.dv + krow + e, 0u, 0u, 0u, 0u);
+          }
+        }
+        continue;
+      }
+#pragma unroll 1
+      for (int i = 0; i < w.nsteps && ok; ++i, ++g) {
+        const int h = w.hk * p.group + i / w.nqb;
+        const int qb = w.qb0 + i % w.nqb;
+        if (!ptx::mbar_wait_warp(bar(L::kBarDQFull), g & 1u, s_abort, tmo)) {
+          record_error(p.status, kErrTimeout, kBSiteDrainDQ);
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        uint32_t v[64];
+        ptx::tmem_ld32(tmem + lane_off + kColDQ, v);
+        ptx::tmem_ld32(tmem + lane_off + kColDQ + 32, v + 32);
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::kBarDQEmpty));
+        if (pending) {
+          if (lane == 0) ptx::bulk_wait_group_read_0();
+          __syncwarp();
+        }
+        // Box of 64 queries x 32 features (this warp's TMEM lanes), row-major.
+        float* const st = reinterpret_cast<float*>(gbase + L::kOffDQ + wq * L::kDQWarpBytes);
+#pragma unroll
+        for (int q = 0; q < kBwdBQ; ++q) st[q * 32 + lane] = __uint_as_float(v[q]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int row0 = (w.b * p.H + h) * p.nq_pad + qb * kBwdBQ;
+          ptx::tma_reduce_add_2d(&tm_dq, stage, wq * 32, row0);
+          ptx::bulk_commit_group();
+        }
+        pending = true;
+      }
+      if (!ok) break;
+      // Unit done: dK (times the scale) and dV to bf16, one key row per thread.
+      if (!ptx::mbar_wait_warp(bar(L::kBarAccFull), uc & 1u, s_abort, tmo)) {
+        record_error(p.status, kErrTimeout, kBSiteDrainAcc);
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which == 0 ? kColDV : kColDK;
+        const float mul = which == 0 ? 1.f : p.scale;
+        __nv_bfloat16* const dst = which == 0 ? p.dv : p.dk;
+#pragma unroll
+        for (int c4 = 0; c4 < D / 32; ++c4) {
+          uint32_t a[32];
+          ptx::tmem_ld32(tmem + lane_off + col + c4 * 32, a);
+          ptx::tmem_wait_ld();
+          if (kj < p.Nk) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint32_t wv[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                wv[e] = ptx::pack_bf16x2(__uint_as_float(a[8 * q4 + 2 * e]) * mul,
+                                         __uint_as_float(a[8 * q4 + 2 * e + 1]) * mul);
+              ptx::st_global_v4(dst + krow + c4 * 32 + q4 * 8, wv[0], wv[1], wv[2], wv[3]);
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(L::kBarAccEmpty));
+      ++uc;
+    }
+    if (lane == 0) ptx::bulk_wait_group_0();
+    __syncwarp();
+  }
+
+  // ---------------------------------------------------------------- teardown
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 12) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace fa

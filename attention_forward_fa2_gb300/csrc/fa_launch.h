@@ -6,6 +6,7 @@
 
 #include <atomic>
 
+#include "fa_bwd_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {
@@ -78,6 +79,18 @@ cudaError_t launch_fwd_split(const LaunchArgs& a);
     kern<<<a.grid, kThreads, smem, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);          \
     return cudaGetLastError();                                                                \
   }
+
+// Backward pass (fa_bwd_kernel.cuh): preprocessing, the key-block kernel and
+// the dQ conversion, enqueued in that order on a.stream.
+struct BwdLaunchArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dq;
+  BwdParams p;
+  dim3 grid;
+  cudaStream_t stream;
+};
+
+template <int D, bool CAUSAL>
+cudaError_t launch_bwd(const BwdLaunchArgs& a);
 
 // Merge of the key splits (fa_combine.cuh); D in {64, 128}.
 cudaError_t launch_combine(int D, const float* ws_o, const float* ws_lse, int S, long long rows, int H,

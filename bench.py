@@ -22,7 +22,9 @@ cpu_baseline  the fp64 CPU oracle (test infrastructure) timed on a bounded
 
 --impl reference times that oracle as the reference arm (the pages ship no
 implementation; the oracle is the reference), printing the same JSON line.
-Rank 0 prints one JSON line on stdout.
+--bwd times the backward pass instead (fa_bwd: preprocessing, key-block kernel,
+dQ conversion), FLOPs counted as 2.5x the forward's (five matrix products
+against two).  Rank 0 prints one JSON line on stdout.
 """
 from __future__ import annotations
 
@@ -426,6 +428,119 @@ def run_ours(args, w):
     return 0
 
 
+BWD_METRIC = "attention bwd TFLOP/s (bf16, 2.5x forward FLOPs) and % of GB300 bf16 peak"
+
+
+def run_bwd(args, w):
+    """Backward pass over the (dense, d = 128) workload: device time per step
+    with inputs resident, and the same through the public call with host
+    buffers (q, k, v, o, lse, dO in; dq, dk, dv out)."""
+    import torch
+    import attention_forward_fa2_gb300 as fa
+    from attention_forward_fa2_gb300 import build as fabuild
+    from attention_forward_fa2_gb300 import inputs as I
+
+    if w.varlen or w.d != 128:
+        raise SystemExit("--bwd takes dense d = 128 workloads")
+    rank, local, world = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    fabuild.build()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    q, k, v, _, _ = I.make(w)
+    dout = I.randn_bf16(tuple(q.shape), torch.Generator().manual_seed(w.seed + 1000))
+    dq, dk, dv, ddo = q.to(dev), k.to(dev), v.to(dev), dout.to(dev)
+    o, lse = fa.forward_qk(dq, dk, dv, causal=args.causal)
+    ws = torch.empty(fa.bwd_workspace_bytes(w.B, w.Nq, w.H, w.d), dtype=torch.uint8, device=dev)
+    gq, gk, gv = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
+
+    def step():
+        fa.backward(dq, dk, dv, o, lse, ddo, causal=args.causal, workspace=ws, dq=gq, dk=gk, dv=gv)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    rc, info = fa.check_status()
+    if rc != fa.FA_OK:
+        raise SystemExit("device error during warm-up: %s %s" % (fa.strerror(rc), info))
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    sampler = ClockSampler("GPU-%s" % uuid if uuid is not None else str(local))
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    rc, info = fa.check_status()
+    if rc != fa.FA_OK:
+        raise SystemExit("device error in the timed region: %s %s" % (fa.strerror(rc), info))
+    ms_max = max_over_ranks(ms, world)
+    flops = 2.5 * w.flops(causal=args.causal)
+    value = world * flops / (ms_max * 1e-3) / 1e12
+    step_tflops = flops / (ms * 1e-3) / 1e12
+
+    e2e_steps = max(3, min(args.steps, 10))
+    hosts = [t.pin_memory() for t in (q, k, v, o.cpu(), lse.cpu(), dout)]
+    devs = [dq, dk, dv, o, lse, ddo]
+    outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (gq, gk, gv)]
+
+    def e2e_step():
+        for d_, h_ in zip(devs, hosts):
+            d_.copy_(h_, non_blocking=True)
+        step()
+        for h_, d_ in zip(outs, (gq, gk, gv)):
+            h_.copy_(d_, non_blocking=True)
+
+    e2e_step()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    if rank != 0:
+        return 0
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    line = {
+        "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q, k, v, dO; o and lse from the forward)",
+        "config": dict(workload_config(w, None, args.causal), launch="stream launches",
+                       form="backward (fa_bwd)"),
+        "pct_of_peak": 100.0 * step_tflops / peak,
+        "roofline": {"bound": "tensor", "achieved": step_tflops, "peak": peak, "unit": UNIT,
+                     "frac": step_tflops / peak, "traffic": None,
+                     "peak_source": "%s bf16 dense burst (MEASURED_PEAKS.json)" % src
+                     if src == "measured" else "fallback 1.9 PFLOP/s bf16",
+                     "kernel": "fa_bwd step (prep + fa_bwd_kernel<128> + dq conversion); achieved is "
+                               "per step, a lower bound for the key-block kernel",
+                     "algorithmic_flops_per_launch": flops},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hosts),
+                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs),
+                "ms_per_step": e2e_ms, "steps": e2e_steps},
+        "gpu_launches": args.steps * 3,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     from attention_forward_fa2_gb300 import inputs as I
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -441,6 +556,7 @@ def main(argv=None):
                     help="key-split form (short query sets); launches also count the merge kernel")
     ap.add_argument("--causal", action="store_true",
                     help="causal mask (FLOPs count the visible query/key pairs only)")
+    ap.add_argument("--bwd", action="store_true", help="time the backward pass instead")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
@@ -449,6 +565,8 @@ def main(argv=None):
     w = I.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.bwd:
+        return run_bwd(args, w)
     return run_ours(args, w)
 
 

@@ -175,6 +175,35 @@ const char* fa_strerror(int code);
 int fa_last_cuda_error(void);
 
 /*
+ * Backward pass ("GPU 内核与 FlashAttention" §13.2, FlashAttention-2's blockwise
+ * backward): gradients of O = softmax(scale * Q K^T) V with respect to q, k
+ * and v, given dout = dLoss/dO, the forward's output o and its log-sum-exp.
+ *   q, o, dout, dq : [B, Nq, H, d] bf16, contiguous
+ *   k, v, dk, dv   : [B, Nk, Hk, d] bf16, contiguous (H a multiple of Hk; the
+ *                    key/value gradients of the H/Hk query heads sharing a
+ *                    key/value head are summed, §14.2)
+ *   lse            : [B, H, Nq] fp32, natural log, as written by the forward
+ *                    with the same flags (rows with lse = -inf get no gradient)
+ *   flags          : 0 or FA_FLAG_CAUSAL (the forward's mask)
+ *   workspace      : device memory of at least fa_bwd_workspace_bytes(B, Nq, H,
+ *                    d) bytes, 16-byte aligned, owned by the caller; fully
+ *                    overwritten (the fp32 dQ accumulator, D = rowsum(dO o O)
+ *                    and the scaled log-sum-exp), nothing needs to persist.
+ * d = 128 only (FA_ERR_UNSUPPORTED otherwise); dense tensors only.  Three
+ * kernels are enqueued on `stream`: preprocessing (D and a cleared
+ * accumulator), the key-block kernel (writes dk, dv; adds dQ into the
+ * accumulator) and the conversion of the accumulator to bf16 dq.  Errors as
+ * fa_fwd_ex; FA_ERR_INVALID_ARG also for a missing or short workspace.
+ * B = 0 or H = 0 (or Nq = Nk = 0) is a no-op; Nq > 0 with Nk = 0 is
+ * FA_ERR_INVALID_ARG as in the forward; Nq = 0 writes dk = dv = 0.
+ * fa_bwd_workspace_bytes returns the size, or a negative FA_* code.
+ */
+long long fa_bwd_workspace_bytes(int B, int Nq, int H, int d);
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, int B, int Nq, int Nk, int H, int Hk,
+           int d, float scale, int flags, void* workspace, long long workspace_bytes, void* stream);
+
+/*
  * fa_set_timeout_ns -- limit for every device-side wait (mbarrier waits) in
  * later launches.  On expiry the kernel records FA_ERR_TIMEOUT, drains its
  * own copies and MMAs, releases tensor memory and exits.  Default 1e9 ns.

@@ -166,3 +166,31 @@ def test_splitkv_workspace_arithmetic(L):
     assert L.fa_splitkv_workspace_bytes(1, 64, 1, 128, 129) == fa.FA_ERR_INVALID_ARG
     # variable-length tensors are not accepted by the key-split form
     assert L.fa_splitkv_num_splits(1, 64, 4096, 1, 96, 0) == fa.FA_ERR_INVALID_ARG
+
+
+def test_backward_workspace_and_argument_errors(L):
+    """Backward sizes and the checks made before any device work."""
+    rows = 2 * 3 * 128  # B * H * Nq rounded up to 64-query blocks (100 -> 128)
+    assert fa.bwd_workspace_bytes(2, 100, 3, 128) == rows * (128 + 2) * 4
+    assert fa.bwd_workspace_bytes(1, 0, 1, 128) == 0
+    with pytest.raises(fa.FaError) as e:
+        fa.bwd_workspace_bytes(1, 64, 1, 64)
+    assert e.value.code == fa.FA_ERR_UNSUPPORTED
+    with pytest.raises(fa.FaError):
+        fa.bwd_workspace_bytes(-1, 64, 1, 128)
+    args = dict(q=16, k=16, v=16, o=16, dout=16, lse=16, dq=16, dk=16, dv=16, B=1, Nq=64, Nk=64, H=1,
+                Hk=1, d=128, scale=0.1, flags=0, workspace=16, workspace_bytes=1 << 20, stream=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return fa.fa_bwd(*a.values())
+
+    assert call(d=64) == fa.FA_ERR_UNSUPPORTED
+    assert call(flags=4) == fa.FA_ERR_INVALID_ARG
+    assert call(scale=0.0) == fa.FA_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert call(H=3, Hk=2) == fa.FA_ERR_INVALID_ARG
+    assert call(B=-1) == fa.FA_ERR_INVALID_ARG
+    assert call(B=0) == fa.FA_OK   # nothing to do
+    assert call(Nk=0) == fa.FA_ERR_INVALID_ARG  # queries without keys, as in the forward
+    assert call(Nk=0, Nq=0) == fa.FA_OK

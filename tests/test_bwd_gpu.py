@@ -1,0 +1,138 @@
+"""GPU parity of the backward pass (fa_bwd through the C ABI) against the fp64 oracle.
+
+Bar (derived from the arithmetic): P and dS enter the tensor-core products as
+bf16 (relative rounding 2^-9, unbiased), accumulation is fp32 and the outputs
+are rounded to bf16 (2^-9 relative), so each gradient tensor must satisfy
+max|g - g_ref| <= 2e-2 * max|g_ref| and rms(g - g_ref) <= 1e-2 * rms(g_ref),
+plus an absolute floor of 1e-4 (1e-5 for the rms) for gradients that vanish
+exactly (one key: dQ = 0), where fp32 rounding of dP - D is all that is left.
+The forward O and LSE that feed the backward come from the GPU forward.
+"""
+import numpy as np
+import pytest
+import torch
+
+import attention_forward_fa2_gb300 as fa
+from attention_forward_fa2_gb300 import build as fabuild
+from attention_forward_fa2_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+MAX_REL = 2e-2
+RMS_REL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    fabuild.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _inputs(B, Nq, Nk, H, Hk, d, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = I.randn_bf16((B, Nq, H, d), g)
+    k = I.randn_bf16((B, Nk, Hk, d), g)
+    v = I.randn_bf16((B, Nk, Hk, d), g)
+    do = I.randn_bf16((B, Nq, H, d), g)
+    return q, k, v, do
+
+
+def _gpu_grads(q, k, v, do, causal):
+    dq_, dk_, dv_, ddo = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = fa.forward_qk(dq_, dk_, dv_, causal=causal)
+    gq, gk, gv = fa.backward(dq_, dk_, dv_, o, lse, ddo, causal=causal)
+    rc, info = fa.check_status()
+    assert rc == fa.FA_OK, (fa.strerror(rc), info)
+    return tuple(t.double().cpu().numpy() for t in (gq, gk, gv))
+
+
+def _assert_grads(got, ref, what):
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        assert np.all(np.isfinite(g)), "%s %s: non-finite" % (what, name)
+        mx = float(np.abs(r).max()) if r.size else 0.0
+        err = float(np.abs(g - r).max()) if r.size else 0.0
+        rms_r = float(np.sqrt(np.mean(r ** 2))) if r.size else 0.0
+        rms_e = float(np.sqrt(np.mean((g - r) ** 2))) if r.size else 0.0
+        assert err <= MAX_REL * mx + 1e-4, "%s %s: max err %.3g vs max|ref| %.3g" % (what, name, err, mx)
+        assert rms_e <= RMS_REL * rms_r + 1e-5, "%s %s: rms err %.3g vs rms ref %.3g" % (what, name, rms_e, rms_r)
+
+
+@pytest.mark.parametrize("B,Nq,Nk,H,Hk", [
+    (1, 256, 256, 2, 2),     # tiny: two key blocks, four query steps
+    (2, 200, 333, 4, 2),     # ragged in both lengths, grouped heads
+    (1, 1, 1, 1, 1),         # one query, one key
+    (1, 65, 129, 2, 1),      # one row past a query step, one key past a key block (MQA)
+    (1, 300, 100, 2, 2),     # more queries than keys
+    (1, 1024, 1024, 2, 1),   # many steps per unit
+    (3, 130, 260, 6, 3),
+])
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_oracle(oracle_mod, B, Nq, Nk, H, Hk, causal):
+    q, k, v, do = _inputs(B, Nq, Nk, H, Hk, 128, 1000 + Nq + Nk + causal)
+    got = _gpu_grads(q, k, v, do, causal)
+    ref = oracle_mod.attn_bwd_dense(I.bf16_bits(q), I.bf16_bits(k), I.bf16_bits(v), I.bf16_bits(do),
+                                    causal=causal)[:3]
+    _assert_grads(got, ref, "B%d Nq%d Nk%d H%d Hk%d causal%d" % (B, Nq, Nk, H, Hk, causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_page_workload_sampled_heads(oracle_mod, causal):
+    """The page workload (B16 N4096 H16 d128) in one call; two heads, the
+    first and the last, checked in full against the oracle."""
+    w = I.PAGE
+    q, k, v, _, _ = I.make(w)
+    do = I.randn_bf16(tuple(q.shape), torch.Generator().manual_seed(77))
+    got = _gpu_grads(q, k, v, do, causal)
+    for b, h in ((0, 0), (w.B - 1, w.H - 1)):
+        sl = lambda t: t[b:b + 1, :, h:h + 1].contiguous()
+        ref = oracle_mod.attn_bwd_dense(I.bf16_bits(sl(q)), I.bf16_bits(sl(k)), I.bf16_bits(sl(v)),
+                                        I.bf16_bits(sl(do)), causal=causal)[:3]
+        mine = tuple(g[b:b + 1, :, h:h + 1] for g in got)
+        _assert_grads(mine, ref, "page b%d h%d causal%d" % (b, h, causal))
+
+
+def test_key_gradients_sum_to_zero_on_gpu():
+    """sum_j dK_j = 0 for every (b, head) (softmax rows annihilate constants)."""
+    q, k, v, do = _inputs(2, 512, 640, 4, 4, 128, 5)
+    _, gk, _ = _gpu_grads(q, k, v, do, False)
+    col = np.abs(gk.sum(axis=1)).max()
+    assert col <= 2e-2 * np.abs(gk).max() * np.sqrt(640), col
+
+
+def test_no_queries_gives_zero_key_gradients():
+    k = torch.randn(1, 200, 2, 128, dtype=torch.bfloat16, device="cuda")
+    v = torch.randn_like(k)
+    q = torch.empty(1, 0, 2, 128, dtype=torch.bfloat16, device="cuda")
+    o, do = torch.empty_like(q), torch.empty_like(q)
+    lse = torch.empty(1, 2, 0, dtype=torch.float32, device="cuda")
+    dk = torch.full_like(k, 7.0)
+    dv = torch.full_like(v, 7.0)
+    _, gk, gv = fa.backward(q, k, v, o, lse, do, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert fa.check_status()[0] == fa.FA_OK
+    assert torch.all(gk == 0) and torch.all(gv == 0)
+
+
+def test_backward_errors():
+    q = torch.randn(1, 64, 2, 64, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(1, 2, 64, device="cuda")
+    with pytest.raises(fa.FaError) as e:
+        fa.backward(q, q, q, q, lse, q)  # d = 64: not built
+    assert e.value.code == fa.FA_ERR_UNSUPPORTED
+    q = torch.randn(1, 64, 2, 128, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fa.FaError) as e:
+        fa.backward(q, q, q, q, lse, q, workspace=ws)
+    assert e.value.code == fa.FA_ERR_INVALID_ARG
+
+
+def test_backward_is_repeatable():
+    """dK and dV are sums in a fixed order (bit-identical reruns); dQ is
+    accumulated with L2 reduce-adds whose order varies, so it is compared
+    within rounding."""
+    q, k, v, do = _inputs(1, 512, 512, 2, 2, 128, 9)
+    a = _gpu_grads(q, k, v, do, False)
+    b = _gpu_grads(q, k, v, do, False)
+    assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+    assert np.abs(a[0] - b[0]).max() <= 1e-2 * np.abs(a[0]).max()
