@@ -521,17 +521,11 @@ int run_bwd(const BwdProblem& P) {
   cuuint64_t sk4[3] = {D * esz, (cuuint64_t)P.Hk * D * esz, (cuuint64_t)P.Nk * P.Hk * D * esz};
   cuuint32_t box_q[4] = {64, 1, (cuuint32_t)fa::kBwdBQ, 1};
   cuuint32_t box_k[4] = {64, 1, (cuuint32_t)fa::kBwdBK, 1};
-  cuuint64_t dacc[2] = {(cuuint64_t)D, (cuuint64_t)(rows_pad > 0 ? rows_pad : 1)};
-  cuuint64_t sacc[1] = {(cuuint64_t)D * 4};
-  cuuint32_t box_acc[2] = {32, (cuuint32_t)fa::kBwdBQ};
   int e;
   if ((e = encode(&a.tm_q, qptr, 4, dq4, sq4, box_q)) != FA_OK) return e;
   if ((e = encode(&a.tm_do, doptr, 4, dq4, sq4, box_q)) != FA_OK) return e;
   if ((e = encode(&a.tm_k, P.k, 4, dk4, sk4, box_k)) != FA_OK) return e;
   if ((e = encode(&a.tm_v, P.v, 4, dk4, sk4, box_k)) != FA_OK) return e;
-  if ((e = encode(&a.tm_dq, P.ws, 2, dacc, sacc, box_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                  CU_TENSOR_MAP_SWIZZLE_NONE)) != FA_OK)
-    return e;
   a.grid = dim3(static_cast<unsigned>(p.num_items < st->num_sms ? p.num_items : st->num_sms), 1, 1);
   a.stream = P.stream;
   const cudaError_t ce = p.causal ? fa::launch_bwd<128, true>(a) : fa::launch_bwd<128, false>(a);

@@ -4,7 +4,7 @@
 namespace fa {
 
 namespace {
-constexpr int kBwdStages = 2;
+constexpr int kBwdStages = 4;
 
 template <int D, bool CAUSAL>
 cudaError_t launch_bwd_impl(const BwdLaunchArgs& a) {
@@ -21,7 +21,7 @@ cudaError_t launch_bwd_impl(const BwdLaunchArgs& a) {
   static std::atomic<unsigned long long> done{0};
   e = set_smem_once(reinterpret_cast<const void*>(kern), smem, done);
   if (e != cudaSuccess) return e;
-  kern<<<a.grid, kThreads, smem, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq, a.p);
+  kern<<<a.grid, kThreads, smem, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (dq_rows > 0) fa_bwd_dq_kernel<D><<<static_cast<unsigned>((dq_rows + 7) / 8), 256, 0, a.stream>>>(a.p);

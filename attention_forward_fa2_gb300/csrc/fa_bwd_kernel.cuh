@@ -15,25 +15,36 @@
 // unit, loops over every query block of every query head that reads this
 // key/value head (grouped heads are summed here, §14.2), and adds its share
 // of dQ into an fp32 accumulator in global memory (§14.3: dQ is the one
-// shared write; here the add is a TMA reduce-add performed at L2 instead of
-// per-element atomics).  A last kernel scales the accumulator into bf16 dQ.
+// shared write, accumulated with atomic adds; here reductions straight from
+// registers, performed at L2).  A last kernel scales the accumulator into
+// bf16 dQ.
 //
 // Main kernel, per step (one block of 64 queries of one head):
 //   S^T  = K Q^T        M=128 keys, N=64 queries, K=d     tensor memory S[g%2]
-//   dP^T = V dO^T       M=128 keys, N=64                  tensor memory dP
+//   dP^T = V dO^T       M=128 keys, N=64                  tensor memory dP[g%2]
 //   P^T  = 2^(S^T * scale * log2 e - L * log2 e)           softmax warps, bf16 over S
 //   dS^T = P^T o (dP^T - D)                                bf16 over dP, and to
 //                                                          shared memory
 //   dV  += P^T dO       M=128 keys, N=d, K=64              P^T from tensor memory
 //   dK  += dS^T Q       M=128 keys, N=d, K=64              dS^T from tensor memory
-//   dQ^T = K^T dS^T     M=d, N=64 queries, K=128 keys      both from shared memory
+//   dQ^T = K^T dS^T     M=d, N=64 queries, K=128 keys      both from shared memory,
+//                                                          result over dP[g%2]
 // Computing dQ transposed keeps every MMA at M = 128 and makes each TMEM lane a
-// feature index, so the drain warps write whole 128-byte rows of the fp32
-// accumulator.  Keys are TMEM lanes in the other products: one thread owns
+// feature index: for each query the 32 lanes of a drain warp hold 32
+// consecutive features, one 128-byte line of the [B, H, queries, d]
+// accumulator, so one reduction instruction per query adds a whole line and
+// nothing is staged in shared memory (shared-memory bandwidth, not the tensor
+// pipe, is what limits this kernel).  Keys are TMEM lanes in the other products: one thread owns
 // one key row and half of the 64 query columns of a step.
-// Tensor memory (512 columns): S0 [0,64) S1 [64,128) dP [128,192)
-// dQ^T [192,256) dV [256,384) dK [384,512).  S is double-buffered, so the
-// next step's S = K Q^T runs while the softmax warps work on this step.
+// Tensor memory (512 columns): S0 [0,64) S1 [64,128) dP0 [128,192)
+// dP1 [192,256) dV [256,384) dK [384,512); dQ^T(g) reuses dP[g%2] once dK(g)
+// has read dS^T from it.  The single MMA thread issues, per step g:
+//   dV(g) | S(g+2) | dP(g+1) | dK(g) dQ^T(g)
+// so S runs two steps and dP one step ahead of the softmax warps, which
+// therefore never wait for the tensor core while it has work queued.  Every
+// handshake barrier between these roles is doubled per buffer (step parity),
+// so a barrier's next completion always needs an action of its own waiter
+// first and no waiter can miss a phase.
 // Softmax warpgroup c reads columns [32c, 32c + 32) of S and dP and writes
 // its 16 packed bf16 words (P^T, dS^T) over the first 16 of those columns --
 // columns no other warp reads -- so the K = 64 operand of the dV and dK
@@ -41,7 +52,7 @@
 //
 // Roles (512 threads):
 //   warps 0-7   softmax: P, dS (warps 0-3 query columns 0-31, 4-7 columns 32-63)
-//   warps 8-11  dQ drain (TMEM -> shared -> TMA reduce-add) and the dK/dV epilogue
+//   warps 8-11  dQ drain (TMEM -> registers -> L2 reductions) and the dK/dV epilogue
 //   warp 12     MMA issue (one thread) + TMEM allocation
 //   warp 13     TMA loads (one thread)
 //   warps 14-15 idle
@@ -150,26 +161,24 @@ struct BwdSmem {
   static constexpr int kQPanel = kBwdBQ * 128;
   static constexpr int kSlotBytes = 2 * kQBytes;         // Q then dO
   static constexpr int kDSBytes = kBwdBK * kBwdBQ * 2;   // dS^T, keys x queries
-  static constexpr int kDQWarpBytes = kBwdBQ * 32 * 4;   // 64 queries x 32 features fp32
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKVBytes;
   static constexpr int kOffQ = kOffV + kKVBytes;
   static constexpr int kOffDS = kOffQ + STAGES * kSlotBytes;
-  static constexpr int kOffDQ = kOffDS + kDSBytes;
-  static constexpr int kOffLD = kOffDQ + 4 * kDQWarpBytes;  // per slot: lse2[64], delta[64]
+  static constexpr int kOffLD = kOffDS + kDSBytes;  // per slot: lse2[64], delta[64]
   static constexpr int kLDBytes = 2 * kBwdBQ * 4;
   static constexpr int kOffBar = kOffLD + STAGES * kLDBytes;
   static constexpr int kBarKVFull = 0;
   static constexpr int kBarKVEmpty = 1;
   static constexpr int kBarQFull = 2;
   static constexpr int kBarQEmpty = kBarQFull + STAGES;
-  static constexpr int kBarSFull = kBarQEmpty + STAGES;  // two
-  static constexpr int kBarDPFull = kBarSFull + 2;
-  static constexpr int kBarPFull = kBarDPFull + 1;
-  static constexpr int kBarDSFull = kBarPFull + 1;
-  static constexpr int kBarDQFull = kBarDSFull + 1;
-  static constexpr int kBarDQEmpty = kBarDQFull + 1;
-  static constexpr int kBarAccFull = kBarDQEmpty + 1;
+  static constexpr int kBarSFull = kBarQEmpty + STAGES;  // two, one per S buffer
+  static constexpr int kBarDPFull = kBarSFull + 2;       // two, one per dP buffer
+  static constexpr int kBarPFull = kBarDPFull + 2;       // two
+  static constexpr int kBarDSFull = kBarPFull + 2;       // two
+  static constexpr int kBarDQFull = kBarDSFull + 2;    // two
+  static constexpr int kBarDQEmpty = kBarDQFull + 2;   // two
+  static constexpr int kBarAccFull = kBarDQEmpty + 2;
   static constexpr int kBarAccEmpty = kBarAccFull + 1;
   static constexpr int kBarTeardown = kBarAccEmpty + 1;
   static constexpr int kNumBars = kBarTeardown + 1;
@@ -177,7 +186,7 @@ struct BwdSmem {
   static constexpr int kOffAbort = kOffTmem + 16;
   static constexpr int kBytes = kOffAbort + 16;
   static constexpr int kAlloc = kBytes + 1024;
-  static_assert(kOffV % 1024 == 0 && kOffQ % 1024 == 0 && kOffDS % 1024 == 0 && kOffDQ % 1024 == 0,
+  static_assert(kOffV % 1024 == 0 && kOffQ % 1024 == 0 && kOffDS % 1024 == 0,
                 "swizzled tiles need 1 KiB alignment");
   static_assert(kAlloc <= 232448, "shared memory budget exceeded");
 };
@@ -234,10 +243,14 @@ template <int D, int STAGES, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+                  const BwdParams p) {
   static_assert(D == 128, "backward kernel: d = 128");
+  // S runs two steps ahead: the Q/dO slot of step g + 2 must not be the slot
+  // step g still reads (with two slots the MMA thread would wait for a load
+  // that waits for it); with three the next load starts only one step ahead.
+  static_assert(STAGES >= 4, "backward ring depth");
   using L = BwdSmem<D, STAGES>;
-  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 192, kColDV = 256, kColDK = 384;
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
   constexpr int kDPanels = D / 64;
 
   extern __shared__ uint8_t smem_raw[];
@@ -259,7 +272,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tm_k);
     ptx::prefetch_tmap(&tm_v);
     ptx::prefetch_tmap(&tm_do);
-    ptx::prefetch_tmap(&tm_dq);
   }
   if (threadIdx.x == 0) {
     *s_abort = 0;
@@ -269,13 +281,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(L::kBarQFull + s), 1);
       ptx::mbar_init(bar(L::kBarQEmpty + s), 1);
     }
-    ptx::mbar_init(bar(L::kBarSFull), 1);
-    ptx::mbar_init(bar(L::kBarSFull + 1), 1);
-    ptx::mbar_init(bar(L::kBarDPFull), 1);
-    ptx::mbar_init(bar(L::kBarPFull), 256);
-    ptx::mbar_init(bar(L::kBarDSFull), 256);
-    ptx::mbar_init(bar(L::kBarDQFull), 1);
-    ptx::mbar_init(bar(L::kBarDQEmpty), 128);
+    for (int b2 = 0; b2 < 2; ++b2) {
+      ptx::mbar_init(bar(L::kBarSFull + b2), 1);
+      ptx::mbar_init(bar(L::kBarDPFull + b2), 1);
+      ptx::mbar_init(bar(L::kBarPFull + b2), 256);
+      ptx::mbar_init(bar(L::kBarDSFull + b2), 256);
+      ptx::mbar_init(bar(L::kBarDQFull + b2), 1);
+      ptx::mbar_init(bar(L::kBarDQEmpty + b2), 128);
+    }
     ptx::mbar_init(bar(L::kBarAccFull), 1);
     ptx::mbar_init(bar(L::kBarAccEmpty), 128);
     ptx::mbar_init(bar(L::kBarTeardown), 1);
@@ -359,18 +372,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         return false;
       };
-      // S^T(step) = K Q^T into S[step % 2].
-      auto issue_s = [&](uint32_t step) {
-        const uint32_t sq = base + L::kOffQ + (step % STAGES) * L::kSlotBytes;
-        const uint32_t dS = tmem + kColS + (step & 1u) * kBwdBQ;
+      // S^T(t) = K Q(t)^T into S[t % 2]; dP^T(t) = V dO(t)^T into dP[t % 2].
+      auto issue_s = [&](uint32_t t) {
+        const uint32_t sq = base + L::kOffQ + (t % STAGES) * L::kSlotBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oa = (kk / 4) * L::kKVPanel + (kk % 4) * 32;
           const uint32_t ob = (kk / 4) * L::kQPanel + (kk % 4) * 32;
-          ptx::mma_ss(dS, ptx::sw128_desc(base + L::kOffK + oa, 16, 1024), ptx::sw128_desc(sq + ob, 16, 1024),
-                      id_s, kk > 0 ? 1u : 0u);
+          ptx::mma_ss(tmem + kColS + (t & 1u) * kBwdBQ, ptx::sw128_desc(base + L::kOffK + oa, 16, 1024),
+                      ptx::sw128_desc(sq + ob, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(bar(L::kBarSFull + (step & 1u)));
+        ptx::mma_commit(bar(L::kBarSFull + (t & 1u)));
+      };
+      auto issue_dp = [&](uint32_t t) {
+        const uint32_t sdo = base + L::kOffQ + (t % STAGES) * L::kSlotBytes + L::kQBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t oa = (kk / 4) * L::kKVPanel + (kk % 4) * 32;
+          const uint32_t ob = (kk / 4) * L::kQPanel + (kk % 4) * 32;
+          ptx::mma_ss(tmem + kColDP + (t & 1u) * kBwdBQ, ptx::sw128_desc(base + L::kOffV + oa, 16, 1024),
+                      ptx::sw128_desc(sdo + ob, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(bar(L::kBarDPFull + (t & 1u)));
+      };
+      // Q(t) / dO(t) loaded.
+      auto wait_q = [&](uint32_t t) -> bool {
+        if (!wait(bar(L::kBarQFull + t % STAGES), (t / STAGES) & 1u, kBSiteMmaQ)) return false;
+        ptx::tc_fence_after();
+        return true;
+      };
+      // dP[t % 2] last held dQ^T(t - 2): the drain must have read it.
+      auto wait_dq_read = [&](uint32_t t) -> bool {
+        if (t < 2) return true;
+        if (!wait(bar(L::kBarDQEmpty + (t & 1u)), ((t - 2) >> 1) & 1u, kBSiteMmaDQ)) return false;
+        ptx::tc_fence_after();
+        return true;
       };
 #pragma unroll 1
       FA_BWD_FOR_EACH_UNIT(u) {
@@ -378,55 +414,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w.nsteps == 0) continue;
         if (!wait(bar(L::kBarKVFull), uc & 1u, kBSiteMmaKV)) break;
         ptx::tc_fence_after();
-        if (!wait(bar(L::kBarQFull + g % STAGES), (g / STAGES) & 1u, kBSiteMmaQ)) break;
-        ptx::tc_fence_after();
+        // Prologue: S of the first two steps, dP of the first.
+        if (!wait_q(g)) break;
         issue_s(g);
+        if (w.nsteps > 1) {
+          if (!wait_q(g + 1)) break;
+          issue_s(g + 1);
+        }
+        if (!wait_dq_read(g)) break;
+        issue_dp(g);
 #pragma unroll 1
         for (int i = 0; i < w.nsteps && ok; ++i, ++g) {
           const uint32_t slot = g % STAGES;
           const uint32_t sq = base + L::kOffQ + slot * L::kSlotBytes;
           const uint32_t sdo = sq + L::kQBytes;
-          // dP^T = V dO^T (the previous step's dK, which read dS^T from these
-          // columns, was issued before and runs first).
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t oa = (kk / 4) * L::kKVPanel + (kk % 4) * 32;
-            const uint32_t ob = (kk / 4) * L::kQPanel + (kk % 4) * 32;
-            ptx::mma_ss(tmem + kColDP, ptx::sw128_desc(base + L::kOffV + oa, 16, 1024),
-                        ptx::sw128_desc(sdo + ob, 16, 1024), id_s, kk > 0 ? 1u : 0u);
-          }
-          ptx::mma_commit(bar(L::kBarDPFull));
-          // dV += P^T dO once the softmax warps have written P^T.
-          if (!wait(bar(L::kBarPFull), g & 1u, kBSiteMmaP)) break;
+          const uint32_t b2 = g & 1u;
+          // dV += P^T dO once the softmax warps have written P^T(g).
+          if (!wait(bar(L::kBarPFull + b2), (g >> 1) & 1u, kBSiteMmaP)) break;
           if (i == 0 && uc > 0 && !wait(bar(L::kBarAccEmpty), (uc - 1) & 1u, kBSiteMmaAcc)) break;
           ptx::tc_fence_after();
-          const uint32_t tP = tmem + kColS + (g & 1u) * kBwdBQ;
 #pragma unroll
           for (int kk = 0; kk < kBwdBQ / 16; ++kk)
-            ptx::mma_ts(tmem + kColDV, tP + (kk >> 1) * 32 + (kk & 1) * 8,
+            ptx::mma_ts(tmem + kColDV, tmem + kColS + b2 * kBwdBQ + (kk >> 1) * 32 + (kk & 1) * 8,
                         ptx::sw128_desc(sdo + kk * 2048, L::kQPanel, 1024), id_acc, (i > 0 || kk > 0) ? 1u : 0u);
-          // Next step's S into the other buffer (its P^T was read by the
-          // previous dV, issued earlier).  Issued only after P(g) is in, so
-          // the P-full barrier cannot run two phases ahead of this thread.
-          if (i + 1 < w.nsteps) {
-            if (!wait(bar(L::kBarQFull + (g + 1) % STAGES), ((g + 1) / STAGES) & 1u, kBSiteMmaQ)) break;
-            ptx::tc_fence_after();
-            issue_s(g + 1);
+          // S(g + 2) over P(g) (read by the dV just issued, which runs first).
+          if (i + 2 < w.nsteps) {
+            if (!wait_q(g + 2)) break;
+            issue_s(g + 2);
           }
-          // dK += dS^T Q and dQ^T = K^T dS^T once dS^T is written.
-          if (!wait(bar(L::kBarDSFull), g & 1u, kBSiteMmaDS)) break;
+          // dP(g + 1) into the other dP buffer.
+          if (i + 1 < w.nsteps) {
+            if (!wait_dq_read(g + 1)) break;
+            issue_dp(g + 1);
+          }
+          // dK += dS^T Q, then dQ^T = K^T dS^T over dP[g % 2] (after dK has read dS^T).
+          if (!wait(bar(L::kBarDSFull + b2), (g >> 1) & 1u, kBSiteMmaDS)) break;
           ptx::tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kBwdBQ / 16; ++kk)
-            ptx::mma_ts(tmem + kColDK, tmem + kColDP + (kk >> 1) * 32 + (kk & 1) * 8,
+            ptx::mma_ts(tmem + kColDK, tmem + kColDP + b2 * kBwdBQ + (kk >> 1) * 32 + (kk & 1) * 8,
                         ptx::sw128_desc(sq + kk * 2048, L::kQPanel, 1024), id_acc, (i > 0 || kk > 0) ? 1u : 0u);
-          if (g > 0 && !wait(bar(L::kBarDQEmpty), (g - 1) & 1u, kBSiteMmaDQ)) break;
-          ptx::tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kBwdBK / 16; ++kk)
-            ptx::mma_ss(tmem + kColDQ, ptx::sw128_desc(base + L::kOffK + kk * 2048, L::kKVPanel, 1024),
+            ptx::mma_ss(tmem + kColDP + b2 * kBwdBQ, ptx::sw128_desc(base + L::kOffK + kk * 2048, L::kKVPanel, 1024),
                         ptx::sw128_desc(base + L::kOffDS + kk * 2048, L::kDSBytes, 1024), id_dq, kk > 0 ? 1u : 0u);
-          ptx::mma_commit(bar(L::kBarDQFull));
+          ptx::mma_commit(bar(L::kBarDQFull + b2));
           ptx::mma_commit(bar(L::kBarQEmpty + slot));
         }
         if (!ok) break;
@@ -455,7 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < w.nsteps && ok; ++i, ++g) {
         const uint32_t slot = g % STAGES;
         const int qb = w.qb0 + i % w.nqb;
-        if (!ptx::mbar_wait_warp(bar(L::kBarSFull + (g & 1u)), (g >> 1) & 1u, s_abort, tmo) ||
+        const uint32_t b2 = g & 1u;
+        if (!ptx::mbar_wait_warp(bar(L::kBarSFull + b2), (g >> 1) & 1u, s_abort, tmo) ||
             !ptx::mbar_wait_warp(bar(L::kBarQFull + slot), (g / STAGES) & 1u, s_abort, tmo)) {
           record_error(p.status, kErrTimeout, kBSiteSoftS);
           ok = false;
@@ -463,10 +496,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         uint32_t sr[32];
-        ptx::tmem_ld32(tmem + lane_off + kColS + (g & 1u) * kBwdBQ + c * 32, sr);
+        ptx::tmem_ld32(tmem + lane_off + kColS + b2 * kBwdBQ + c * 32, sr);
         ptx::tmem_wait_ld();
-        const float* lse2 = s_ld + slot * (L::kLDBytes / 4) + c * 32;
-        const float* dlt = lse2 + kBwdBQ;
+        // 128-bit broadcast loads (all lanes read the same words), D too,
+        // so that no shared load sits on the dS path.
+        float lse2[32], dlt[32];
+        {
+          const float4* l4 = reinterpret_cast<const float4*>(s_ld + slot * (L::kLDBytes / 4) + c * 32);
+          const float4* d4 = reinterpret_cast<const float4*>(s_ld + slot * (L::kLDBytes / 4) + kBwdBQ + c * 32);
+#pragma unroll
+          for (int k4 = 0; k4 < 8; ++k4) {
+            const float4 x = l4[k4];
+            lse2[4 * k4] = x.x;
+            lse2[4 * k4 + 1] = x.y;
+            lse2[4 * k4 + 2] = x.z;
+            lse2[4 * k4 + 3] = x.w;
+            const float4 y = d4[k4];
+            dlt[4 * k4] = y.x;
+            dlt[4 * k4 + 1] = y.y;
+            dlt[4 * k4 + 2] = y.z;
+            dlt[4 * k4 + 3] = y.w;
+          }
+        }
         // Keys past Nk, and (causal) keys after a query's limit, get P = 0.
         const int q0 = qb * kBwdBQ + c * 32;
         const int lim = CAUSAL ? kj - off - q0 : -1;  // column k is masked when k < lim
@@ -491,19 +542,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) pk[k] = ptx::pack_bf16x2(pr[2 * k], pr[2 * k + 1]);
-        ptx::tmem_st16(tmem + lane_off + kColS + (g & 1u) * kBwdBQ + c * 32, pk);
+        ptx::tmem_st16(tmem + lane_off + kColS + b2 * kBwdBQ + c * 32, pk);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(L::kBarPFull));
+        ptx::mbar_arrive(bar(L::kBarPFull + b2));
         // dS^T = P^T o (dP^T - D)
-        if (!ptx::mbar_wait_warp(bar(L::kBarDPFull), g & 1u, s_abort, tmo)) {
+        if (!ptx::mbar_wait_warp(bar(L::kBarDPFull + b2), (g >> 1) & 1u, s_abort, tmo)) {
           record_error(p.status, kErrTimeout, kBSiteSoftDP);
           ok = false;
           break;
         }
         ptx::tc_fence_after();
         uint32_t dr[32];
-        ptx::tmem_ld32(tmem + lane_off + kColDP + c * 32, dr);
+        ptx::tmem_ld32(tmem + lane_off + kColDP + b2 * kBwdBQ + c * 32, dr);
         ptx::tmem_wait_ld();
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
@@ -511,11 +562,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float d1 = pr[2 * k + 1] * (__uint_as_float(dr[2 * k + 1]) - dlt[2 * k + 1]);
           pk[k] = ptx::pack_bf16x2(d0, d1);
         }
-        ptx::tmem_st16(tmem + lane_off + kColDP + c * 32, pk);
+        ptx::tmem_st16(tmem + lane_off + kColDP + b2 * kBwdBQ + c * 32, pk);
         // The same bf16 dS^T row into shared memory (B operand of dQ^T):
         // 128 keys x 64 queries, 128-byte rows, 128-byte swizzle.  The
         // previous step's dQ^T MMA must have read the buffer.
-        if (g > 0 && !ptx::mbar_wait_warp(bar(L::kBarDQFull), (g - 1) & 1u, s_abort, tmo)) {
+        if (g > 0 && !ptx::mbar_wait_warp(bar(L::kBarDQFull + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u, s_abort, tmo)) {
           record_error(p.status, kErrTimeout, kBSiteSoftDQ);
           ok = false;
           break;
@@ -530,16 +581,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_proxy_async_smem();
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(L::kBarDSFull));
+        ptx::mbar_arrive(bar(L::kBarDSFull + b2));
       }
     }
   } else {
     // ======================================== dQ drain and the dK / dV epilogue
     const int wq = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(wq << 5) << 16;
-    const uint32_t stage = base + L::kOffDQ + wq * L::kDQWarpBytes;
     uint32_t g = 0, uc = 0;
-    bool pending = false;
     bool ok = true;
 #pragma unroll 1
     FA_BWD_FOR_EACH_UNIT(u) {
@@ -560,34 +609,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < w.nsteps && ok; ++i, ++g) {
         const int h = w.hk * p.group + i / w.nqb;
         const int qb = w.qb0 + i % w.nqb;
-        if (!ptx::mbar_wait_warp(bar(L::kBarDQFull), g & 1u, s_abort, tmo)) {
+        if (!ptx::mbar_wait_warp(bar(L::kBarDQFull + (g & 1u)), (g >> 1) & 1u, s_abort, tmo)) {
           record_error(p.status, kErrTimeout, kBSiteDrainDQ);
           ok = false;
           break;
         }
         ptx::tc_fence_after();
         uint32_t v[64];
-        ptx::tmem_ld32(tmem + lane_off + kColDQ, v);
-        ptx::tmem_ld32(tmem + lane_off + kColDQ + 32, v + 32);
+        ptx::tmem_ld32(tmem + lane_off + kColDP + (g & 1u) * kBwdBQ, v);
+        ptx::tmem_ld32(tmem + lane_off + kColDP + (g & 1u) * kBwdBQ + 32, v + 32);
         ptx::tmem_wait_ld();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(L::kBarDQEmpty));
-        if (pending) {
-          if (lane == 0) ptx::bulk_wait_group_read_0();
-          __syncwarp();
-        }
-        // Box of 64 queries x 32 features (this warp's TMEM lanes), row-major.
-        float* const st = reinterpret_cast<float*>(gbase + L::kOffDQ + wq * L::kDQWarpBytes);
+        ptx::mbar_arrive(bar(L::kBarDQEmpty + (g & 1u)));
+        // Query q of the block: the warp's 32 features are one 128-byte line.
+        float* const dst = p.dq_acc + (static_cast<size_t>(w.b * p.H + h) * p.nq_pad + static_cast<size_t>(qb) * kBwdBQ) * D +
+                           (wq << 5) + lane;
 #pragma unroll
-        for (int q = 0; q < kBwdBQ; ++q) st[q * 32 + lane] = __uint_as_float(v[q]);
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          const int row0 = (w.b * p.H + h) * p.nq_pad + qb * kBwdBQ;
-          ptx::tma_reduce_add_2d(&tm_dq, stage, wq * 32, row0);
-          ptx::bulk_commit_group();
-        }
-        pending = true;
+        for (int q = 0; q < kBwdBQ; ++q) ptx::red_add(dst + static_cast<size_t>(q) * D, __uint_as_float(v[q]));
       }
       if (!ok) break;
       // Unit done: dK (times the scale) and dV to bf16, one key row per thread.
@@ -624,8 +662,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_arrive(bar(L::kBarAccEmpty));
       ++uc;
     }
-    if (lane == 0) ptx::bulk_wait_group_0();
-    __syncwarp();
   }
 
   // ---------------------------------------------------------------- teardown

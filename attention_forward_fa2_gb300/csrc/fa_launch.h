@@ -83,7 +83,7 @@ cudaError_t launch_fwd_split(const LaunchArgs& a);
 // Backward pass (fa_bwd_kernel.cuh): preprocessing, the key-block kernel and
 // the dQ conversion, enqueued in that order on a.stream.
 struct BwdLaunchArgs {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dq;
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;
   BwdParams p;
   dim3 grid;
   cudaStream_t stream;

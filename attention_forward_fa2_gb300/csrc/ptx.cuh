@@ -159,14 +159,10 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-// Element-wise add of a shared-memory box into global memory (the tensor
-// map's element type, here fp32), performed at L2.
-__device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, uint32_t src, int c0, int c1) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(tmap)),
-      "r"(src), "r"(c0), "r"(c1)
-      : "memory");
+// Reduction (add) of one float into global memory, performed at L2.  A warp
+// whose lanes address one 128-byte line issues a single request.
+__device__ __forceinline__ void red_add(float* ptr, float a) {
+  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(ptr), "f"(a) : "memory");
 }
 
 __device__ __forceinline__ void bulk_commit_group() {
