@@ -19,6 +19,10 @@ in ``attn_ref.c``:
                       §11.3 and §14.1), used only to check that it is exact
 * ``attn_bwd_dense``  the backward pass (§13.1): dQ, dK, dV and D_i from the full
                       materialised P, with the causal mask and grouped heads
+* ``e4m3_decode`` / ``e4m3_encode`` / ``quantize_fp8``  the e4m3 format from its
+                      definition and block quantisation (§15.5): the reference for
+                      the quantiser
+* ``attn_fp8_dense``  the definition evaluated on dequantised e4m3 inputs
 
 Inputs are bf16 bit patterns (``numpy.uint16``); outputs are float64.
 """
@@ -74,8 +78,19 @@ def _load():
                                            f64p, f64p]
         lib.oracle_attn_bwd_dense.argtypes = [u16p, u16p, u16p, u16p, ci, ci, ci, ci, ci, ci, cd,
                                               ci, f64p, f64p, f64p, f64p]
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        f32p = ctypes.POINTER(ctypes.c_float)
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_decode.restype = ctypes.c_double
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_quantize_e4m3.argtypes = [f32p, ctypes.c_longlong, ctypes.c_float, u8p]
+        lib.oracle_quantize_e4m3.restype = None
+        lib.oracle_attn_fp8_dense.argtypes = [u8p, u8p, u8p, f32p, f32p, f32p, ci, ci, ci, ci, ci, ci, ci,
+                                              cd, ci, f64p, f64p]
         for name in ("oracle_attn_dense", "oracle_attn_dense_rows", "oracle_attn_varlen",
-                     "oracle_attn_online", "oracle_attn_bwd_dense", "oracle_num_threads"):
+                     "oracle_attn_online", "oracle_attn_bwd_dense", "oracle_attn_fp8_dense",
+                     "oracle_num_threads"):
             getattr(lib, name).restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ci]
         lib.oracle_set_num_threads.restype = None
@@ -211,3 +226,83 @@ def attn_bwd_dense(q, k, v, dout, scale=None, causal=False):
     if rc != 0:
         raise MemoryError("oracle_attn_bwd_dense failed (%d)" % rc)
     return dq, dk, dv, delta
+
+
+def e4m3_decode(codes):
+    """Values of e4m3 codes (uint8 array -> float64 array)."""
+    lib = _load()
+    table = np.array([lib.oracle_e4m3_decode(c) for c in range(256)], np.float64)
+    return table[np.asarray(codes, np.uint8)]
+
+
+def e4m3_encode(x):
+    """Nearest e4m3 codes of float64 values (ties to even, saturating)."""
+    lib = _load()
+    x = np.asarray(x, np.float64)
+    return np.array([lib.oracle_e4m3_encode(float(v)) for v in x.ravel()], np.uint8).reshape(x.shape)
+
+
+def _quantize_block(x, scale):
+    x = np.ascontiguousarray(x, np.float32)
+    out = np.empty(x.shape, np.uint8)
+    _load().oracle_quantize_e4m3(_ptr(x, ctypes.c_float), x.size, ctypes.c_float(scale),
+                                 _ptr(out, ctypes.c_uint8))
+    return out
+
+
+def _block_scale(x):
+    amax = np.float32(np.abs(np.asarray(x, np.float32)).max()) if np.asarray(x).size else np.float32(0)
+    return np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+
+
+def quantize_fp8(q, k, v):
+    """Block quantisation of bf16 bit arrays q [B, Nq, H, d], k/v [B, Nk, Hk, d]:
+    returns (q8, k8, vt8 [B, Hk, d, nk_pad], q_scale [B, H, qb], k_scale [B, Hk, kb],
+    v_scale [B, Hk]) with scale = amax / 448 in float32 and codes of x / scale."""
+    import torch
+    f = lambda bits: torch.from_numpy(np.ascontiguousarray(bits, np.uint16).view(np.int16)).view(
+        torch.bfloat16).to(torch.float32).numpy()
+    qf, kf, vf = f(q), f(k), f(v)
+    B, Nq, H, d = qf.shape
+    Nk, Hk = kf.shape[1], kf.shape[2]
+    qb, kb, nkp = (Nq + 127) // 128, (Nk + 127) // 128, (Nk + 15) // 16 * 16
+    q8 = np.zeros(qf.shape, np.uint8)
+    k8 = np.zeros(kf.shape, np.uint8)
+    vt8 = np.zeros((B, Hk, d, nkp), np.uint8)
+    qs = np.zeros((B, H, qb), np.float32)
+    ks = np.zeros((B, Hk, kb), np.float32)
+    vs = np.zeros((B, Hk), np.float32)
+    for b in range(B):
+        for h in range(H):
+            for i in range(qb):
+                blk = qf[b, i * 128:(i + 1) * 128, h]
+                qs[b, h, i] = _block_scale(blk)
+                q8[b, i * 128:(i + 1) * 128, h] = _quantize_block(blk, qs[b, h, i])
+        for h in range(Hk):
+            for j in range(kb):
+                blk = kf[b, j * 128:(j + 1) * 128, h]
+                ks[b, h, j] = _block_scale(blk)
+                k8[b, j * 128:(j + 1) * 128, h] = _quantize_block(blk, ks[b, h, j])
+            vs[b, h] = _block_scale(vf[b, :, h])
+            vt8[b, h, :, :Nk] = _quantize_block(vf[b, :, h].T, vs[b, h])
+    return q8, k8, vt8, qs, ks, vs
+
+
+def attn_fp8_dense(q8, k8, vt8, q_scale, k_scale, v_scale, Nq, Nk, scale=None, causal=False):
+    """The attention definition on dequantised e4m3 inputs (layouts of quantize_fp8).
+
+    Returns (o [B, Nq, H, d], lse [B, H, Nq]) in float64."""
+    q8, k8, vt8 = (np.ascontiguousarray(x, np.uint8) for x in (q8, k8, vt8))
+    qs, ks, vs = (np.ascontiguousarray(x, np.float32) for x in (q_scale, k_scale, v_scale))
+    B, _, H, d = q8.shape
+    Hk, nkp = vt8.shape[1], vt8.shape[3]
+    o = np.zeros((B, Nq, H, d), np.float64)
+    lse = np.zeros((B, H, Nq), np.float64)
+    rc = _load().oracle_attn_fp8_dense(_ptr(q8, ctypes.c_uint8), _ptr(k8, ctypes.c_uint8),
+                                       _ptr(vt8, ctypes.c_uint8), _ptr(qs, ctypes.c_float),
+                                       _ptr(ks, ctypes.c_float), _ptr(vs, ctypes.c_float), B, Nq, Nk, H,
+                                       Hk, d, nkp, _default_scale(d, scale), int(bool(causal)),
+                                       _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double))
+    if rc != 0:
+        raise MemoryError("oracle_attn_fp8_dense failed (%d)" % rc)
+    return o, lse

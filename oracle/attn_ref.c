@@ -51,6 +51,15 @@
  * key/value gradients of the G query heads that share a K/V head are summed
  * ([GKFA] §14.2).  Rows that see no key have P = 0 and contribute nothing.
  *
+ * FP8 ([GKFA] §15.5, block quantisation), oracle_attn_fp8_dense(): the inputs
+ * are e4m3 codes with fp32 scales; each value is decoded from the e4m3 format
+ * definition (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits;
+ * exponent field 0 is subnormal, m/8 * 2^-6; code 0x7f/0xff is NaN; no
+ * infinities) and multiplied by its block scale, and the definition above is
+ * evaluated on those values in double.  oracle_e4m3_encode() is the nearest
+ * code (ties to the even mantissa, saturating to +-448), found by comparing
+ * against every finite code: the reference for the quantiser.
+ *
  * oracle_attn_online() restates the blockwise recurrence of [GKFA] §11.3 with
  * the deferred division of §14.1, again in double.  It exists only so tests can
  * check the pages' claim that the recurrence is exact (it must agree with the
@@ -292,6 +301,140 @@ int oracle_attn_bwd_dense(const uint16_t *q, const uint16_t *k, const uint16_t *
                                           dk + kvoff, dv + kvoff,
                                           delta + ((size_t)b * H + h) * Nq, 1);
             }
+        }
+    }
+    return err ? -1 : 0;
+}
+
+/* e4m3 code -> value (NaN for 0x7f / 0xff). */
+double oracle_e4m3_decode(uint8_t c)
+{
+    const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    const double mag = (e == 0) ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/* Nearest e4m3 code to x: round to nearest, ties to the even mantissa,
+   saturating to the largest finite magnitude (448); NaN -> 0x7f. */
+uint8_t oracle_e4m3_encode(double x)
+{
+    if (x != x)
+        return 0x7f;
+    const int neg = x < 0 || (x == 0 && signbit(x));
+    const double a = fabs(x);
+    int best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c <= 0x7e; ++c) {
+        const double v = oracle_e4m3_decode((uint8_t)c);
+        const double dd = fabs(v - a);
+        if (dd < best_d || (dd == best_d && (c & 1) == 0 && (best & 1) == 1)) {
+            best_d = dd;
+            best = c;
+        }
+    }
+    if (a >= 448.0)
+        best = 0x7e;
+    return (uint8_t)(best | (neg ? 0x80 : 0));
+}
+
+/* codes[i] = nearest code to x[i] / scale, the division done in float. */
+void oracle_quantize_e4m3(const float *x, long long n, float scale, uint8_t *codes)
+{
+    for (long long i = 0; i < n; ++i) {
+        const float y = x[i] / scale;
+        codes[i] = oracle_e4m3_encode((double)y);
+    }
+}
+
+/* One head in double: nq query rows (q row i at q + i * d), nk keys (k row j
+   at k + j * d, v row j at v + j * d); o row i at o + i * o_rs. */
+static int head_attention_f64(const double *q, int nq, const double *k, const double *v, int nk, int d,
+                              double scale, int causal, long offset, double *o, size_t o_rs,
+                              double *lse)
+{
+    double *S = (double *)malloc((size_t)(nq > 0 ? nq : 1) * (size_t)(nk > 0 ? nk : 1) * sizeof(double));
+    if (!S)
+        return -1;
+    for (int i = 0; i < nq; ++i) {
+        double *row = S + (size_t)i * nk;
+        double m = -INFINITY;
+        for (int j = 0; j < nk; ++j) {
+            if (causal && (long)j > i + offset) {
+                row[j] = -INFINITY;
+                continue;
+            }
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c)
+                acc += q[(size_t)i * d + c] * k[(size_t)j * d + c];
+            row[j] = scale * acc;
+            if (row[j] > m)
+                m = row[j];
+        }
+        double *oi = o + (size_t)i * o_rs;
+        for (int c = 0; c < d; ++c)
+            oi[c] = 0.0;
+        if (m == -INFINITY) {
+            lse[i] = -INFINITY;
+            continue;
+        }
+        double l = 0.0;
+        for (int j = 0; j < nk; ++j) {
+            row[j] = exp(row[j] - m);
+            l += row[j];
+        }
+        for (int j = 0; j < nk; ++j) {
+            const double pj = row[j] / l;
+            for (int c = 0; c < d; ++c)
+                oi[c] += pj * v[(size_t)j * d + c];
+        }
+        lse[i] = m + log(l);
+    }
+    free(S);
+    return 0;
+}
+
+/*
+ * FP8 dense form.  q8: [B, Nq, H, d] codes, k8: [B, Nk, Hk, d], vt8: [B, Hk, d,
+ * nk_pad] (V transposed); q_scale [B, H, ceil(Nq/128)], k_scale [B, Hk,
+ * ceil(Nk/128)], v_scale [B, Hk].  o: [B, Nq, H, d], lse: [B, H, Nq] (double).
+ */
+int oracle_attn_fp8_dense(const uint8_t *q8, const uint8_t *k8, const uint8_t *vt8, const float *q_scale,
+                          const float *k_scale, const float *v_scale, int B, int Nq, int Nk, int H, int Hk,
+                          int d, int nk_pad, double scale, int causal, double *o, double *lse)
+{
+    if (Hk <= 0 || H % Hk != 0)
+        return -1;
+    const int G = H / Hk, qb = (Nq + 127) / 128, kb = (Nk + 127) / 128;
+    int err = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1) reduction(| : err)
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < H; ++h) {
+            const int hk = h / G;
+            double *q = (double *)malloc((size_t)(Nq > 0 ? Nq : 1) * d * sizeof(double));
+            double *k = (double *)malloc((size_t)(Nk > 0 ? Nk : 1) * d * sizeof(double));
+            double *v = (double *)malloc((size_t)(Nk > 0 ? Nk : 1) * d * sizeof(double));
+            if (!q || !k || !v) {
+                free(q); free(k); free(v);
+                err |= 1;
+                continue;
+            }
+            for (int i = 0; i < Nq; ++i)
+                for (int c = 0; c < d; ++c)
+                    q[(size_t)i * d + c] = oracle_e4m3_decode(q8[(((size_t)b * Nq + i) * H + h) * d + c]) *
+                                           (double)q_scale[((size_t)b * H + h) * qb + i / 128];
+            for (int j = 0; j < Nk; ++j)
+                for (int c = 0; c < d; ++c) {
+                    k[(size_t)j * d + c] = oracle_e4m3_decode(k8[(((size_t)b * Nk + j) * Hk + hk) * d + c]) *
+                                           (double)k_scale[((size_t)b * Hk + hk) * kb + j / 128];
+                    v[(size_t)j * d + c] = oracle_e4m3_decode(vt8[(((size_t)b * Hk + hk) * d + c) * nk_pad + j]) *
+                                           (double)v_scale[(size_t)b * Hk + hk];
+                }
+            err |= head_attention_f64(q, Nq, k, v, Nk, d, scale, causal, (long)Nk - Nq,
+                                      o + (size_t)b * Nq * H * d + (size_t)h * d, (size_t)H * d,
+                                      lse + ((size_t)b * H + h) * Nq);
+            free(q); free(k); free(v);
         }
     }
     return err ? -1 : 0;
