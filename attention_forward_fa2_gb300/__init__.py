@@ -41,7 +41,7 @@ EXPORTS = (
     "fa_set_timeout_ns", "fa_set_config", "fa_get_config", "fa_autotune",
     "fa_selftest_wait_timeout", "fa_version", "fa_splitkv_num_splits",
     "fa_splitkv_workspace_bytes", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc",
-    "fa_bwd_workspace_bytes", "fa_bwd",
+    "fa_bwd_workspace_bytes", "fa_bwd", "fa_fp8_sizes", "fa_quantize_fp8", "fa_fwd_fp8",
 )
 
 
@@ -90,6 +90,9 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci]
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp,
                              ctypes.c_longlong, vp]
+        L.fa_fp8_sizes.argtypes = [ci, ci, ci, ci, ci, ci, ctypes.POINTER(ctypes.c_longlong)]
+        L.fa_quantize_fp8.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, vp]
+        L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp]
         for name in EXPORTS:
             if name != "fa_strerror":
                 getattr(L, name).restype = ci
@@ -150,6 +153,25 @@ def bwd_workspace_bytes(B, Nq, H, d) -> int:
     if n < 0:
         raise FaError(int(n), "fa_bwd_workspace_bytes")
     return int(n)
+
+
+def fp8_sizes(B, Nq, Nk, H, Hk, d):
+    """(q8 bytes, k8 bytes, vt8 bytes, q_scale, k_scale, v_scale element counts)."""
+    out = (ctypes.c_longlong * 6)()
+    rc = lib().fa_fp8_sizes(B, Nq, Nk, H, Hk, d, out)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fp8_sizes")
+    return tuple(int(x) for x in out)
+
+
+def fa_quantize_fp8(q, k, v, B, Nq, Nk, H, Hk, d, q8, k8, vt8, q_scale, k_scale, v_scale, stream) -> int:
+    return lib().fa_quantize_fp8(q, k, v, B, Nq, Nk, H, Hk, d, q8, k8, vt8, q_scale, k_scale, v_scale, stream)
+
+
+def fa_fwd_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, o, lse, B, Nq, Nk, H, Hk, d, scale, flags,
+               stream) -> int:
+    return lib().fa_fwd_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, o, lse, B, Nq, Nk, H, Hk, d, scale,
+                            flags, stream)
 
 
 def fa_check_status(stream=None):
@@ -406,3 +428,55 @@ def backward(q, k, v, o, lse, dout, scale=None, causal=False, workspace=None, dq
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd")
     return dq, dk, dv
+
+
+class Fp8Tensors:
+    """e4m3 codes and scales of one (q, k, v) triple (see quantize_fp8)."""
+
+    def __init__(self, q8, k8, vt8, q_scale, k_scale, v_scale, shape):
+        self.q8, self.k8, self.vt8 = q8, k8, vt8
+        self.q_scale, self.k_scale, self.v_scale = q_scale, k_scale, v_scale
+        self.B, self.Nq, self.Nk, self.H, self.Hk, self.d = shape
+
+
+def quantize_fp8(q, k, v, stream=None):
+    """Block-quantise bf16 q [B, Nq, H, d], k/v [B, Nk, Hk, d] to e4m3 (d = 128)."""
+    import torch
+    B, Nq, H, d = q.shape
+    Nk, Hk = k.shape[1], k.shape[2]
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+    n_q8, n_k8, n_vt8, n_qs, n_ks, n_vs = fp8_sizes(B, Nq, Nk, H, Hk, d)
+    dev = q.device
+    q8 = torch.empty(max(n_q8, 16), dtype=torch.uint8, device=dev)
+    k8 = torch.empty(max(n_k8, 16), dtype=torch.uint8, device=dev)
+    vt8 = torch.empty(max(n_vt8, 16), dtype=torch.uint8, device=dev)
+    qs = torch.empty(max(n_qs, 1), dtype=torch.float32, device=dev)
+    ks = torch.empty(max(n_ks, 1), dtype=torch.float32, device=dev)
+    vs = torch.empty(max(n_vs, 1), dtype=torch.float32, device=dev)
+    with _on_device(dev):
+        rc = fa_quantize_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, Nq, Nk, H, Hk, d, q8.data_ptr(),
+                             k8.data_ptr(), vt8.data_ptr(), qs.data_ptr(), ks.data_ptr(), vs.data_ptr(),
+                             _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_quantize_fp8")
+    return Fp8Tensors(q8, k8, vt8, qs, ks, vs, (B, Nq, Nk, H, Hk, d))
+
+
+def forward_fp8(t, scale=None, causal=False, out=None, lse=None, stream=None):
+    """FP8 forward on Fp8Tensors t; returns (o bf16 [B, Nq, H, d], lse fp32 [B, H, Nq])."""
+    import torch
+    dev = t.q8.device
+    if scale is None:
+        scale = 1.0 / math.sqrt(t.d)
+    out = torch.empty((t.B, t.Nq, t.H, t.d), dtype=torch.bfloat16, device=dev) if out is None else out
+    lse = torch.empty((t.B, t.H, t.Nq), dtype=torch.float32, device=dev) if lse is None else lse
+    with _on_device(dev):
+        rc = fa_fwd_fp8(t.q8.data_ptr(), t.k8.data_ptr(), t.vt8.data_ptr(), t.q_scale.data_ptr(),
+                        t.k_scale.data_ptr(), t.v_scale.data_ptr(), out.data_ptr(), lse.data_ptr(), t.B,
+                        t.Nq, t.Nk, t.H, t.Hk, t.d, float(scale), FA_FLAG_CAUSAL if causal else 0,
+                        _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_fp8")
+    return out, lse

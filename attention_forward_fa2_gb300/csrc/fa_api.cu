@@ -533,6 +533,18 @@ int run_bwd(const BwdProblem& P) {
   return FA_OK;
 }
 
+// ------------------------------------------------------------------ FP8
+int fp8_nk_pad(int Nk) { return (Nk + 15) / 16 * 16; }
+
+int fp8_check_shape(int B, int Nq, int Nk, int H, int Hk, int d) {
+  if (B < 0 || Nq < 0 || Nk < 0 || H < 0 || Hk < 0) return FA_ERR_INVALID_ARG;
+  if (H > 0 && (Hk == 0 || H % Hk != 0)) return FA_ERR_INVALID_ARG;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Nq * H > 0x7fffffffLL || static_cast<long long>(B) * Nk * Hk > 0x7fffffffLL)
+    return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
 __global__ void wait_timeout_kernel(unsigned long long timeout_ns, int* status) {
   __shared__ __align__(8) unsigned long long bar;
   __shared__ int abort_flag;
@@ -723,6 +735,81 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   BwdProblem P{q, k, v, o, dout, lse, dq, dk, dv, B, Nq, Nk, H, Hk, d, scale, flags, workspace,
                workspace_bytes, static_cast<cudaStream_t>(stream)};
   return run_bwd(P);
+}
+
+int fa_fp8_sizes(int B, int Nq, int Nk, int H, int Hk, int d, long long* sizes) {
+  if (!sizes) return FA_ERR_INVALID_ARG;
+  const int rc = fp8_check_shape(B, Nq, Nk, H, Hk, d);
+  if (rc != FA_OK) return rc;
+  const long long qb = (Nq + fa::kBR - 1) / fa::kBR, kb = (Nk + fa::kBR - 1) / fa::kBR;
+  sizes[0] = static_cast<long long>(B) * Nq * H * d;
+  sizes[1] = static_cast<long long>(B) * Nk * Hk * d;
+  sizes[2] = static_cast<long long>(B) * Hk * d * fp8_nk_pad(Nk);
+  sizes[3] = static_cast<long long>(B) * H * qb;
+  sizes[4] = static_cast<long long>(B) * Hk * kb;
+  sizes[5] = static_cast<long long>(B) * Hk;
+  return FA_OK;
+}
+
+int fa_quantize_fp8(const void* q, const void* k, const void* v, int B, int Nq, int Nk, int H, int Hk, int d,
+                    void* q8, void* k8, void* vt8, float* q_scale, float* k_scale, float* v_scale, void* stream) {
+  int rc = fp8_check_shape(B, Nq, Nk, H, Hk, d);
+  if (rc != FA_OK) return rc;
+  if (B == 0 || H == 0 || (Nq == 0 && Nk == 0)) return FA_OK;
+  if ((Nq > 0 && (!q || !q8 || !q_scale)) || (Nk > 0 && (!k || !v || !k8 || !vt8 || !k_scale)) || !v_scale)
+    return FA_ERR_INVALID_ARG;
+  for (const void* ptr : {q, k, v, static_cast<const void*>(q8), static_cast<const void*>(k8), static_cast<const void*>(vt8)})
+    if (ptr && !aligned16(ptr)) return FA_ERR_ALIGN;
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != FA_OK) return rc;
+  fa::Fp8QuantParams p{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+                       static_cast<const __nv_bfloat16*>(v), static_cast<uint8_t*>(q8), static_cast<uint8_t*>(k8),
+                       static_cast<uint8_t*>(vt8), q_scale, k_scale, v_scale, B, Nq, Nk, H, Hk, d, fp8_nk_pad(Nk)};
+  const cudaError_t e = fa::launch_fp8_quantize(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_scale, const float* k_scale,
+               const float* v_scale, void* o, float* lse, int B, int Nq, int Nk, int H, int Hk, int d, float scale,
+               int flags, void* stream) {
+  int rc = fp8_check_shape(B, Nq, Nk, H, Hk, d);
+  if (rc != FA_OK) return rc;
+  Problem P{q8, k8, vt8, o, lse, B, Nq, Nk, H, Hk, d, scale, nullptr, nullptr, flags,
+            static_cast<cudaStream_t>(stream)};
+  rc = validate(P);
+  if (rc != FA_OK) return rc == 1 ? FA_OK : rc;
+  if (!q_scale || !k_scale || !v_scale) return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q_scale) | reinterpret_cast<uintptr_t>(k_scale) |
+       reinterpret_cast<uintptr_t>(v_scale)) & 3u)
+    return FA_ERR_ALIGN;
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != FA_OK) return rc;
+  fa::LaunchArgs a;
+  // Parameters and the bf16 output map as for the bf16 forward (128-key
+  // tiles, 256-row units), then the e4m3 input maps.
+  const Config cfg{128, 2, 2, 8.f, 0};
+  if ((rc = prepare(P, cfg, st, a)) != FA_OK) return rc;
+  const int nkp = fp8_nk_pad(Nk);
+  cuuint64_t dq[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)Nq, (cuuint64_t)B};
+  cuuint64_t sq[3] = {(cuuint64_t)d, (cuuint64_t)H * d, (cuuint64_t)Nq * H * d};
+  cuuint64_t dk[4] = {(cuuint64_t)d, (cuuint64_t)Hk, (cuuint64_t)Nk, (cuuint64_t)B};
+  cuuint64_t sk[3] = {(cuuint64_t)d, (cuuint64_t)Hk * d, (cuuint64_t)Nk * Hk * d};
+  cuuint64_t dv[4] = {(cuuint64_t)nkp, (cuuint64_t)d, (cuuint64_t)Hk, (cuuint64_t)B};
+  cuuint64_t sv[3] = {(cuuint64_t)nkp, (cuuint64_t)d * nkp, (cuuint64_t)Hk * d * nkp};
+  cuuint32_t box_q[4] = {128, 1, (cuuint32_t)fa::kBR, 1};
+  cuuint32_t box_k[4] = {128, 1, (cuuint32_t)fa::kBC, 1};
+  cuuint32_t box_v[4] = {(cuuint32_t)fa::kBC, 128, 1, 1};
+  if ((rc = encode(&a.tm_q, q8, 4, dq, sq, box_q, CU_TENSOR_MAP_DATA_TYPE_UINT8)) != FA_OK) return rc;
+  if ((rc = encode(&a.tm_k, k8, 4, dk, sk, box_k, CU_TENSOR_MAP_DATA_TYPE_UINT8)) != FA_OK) return rc;
+  if ((rc = encode(&a.tm_v, vt8, 4, dv, sv, box_v, CU_TENSOR_MAP_DATA_TYPE_UINT8)) != FA_OK) return rc;
+  a.p.q_scale = q_scale;
+  a.p.k_scale = k_scale;
+  a.p.v_scale = v_scale;
+  a.p.q_blocks = (Nq + fa::kBR - 1) / fa::kBR;
+  a.p.k_blocks = (Nk + fa::kBR - 1) / fa::kBR;
+  a.grid = dim3(static_cast<unsigned>(a.p.num_items < st->num_sms ? a.p.num_items : st->num_sms), 1, 1);
+  const cudaError_t e = fa::launch_fwd_fp8((flags & FA_FLAG_CAUSAL) != 0, a);
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 
 int fa_splitkv_num_splits(int B, int Nq, int Nk, int H, int d, int requested) {

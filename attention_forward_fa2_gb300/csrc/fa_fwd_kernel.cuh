@@ -59,6 +59,15 @@
 //
 // Scale folding ("Flash Attention 2 Chapter6", Kernel 6): p = 2^(s * c - m * c)
 // with c = scale * log2(e), one FFMA feeding the ex2 unit per score.
+//
+// FP8 ("GPU 内核与 FlashAttention" §15.5, block quantization): Q, K and V arrive
+// as e4m3 codes with one fp32 scale per 128 query rows, per 128 keys and per
+// key/value head; V is stored transposed ([B, Hk, d, keys]) so that both
+// operands of every product are K-major.  S = Q K^T runs as kind::f8f6f4 MMAs
+// (32 elements per instruction), the scales fold into the exp2 coefficient of
+// each key tile (the row maximum is then kept in scaled log2 units), P is
+// rounded to e4m3 (four per TMEM column) for O += P V, and the V scale joins
+// the final 1/l.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -117,6 +126,10 @@ struct FwdParams {
   float scale;                 // softmax scale (natural units)
   float scale_log2;            // scale * log2(e)
   float rescale_threshold;     // log2 units; the O rescale is skipped while the max grows less
+  const float* q_scale;        // FP8: [B, H, q_blocks] dequantisation scales of 128 query rows
+  const float* k_scale;        // FP8: [B, Hk, k_blocks] of 128 keys
+  const float* v_scale;        // FP8: [B, Hk] of a key/value head
+  int q_blocks, k_blocks;
   unsigned long long timeout_ns;
   int* status;                 // [4]: code, block, warp, site
 };
@@ -133,11 +146,11 @@ __device__ __forceinline__ void record_error(int* status, int code, int site) {
   }
 }
 
-template <int D, int BC, int STAGES>
+template <int D, int BC, int STAGES, int ESZ = 2>
 struct SmemLayout {
-  static constexpr int kQTileBytes = kBR * D * 2;
+  static constexpr int kQTileBytes = kBR * D * ESZ;
   static constexpr int kQPanelBytes = kBR * 128;
-  static constexpr int kKVTileBytes = BC * D * 2;
+  static constexpr int kKVTileBytes = BC * D * ESZ;
   static constexpr int kKVPanelBytes = BC * 128;
   static constexpr int kSlotBytes = 2 * kKVTileBytes;  // K(j) then V(j-1)
   static constexpr int kStageWarpBytes = 32 * D * 2;   // 32 output rows per epilogue warp
@@ -289,18 +302,23 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
     for (int sub_ = 0, u = it_ * p.units_per_item;                                     \
          sub_ < p.units_per_item && u < p.num_units && ok; ++sub_, ++u)
 
-template <int D, int BC, int STAGES, bool VARLEN, bool CAUSAL, bool SPLIT = false, bool QUAD = false>
+template <int D, int BC, int STAGES, bool VARLEN, bool CAUSAL, bool SPLIT = false, bool QUAD = false,
+          bool FP8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const FwdParams p) {
-  using L = SmemLayout<D, BC, STAGES>;
+  using L = SmemLayout<D, BC, STAGES, FP8 ? 1 : 2>;
   static_assert(D == 64 || D == 128, "head dim");
+  static_assert(!FP8 || (D == 128 && BC == 128 && !VARLEN && !SPLIT && !QUAD), "FP8: d 128, dense");
   static_assert(BC == 64 || BC == 128, "key tile");
   static_assert(2 * BC + 2 * D <= 512, "TMEM columns");
   static_assert(!QUAD || (BC == 128 && !CAUSAL && !SPLIT), "quad reduction: 128-key tiles, no mask or split");
   constexpr int kTmemCols = 512;
-  constexpr int kDPanels = D / kPanel;
+  // 128-byte swizzle panels along d: 64 bf16 or 128 e4m3 elements each.
+  constexpr int kPanelElems = FP8 ? 128 : kPanel;
+  constexpr int kDPanels = D / kPanelElems;  // input (Q, K, V) panels
+  constexpr int kOutPanels = D / kPanel;     // bf16 output panels
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = ptx::smem_u32(smem_raw);
@@ -380,9 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int pnl = 0; pnl < kDPanels; ++pnl) {
             const uint32_t dst = base + L::kOffQ + t * L::kQTileBytes + pnl * L::kQPanelBytes;
             if constexpr (VARLEN)
-              ptx::tma_load_3d(dst, &tm_q, bar(L::kBarQFull), pnl * kPanel, w.h, w.qwin[t].load_row);
+              ptx::tma_load_3d(dst, &tm_q, bar(L::kBarQFull), pnl * kPanelElems, w.h, w.qwin[t].load_row);
             else
-              ptx::tma_load_4d(dst, &tm_q, bar(L::kBarQFull), pnl * kPanel, w.h, w.qwin[t].load_row, w.b);
+              ptx::tma_load_4d(dst, &tm_q, bar(L::kBarQFull), pnl * kPanelElems, w.h, w.qwin[t].load_row, w.b);
           }
         }
 #pragma unroll 1
@@ -403,20 +421,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int pnl = 0; pnl < kDPanels; ++pnl) {
               const uint32_t dst = sbase + pnl * L::kKVPanelBytes;
               if constexpr (VARLEN)
-                ptx::tma_load_3d(dst, &tm_k, bar(L::kBarKVFull + slot), pnl * kPanel, w.hk, kw.load_row);
+                ptx::tma_load_3d(dst, &tm_k, bar(L::kBarKVFull + slot), pnl * kPanelElems, w.hk, kw.load_row);
               else
-                ptx::tma_load_4d(dst, &tm_k, bar(L::kBarKVFull + slot), pnl * kPanel, w.hk, kw.load_row, w.b);
+                ptx::tma_load_4d(dst, &tm_k, bar(L::kBarKVFull + slot), pnl * kPanelElems, w.hk, kw.load_row, w.b);
             }
           }
           if (j >= 1) {
             const RowWindow vw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + (w.j0 + j - 1) * BC, BC);
+            if constexpr (FP8) {
+              // V^T tile: d rows x 128 keys (one box, keys innermost).
+              ptx::tma_load_4d(sbase + L::kKVTileBytes, &tm_v, bar(L::kBarKVFull + slot), vw.load_row, 0, w.hk, w.b);
+            } else {
 #pragma unroll
-            for (int pnl = 0; pnl < kDPanels; ++pnl) {
-              const uint32_t dst = sbase + L::kKVTileBytes + pnl * L::kKVPanelBytes;
-              if constexpr (VARLEN)
-                ptx::tma_load_3d(dst, &tm_v, bar(L::kBarKVFull + slot), pnl * kPanel, w.hk, vw.load_row);
-              else
-                ptx::tma_load_4d(dst, &tm_v, bar(L::kBarKVFull + slot), pnl * kPanel, w.hk, vw.load_row, w.b);
+              for (int pnl = 0; pnl < kDPanels; ++pnl) {
+                const uint32_t dst = sbase + L::kKVTileBytes + pnl * L::kKVPanelBytes;
+                if constexpr (VARLEN)
+                  ptx::tma_load_3d(dst, &tm_v, bar(L::kBarKVFull + slot), pnl * kPanel, w.hk, vw.load_row);
+                else
+                  ptx::tma_load_4d(dst, &tm_v, bar(L::kBarKVFull + slot), pnl * kPanel, w.hk, vw.load_row, w.b);
+              }
             }
           }
         }
@@ -432,8 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == 12 && lane == 0) {
       // ========================================================== MMA issue
-      constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(kBR, BC, 0, 0);
-      constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(kBR, D, 0, 1);
+      constexpr uint32_t idesc_qk = FP8 ? ptx::idesc_e4m3_f32(kBR, BC) : ptx::idesc_bf16_f32(kBR, BC, 0, 0);
+      constexpr uint32_t idesc_pv = FP8 ? ptx::idesc_e4m3_f32(kBR, D) : ptx::idesc_bf16_f32(kBR, D, 0, 1);
       uint32_t qcount = 0, g = 0;
       uint32_t pc[kQT] = {0, 0};  // P-full completions consumed, per tile
       uint32_t uc[kQT] = {0, 0};  // units with the tile active, per tile
@@ -483,26 +506,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
               }
               ptx::tc_fence_after();
+              if constexpr (FP8) {
 #pragma unroll
-              for (int kk = 0; kk < BC / 16; ++kk) {
-                // V is MN-major: 16 keys = two 8-row swizzle atoms = 2048 bytes;
-                // the two 64-column halves of d sit one panel (BC * 128 bytes) apart.
-                const uint64_t bdesc = ptx::sw128_desc(v_base + kk * 2048, L::kKVPanelBytes, 1024);
-                ptx::mma_ts(tO, tP + kk * 8, bdesc, idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < BC / 32; ++kk) {
+                  // P: 32 e4m3 per step = 8 TMEM columns; V^T is K-major (keys
+                  // along the 128-byte rows): 32 keys = 32 bytes.
+                  const uint64_t bdesc = ptx::sw128_desc(v_base + kk * 32, 16, 1024);
+                  ptx::mma_ts_f8(tO, tP + kk * 8, bdesc, idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+                }
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < BC / 16; ++kk) {
+                  // V is MN-major: 16 keys = two 8-row swizzle atoms = 2048 bytes;
+                  // the two 64-column halves of d sit one panel (BC * 128 bytes) apart.
+                  const uint64_t bdesc = ptx::sw128_desc(v_base + kk * 2048, L::kKVPanelBytes, 1024);
+                  ptx::mma_ts(tO, tP + kk * 8, bdesc, idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+                }
               }
               if (j == nt) ptx::mma_commit(bar(L::kBarOFinal + t));
             }
             if (j < nt) {
               // S_t = Q_t K(j)^T
               const uint32_t q_base = base + L::kOffQ + t * L::kQTileBytes;
+              if constexpr (FP8) {
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                // K-major, 128-byte swizzle: 16 columns = 32 bytes inside a panel.
-                const uint32_t off_q = (kk / 4) * L::kQPanelBytes + (kk % 4) * 32;
-                const uint32_t off_k = (kk / 4) * L::kKVPanelBytes + (kk % 4) * 32;
-                const uint64_t adesc = ptx::sw128_desc(q_base + off_q, 16, 1024);
-                const uint64_t bdesc = ptx::sw128_desc(k_base + off_k, 16, 1024);
-                ptx::mma_ss(tS, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < D / 32; ++kk) {
+                  // 32 e4m3 = 32 bytes inside the single 128-byte panel.
+                  ptx::mma_ss_f8(tS, ptx::sw128_desc(q_base + kk * 32, 16, 1024),
+                                 ptx::sw128_desc(k_base + kk * 32, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                }
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                  // K-major, 128-byte swizzle: 16 columns = 32 bytes inside a panel.
+                  const uint32_t off_q = (kk / 4) * L::kQPanelBytes + (kk % 4) * 32;
+                  const uint32_t off_k = (kk / 4) * L::kKVPanelBytes + (kk % 4) * 32;
+                  const uint64_t adesc = ptx::sw128_desc(q_base + off_q, 16, 1024);
+                  const uint64_t bdesc = ptx::sw128_desc(k_base + off_k, 16, 1024);
+                  ptx::mma_ss(tS, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+                }
               }
               ptx::mma_commit(bar(L::kBarSFull + t));
             }
@@ -686,10 +728,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        float m_ref = -INFINITY;
+        float m_ref = -INFINITY;  // FP8: in scaled log2 units
         float l = 0.f;
+        // FP8: dequantisation scales of this query tile and key/value head.
+        float cq = 0.f, vsc = 1.f;
+        if constexpr (FP8) {
+          cq = c2 * p.q_scale[(w.b * p.H + w.h) * p.q_blocks + qw.load_row / kBR];
+          vsc = p.v_scale[w.b * (p.H / p.group) + w.hk];
+        }
   #pragma unroll 1
         for (int j = 0; j < nt; ++j) {
+          // FP8: exp2 coefficient of this key tile (query and key scales folded in).
+          const float c2j = FP8 ? cq * p.k_scale[(w.b * (p.H / p.group) + w.hk) * p.k_blocks + w.j0 + j] : c2;
           if (!ptx::mbar_wait_warp(bar(L::kBarSFull + t), sc & 1u, s_abort, tmo)) {
             record_error(p.status, kErrTimeout, kSiteSoftS);
             ok = false;
@@ -738,13 +788,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           // than the threshold (log2 units): the merge identity of §11.2 holds
           // for any common reference value, so results stay exact.
           float m_new = m_ref;
-          if (bm > m_ref && (m_ref == -INFINITY || (bm - m_ref) * c2 > p.rescale_threshold)) m_new = bm;
-          const float alpha = (m_new == m_ref) ? 1.f : ptx::ex2((m_ref - m_new) * c2);
-          m_ref = m_new;
-          const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref * c2;
+          float alpha, neg;
+          if constexpr (FP8) {
+            // Maximum compared in scaled log2 units (the coefficient changes per key tile).
+            const float bms = bm * c2j;
+            if (bms > m_ref && (m_ref == -INFINITY || bms - m_ref > p.rescale_threshold)) m_new = bms;
+            alpha = (m_new == m_ref) ? 1.f : ptx::ex2(m_ref - m_new);
+            m_ref = m_new;
+            neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+          } else {
+            if (bm > m_ref && (m_ref == -INFINITY || (bm - m_ref) * c2 > p.rescale_threshold)) m_new = bm;
+            alpha = (m_new == m_ref) ? 1.f : ptx::ex2((m_ref - m_new) * c2);
+            m_ref = m_new;
+            neg = (m_ref == -INFINITY) ? 0.f : -m_ref * c2;
+          }
           // p = 2^(s*c2 - m*c2): one packed FFMA per two scores, then ex2 each;
-          // row sums in four packed accumulators; P stored in 16-column chunks.
-          const uint64_t c2x2 = ptx::f2_pack(c2, c2);
+          // row sums in four packed accumulators; P stored in 16-column chunks
+          // (FP8: rounded to e4m3, four per column, 8 columns per 32 scores).
+          const uint64_t c2x2 = ptx::f2_pack(c2j, c2j);
           const uint64_t negx2 = ptx::f2_pack(neg, neg);
           uint64_t acc[4] = {0, 0, 0, 0};
   #pragma unroll
@@ -757,9 +818,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1);
               const uint64_t e01 = ptx::f2_pack(e0, e1);
               acc[(c >> 1) & 3] = ptx::f2_add(acc[(c >> 1) & 3], e01);
-              pk[(c - c0) / 2] = ptx::pack_bf16x2(e0, e1);
+              if constexpr (FP8) {
+                const uint32_t h = ptx::pack_e4m3x2(e0, e1);
+                const int k = (c - c0) / 2;  // pair index 0..15; words hold two pairs
+                if (k & 1)
+                  pk[k >> 1] |= h << 16;
+                else
+                  pk[k >> 1] = h;
+              } else {
+                pk[(c - c0) / 2] = ptx::pack_bf16x2(e0, e1);
+              }
             }
-            ptx::tmem_st16(tP + c0 / 2, pk);
+            if constexpr (FP8)
+              ptx::tmem_st8(tP + c0 / 4, pk);
+            else
+              ptx::tmem_st16(tP + c0 / 2, pk);
           }
           float a0, a1, a2, a3, a4, a5, a6, a7;
           ptx::f2_unpack(acc[0], a0, a1);
@@ -796,9 +869,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         // Final message for the epilogue: 1 / l, and the row's log-sum-exp.
         const bool has = l > 0.f;
-        s_invl[t * kBR + row] = has ? 1.f / l : 0.f;
+        s_invl[t * kBR + row] = has ? vsc / l : 0.f;
         if (row >= qw.lo && row < qw.hi) {
-          const float lse = has ? (m_ref * p.scale + log2f(l) * 0.69314718055994530942f) : -INFINITY;
+          const float lse = !has ? -INFINITY
+                            : FP8 ? (m_ref + log2f(l)) * 0.69314718055994530942f
+                                  : (m_ref * p.scale + log2f(l) * 0.69314718055994530942f);
           const int i_seq = qw.load_row - w.q_start + row;
           if constexpr (SPLIT)
             p.ws_lse[static_cast<size_t>(w.split) * p.B * p.H * p.Nq + w.lse_base + i_seq] = lse;
@@ -932,7 +1007,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) {
 #pragma unroll
-            for (int pnl = 0; pnl < kDPanels; ++pnl) {
+            for (int pnl = 0; pnl < kOutPanels; ++pnl) {
               if constexpr (VARLEN)
                 ptx::tma_store_3d(&tm_o, stage + pnl * 4096, pnl * kPanel, w.h, qw.load_row + (wq << 5));
               else

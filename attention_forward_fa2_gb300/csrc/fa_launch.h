@@ -92,6 +92,18 @@ struct BwdLaunchArgs {
 template <int D, bool CAUSAL>
 cudaError_t launch_bwd(const BwdLaunchArgs& a);
 
+// FP8 path (fa_fp8.cu).
+struct Fp8QuantParams {
+  const __nv_bfloat16 *q, *k, *v;  // bf16 inputs, [B, Nq, H, D] and [B, Nk, Hk, D]
+  uint8_t *q8, *k8;                // e4m3 codes, same layouts
+  uint8_t* vt8;                    // e4m3 codes of V, [B, Hk, D, nk_pad]
+  float *q_scale, *k_scale, *v_scale;
+  int B, Nq, Nk, H, Hk, D, nk_pad;
+};
+cudaError_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream);
+cudaError_t launch_fwd_fp8(bool causal, const LaunchArgs& a);
+int fp8_smem_bytes();
+
 // Merge of the key splits (fa_combine.cuh); D in {64, 128}.
 cudaError_t launch_combine(int D, const float* ws_o, const float* ws_lse, int S, long long rows, int H,
                            int Nq, __nv_bfloat16* o, float* lse, cudaStream_t stream);

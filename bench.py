@@ -22,6 +22,9 @@ cpu_baseline  the fp64 CPU oracle (test infrastructure) timed on a bounded
 
 --impl reference times that oracle as the reference arm (the pages ship no
 implementation; the oracle is the reference), printing the same JSON line.
+--fp8 times the e4m3 forward (fa_fwd_fp8) on the workload quantised once
+beforehand (block scales; the quantisation is not timed), against the fp8
+dense peak taken as twice the measured bf16 one (the nominal ratio).
 --bwd times the backward pass instead (fa_bwd: preprocessing, key-block kernel,
 dQ conversion), FLOPs counted as 2.5x the forward's (five matrix products
 against two).  Rank 0 prints one JSON line on stdout.
@@ -267,6 +270,8 @@ def add_mode(cfg, args):
     cfg["launch"] = "cuda graph replay" if args.graph else "stream launches"
     if args.split:
         cfg["form"] = "key-split (fa_fwd_splitkv)"
+    if getattr(args, "fp8", False):
+        cfg["form"] = "fp8 e4m3, block-quantised (fa_fwd_fp8)"
     return cfg
 
 
@@ -290,7 +295,17 @@ def run_ours(args, w):
     Nq = maxlen if w.varlen else w.Nq
     lse = torch.empty((w.B, w.H, Nq), dtype=torch.float32, device=dev)
 
+    t8 = None
+    if args.fp8:
+        if w.varlen or w.d != 128 or args.split:
+            raise SystemExit("--fp8 takes dense d = 128 workloads")
+        t8 = fa.quantize_fp8(dq, dk, dv)
+        torch.cuda.synchronize(dev)
+
     def step():
+        if args.fp8:
+            fa.forward_fp8(t8, causal=args.causal, out=o, lse=lse)
+            return
         if args.split:
             fa.forward_splitkv(dq, dk, dv, out=o, lse=lse, causal=args.causal, workspace=ws)
         elif w.varlen:
@@ -359,6 +374,10 @@ def run_ours(args, w):
 
     # -------------------------------------------------------- end to end
     e2e_steps = max(3, min(args.steps, 20))
+    if args.fp8:
+        # the step's inputs are the e4m3 codes and scales
+        q, k, v = t8.q8.cpu(), t8.k8.cpu(), t8.vt8.cpu()
+        dq, dk, dv = t8.q8, t8.k8, t8.vt8
     hq, hk, hv = (t.pin_memory() for t in (q, k, v))
     ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
     hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
@@ -395,19 +414,22 @@ def run_ours(args, w):
         return 0
     peaks, src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    traffic = load_traffic(w.name)
+    peak_note = "%s bf16 dense burst (MEASURED_PEAKS.json)" % src if src == "measured" else "fallback 1.9 PFLOP/s bf16"
+    if args.fp8:
+        peak *= 2.0
+        peak_note = "fp8 dense = 2 x " + peak_note + " (nominal fp8/bf16 ratio 4.5/2.25)"
+    traffic = None if args.fp8 else load_traffic(w.name)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)" if args.fp8 else "bf16",
         "data": "synthetic (seeded N(0,1), generated on the host)",
-        "config": add_mode(workload_config(w, kernel_cfg, args.causal), args),
+        "config": add_mode(workload_config(w, None if args.fp8 else kernel_cfg, args.causal), args),
         "pct_of_peak": 100.0 * kernel_tflops / peak,
         "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": UNIT,
                      "frac": kernel_tflops / peak, "traffic": traffic,
-                     "peak_source": "%s bf16 dense burst (MEASURED_PEAKS.json)" % src
-                     if src == "measured" else "fallback 1.9 PFLOP/s bf16",
-                     "kernel": "fa_fwd_kernel<%d,128,*>" % w.d,
+                     "peak_source": peak_note,
+                     "kernel": "fa_fwd_kernel<128,128,4,fp8>" if args.fp8 else "fa_fwd_kernel<%d,128,*>" % w.d,
                      "algorithmic_flops_per_launch": flops},
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
@@ -557,6 +579,7 @@ def main(argv=None):
     ap.add_argument("--causal", action="store_true",
                     help="causal mask (FLOPs count the visible query/key pairs only)")
     ap.add_argument("--bwd", action="store_true", help="time the backward pass instead")
+    ap.add_argument("--fp8", action="store_true", help="time the e4m3 forward instead")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

@@ -204,6 +204,36 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            int d, float scale, int flags, void* workspace, long long workspace_bytes, void* stream);
 
 /*
+ * FP8 forward ("GPU 内核与 FlashAttention" §15.5: e4m3 inputs with block
+ * quantisation).  Quantisation: every block of values shares one fp32 scale
+ * s = amax(block) / 448 (1 for an all-zero block) and a value x is stored as
+ * the e4m3 code nearest to x / s (round to nearest even, saturating).
+ * Blocks: 128 query rows of one head (Q), 128 keys of one key/value head (K),
+ * one key/value head (V).  V is stored transposed.
+ *
+ * fa_fp8_sizes     -- sizes[0..5] = bytes of q8 [B, Nq, H, d], k8 [B, Nk, Hk, d],
+ *                     vt8 [B, Hk, d, nk_pad] (nk_pad = Nk rounded up to 16),
+ *                     and element counts of q_scale [B, H, ceil(Nq/128)],
+ *                     k_scale [B, Hk, ceil(Nk/128)], v_scale [B, Hk] (fp32).
+ * fa_quantize_fp8  -- fills those from bf16 q, k, v (layouts of fa_fwd_ex);
+ *                     all device pointers, code buffers 16-byte aligned.
+ * fa_fwd_fp8       -- the forward pass on them: o (bf16 [B, Nq, H, d]) and
+ *                     lse (fp32 [B, H, Nq]) as fa_fwd_ex, scale the natural
+ *                     softmax scale applied to the dequantised scores, flags 0
+ *                     or FA_FLAG_CAUSAL.  S = Q K^T and O += P V run on the
+ *                     tensor cores in e4m3 with fp32 accumulation; P is rounded
+ *                     to e4m3 for the second product (the row sums use the
+ *                     unrounded fp32 values).  Dense tensors, d = 128 only
+ *                     (FA_ERR_UNSUPPORTED otherwise).
+ */
+int fa_fp8_sizes(int B, int Nq, int Nk, int H, int Hk, int d, long long* sizes);
+int fa_quantize_fp8(const void* q, const void* k, const void* v, int B, int Nq, int Nk, int H, int Hk, int d,
+                    void* q8, void* k8, void* vt8, float* q_scale, float* k_scale, float* v_scale, void* stream);
+int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_scale, const float* k_scale,
+               const float* v_scale, void* o, float* lse, int B, int Nq, int Nk, int H, int Hk, int d, float scale,
+               int flags, void* stream);
+
+/*
  * fa_set_timeout_ns -- limit for every device-side wait (mbarrier waits) in
  * later launches.  On expiry the kernel records FA_ERR_TIMEOUT, drains its
  * own copies and MMAs, releases tensor memory and exits.  Default 1e9 ns.
