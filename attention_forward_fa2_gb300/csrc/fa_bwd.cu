@@ -4,7 +4,7 @@
 namespace fa {
 
 namespace {
-constexpr int kBwdStages = 4;
+constexpr int kBwdStages = 2;
 
 template <int D, bool CAUSAL>
 cudaError_t launch_bwd_impl(const BwdLaunchArgs& a) {

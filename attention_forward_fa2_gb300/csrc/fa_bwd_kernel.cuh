@@ -19,40 +19,35 @@
 // registers, performed at L2).  A last kernel scales the accumulator into
 // bf16 dQ.
 //
-// Main kernel, per step (one block of 64 queries of one head):
-//   S^T  = K Q^T        M=128 keys, N=64 queries, K=d     tensor memory S[g%2]
-//   dP^T = V dO^T       M=128 keys, N=64                  tensor memory dP[g%2]
+// Main kernel, per step (one block of 128 queries of one head):
+//   S^T  = K Q^T        M=128 keys, N=128 queries, K=d    tensor memory S
+//   dP^T = V dO^T       M=128 keys, N=128                 tensor memory dP
 //   P^T  = 2^(S^T * scale * log2 e - L * log2 e)           softmax warps, bf16 over S
 //   dS^T = P^T o (dP^T - D)                                bf16 over dP, and to
 //                                                          shared memory
-//   dV  += P^T dO       M=128 keys, N=d, K=64              P^T from tensor memory
-//   dK  += dS^T Q       M=128 keys, N=d, K=64              dS^T from tensor memory
-//   dQ^T = K^T dS^T     M=d, N=64 queries, K=128 keys      both from shared memory,
-//                                                          result over dP[g%2]
+//   dV  += P^T dO       M=128 keys, N=d, K=128             P^T from tensor memory
+//   dK  += dS^T Q       M=128 keys, N=d, K=128             dS^T from tensor memory
+//   dQ^T = K^T dS^T     M=d, N=128 queries, K=128 keys     both from shared memory,
+//                                                          result over dP
+// Every product is N = 128 (the full tensor rate; N = 64 products are bound by
+// shared-memory operand reads) and a step issues 40 MMAs for 21 MFLOP.
 // Computing dQ transposed keeps every MMA at M = 128 and makes each TMEM lane a
 // feature index: for each query the 32 lanes of a drain warp hold 32
 // consecutive features, one 128-byte line of the [B, H, queries, d]
 // accumulator, so one reduction instruction per query adds a whole line and
-// nothing is staged in shared memory (shared-memory bandwidth, not the tensor
-// pipe, is what limits this kernel).  Keys are TMEM lanes in the other products: one thread owns
-// one key row and half of the 64 query columns of a step.
-// Tensor memory (512 columns): S0 [0,64) S1 [64,128) dP0 [128,192)
-// dP1 [192,256) dV [256,384) dK [384,512); dQ^T(g) reuses dP[g%2] once dK(g)
-// has read dS^T from it.  The single MMA thread issues, per step g:
-//   dV(g) | S(g+2) | dP(g+1) | dK(g) dQ^T(g)
-// so S runs two steps and dP one step ahead of the softmax warps, which
-// therefore never wait for the tensor core while it has work queued.  Every
-// handshake barrier between these roles is doubled per buffer (step parity),
-// so a barrier's next completion always needs an action of its own waiter
-// first and no waiter can miss a phase.
-// Softmax warpgroup c reads columns [32c, 32c + 32) of S and dP and writes
-// its 16 packed bf16 words (P^T, dS^T) over the first 16 of those columns --
-// columns no other warp reads -- so the K = 64 operand of the dV and dK
-// MMAs sits at word offsets 0, 8 (queries 0-31) and 32, 40 (queries 32-63).
+// nothing is staged in shared memory.
+// Tensor memory (512 columns): S [0,128) dP [128,256) dV [256,384)
+// dK [384,512); dQ^T(g) reuses dP's columns once dK(g) has read dS^T.  The
+// single MMA thread issues, per step g:
+//   dV(g) | S(g+1) | dK(g) dQ^T(g) | dP(g+1)   (dP(g+1) after the drain read dQ^T(g))
+// Softmax warpgroup c reads columns [64c, 64c + 64) of S and dP and writes
+// its packed bf16 words over the first 32 of them, 32 columns at a time.
 //
 // Roles (512 threads):
-//   warps 0-7   softmax: P, dS (warps 0-3 query columns 0-31, 4-7 columns 32-63)
+//   warps 0-7   softmax: P, dS (warps 0-3 query columns 0-63, 4-7 columns 64-127)
 //   warps 8-11  dQ drain (TMEM -> registers -> L2 reductions) and the dK/dV epilogue
+//               (168 registers: all 128 accumulator columns are held at once, so
+//               the tensor memory is released before the reductions are issued)
 //   warp 12     MMA issue (one thread) + TMEM allocation
 //   warp 13     TMA loads (one thread)
 //   warps 14-15 idle
@@ -69,7 +64,7 @@
 namespace fa {
 
 constexpr int kBwdBK = 128;  // keys per work unit (M of the key-row products)
-constexpr int kBwdBQ = 64;   // queries per step
+constexpr int kBwdBQ = 128;  // queries per step
 
 struct BwdParams {
   int B, Nq, Nk, H, Hk, group;
@@ -158,27 +153,26 @@ struct BwdSmem {
   static constexpr int kKVBytes = kBwdBK * D * 2;        // one K or V block
   static constexpr int kKVPanel = kBwdBK * 128;          // 64 features x 128 rows
   static constexpr int kQBytes = kBwdBQ * D * 2;         // one Q or dO block
-  static constexpr int kQPanel = kBwdBQ * 128;
+  static constexpr int kQPanel = kBwdBQ * 128;           // 64 features x 128 queries
   static constexpr int kSlotBytes = 2 * kQBytes;         // Q then dO
-  static constexpr int kDSBytes = kBwdBK * kBwdBQ * 2;   // dS^T, keys x queries
+  static constexpr int kDSPanel = kBwdBK * 128;          // dS^T: 64 queries x 128 keys
+  static constexpr int kDSBytes = kBwdBK * kBwdBQ * 2;   // two query panels
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKVBytes;
   static constexpr int kOffQ = kOffV + kKVBytes;
   static constexpr int kOffDS = kOffQ + STAGES * kSlotBytes;
-  static constexpr int kOffLD = kOffDS + kDSBytes;  // per slot: lse2[64], delta[64]
-  static constexpr int kLDBytes = 2 * kBwdBQ * 4;
-  static constexpr int kOffBar = kOffLD + STAGES * kLDBytes;
+  static constexpr int kOffBar = kOffDS + kDSBytes;
   static constexpr int kBarKVFull = 0;
   static constexpr int kBarKVEmpty = 1;
   static constexpr int kBarQFull = 2;
   static constexpr int kBarQEmpty = kBarQFull + STAGES;
-  static constexpr int kBarSFull = kBarQEmpty + STAGES;  // two, one per S buffer
-  static constexpr int kBarDPFull = kBarSFull + 2;       // two, one per dP buffer
-  static constexpr int kBarPFull = kBarDPFull + 2;       // two
-  static constexpr int kBarDSFull = kBarPFull + 2;       // two
-  static constexpr int kBarDQFull = kBarDSFull + 2;    // two
-  static constexpr int kBarDQEmpty = kBarDQFull + 2;   // two
-  static constexpr int kBarAccFull = kBarDQEmpty + 2;
+  static constexpr int kBarSFull = kBarQEmpty + STAGES;
+  static constexpr int kBarDPFull = kBarSFull + 1;
+  static constexpr int kBarPFull = kBarDPFull + 1;
+  static constexpr int kBarDSFull = kBarPFull + 1;
+  static constexpr int kBarDQFull = kBarDSFull + 1;
+  static constexpr int kBarDQEmpty = kBarDQFull + 1;
+  static constexpr int kBarAccFull = kBarDQEmpty + 1;
   static constexpr int kBarAccEmpty = kBarAccFull + 1;
   static constexpr int kBarTeardown = kBarAccEmpty + 1;
   static constexpr int kNumBars = kBarTeardown + 1;
@@ -239,16 +233,23 @@ enum BwdSite : int {
   kBSiteSoftDQ = 111, kBSiteSoftQ = 112, kBSiteDrainDQ = 113, kBSiteDrainAcc = 114, kBSiteTeardown = 115
 };
 
+// Register split (setmaxnreg): softmax warpgroups 128, the drain warpgroup
+// 168 (all 128 accumulator columns in registers), MMA / load warpgroup 88.
+struct BwdRegSplit {
+  static constexpr int kSoftmax = 128;  // the launch allocation (__launch_bounds__(512, 1))
+  static constexpr int kDrain = 168;
+  static constexpr int kOther = 88;
+  static_assert(2 * 128 * kSoftmax + 128 * kDrain + 128 * kOther <= 65536,
+                "register split exceeds the launch allocation");
+};
+
 template <int D, int STAGES, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const BwdParams p) {
   static_assert(D == 128, "backward kernel: d = 128");
-  // S runs two steps ahead: the Q/dO slot of step g + 2 must not be the slot
-  // step g still reads (with two slots the MMA thread would wait for a load
-  // that waits for it); with three the next load starts only one step ahead.
-  static_assert(STAGES >= 4, "backward ring depth");
+  static_assert(STAGES >= 2, "backward ring depth");
   using L = BwdSmem<D, STAGES>;
   constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
   constexpr int kDPanels = D / 64;
@@ -264,7 +265,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
   volatile uint32_t* const s_tmem = reinterpret_cast<volatile uint32_t*>(gbase + L::kOffTmem);
   volatile int* const s_abort = reinterpret_cast<volatile int*>(gbase + L::kOffAbort);
-  const float* const s_ld = reinterpret_cast<const float*>(gbase + L::kOffLD);
   const uint64_t tmo = p.timeout_ns;
 
   if (warp == 13 && lane == 0) {
@@ -281,14 +281,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(L::kBarQFull + s), 1);
       ptx::mbar_init(bar(L::kBarQEmpty + s), 1);
     }
-    for (int b2 = 0; b2 < 2; ++b2) {
-      ptx::mbar_init(bar(L::kBarSFull + b2), 1);
-      ptx::mbar_init(bar(L::kBarDPFull + b2), 1);
-      ptx::mbar_init(bar(L::kBarPFull + b2), 256);
-      ptx::mbar_init(bar(L::kBarDSFull + b2), 256);
-      ptx::mbar_init(bar(L::kBarDQFull + b2), 1);
-      ptx::mbar_init(bar(L::kBarDQEmpty + b2), 128);
-    }
+    ptx::mbar_init(bar(L::kBarSFull), 1);
+    ptx::mbar_init(bar(L::kBarDPFull), 1);
+    ptx::mbar_init(bar(L::kBarPFull), 256);
+    ptx::mbar_init(bar(L::kBarDSFull), 256);
+    ptx::mbar_init(bar(L::kBarDQFull), 1);
+    ptx::mbar_init(bar(L::kBarDQEmpty), 128);
     ptx::mbar_init(bar(L::kBarAccFull), 1);
     ptx::mbar_init(bar(L::kBarAccEmpty), 128);
     ptx::mbar_init(bar(L::kBarTeardown), 1);
@@ -304,7 +302,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *s_tmem;
   const int off = p.Nk - p.Nq;
 
+  // Handshake barriers are single: each one's next completion needs an action
+  // of its own waiter first (S(g+1) is issued after P(g) is seen, dP(g+1)
+  // after the drain has read dQ^T(g), which follows dS(g), and so on).
   if (warp >= 12) {
+    ptx::setmaxnreg_dec<BwdRegSplit::kOther>();
     if (warp == 13 && lane == 0) {
       // ============================================================ TMA loads
       uint32_t g = 0, uc = 0;
@@ -338,17 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int h = w.hk * p.group + i / w.nqb;
           const int qb = w.qb0 + i % w.nqb;
           const uint32_t fb = bar(L::kBarQFull + slot);
-          ptx::mbar_arrive_expect_tx(fb, L::kSlotBytes + L::kLDBytes);
+          ptx::mbar_arrive_expect_tx(fb, L::kSlotBytes);
           const uint32_t sq = base + L::kOffQ + slot * L::kSlotBytes;
 #pragma unroll
           for (int pn = 0; pn < kDPanels; ++pn) {
             ptx::tma_load_4d(sq + pn * L::kQPanel, &tm_q, fb, pn * 64, h, qb * kBwdBQ, w.b);
             ptx::tma_load_4d(sq + L::kQBytes + pn * L::kQPanel, &tm_do, fb, pn * 64, h, qb * kBwdBQ, w.b);
           }
-          const size_t ro = (static_cast<size_t>(w.b) * p.H + h) * p.nq_pad + static_cast<size_t>(qb) * kBwdBQ;
-          const uint32_t sld = base + L::kOffLD + slot * L::kLDBytes;
-          ptx::bulk_load(sld, p.lse2 + ro, kBwdBQ * 4, fb);
-          ptx::bulk_load(sld + kBwdBQ * 4, p.delta + ro, kBwdBQ * 4, fb);
         }
       }
       // Drain: every issued copy must land before the CTA exits.
@@ -372,17 +370,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         return false;
       };
-      // S^T(t) = K Q(t)^T into S[t % 2]; dP^T(t) = V dO(t)^T into dP[t % 2].
       auto issue_s = [&](uint32_t t) {
         const uint32_t sq = base + L::kOffQ + (t % STAGES) * L::kSlotBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oa = (kk / 4) * L::kKVPanel + (kk % 4) * 32;
           const uint32_t ob = (kk / 4) * L::kQPanel + (kk % 4) * 32;
-          ptx::mma_ss(tmem + kColS + (t & 1u) * kBwdBQ, ptx::sw128_desc(base + L::kOffK + oa, 16, 1024),
+          ptx::mma_ss(tmem + kColS, ptx::sw128_desc(base + L::kOffK + oa, 16, 1024),
                       ptx::sw128_desc(sq + ob, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(bar(L::kBarSFull + (t & 1u)));
+        ptx::mma_commit(bar(L::kBarSFull));
       };
       auto issue_dp = [&](uint32_t t) {
         const uint32_t sdo = base + L::kOffQ + (t % STAGES) * L::kSlotBytes + L::kQBytes;
@@ -390,23 +387,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oa = (kk / 4) * L::kKVPanel + (kk % 4) * 32;
           const uint32_t ob = (kk / 4) * L::kQPanel + (kk % 4) * 32;
-          ptx::mma_ss(tmem + kColDP + (t & 1u) * kBwdBQ, ptx::sw128_desc(base + L::kOffV + oa, 16, 1024),
+          ptx::mma_ss(tmem + kColDP, ptx::sw128_desc(base + L::kOffV + oa, 16, 1024),
                       ptx::sw128_desc(sdo + ob, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(bar(L::kBarDPFull + (t & 1u)));
-      };
-      // Q(t) / dO(t) loaded.
-      auto wait_q = [&](uint32_t t) -> bool {
-        if (!wait(bar(L::kBarQFull + t % STAGES), (t / STAGES) & 1u, kBSiteMmaQ)) return false;
-        ptx::tc_fence_after();
-        return true;
-      };
-      // dP[t % 2] last held dQ^T(t - 2): the drain must have read it.
-      auto wait_dq_read = [&](uint32_t t) -> bool {
-        if (t < 2) return true;
-        if (!wait(bar(L::kBarDQEmpty + (t & 1u)), ((t - 2) >> 1) & 1u, kBSiteMmaDQ)) return false;
-        ptx::tc_fence_after();
-        return true;
+        ptx::mma_commit(bar(L::kBarDPFull));
       };
 #pragma unroll 1
       FA_BWD_FOR_EACH_UNIT(u) {
@@ -414,52 +398,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w.nsteps == 0) continue;
         if (!wait(bar(L::kBarKVFull), uc & 1u, kBSiteMmaKV)) break;
         ptx::tc_fence_after();
-        // Prologue: S of the first two steps, dP of the first.
-        if (!wait_q(g)) break;
+        if (!wait(bar(L::kBarQFull + g % STAGES), (g / STAGES) & 1u, kBSiteMmaQ)) break;
+        ptx::tc_fence_after();
         issue_s(g);
-        if (w.nsteps > 1) {
-          if (!wait_q(g + 1)) break;
-          issue_s(g + 1);
-        }
-        if (!wait_dq_read(g)) break;
+        // dP's columns last held dQ^T(g - 1) (the previous unit's last step).
+        if (g > 0 && !wait(bar(L::kBarDQEmpty), (g - 1) & 1u, kBSiteMmaDQ)) break;
+        ptx::tc_fence_after();
         issue_dp(g);
 #pragma unroll 1
         for (int i = 0; i < w.nsteps && ok; ++i, ++g) {
           const uint32_t slot = g % STAGES;
           const uint32_t sq = base + L::kOffQ + slot * L::kSlotBytes;
           const uint32_t sdo = sq + L::kQBytes;
-          const uint32_t b2 = g & 1u;
-          // dV += P^T dO once the softmax warps have written P^T(g).
-          if (!wait(bar(L::kBarPFull + b2), (g >> 1) & 1u, kBSiteMmaP)) break;
+          // dV += P^T dO (P^T of warpgroup c at columns 64c .. 64c + 31).
+          if (!wait(bar(L::kBarPFull), g & 1u, kBSiteMmaP)) break;
           if (i == 0 && uc > 0 && !wait(bar(L::kBarAccEmpty), (uc - 1) & 1u, kBSiteMmaAcc)) break;
           ptx::tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kBwdBQ / 16; ++kk)
-            ptx::mma_ts(tmem + kColDV, tmem + kColS + b2 * kBwdBQ + (kk >> 1) * 32 + (kk & 1) * 8,
+            ptx::mma_ts(tmem + kColDV, tmem + kColS + (kk >> 2) * 64 + (kk & 3) * 8,
                         ptx::sw128_desc(sdo + kk * 2048, L::kQPanel, 1024), id_acc, (i > 0 || kk > 0) ? 1u : 0u);
-          // S(g + 2) over P(g) (read by the dV just issued, which runs first).
-          if (i + 2 < w.nsteps) {
-            if (!wait_q(g + 2)) break;
-            issue_s(g + 2);
-          }
-          // dP(g + 1) into the other dP buffer.
+          // S(g + 1) over P(g) (read by the dV just issued, which runs first).
           if (i + 1 < w.nsteps) {
-            if (!wait_dq_read(g + 1)) break;
-            issue_dp(g + 1);
+            if (!wait(bar(L::kBarQFull + (g + 1) % STAGES), ((g + 1) / STAGES) & 1u, kBSiteMmaQ)) break;
+            ptx::tc_fence_after();
+            issue_s(g + 1);
           }
-          // dK += dS^T Q, then dQ^T = K^T dS^T over dP[g % 2] (after dK has read dS^T).
-          if (!wait(bar(L::kBarDSFull + b2), (g >> 1) & 1u, kBSiteMmaDS)) break;
+          // dK += dS^T Q, then dQ^T = K^T dS^T over dP (after dK has read dS^T).
+          if (!wait(bar(L::kBarDSFull), g & 1u, kBSiteMmaDS)) break;
           ptx::tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kBwdBQ / 16; ++kk)
-            ptx::mma_ts(tmem + kColDK, tmem + kColDP + b2 * kBwdBQ + (kk >> 1) * 32 + (kk & 1) * 8,
+            ptx::mma_ts(tmem + kColDK, tmem + kColDP + (kk >> 2) * 64 + (kk & 3) * 8,
                         ptx::sw128_desc(sq + kk * 2048, L::kQPanel, 1024), id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_commit(bar(L::kBarQEmpty + slot));  // Q(g) and dO(g) read
 #pragma unroll
           for (int kk = 0; kk < kBwdBK / 16; ++kk)
-            ptx::mma_ss(tmem + kColDP + b2 * kBwdBQ, ptx::sw128_desc(base + L::kOffK + kk * 2048, L::kKVPanel, 1024),
-                        ptx::sw128_desc(base + L::kOffDS + kk * 2048, L::kDSBytes, 1024), id_dq, kk > 0 ? 1u : 0u);
-          ptx::mma_commit(bar(L::kBarDQFull + b2));
-          ptx::mma_commit(bar(L::kBarQEmpty + slot));
+            ptx::mma_ss(tmem + kColDP, ptx::sw128_desc(base + L::kOffK + kk * 2048, L::kKVPanel, 1024),
+                        ptx::sw128_desc(base + L::kOffDS + kk * 2048, L::kDSPanel, 1024), id_dq, kk > 0 ? 1u : 0u);
+          ptx::mma_commit(bar(L::kBarDQFull));
+          // dP(g + 1) once the drain has read dQ^T(g) out of those columns.
+          if (i + 1 < w.nsteps) {
+            if (!wait(bar(L::kBarDQEmpty), g & 1u, kBSiteMmaDQ)) break;
+            ptx::tc_fence_after();
+            issue_dp(g + 1);
+          }
         }
         if (!ok) break;
         ptx::mma_commit(bar(L::kBarAccFull));
@@ -470,10 +453,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ptx::mbar_wait_drain(bar(L::kBarTeardown), 0, tmo)) record_error(p.status, kErrTimeout, kBSiteTeardown);
     }
   } else if (warp < 8) {
+    // (softmax warpgroups keep the launch allocation, BwdRegSplit::kSoftmax)
     // ================================================================ softmax
-    const int c = warp >> 2;                    // query columns [32c, 32c + 32)
+    const int c = warp >> 2;                    // query columns [64c, 64c + 64)
     const int r = ((warp & 3) << 5) + lane;     // key row of the block
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
+    const uint32_t tSc = tmem + lane_off + kColS + c * 64;
+    const uint32_t tDc = tmem + lane_off + kColDP + c * 64;
     const float c2 = p.scale_log2;
     uint32_t g = 0;
     bool ok = true;
@@ -485,106 +471,98 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool key_ok = kj < p.Nk;
 #pragma unroll 1
       for (int i = 0; i < w.nsteps && ok; ++i, ++g) {
-        const uint32_t slot = g % STAGES;
+        const int h = w.hk * p.group + i / w.nqb;
         const int qb = w.qb0 + i % w.nqb;
-        const uint32_t b2 = g & 1u;
-        if (!ptx::mbar_wait_warp(bar(L::kBarSFull + b2), (g >> 1) & 1u, s_abort, tmo) ||
-            !ptx::mbar_wait_warp(bar(L::kBarQFull + slot), (g / STAGES) & 1u, s_abort, tmo)) {
+        const int q0 = qb * kBwdBQ + c * 64;  // first query of this warpgroup's columns
+        const size_t row0 = (static_cast<size_t>(w.b) * p.H + h) * p.nq_pad + q0;
+        const float4* l2g = reinterpret_cast<const float4*>(p.lse2 + row0);
+        const float4* dlg = reinterpret_cast<const float4*>(p.delta + row0);
+        if (!ptx::mbar_wait_warp(bar(L::kBarSFull), g & 1u, s_abort, tmo)) {
           record_error(p.status, kErrTimeout, kBSiteSoftS);
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        uint32_t sr[32];
-        ptx::tmem_ld32(tmem + lane_off + kColS + b2 * kBwdBQ + c * 32, sr);
-        ptx::tmem_wait_ld();
-        // 128-bit broadcast loads (all lanes read the same words), D too,
-        // so that no shared load sits on the dS path.
-        float lse2[32], dlt[32];
-        {
-          const float4* l4 = reinterpret_cast<const float4*>(s_ld + slot * (L::kLDBytes / 4) + c * 32);
-          const float4* d4 = reinterpret_cast<const float4*>(s_ld + slot * (L::kLDBytes / 4) + kBwdBQ + c * 32);
+        // P^T = 2^(S^T c2 - L log2 e), 32 columns at a time; keys past Nk and
+        // (causal) keys after a query's limit get 0; the bf16 pairs of half hh
+        // go to columns 16 hh .. 16 hh + 15 (already read).  The packed pairs
+        // stay in registers for dS: S(g + 1) overwrites these columns as soon
+        // as dV(g) has read them.
+        uint32_t pk[32];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t sr[32];
+          ptx::tmem_ld32(tSc + hh * 32, sr);
+          ptx::tmem_wait_ld();
+          const int lim = CAUSAL ? kj - off - (q0 + hh * 32) : -1;  // column k masked when k < lim
 #pragma unroll
           for (int k4 = 0; k4 < 8; ++k4) {
-            const float4 x = l4[k4];
-            lse2[4 * k4] = x.x;
-            lse2[4 * k4 + 1] = x.y;
-            lse2[4 * k4 + 2] = x.z;
-            lse2[4 * k4 + 3] = x.w;
-            const float4 y = d4[k4];
-            dlt[4 * k4] = y.x;
-            dlt[4 * k4 + 1] = y.y;
-            dlt[4 * k4 + 2] = y.z;
-            dlt[4 * k4 + 3] = y.w;
+            const float4 l = __ldg(l2g + hh * 8 + k4);
+#pragma unroll
+            for (int k = 4 * k4; k < 4 * k4 + 4; k += 2) {
+              const float la = (k & 3) == 0 ? l.x : l.z, lb = (k & 3) == 0 ? l.y : l.w;
+              float x0, x1;
+              ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])),
+                                         ptx::f2_pack(c2, c2), ptx::f2_pack(-la, -lb)),
+                             x0, x1);
+              float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1);
+              if (!key_ok || (CAUSAL && k < lim)) e0 = 0.f;
+              if (!key_ok || (CAUSAL && k + 1 < lim)) e1 = 0.f;
+              pk[16 * hh + k / 2] = ptx::pack_bf16x2(e0, e1);
+            }
           }
+          ptx::tmem_st16(tSc + hh * 16, &pk[16 * hh]);
         }
-        // Keys past Nk, and (causal) keys after a query's limit, get P = 0.
-        const int q0 = qb * kBwdBQ + c * 32;
-        const int lim = CAUSAL ? kj - off - q0 : -1;  // column k is masked when k < lim
-        float pr[32];
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          float x0, x1;
-          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])),
-                                     ptx::f2_pack(c2, c2), ptx::f2_pack(-lse2[k], -lse2[k + 1])),
-                         x0, x1);
-          pr[k] = ptx::ex2(x0);
-          pr[k + 1] = ptx::ex2(x1);
-        }
-        if (!key_ok) {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) pr[k] = 0.f;
-        } else if (CAUSAL && lim > 0) {
-#pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (k < lim) pr[k] = 0.f;
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) pk[k] = ptx::pack_bf16x2(pr[2 * k], pr[2 * k + 1]);
-        ptx::tmem_st16(tmem + lane_off + kColS + b2 * kBwdBQ + c * 32, pk);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(L::kBarPFull + b2));
-        // dS^T = P^T o (dP^T - D)
-        if (!ptx::mbar_wait_warp(bar(L::kBarDPFull + b2), (g >> 1) & 1u, s_abort, tmo)) {
+        ptx::mbar_arrive(bar(L::kBarPFull));
+        // dS^T = P^T o (dP^T - D), from the bf16 P^T pairs held above.
+        if (!ptx::mbar_wait_warp(bar(L::kBarDPFull), g & 1u, s_abort, tmo)) {
           record_error(p.status, kErrTimeout, kBSiteSoftDP);
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        uint32_t dr[32];
-        ptx::tmem_ld32(tmem + lane_off + kColDP + b2 * kBwdBQ + c * 32, dr);
-        ptx::tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float d0 = pr[2 * k] * (__uint_as_float(dr[2 * k]) - dlt[2 * k]);
-          const float d1 = pr[2 * k + 1] * (__uint_as_float(dr[2 * k + 1]) - dlt[2 * k + 1]);
-          pk[k] = ptx::pack_bf16x2(d0, d1);
-        }
-        ptx::tmem_st16(tmem + lane_off + kColDP + b2 * kBwdBQ + c * 32, pk);
-        // The same bf16 dS^T row into shared memory (B operand of dQ^T):
-        // 128 keys x 64 queries, 128-byte rows, 128-byte swizzle.  The
-        // previous step's dQ^T MMA must have read the buffer.
-        if (g > 0 && !ptx::mbar_wait_warp(bar(L::kBarDQFull + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u, s_abort, tmo)) {
+        // The previous step's dQ^T MMA must have read the shared dS^T buffer.
+        if (g > 0 && !ptx::mbar_wait_warp(bar(L::kBarDQFull), (g - 1) & 1u, s_abort, tmo)) {
           record_error(p.status, kErrTimeout, kBSiteSoftDQ);
           ok = false;
           break;
         }
-        const uint32_t row_addr = base + L::kOffDS + r * 128;
+        // Row r of panel c (64 queries) of the shared dS^T: 128 bytes, 128-byte swizzle.
+        const uint32_t row_addr = base + L::kOffDS + c * L::kDSPanel + r * 128;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int chunk = 4 * c + q4;
-          ptx::st_shared_v4(row_addr + ((chunk ^ (r & 7)) << 4), pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2],
-                            pk[4 * q4 + 3]);
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t dr[32], ds[16];
+          ptx::tmem_ld32(tDc + hh * 32, dr);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int k4 = 0; k4 < 8; ++k4) {
+            const float4 dl = __ldg(dlg + hh * 8 + k4);
+#pragma unroll
+            for (int k = 4 * k4; k < 4 * k4 + 4; k += 2) {
+              const float da = (k & 3) == 0 ? dl.x : dl.z, db = (k & 3) == 0 ? dl.y : dl.w;
+              const uint32_t pw = pk[16 * hh + k / 2];
+              const float p0 = __uint_as_float(pw << 16), p1 = __uint_as_float(pw & 0xffff0000u);
+              ds[k / 2] = ptx::pack_bf16x2(p0 * (__uint_as_float(dr[k]) - da), p1 * (__uint_as_float(dr[k + 1]) - db));
+            }
+          }
+          ptx::tmem_st16(tDc + hh * 16, ds);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int chunk = 4 * hh + q4;
+            ptx::st_shared_v4(row_addr + ((chunk ^ (r & 7)) << 4), ds[4 * q4], ds[4 * q4 + 1], ds[4 * q4 + 2],
+                              ds[4 * q4 + 3]);
+          }
         }
         ptx::fence_proxy_async_smem();
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(L::kBarDSFull + b2));
+        ptx::mbar_arrive(bar(L::kBarDSFull));
       }
     }
   } else {
+    ptx::setmaxnreg_inc<BwdRegSplit::kDrain>();
     // ======================================== dQ drain and the dK / dV epilogue
     const int wq = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(wq << 5) << 16;
@@ -609,18 +587,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < w.nsteps && ok; ++i, ++g) {
         const int h = w.hk * p.group + i / w.nqb;
         const int qb = w.qb0 + i % w.nqb;
-        if (!ptx::mbar_wait_warp(bar(L::kBarDQFull + (g & 1u)), (g >> 1) & 1u, s_abort, tmo)) {
+        if (!ptx::mbar_wait_warp(bar(L::kBarDQFull), g & 1u, s_abort, tmo)) {
           record_error(p.status, kErrTimeout, kBSiteDrainDQ);
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        uint32_t v[64];
-        ptx::tmem_ld32(tmem + lane_off + kColDP + (g & 1u) * kBwdBQ, v);
-        ptx::tmem_ld32(tmem + lane_off + kColDP + (g & 1u) * kBwdBQ + 32, v + 32);
+        uint32_t v[128];
+#pragma unroll
+        for (int q32 = 0; q32 < 4; ++q32) ptx::tmem_ld32(tmem + lane_off + kColDP + q32 * 32, v + 32 * q32);
         ptx::tmem_wait_ld();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(L::kBarDQEmpty + (g & 1u)));
+        ptx::mbar_arrive(bar(L::kBarDQEmpty));
         // Query q of the block: the warp's 32 features are one 128-byte line.
         float* const dst = p.dq_acc + (static_cast<size_t>(w.b * p.H + h) * p.nq_pad + static_cast<size_t>(qb) * kBwdBQ) * D +
                            (wq << 5) + lane;
