@@ -237,8 +237,8 @@ enum BwdSite : int {
 // 168 (all 128 accumulator columns in registers), MMA / load warpgroup 88.
 struct BwdRegSplit {
   static constexpr int kSoftmax = 128;  // the launch allocation (__launch_bounds__(512, 1))
-  static constexpr int kDrain = 168;
-  static constexpr int kOther = 88;
+  static constexpr int kDrain = 152;
+  static constexpr int kOther = 104;
   static_assert(2 * 128 * kSoftmax + 128 * kDrain + 128 * kOther <= 65536,
                 "register split exceeds the launch allocation");
 };
@@ -370,25 +370,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         return false;
       };
+      // Shared-memory descriptors advance by byte offset / 16 in their low
+      // word (the address field cannot carry below 256 KiB), so each MMA
+      // costs the issuing thread an add instead of a descriptor build.
+      const uint64_t kdesc = ptx::sw128_desc(base + L::kOffK, 16, 1024);
+      const uint64_t vdesc = ptx::sw128_desc(base + L::kOffV, 16, 1024);
+      const uint64_t kdesc_mn = ptx::sw128_desc(base + L::kOffK, L::kKVPanel, 1024);
+      const uint64_t dsdesc_mn = ptx::sw128_desc(base + L::kOffDS, L::kDSPanel, 1024);
       auto issue_s = [&](uint32_t t) {
-        const uint32_t sq = base + L::kOffQ + (t % STAGES) * L::kSlotBytes;
+        const uint64_t qdesc = ptx::sw128_desc(base + L::kOffQ + (t % STAGES) * L::kSlotBytes, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oa = (kk / 4) * L::kKVPanel + (kk % 4) * 32;
           const uint32_t ob = (kk / 4) * L::kQPanel + (kk % 4) * 32;
-          ptx::mma_ss(tmem + kColS, ptx::sw128_desc(base + L::kOffK + oa, 16, 1024),
-                      ptx::sw128_desc(sq + ob, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+          ptx::mma_ss(tmem + kColS, kdesc + (oa >> 4), qdesc + (ob >> 4), id_s, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(bar(L::kBarSFull));
       };
       auto issue_dp = [&](uint32_t t) {
-        const uint32_t sdo = base + L::kOffQ + (t % STAGES) * L::kSlotBytes + L::kQBytes;
+        const uint64_t dodesc =
+            ptx::sw128_desc(base + L::kOffQ + (t % STAGES) * L::kSlotBytes + L::kQBytes, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oa = (kk / 4) * L::kKVPanel + (kk % 4) * 32;
           const uint32_t ob = (kk / 4) * L::kQPanel + (kk % 4) * 32;
-          ptx::mma_ss(tmem + kColDP, ptx::sw128_desc(base + L::kOffV + oa, 16, 1024),
-                      ptx::sw128_desc(sdo + ob, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+          ptx::mma_ss(tmem + kColDP, vdesc + (oa >> 4), dodesc + (ob >> 4), id_s, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(bar(L::kBarDPFull));
       };
@@ -414,10 +420,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait(bar(L::kBarPFull), g & 1u, kBSiteMmaP)) break;
           if (i == 0 && uc > 0 && !wait(bar(L::kBarAccEmpty), (uc - 1) & 1u, kBSiteMmaAcc)) break;
           ptx::tc_fence_after();
+          const uint64_t dodesc_mn = ptx::sw128_desc(sdo, L::kQPanel, 1024);
 #pragma unroll
           for (int kk = 0; kk < kBwdBQ / 16; ++kk)
-            ptx::mma_ts(tmem + kColDV, tmem + kColS + (kk >> 2) * 64 + (kk & 3) * 8,
-                        ptx::sw128_desc(sdo + kk * 2048, L::kQPanel, 1024), id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_ts(tmem + kColDV, tmem + kColS + (kk >> 2) * 64 + (kk & 3) * 8, dodesc_mn + kk * 128, id_acc,
+                        (i > 0 || kk > 0) ? 1u : 0u);
           // S(g + 1) over P(g) (read by the dV just issued, which runs first).
           if (i + 1 < w.nsteps) {
             if (!wait(bar(L::kBarQFull + (g + 1) % STAGES), ((g + 1) / STAGES) & 1u, kBSiteMmaQ)) break;
@@ -427,15 +434,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           // dK += dS^T Q, then dQ^T = K^T dS^T over dP (after dK has read dS^T).
           if (!wait(bar(L::kBarDSFull), g & 1u, kBSiteMmaDS)) break;
           ptx::tc_fence_after();
+          const uint64_t qdesc_mn = ptx::sw128_desc(sq, L::kQPanel, 1024);
 #pragma unroll
           for (int kk = 0; kk < kBwdBQ / 16; ++kk)
-            ptx::mma_ts(tmem + kColDK, tmem + kColDP + (kk >> 2) * 64 + (kk & 3) * 8,
-                        ptx::sw128_desc(sq + kk * 2048, L::kQPanel, 1024), id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_ts(tmem + kColDK, tmem + kColDP + (kk >> 2) * 64 + (kk & 3) * 8, qdesc_mn + kk * 128, id_acc,
+                        (i > 0 || kk > 0) ? 1u : 0u);
           ptx::mma_commit(bar(L::kBarQEmpty + slot));  // Q(g) and dO(g) read
 #pragma unroll
           for (int kk = 0; kk < kBwdBK / 16; ++kk)
-            ptx::mma_ss(tmem + kColDP, ptx::sw128_desc(base + L::kOffK + kk * 2048, L::kKVPanel, 1024),
-                        ptx::sw128_desc(base + L::kOffDS + kk * 2048, L::kDSPanel, 1024), id_dq, kk > 0 ? 1u : 0u);
+            ptx::mma_ss(tmem + kColDP, kdesc_mn + kk * 128, dsdesc_mn + kk * 128, id_dq, kk > 0 ? 1u : 0u);
           ptx::mma_commit(bar(L::kBarDQFull));
           // dP(g + 1) once the drain has read dQ^T(g) out of those columns.
           if (i + 1 < w.nsteps) {

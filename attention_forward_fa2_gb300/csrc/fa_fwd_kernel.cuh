@@ -82,13 +82,15 @@ constexpr int kQT = 2;         // query tiles per work unit
 constexpr int kThreads = 512;  // 16 warps
 constexpr int kPanel = 64;     // bf16 columns per 128-byte swizzle row
 
-// Register split after setmaxnreg (must sum to 65536 over 512 threads); the
-// variable-length form needs a little more in the softmax warps (window masks).
+// Register split after setmaxnreg (must sum to 65536 over 512 threads).  The
+// MMA-issue/load warps get more than the correction warps: with fewer they
+// spill in the issue loop, whose instruction slots the softmax warps of the
+// same scheduler compete for.
 template <bool VARLEN>
 struct RegSplit {
-  static constexpr int kSoftmax = VARLEN ? 184 : 176;
-  static constexpr int kCorrection = VARLEN ? 72 : 80;
-  static constexpr int kOther = VARLEN ? 72 : 80;
+  static constexpr int kSoftmax = 176;
+  static constexpr int kCorrection = 64;
+  static constexpr int kOther = 96;
   static_assert(2 * 128 * kSoftmax + 128 * kCorrection + 128 * kOther <= 65536,
                 "register split exceeds the launch allocation");
 };
@@ -506,44 +508,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
               }
               ptx::tc_fence_after();
+              // Descriptors advance by byte offset / 16 in their low word (the
+              // address field cannot carry: shared addresses stay below 256 KiB);
+              // building each one from scratch per MMA costs the issuing
+              // thread instruction slots it shares with two softmax warps.
               if constexpr (FP8) {
+                // P: 32 e4m3 per step = 8 TMEM columns; V^T is K-major (keys
+                // along the 128-byte rows): 32 keys = 32 bytes.
+                const uint64_t vdesc = ptx::sw128_desc(v_base, 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < BC / 32; ++kk) {
-                  // P: 32 e4m3 per step = 8 TMEM columns; V^T is K-major (keys
-                  // along the 128-byte rows): 32 keys = 32 bytes.
-                  const uint64_t bdesc = ptx::sw128_desc(v_base + kk * 32, 16, 1024);
-                  ptx::mma_ts_f8(tO, tP + kk * 8, bdesc, idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < BC / 32; ++kk)
+                  ptx::mma_ts_f8(tO, tP + kk * 8, vdesc + static_cast<uint64_t>(kk * 2), idesc_pv,
+                                 (j - 1 > 0 || kk > 0) ? 1u : 0u);
               } else {
+                // V is MN-major: 16 keys = two 8-row swizzle atoms = 2048 bytes;
+                // the two 64-column halves of d sit one panel (BC * 128 bytes) apart.
+                const uint64_t vdesc = ptx::sw128_desc(v_base, L::kKVPanelBytes, 1024);
 #pragma unroll
-                for (int kk = 0; kk < BC / 16; ++kk) {
-                  // V is MN-major: 16 keys = two 8-row swizzle atoms = 2048 bytes;
-                  // the two 64-column halves of d sit one panel (BC * 128 bytes) apart.
-                  const uint64_t bdesc = ptx::sw128_desc(v_base + kk * 2048, L::kKVPanelBytes, 1024);
-                  ptx::mma_ts(tO, tP + kk * 8, bdesc, idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < BC / 16; ++kk)
+                  ptx::mma_ts(tO, tP + kk * 8, vdesc + static_cast<uint64_t>(kk * 128), idesc_pv,
+                              (j - 1 > 0 || kk > 0) ? 1u : 0u);
               }
               if (j == nt) ptx::mma_commit(bar(L::kBarOFinal + t));
             }
             if (j < nt) {
               // S_t = Q_t K(j)^T
               const uint32_t q_base = base + L::kOffQ + t * L::kQTileBytes;
+              const uint64_t qdesc = ptx::sw128_desc(q_base, 16, 1024);
+              const uint64_t kdesc = ptx::sw128_desc(k_base, 16, 1024);
               if constexpr (FP8) {
 #pragma unroll
-                for (int kk = 0; kk < D / 32; ++kk) {
-                  // 32 e4m3 = 32 bytes inside the single 128-byte panel.
-                  ptx::mma_ss_f8(tS, ptx::sw128_desc(q_base + kk * 32, 16, 1024),
-                                 ptx::sw128_desc(k_base + kk * 32, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
-                }
+                for (int kk = 0; kk < D / 32; ++kk)  // 32 e4m3 = 32 bytes inside the single 128-byte panel
+                  ptx::mma_ss_f8(tS, qdesc + static_cast<uint64_t>(kk * 2), kdesc + static_cast<uint64_t>(kk * 2),
+                                 idesc_qk, kk > 0 ? 1u : 0u);
               } else {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                   // K-major, 128-byte swizzle: 16 columns = 32 bytes inside a panel.
                   const uint32_t off_q = (kk / 4) * L::kQPanelBytes + (kk % 4) * 32;
                   const uint32_t off_k = (kk / 4) * L::kKVPanelBytes + (kk % 4) * 32;
-                  const uint64_t adesc = ptx::sw128_desc(q_base + off_q, 16, 1024);
-                  const uint64_t bdesc = ptx::sw128_desc(k_base + off_k, 16, 1024);
-                  ptx::mma_ss(tS, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+                  ptx::mma_ss(tS, qdesc + static_cast<uint64_t>(off_q >> 4), kdesc + static_cast<uint64_t>(off_k >> 4),
+                              idesc_qk, kk > 0 ? 1u : 0u);
                 }
               }
               ptx::mma_commit(bar(L::kBarSFull + t));
