@@ -157,11 +157,13 @@ struct BwdSmem {
   static constexpr int kSlotBytes = 2 * kQBytes;         // Q then dO
   static constexpr int kDSPanel = kBwdBK * 128;          // dS^T: 64 queries x 128 keys
   static constexpr int kDSBytes = kBwdBK * kBwdBQ * 2;   // two query panels
+  static constexpr int kLDBytes = 2 * kBwdBQ * 4;        // scaled LSE then D of a query block
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKVBytes;
   static constexpr int kOffQ = kOffV + kKVBytes;
   static constexpr int kOffDS = kOffQ + STAGES * kSlotBytes;
-  static constexpr int kOffBar = kOffDS + kDSBytes;
+  static constexpr int kOffLD = kOffDS + kDSBytes;       // one kLDBytes block per Q/dO slot
+  static constexpr int kOffBar = kOffLD + STAGES * kLDBytes;
   static constexpr int kBarKVFull = 0;
   static constexpr int kBarKVEmpty = 1;
   static constexpr int kBarQFull = 2;
@@ -179,10 +181,14 @@ struct BwdSmem {
   static constexpr int kOffTmem = kOffBar + ((kNumBars * 8 + 15) / 16) * 16;
   static constexpr int kOffAbort = kOffTmem + 16;
   static constexpr int kBytes = kOffAbort + 16;
-  static constexpr int kAlloc = kBytes + 1024;
+  // Up to 1 KiB of slack aligns the tiles when the dynamic window does not
+  // start on a 1 KiB boundary; the budget leaves less than that, so the
+  // kernel checks at run time that its aligned layout fits (it does when the
+  // window starts 1 KiB-aligned, as it does with no static shared memory).
+  static constexpr int kAlloc = kBytes + 1024 <= 232448 ? kBytes + 1024 : 232448;
   static_assert(kOffV % 1024 == 0 && kOffQ % 1024 == 0 && kOffDS % 1024 == 0,
                 "swizzled tiles need 1 KiB alignment");
-  static_assert(kAlloc <= 232448, "shared memory budget exceeded");
+  static_assert(kBytes <= 232448, "shared memory budget exceeded");
 };
 
 // One work unit: key block kb of key/value head hk in batch b, and the query
@@ -230,7 +236,8 @@ __device__ __forceinline__ BwdUnit bwd_decode(const BwdParams& p, int u) {
 enum BwdSite : int {
   kBSiteLoadKV = 101, kBSiteLoadQ = 102, kBSiteMmaKV = 103, kBSiteMmaQ = 104, kBSiteMmaP = 105,
   kBSiteMmaDS = 106, kBSiteMmaDQ = 107, kBSiteMmaAcc = 108, kBSiteSoftS = 109, kBSiteSoftDP = 110,
-  kBSiteSoftDQ = 111, kBSiteSoftQ = 112, kBSiteDrainDQ = 113, kBSiteDrainAcc = 114, kBSiteTeardown = 115
+  kBSiteSoftDQ = 111, kBSiteSoftQ = 112, kBSiteDrainDQ = 113, kBSiteDrainAcc = 114, kBSiteTeardown = 115,
+  kBSiteSmemWindow = 116
 };
 
 // Register split (setmaxnreg): softmax warpgroups 128, the drain warpgroup
@@ -258,6 +265,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_base = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - raw_base);
+  if ((base - raw_base) + static_cast<uint32_t>(L::kBytes) > static_cast<uint32_t>(L::kAlloc)) {
+    // The aligned layout would run past the allocation (uniform over the CTA,
+    // decided before any barrier or tensor-memory use).
+    if (threadIdx.x == 0) record_error(p.status, kErrUnsupported, kBSiteSmemWindow);
+    return;
+  }
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -340,13 +353,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int h = w.hk * p.group + i / w.nqb;
           const int qb = w.qb0 + i % w.nqb;
           const uint32_t fb = bar(L::kBarQFull + slot);
-          ptx::mbar_arrive_expect_tx(fb, L::kSlotBytes);
+          ptx::mbar_arrive_expect_tx(fb, L::kSlotBytes + L::kLDBytes);
           const uint32_t sq = base + L::kOffQ + slot * L::kSlotBytes;
 #pragma unroll
           for (int pn = 0; pn < kDPanels; ++pn) {
             ptx::tma_load_4d(sq + pn * L::kQPanel, &tm_q, fb, pn * 64, h, qb * kBwdBQ, w.b);
             ptx::tma_load_4d(sq + L::kQBytes + pn * L::kQPanel, &tm_do, fb, pn * 64, h, qb * kBwdBQ, w.b);
           }
+          // The block's scaled LSE and D rows (512 bytes each, 512-byte aligned:
+          // nq_pad is a multiple of the block) for the softmax warps.
+          const size_t ro = (static_cast<size_t>(w.b) * p.H + h) * p.nq_pad + static_cast<size_t>(qb) * kBwdBQ;
+          const uint32_t sld = base + L::kOffLD + slot * L::kLDBytes;
+          ptx::bulk_load(sld, p.lse2 + ro, kBwdBQ * 4, fb);
+          ptx::bulk_load(sld + kBwdBQ * 4, p.delta + ro, kBwdBQ * 4, fb);
         }
       }
       // Drain: every issued copy must land before the CTA exits.
@@ -481,10 +500,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = w.hk * p.group + i / w.nqb;
         const int qb = w.qb0 + i % w.nqb;
         const int q0 = qb * kBwdBQ + c * 64;  // first query of this warpgroup's columns
-        const size_t row0 = (static_cast<size_t>(w.b) * p.H + h) * p.nq_pad + q0;
-        const float4* l2g = reinterpret_cast<const float4*>(p.lse2 + row0);
-        const float4* dlg = reinterpret_cast<const float4*>(p.delta + row0);
-        if (!ptx::mbar_wait_warp(bar(L::kBarSFull), g & 1u, s_abort, tmo)) {
+        // Scaled LSE and D of this warpgroup's 64 queries, staged with Q(g)
+        // (shared-memory broadcasts instead of dependent global loads).
+        const uint32_t slot = g % STAGES;
+        const float4* l2g = reinterpret_cast<const float4*>(gbase + L::kOffLD + slot * L::kLDBytes) + c * 16;
+        const float4* dlg = l2g + kBwdBQ / 4;
+        if (!ptx::mbar_wait_warp(bar(L::kBarSFull), g & 1u, s_abort, tmo) ||
+            !ptx::mbar_wait_warp(bar(L::kBarQFull + slot), (g / STAGES) & 1u, s_abort, tmo)) {
           record_error(p.status, kErrTimeout, kBSiteSoftS);
           ok = false;
           break;
@@ -504,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int lim = CAUSAL ? kj - off - (q0 + hh * 32) : -1;  // column k masked when k < lim
 #pragma unroll
           for (int k4 = 0; k4 < 8; ++k4) {
-            const float4 l = __ldg(l2g + hh * 8 + k4);
+            const float4 l = l2g[hh * 8 + k4];
 #pragma unroll
             for (int k = 4 * k4; k < 4 * k4 + 4; k += 2) {
               const float la = (k & 3) == 0 ? l.x : l.z, lb = (k & 3) == 0 ? l.y : l.w;
@@ -545,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_wait_ld();
 #pragma unroll
           for (int k4 = 0; k4 < 8; ++k4) {
-            const float4 dl = __ldg(dlg + hh * 8 + k4);
+            const float4 dl = dlg[hh * 8 + k4];
 #pragma unroll
             for (int k = 4 * k4; k < 4 * k4 + 4; k += 2) {
               const float da = (k & 3) == 0 ? dl.x : dl.z, db = (k & 3) == 0 ? dl.y : dl.w;

@@ -137,6 +137,7 @@ struct FwdParams {
 };
 
 // Error codes shared with the C-ABI header.
+constexpr int kErrUnsupported = -2;
 constexpr int kErrTimeout = -5;
 constexpr int kErrBadSeqlens = -7;
 
