@@ -760,6 +760,9 @@ int fa_quantize_fp8(const void* q, const void* k, const void* v, int B, int Nq, 
     return FA_ERR_INVALID_ARG;
   for (const void* ptr : {q, k, v, static_cast<const void*>(q8), static_cast<const void*>(k8), static_cast<const void*>(vt8)})
     if (ptr && !aligned16(ptr)) return FA_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(q_scale) | reinterpret_cast<uintptr_t>(k_scale) |
+       reinterpret_cast<uintptr_t>(v_scale)) & 3u)
+    return FA_ERR_ALIGN;
   DeviceState* st = nullptr;
   if ((rc = device_state(&st)) != FA_OK) return rc;
   fa::Fp8QuantParams p{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),

@@ -33,93 +33,99 @@ __device__ __forceinline__ float block_amax(float v) {
 
 __device__ __forceinline__ float scale_of(float amax) { return amax > 0.f ? amax / kE4M3Max : 1.f; }
 
-// One block per scale: blockIdx.x < nq -> a 128-row block of Q, then K blocks,
-// then one block per key/value head for V.
-template <int D>
-__global__ void __launch_bounds__(256) fp8_scales_kernel(Fp8QuantParams p) {
-  const int qb = (p.Nq + kBR - 1) / kBR, kb = (p.Nk + kBR - 1) / kBR;
-  const long long nq = static_cast<long long>(p.B) * p.H * qb;
-  const long long nk = static_cast<long long>(p.B) * p.Hk * kb;
-  long long id = blockIdx.x;
-  float m = 0.f;
-  float* out;
-  if (id < nq) {
-    const int blk = static_cast<int>(id % qb);
-    const long long bh = id / qb;
-    const int h = static_cast<int>(bh % p.H), b = static_cast<int>(bh / p.H);
-    const int r0 = blk * kBR, r1 = min(p.Nq, r0 + kBR);
-    for (int e = threadIdx.x; e < (r1 - r0) * D; e += blockDim.x) {
-      const int r = r0 + e / D, c = e % D;
-      m = fmaxf(m, fabsf(__bfloat162float(p.q[((static_cast<size_t>(b) * p.Nq + r) * p.H + h) * D + c])));
-    }
-    out = p.q_scale + id;
-  } else if (id < nq + nk) {
-    id -= nq;
-    const int blk = static_cast<int>(id % kb);
-    const long long bh = id / kb;
-    const int h = static_cast<int>(bh % p.Hk), b = static_cast<int>(bh / p.Hk);
-    const int r0 = blk * kBR, r1 = min(p.Nk, r0 + kBR);
-    for (int e = threadIdx.x; e < (r1 - r0) * D; e += blockDim.x) {
-      const int r = r0 + e / D, c = e % D;
-      m = fmaxf(m, fabsf(__bfloat162float(p.k[((static_cast<size_t>(b) * p.Nk + r) * p.Hk + h) * D + c])));
-    }
-    out = p.k_scale + id;
-  } else {
-    id -= nq + nk;
-    const int h = static_cast<int>(id % p.Hk), b = static_cast<int>(id / p.Hk);
-    for (long long e = threadIdx.x; e < static_cast<long long>(p.Nk) * D; e += blockDim.x) {
-      const long long r = e / D;
-      const int c = static_cast<int>(e % D);
-      m = fmaxf(m, fabsf(__bfloat162float(p.v[((static_cast<size_t>(b) * p.Nk + r) * p.Hk + h) * D + c])));
-    }
-    out = p.v_scale + id;
-  }
-  m = block_amax(m);
-  if (threadIdx.x == 0) *out = scale_of(m);
-}
-
 __device__ __forceinline__ uint32_t to_e4m3x2(float lo, float hi) { return ptx::pack_e4m3x2(lo, hi); }
 
-// Q and K codes, same layout as the bf16 input; 8 elements per thread.
-template <int D>
-__global__ void __launch_bounds__(256) fp8_quant_qk_kernel(Fp8QuantParams p) {
-  const long long nq8 = static_cast<long long>(p.B) * p.Nq * p.H * D / 8;
-  const long long nk8 = static_cast<long long>(p.B) * p.Nk * p.Hk * D / 8;
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= nq8 + nk8) return;
-  const bool isq = i < nq8;
-  const long long e = (isq ? i : i - nq8) * 8;  // first element
-  const int Hx = isq ? p.H : p.Hk, Nx = isq ? p.Nq : p.Nk;
-  const long long row = e / D;                  // (b * N + n) * Hx + h
-  const int h = static_cast<int>(row % Hx);
-  const long long bn = row / Hx;
-  const int n = static_cast<int>(bn % Nx), b = static_cast<int>(bn / Nx);
-  const int blocks = (Nx + kBR - 1) / kBR;
-  const float s = isq ? p.q_scale[(static_cast<size_t>(b) * p.H + h) * blocks + n / kBR]
-                      : p.k_scale[(static_cast<size_t>(b) * p.Hk + h) * blocks + n / kBR];
-  const __nv_bfloat16* src = (isq ? p.q : p.k) + e;
-  uint8_t* dst = (isq ? p.q8 : p.k8) + e;
-  uint32_t w[2];
+__device__ __forceinline__ float amax8(uint4 u) {
+  // Largest magnitude of eight bf16 values (the sign bit cleared).
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  float m = 0.f;
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    float x[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) x[k] = __bfloat162float(src[4 * half + k]) / s;
-    w[half] = to_e4m3x2(x[0], x[1]) | (to_e4m3x2(x[2], x[3]) << 16);
+  for (int i = 0; i < 4; ++i) {
+    m = fmaxf(m, __uint_as_float((w[i] << 16) & 0x7fffffffu));
+    m = fmaxf(m, __uint_as_float(w[i] & 0x7fff0000u));
   }
-  *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+  return m;
+}
+
+// One block per 128-row block of Q (blockIdx.x < nq) or of K.  A block's rows
+// are read once into registers (eight 16-byte chunks per thread: 128 rows x
+// 256 bytes), reduced to the block maximum, and written as codes with the
+// block's scale.  K blocks also reduce the same rows of V and fold them into
+// the per-head V maximum (non-negative floats order like their bit patterns,
+// so an integer atomicMax on the bits is exact and order-independent).
+template <int D>
+__global__ void __launch_bounds__(256) fp8_quant_qk_kernel(Fp8QuantParams p, unsigned int* v_amax_bits) {
+  static_assert(D == 128, "16 chunks of 16 bytes per row");
+  const int qb = (p.Nq + kBR - 1) / kBR, kb = (p.Nk + kBR - 1) / kBR;
+  const long long nq = static_cast<long long>(p.B) * p.H * qb;
+  long long id = blockIdx.x;
+  const bool isq = id < nq;
+  if (!isq) id -= nq;
+  const int blocks = isq ? qb : kb;
+  const int Hx = isq ? p.H : p.Hk, Nx = isq ? p.Nq : p.Nk;
+  const int blk = static_cast<int>(id % blocks);
+  const long long bh = id / blocks;
+  const int h = static_cast<int>(bh % Hx), b = static_cast<int>(bh / Hx);
+  const int r0 = blk * kBR, rows = min(Nx - r0, kBR);
+  const __nv_bfloat16* src = isq ? p.q : p.k;
+  uint8_t* dst = isq ? p.q8 : p.k8;
+  uint4 x[8];
+  float m = 0.f, mv = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = threadIdx.x + 256 * i;  // chunk index in the block: row e / 16, chunk e % 16
+    const int r = e >> 4, c = e & 15;
+    x[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (r < rows) {
+      const size_t off = ((static_cast<size_t>(b) * Nx + r0 + r) * Hx + h) * D + c * 8;
+      x[i] = *reinterpret_cast<const uint4*>(src + off);
+      m = fmaxf(m, amax8(x[i]));
+      if (!isq) mv = fmaxf(mv, amax8(*reinterpret_cast<const uint4*>(p.v + off)));
+    }
+  }
+  m = block_amax(m);
+  const float s = scale_of(m);
+  if (threadIdx.x == 0) (isq ? p.q_scale : p.k_scale)[id] = s;
+  if (!isq) {
+    mv = block_amax(mv);
+    if (threadIdx.x == 0) atomicMax(v_amax_bits + bh, __float_as_uint(mv));
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = threadIdx.x + 256 * i;
+    const int r = e >> 4, c = e & 15;
+    if (r < rows) {
+      const uint32_t w[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+      uint32_t o[2];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const float a0 = __uint_as_float(w[2 * half] << 16) / s, a1 = __uint_as_float(w[2 * half] & 0xffff0000u) / s;
+        const float a2 = __uint_as_float(w[2 * half + 1] << 16) / s,
+                    a3 = __uint_as_float(w[2 * half + 1] & 0xffff0000u) / s;
+        o[half] = to_e4m3x2(a0, a1) | (to_e4m3x2(a2, a3) << 16);
+      }
+      const size_t off = ((static_cast<size_t>(b) * Nx + r0 + r) * Hx + h) * D + c * 8;
+      *reinterpret_cast<uint2*>(dst + off) = make_uint2(o[0], o[1]);
+    }
+  }
+}
+
+// The per-head V scales from the reduced maxima (after the transposed codes are written).
+__global__ void fp8_v_scale_kernel(Fp8QuantParams p, const unsigned int* v_amax_bits) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < p.B * p.Hk) p.v_scale[i] = scale_of(__uint_as_float(v_amax_bits[i]));
 }
 
 // V codes, transposed: one block per (b, hk, 64 keys); a 64 x D tile goes
 // through shared memory so that both the reads (rows of d) and the writes
 // (rows of keys) are contiguous.
 template <int D>
-__global__ void __launch_bounds__(256) fp8_quant_vt_kernel(Fp8QuantParams p) {
+__global__ void __launch_bounds__(256) fp8_quant_vt_kernel(Fp8QuantParams p, const unsigned int* v_amax_bits) {
   __shared__ uint8_t tile[D][64 + 4];
   const int kt = blockIdx.x;  // 64-key tile
   const int bh = blockIdx.y;  // b * Hk + hk
   const int h = bh % p.Hk, b = bh / p.Hk;
-  const float s = p.v_scale[bh];
+  const float s = scale_of(__uint_as_float(v_amax_bits[bh]));
   for (int e = threadIdx.x; e < 64 * D; e += blockDim.x) {
     const int r = e / D, c = e % D;
     const int key = kt * 64 + r;
@@ -152,23 +158,25 @@ cudaError_t launch_fwd_fp8_impl(const LaunchArgs& a) {
 
 cudaError_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream) {
   if (p.D != 128) return cudaErrorInvalidValue;
-  const long long qb = (p.Nq + kBR - 1) / kBR, kb = (p.Nk + kBR - 1) / kBR;
-  const long long nscales = static_cast<long long>(p.B) * p.H * qb + static_cast<long long>(p.B) * p.Hk * kb +
-                            static_cast<long long>(p.B) * p.Hk;
-  fp8_scales_kernel<128><<<static_cast<unsigned>(nscales), 256, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  // v_scale holds the bit patterns of the per-head V maxima until the last
+  // kernel turns them into scales (it is the only scratch the call needs).
+  unsigned int* const v_amax_bits = reinterpret_cast<unsigned int*>(p.v_scale);
+  const long long bhk = static_cast<long long>(p.B) * p.Hk;
+  cudaError_t e = cudaMemsetAsync(v_amax_bits, 0, static_cast<size_t>(bhk) * sizeof(unsigned int), stream);
   if (e != cudaSuccess) return e;
-  const long long n8 = (static_cast<long long>(p.B) * p.Nq * p.H + static_cast<long long>(p.B) * p.Nk * p.Hk) * 128 / 8;
-  if (n8 > 0) {
-    fp8_quant_qk_kernel<128><<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(p);
+  const long long qb = (p.Nq + kBR - 1) / kBR, kb = (p.Nk + kBR - 1) / kBR;
+  const long long nblocks = static_cast<long long>(p.B) * p.H * qb + bhk * kb;
+  if (nblocks > 0) {
+    fp8_quant_qk_kernel<128><<<static_cast<unsigned>(nblocks), 256, 0, stream>>>(p, v_amax_bits);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const int kt = (p.nk_pad + 63) / 64;
   if (kt > 0) {
-    fp8_quant_vt_kernel<128><<<dim3(static_cast<unsigned>(kt), static_cast<unsigned>(p.B * p.Hk)), 256, 0, stream>>>(p);
+    fp8_quant_vt_kernel<128><<<dim3(static_cast<unsigned>(kt), static_cast<unsigned>(bhk)), 256, 0, stream>>>(p, v_amax_bits);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  return cudaSuccess;
+  fp8_v_scale_kernel<<<static_cast<unsigned>((bhk + 255) / 256), 256, 0, stream>>>(p, v_amax_bits);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_fp8(bool causal, const LaunchArgs& a) {

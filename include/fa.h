@@ -216,7 +216,11 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
  *                     and element counts of q_scale [B, H, ceil(Nq/128)],
  *                     k_scale [B, Hk, ceil(Nk/128)], v_scale [B, Hk] (fp32).
  * fa_quantize_fp8  -- fills those from bf16 q, k, v (layouts of fa_fwd_ex);
- *                     all device pointers, code buffers 16-byte aligned.
+ *                     all device pointers, code buffers 16-byte aligned, scale
+ *                     buffers 4-byte aligned (FA_ERR_ALIGN otherwise).  Reads
+ *                     Q once and K, V twice (V's scale needs the whole head
+ *                     before its codes); v_scale holds intermediate values until
+ *                     the call's work on `stream` completes.
  * fa_fwd_fp8       -- the forward pass on them: o (bf16 [B, Nq, H, d]) and
  *                     lse (fp32 [B, H, Nq]) as fa_fwd_ex, scale the natural
  *                     softmax scale applied to the dequantised scores, flags 0
