@@ -14,7 +14,9 @@ value      TFLOP/s = 4*B*H*N^2*d / (device time per step), inputs resident in HB
            the forward has no exchange step, so scaling is weak).
 e2e        the same metric through the public call with host buffers: each step
            copies q, k, v from pinned host memory, runs the forward and copies
-           O and LSE back, all inside the timed region.
+           O and LSE back, all inside the timed region; the copies of
+           neighbouring steps overlap the compute (two copy streams, two device
+           buffer sets), as a serving loop would run them.
 roofline   the kernel's achieved TFLOP/s (algorithmic FLOPs / launch time,
            CUDA events on the launch stream) against the measured bf16 peak.
 cpu_baseline  the fp64 CPU oracle (test infrastructure) timed on a bounded
@@ -249,6 +251,58 @@ def run_reference(args, w):
     return 0
 
 
+E2E_COPIES = ("every step copies its inputs in and its results out; the copies of neighbouring steps "
+              "overlap its compute (two copy streams, two device buffer sets)")
+
+
+def pipelined_e2e(torch, dev, stream, sets, host_in, host_out, run, steps, world):
+    """Milliseconds per end-to-end step with the copies of neighbouring steps
+    overlapped: step i's inputs go host -> device on one copy stream while
+    step i-1 computes on `stream` and step i-2's results go device -> host on
+    a second copy stream.  Two device buffer sets alternate; events order each
+    set's reuse (inputs after the compute two steps back has read them,
+    outputs after their copy out).  sets[s] = (device inputs, device outputs),
+    host_in the pinned inputs (every step copies all of them), host_out[s] the
+    pinned outputs of set s, run(s) launches one step on `stream` for set s."""
+    cs_in, cs_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def one(i):
+        s = i % 2
+        with torch.cuda.stream(cs_in):
+            if i >= 2:
+                cs_in.wait_event(ev_comp[s])
+            for d_, h_ in zip(sets[s][0], host_in):
+                d_.copy_(h_, non_blocking=True)
+            ev_in[s].record(cs_in)
+        stream.wait_event(ev_in[s])
+        if i >= 2:
+            stream.wait_event(ev_out[s])
+        run(s)
+        ev_comp[s].record(stream)
+        with torch.cuda.stream(cs_out):
+            cs_out.wait_event(ev_comp[s])
+            for h_, d_ in zip(host_out[s], sets[s][1]):
+                h_.copy_(d_, non_blocking=True)
+            ev_out[s].record(cs_out)
+
+    for i in range(2):
+        one(i)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    cs_in.wait_event(e0)
+    for i in range(2, 2 + steps):
+        one(i)
+    e1.record(cs_out)  # the last copy out is the last work of the region
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    return e0.elapsed_time(e1) / steps
+
+
 def workload_config(w, kernel_cfg, causal=False):
     cfg = {"workload": "%s: %s" % (w.name, w.note or ""), "B": w.B, "H": w.H, "d": w.d,
            "layout": "[batch, seq, heads, d_head] bf16", "causal": bool(causal),
@@ -302,16 +356,19 @@ def run_ours(args, w):
         t8 = fa.quantize_fp8(dq, dk, dv)
         torch.cuda.synchronize(dev)
 
-    def step():
+    def step_on(bq, bk, bv, bcu, bt8, bo, bl):
         if args.fp8:
-            fa.forward_fp8(t8, causal=args.causal, out=o, lse=lse)
+            fa.forward_fp8(bt8, causal=args.causal, out=bo, lse=bl)
             return
         if args.split:
-            fa.forward_splitkv(dq, dk, dv, out=o, lse=lse, causal=args.causal, workspace=ws)
+            fa.forward_splitkv(bq, bk, bv, out=bo, lse=bl, causal=args.causal, workspace=ws)
         elif w.varlen:
-            fa.forward(dq, dk, dv, cu_seqlens=dcu, max_seqlen=maxlen, out=o, lse=lse, causal=args.causal)
+            fa.forward(bq, bk, bv, cu_seqlens=bcu, max_seqlen=maxlen, out=bo, lse=bl, causal=args.causal)
         else:
-            fa.forward_qk(dq, dk, dv, out=o, lse=lse, causal=args.causal)
+            fa.forward_qk(bq, bk, bv, out=bo, lse=bl, causal=args.causal)
+
+    def step():
+        step_on(dq, dk, dv, dcu, t8, o, lse)
 
     ws = None
     if args.split:
@@ -374,37 +431,35 @@ def run_ours(args, w):
 
     # -------------------------------------------------------- end to end
     e2e_steps = max(3, min(args.steps, 20))
+    # Every step copies its inputs from pinned host memory (the e4m3 codes for
+    # --fp8; their block scales stay resident) and its O and LSE back.
     if args.fp8:
-        # the step's inputs are the e4m3 codes and scales
         q, k, v = t8.q8.cpu(), t8.k8.cpu(), t8.vt8.cpu()
-        dq, dk, dv = t8.q8, t8.k8, t8.vt8
-    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
-    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-    hcu = cu_q.pin_memory() if w.varlen else None
+    host_in = [t.pin_memory() for t in (q, k, v)] + ([cu_q.pin_memory()] if w.varlen else [])
 
-    def e2e_step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
+    def device_set(first):
+        if first:
+            ins = [t8.q8, t8.k8, t8.vt8] if args.fp8 else [dq, dk, dv]
+            bt8, bo, bl = t8, o, lse
+        else:
+            ins = [torch.empty_like(t) for t in ((t8.q8, t8.k8, t8.vt8) if args.fp8 else (dq, dk, dv))]
+            bt8 = fa.Fp8Tensors(*ins, t8.q_scale, t8.k_scale, t8.v_scale,
+                                (t8.B, t8.Nq, t8.Nk, t8.H, t8.Hk, t8.d)) if args.fp8 else None
+            bo, bl = torch.empty_like(o), torch.empty_like(lse)
         if w.varlen:
-            dcu.copy_(hcu, non_blocking=True)
-        step()
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
+            ins = ins + [dcu if first else torch.empty_like(dcu)]
+        return ins, [bo, bl], bt8
 
-    for _ in range(2):
-        e2e_step()
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
-    h2d = sum(t.numel() * t.element_size() for t in (q, k, v)) + (cu_q.numel() * 4 if w.varlen else 0)
+    sets = [device_set(True), device_set(False)]
+    host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse)] for _ in range(2)]
+
+    def run_set(si):
+        ins, (bo, bl), bt8 = sets[si]
+        step_on(ins[0], ins[1], ins[2], ins[3] if w.varlen else None, bt8, bo, bl)
+
+    e2e_ms = max_over_ranks(pipelined_e2e(torch, dev, stream, [(s_[0], s_[1]) for s_ in sets], host_in, host_out,
+                                          run_set, e2e_steps, world), world)
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
     rc, info = fa.check_status()
     if rc != fa.FA_OK:
@@ -433,7 +488,7 @@ def run_ours(args, w):
                      "algorithmic_flops_per_launch": flops},
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "steps": e2e_steps},
+                "steps": e2e_steps, "copies": E2E_COPIES},
         "gpu_launches": args.steps * (2 if args.split else 1),
         "clocks": clocks,
     }
@@ -510,26 +565,15 @@ def run_bwd(args, w):
 
     e2e_steps = max(3, min(args.steps, 10))
     hosts = [t.pin_memory() for t in (q, k, v, o.cpu(), lse.cpu(), dout)]
-    devs = [dq, dk, dv, o, lse, ddo]
-    outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (gq, gk, gv)]
+    sets = [([dq, dk, dv, o, lse, ddo], [gq, gk, gv]),
+            ([torch.empty_like(t) for t in (dq, dk, dv, o, lse, ddo)], [torch.empty_like(t) for t in (gq, gk, gv)])]
+    outs = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (gq, gk, gv)] for _ in range(2)]
 
-    def e2e_step():
-        for d_, h_ in zip(devs, hosts):
-            d_.copy_(h_, non_blocking=True)
-        step()
-        for h_, d_ in zip(outs, (gq, gk, gv)):
-            h_.copy_(d_, non_blocking=True)
+    def run_set(si):
+        (bq, bk, bv, bo, bl, bdo), (rq, rk, rv) = sets[si]
+        fa.backward(bq, bk, bv, bo, bl, bdo, causal=args.causal, workspace=ws, dq=rq, dk=rk, dv=rv)
 
-    e2e_step()
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    e2e_ms = max_over_ranks(pipelined_e2e(torch, dev, stream, sets, hosts, outs, run_set, e2e_steps, world), world)
     if rank != 0:
         return 0
     peaks, src = load_peaks()
@@ -551,8 +595,8 @@ def run_bwd(args, w):
                      "algorithmic_flops_per_launch": flops},
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hosts),
-                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs),
-                "ms_per_step": e2e_ms, "steps": e2e_steps},
+                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs[0]),
+                "ms_per_step": e2e_ms, "steps": e2e_steps, "copies": E2E_COPIES},
         "gpu_launches": args.steps * 3,
         "clocks": clocks,
     }
