@@ -577,6 +577,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(t * BC);
     const uint32_t tP = tS + BC / 2;
     const float c2 = p.scale_log2;
+    // Largest block sum for which every p of the block is below 2^T (T the
+    // rescale threshold), with a margin for the rounding of the exponent.
+    const float accept_sum = exp2f(p.rescale_threshold) * 0.9990234375f;
     uint32_t sc = 0;  // S-full completions consumed
     bool ok = true;
 #pragma unroll 1
@@ -753,99 +756,119 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ++sc;
           ptx::tc_fence_after();
-          uint32_t sr[BC];
-  #pragma unroll
-          for (int c = 0; c < BC / 32; ++c) ptx::tmem_ld32(tS + c * 32, &sr[c * 32]);
-          ptx::tmem_wait_ld();
+          // S row of this thread, with the keys outside the row's window at -inf.
           float s[BC];
+          auto load_scores = [&]() {
+            uint32_t sr[BC];
   #pragma unroll
-          for (int c = 0; c < BC; ++c) s[c] = __uint_as_float(sr[c]);
-          if (w.j0 + j >= j_mask) {
-            const RowWindow kw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + (w.j0 + j) * BC, BC);
-            if (kw.lo != 0 || kw.hi != BC) {
-              // Keys outside [lo, hi) of this tile: past the end, or (variable
-              // length) before the sequence start / already seen by the previous tile.
+            for (int c = 0; c < BC / 32; ++c) ptx::tmem_ld32(tS + c * 32, &sr[c * 32]);
+            ptx::tmem_wait_ld();
   #pragma unroll
-              for (int c = 0; c < BC; ++c)
-                if (c < kw.lo || c >= kw.hi) s[c] = -INFINITY;
+            for (int c = 0; c < BC; ++c) s[c] = __uint_as_float(sr[c]);
+            if (w.j0 + j >= j_mask) {
+              const RowWindow kw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + (w.j0 + j) * BC, BC);
+              if (kw.lo != 0 || kw.hi != BC) {
+                // Keys outside [lo, hi) of this tile: past the end, or (variable
+                // length) before the sequence start / already seen by the previous tile.
+  #pragma unroll
+                for (int c = 0; c < BC; ++c)
+                  if (c < kw.lo || c >= kw.hi) s[c] = -INFINITY;
+              }
+              const int kbase = kw.load_row - w.k_start;  // sequence index of column 0
+              if (CAUSAL && kbase + BC - 1 > first_row_lim) {
+                // The tile crosses the diagonal: mask keys above this row's limit.
+                const int lim = key_lim - kbase;
+  #pragma unroll
+                for (int c = 0; c < BC; ++c)
+                  if (c > lim) s[c] = -INFINITY;
+              }
             }
-            const int kbase = kw.load_row - w.k_start;  // sequence index of column 0
-            if (CAUSAL && kbase + BC - 1 > first_row_lim) {
-              // The tile crosses the diagonal: mask keys above this row's limit.
-              const int lim = key_lim - kbase;
+          };
+          // p = 2^(s*c - m*c): one packed FFMA per two scores, then ex2 each;
+          // row sum in four packed accumulators (fixed order); P packed as bf16
+          // pairs (FP8: e4m3, four per word).
+          uint32_t pk[FP8 ? BC / 4 : BC / 2];
+          auto exponentiate = [&](float ng) -> float {
+            const uint64_t c2x2 = ptx::f2_pack(c2j, c2j);
+            const uint64_t negx2 = ptx::f2_pack(ng, ng);
+            uint64_t acc[4] = {0, 0, 0, 0};
   #pragma unroll
-              for (int c = 0; c < BC; ++c)
-                if (c > lim) s[c] = -INFINITY;
-            }
-          }
-          // Row max: four independent chains of three-input maxima.
-          float mx[4] = {s[0], s[1], s[2], s[3]};
-  #pragma unroll
-          for (int c = 4; c < BC; c += 8) {
-            mx[0] = ptx::fmax3(mx[0], s[c], s[c + 1]);
-            mx[1] = ptx::fmax3(mx[1], s[c + 2], s[c + 3]);
-            if (c + 4 < BC) {
-              mx[2] = ptx::fmax3(mx[2], s[c + 4], s[c + 5]);
-              mx[3] = ptx::fmax3(mx[3], s[c + 6], s[c + 7]);
-            }
-          }
-          const float bm = fmaxf(ptx::fmax3(mx[0], mx[1], mx[2]), mx[3]);
-          // Move the reference max only when the block max exceeds it by more
-          // than the threshold (log2 units): the merge identity of §11.2 holds
-          // for any common reference value, so results stay exact.
-          float m_new = m_ref;
-          float alpha, neg;
-          if constexpr (FP8) {
-            // Maximum compared in scaled log2 units (the coefficient changes per key tile).
-            const float bms = bm * c2j;
-            if (bms > m_ref && (m_ref == -INFINITY || bms - m_ref > p.rescale_threshold)) m_new = bms;
-            alpha = (m_new == m_ref) ? 1.f : ptx::ex2(m_ref - m_new);
-            m_ref = m_new;
-            neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-          } else {
-            if (bm > m_ref && (m_ref == -INFINITY || (bm - m_ref) * c2 > p.rescale_threshold)) m_new = bm;
-            alpha = (m_new == m_ref) ? 1.f : ptx::ex2((m_ref - m_new) * c2);
-            m_ref = m_new;
-            neg = (m_ref == -INFINITY) ? 0.f : -m_ref * c2;
-          }
-          // p = 2^(s*c2 - m*c2): one packed FFMA per two scores, then ex2 each;
-          // row sums in four packed accumulators; P stored in 16-column chunks
-          // (FP8: rounded to e4m3, four per column, 8 columns per 32 scores).
-          const uint64_t c2x2 = ptx::f2_pack(c2j, c2j);
-          const uint64_t negx2 = ptx::f2_pack(neg, neg);
-          uint64_t acc[4] = {0, 0, 0, 0};
-  #pragma unroll
-          for (int c0 = 0; c0 < BC; c0 += 32) {
-            uint32_t pk[16];
-  #pragma unroll
-            for (int c = c0; c < c0 + 32; c += 2) {
+            for (int c = 0; c < BC; c += 2) {
               float x0, x1;
               ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[c], s[c + 1]), c2x2, negx2), x0, x1);
               const float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1);
-              const uint64_t e01 = ptx::f2_pack(e0, e1);
-              acc[(c >> 1) & 3] = ptx::f2_add(acc[(c >> 1) & 3], e01);
+              acc[(c >> 1) & 3] = ptx::f2_add(acc[(c >> 1) & 3], ptx::f2_pack(e0, e1));
               if constexpr (FP8) {
                 const uint32_t h = ptx::pack_e4m3x2(e0, e1);
-                const int k = (c - c0) / 2;  // pair index 0..15; words hold two pairs
-                if (k & 1)
-                  pk[k >> 1] |= h << 16;
+                if ((c >> 1) & 1)
+                  pk[c >> 2] |= h << 16;
                 else
-                  pk[k >> 1] = h;
+                  pk[c >> 2] = h;
               } else {
-                pk[(c - c0) / 2] = ptx::pack_bf16x2(e0, e1);
+                pk[c >> 1] = ptx::pack_bf16x2(e0, e1);
               }
             }
-            if constexpr (FP8)
-              ptx::tmem_st8(tP + c0 / 4, pk);
-            else
-              ptx::tmem_st16(tP + c0 / 2, pk);
+            float a0, a1, a2, a3, a4, a5, a6, a7;
+            ptx::f2_unpack(acc[0], a0, a1);
+            ptx::f2_unpack(acc[1], a2, a3);
+            ptx::f2_unpack(acc[2], a4, a5);
+            ptx::f2_unpack(acc[3], a6, a7);
+            return ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
+          };
+          load_scores();
+          // The reference maximum m only moves when a block maximum exceeds it
+          // by more than the threshold T (log2 units); the merge identity of
+          // §11.2 holds for any common reference value, so results stay exact.
+          // Speculation: exponentiate against the current m first.  A block sum
+          // of at most 2^T (1 - 2^-10) bounds every p below 2^T, which is exactly
+          // the case where the maximum rule would leave m in place, so the row
+          // maximum is needed only when the sum says otherwise (rare once m has
+          // settled), or for a row that has seen no key yet.  Either way the
+          // result is the one the maximum rule gives.
+          float alpha = 1.f, lblk = 0.f;
+          bool slow = __all_sync(0xffffffffu, m_ref == -INFINITY);
+          if (!slow) {
+            lblk = exponentiate(m_ref == -INFINITY ? 0.f : (FP8 ? -m_ref : -m_ref * c2));
+            slow = __any_sync(0xffffffffu, m_ref == -INFINITY || !(lblk <= accept_sum));
+            if (slow) load_scores();  // the scores were consumed
           }
-          float a0, a1, a2, a3, a4, a5, a6, a7;
-          ptx::f2_unpack(acc[0], a0, a1);
-          ptx::f2_unpack(acc[1], a2, a3);
-          ptx::f2_unpack(acc[2], a4, a5);
-          ptx::f2_unpack(acc[3], a6, a7);
-          l = l * alpha + (((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)));
+          if (slow) {
+            // Row max: four independent chains of three-input maxima.
+            float mx[4] = {s[0], s[1], s[2], s[3]};
+  #pragma unroll
+            for (int c = 4; c < BC; c += 8) {
+              mx[0] = ptx::fmax3(mx[0], s[c], s[c + 1]);
+              mx[1] = ptx::fmax3(mx[1], s[c + 2], s[c + 3]);
+              if (c + 4 < BC) {
+                mx[2] = ptx::fmax3(mx[2], s[c + 4], s[c + 5]);
+                mx[3] = ptx::fmax3(mx[3], s[c + 6], s[c + 7]);
+              }
+            }
+            const float bm = fmaxf(ptx::fmax3(mx[0], mx[1], mx[2]), mx[3]);
+            float m_new = m_ref, neg;
+            if constexpr (FP8) {
+              // Maximum compared in scaled log2 units (the coefficient changes per key tile).
+              const float bms = bm * c2j;
+              if (bms > m_ref && (m_ref == -INFINITY || bms - m_ref > p.rescale_threshold)) m_new = bms;
+              alpha = (m_new == m_ref) ? 1.f : ptx::ex2(m_ref - m_new);
+              m_ref = m_new;
+              neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            } else {
+              if (bm > m_ref && (m_ref == -INFINITY || (bm - m_ref) * c2 > p.rescale_threshold)) m_new = bm;
+              alpha = (m_new == m_ref) ? 1.f : ptx::ex2((m_ref - m_new) * c2);
+              m_ref = m_new;
+              neg = (m_ref == -INFINITY) ? 0.f : -m_ref * c2;
+            }
+            lblk = exponentiate(neg);
+          }
+  #pragma unroll
+          for (int c0 = 0; c0 < BC; c0 += 32) {
+            if constexpr (FP8)
+              ptx::tmem_st8(tP + c0 / 4, &pk[c0 / 4]);
+            else
+              ptx::tmem_st16(tP + c0 / 2, &pk[c0 / 2]);
+          }
+          l = l * alpha + lblk;
           if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
             // Correction of the unnormalised output: O_t rows of this warp hold
             // the sum over steps < j referenced to the old maximum.  Done after
