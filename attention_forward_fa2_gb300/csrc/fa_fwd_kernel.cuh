@@ -42,7 +42,10 @@
 // by more than a threshold, so rescales are rare after the first blocks; the
 // softmax warp that owns the rows applies it in TMEM itself (its TMEM lane
 // quarter holds exactly its rows of O), after S(j) completed, which implies
-// that P(j-1) V(j-1) has completed.
+// that P(j-1) V(j-1) has completed.  The block maximum itself is computed only
+// when needed: the exponentials are first taken against the current reference,
+// and a block sum of at most 2^threshold proves that no exponent exceeded the
+// threshold, i.e. that the maximum rule would leave the reference in place.
 //
 // Causal masking ("GPU 内核与 FlashAttention" §14.4): key tiles entirely above
 // the diagonal are skipped (each query tile runs only the key tiles its rows

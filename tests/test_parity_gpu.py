@@ -189,6 +189,29 @@ def test_large_scores_stay_finite(oracle_mod):
     assert np.max(np.abs(lse - lse_ref) / np.maximum(1.0, np.abs(lse_ref))) <= LSE_TOL
 
 
+@pytest.mark.parametrize("spec", [None, "threshold=0", "reduce=quad,threshold=8"])
+def test_reference_maximum_paths(oracle_mod, spec):
+    """Key tiles whose scores step up by 0, 6, 20 and 21 (log2 units: the scale
+    ln 2 makes a raw score r contribute 2^r): the second tile's block sum
+    exceeds 2^8 while its maximum stays within the rescale threshold (the
+    reference maximum must stay), the third and fourth move it.  Every
+    output must still match the definition."""
+    B, N, H, d = 1, 512, 2, 128
+    q, k, v = I.make_dense(B, N, N, H, d, 31)
+    q = torch.zeros_like(q)
+    q[..., 0] = 1.0
+    k = torch.zeros_like(k)
+    for t, r in enumerate((0.0, 6.0, 20.0, 21.0)):
+        k[:, 128 * t:128 * (t + 1), :, 0] = r
+    fa.set_config(spec)
+    try:
+        o, lse = gpu_dense(q, k, v, scale=math.log(2.0))
+    finally:
+        fa.set_config(None)
+    o_ref, lse_ref = oracle_mod.attn_dense(bits(q), bits(k), bits(v), scale=math.log(2.0))
+    assert_close(o, lse, o_ref, lse_ref, "reference maximum paths %s" % spec)
+
+
 def test_deterministic():
     q, k, v = I.make_dense(2, 700, 700, 2, 128, 10)
     o1, l1 = gpu_dense(q, k, v)
