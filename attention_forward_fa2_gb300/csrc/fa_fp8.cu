@@ -116,28 +116,50 @@ __global__ void fp8_v_scale_kernel(Fp8QuantParams p, const unsigned int* v_amax_
   if (i < p.B * p.Hk) p.v_scale[i] = scale_of(__uint_as_float(v_amax_bits[i]));
 }
 
-// V codes, transposed: one block per (b, hk, 64 keys); a 64 x D tile goes
-// through shared memory so that both the reads (rows of d) and the writes
-// (rows of keys) are contiguous.
+// V codes, transposed: one block per (64-key tile, b * Hk + hk).  Thread
+// (chunk, kg) = (tid % 16, tid / 16) loads 8 features of keys 4kg .. 4kg+3
+// (16-byte loads; a warp reads two whole 256-byte key rows per instruction),
+// converts them and regroups the bytes into one 32-bit word per feature (four
+// consecutive keys).  The words go through shared memory in feature-major
+// rows of 17 words (conflict-free for both phases) and leave as coalesced
+// 4-byte stores of the transposed rows.
 template <int D>
 __global__ void __launch_bounds__(256) fp8_quant_vt_kernel(Fp8QuantParams p, const unsigned int* v_amax_bits) {
-  __shared__ uint8_t tile[D][64 + 4];
+  static_assert(D == 128, "16 chunks of 8 features per key");
+  constexpr int kRowWords = 17;  // 16 words of 4 keys, one word of padding
+  __shared__ uint32_t tile[D * kRowWords];
   const int kt = blockIdx.x;  // 64-key tile
   const int bh = blockIdx.y;  // b * Hk + hk
   const int h = bh % p.Hk, b = bh / p.Hk;
   const float s = scale_of(__uint_as_float(v_amax_bits[bh]));
-  for (int e = threadIdx.x; e < 64 * D; e += blockDim.x) {
-    const int r = e / D, c = e % D;
-    const int key = kt * 64 + r;
-    float x = 0.f;
-    if (key < p.Nk) x = __bfloat162float(p.v[((static_cast<size_t>(b) * p.Nk + key) * p.Hk + h) * D + c]) / s;
-    tile[c][r] = static_cast<uint8_t>(to_e4m3x2(x, 0.f) & 0xffu);
+  const int chunk = threadIdx.x & 15, kg = threadIdx.x >> 4;
+  uint32_t q2[4][4];  // [key][feature pair]: e4m3 codes of features 2i (low byte) and 2i+1
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int key = kt * 64 + 4 * kg + k;
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    if (key < p.Nk)
+      u = *reinterpret_cast<const uint4*>(p.v + ((static_cast<size_t>(b) * p.Nk + key) * p.Hk + h) * D + chunk * 8);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      q2[k][i] = to_e4m3x2(__uint_as_float(w[i] << 16) / s, __uint_as_float(w[i] & 0xffff0000u) / s);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t t01 = __byte_perm(q2[0][i], q2[1][i], 0x5410);  // k0.f0 k0.f1 k1.f0 k1.f1
+    const uint32_t t23 = __byte_perm(q2[2][i], q2[3][i], 0x5410);
+    tile[(chunk * 8 + 2 * i) * kRowWords + kg] = __byte_perm(t01, t23, 0x6420);      // feature 2i, keys 0..3
+    tile[(chunk * 8 + 2 * i + 1) * kRowWords + kg] = __byte_perm(t01, t23, 0x7531);  // feature 2i+1
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < 64 * D; e += blockDim.x) {
-    const int c = e / 64, r = e % 64;
-    const int key = kt * 64 + r;
-    if (key < p.nk_pad) p.vt8[(static_cast<size_t>(bh) * D + c) * p.nk_pad + key] = tile[c][r];
+#pragma unroll
+  for (int e = threadIdx.x; e < D * 16; e += 256) {
+    const int c = e >> 4, wd = e & 15;
+    const int key0 = kt * 64 + 4 * wd;
+    // nk_pad is a multiple of 16: a word is wholly inside or outside the padded row.
+    if (key0 < p.nk_pad)
+      *reinterpret_cast<uint32_t*>(p.vt8 + (static_cast<size_t>(bh) * D + c) * p.nk_pad + key0) = tile[c * kRowWords + wd];
   }
 }
 
