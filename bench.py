@@ -303,6 +303,15 @@ def pipelined_e2e(torch, dev, stream, sets, host_in, host_out, run, steps, world
     return e0.elapsed_time(e1) / steps
 
 
+def per_step_stats(marks):
+    """Median, minimum and maximum of the per-step device times (ms) from
+    events recorded between the timed steps (empty for a graph replay)."""
+    if len(marks) < 2:
+        return None
+    t = sorted(a.elapsed_time(b) for a, b in zip(marks[:-1], marks[1:]))
+    return {"median": statistics.median(t), "min": t[0], "max": t[-1]}
+
+
 def workload_config(w, kernel_cfg, causal=False):
     cfg = {"workload": "%s: %s" % (w.name, w.note or ""), "B": w.B, "H": w.H, "d": w.d,
            "layout": "[batch, seq, heads, d_head] bf16", "causal": bool(causal),
@@ -410,17 +419,21 @@ def run_ours(args, w):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
+    marks = [] if graph is not None else [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     e0.record(stream)
     if graph is not None:
         graph.replay()
     else:
-        for _ in range(args.steps):
+        for i_ in range(args.steps):
+            marks[i_].record(stream)
             step()
+        marks[-1].record(stream)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     clocks = sampler.stop()
     ms = e0.elapsed_time(e1) / args.steps
+    step_stats = per_step_stats(marks)
     rc, info = fa.check_status()
     if rc != fa.FA_OK:
         raise SystemExit("device error in the timed region: %s %s" % (fa.strerror(rc), info))
@@ -476,7 +489,7 @@ def run_ours(args, w):
     traffic = load_traffic(w.name + ("_fp8" if args.fp8 else ""))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": ms_max, "step_ms": step_stats, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)" if args.fp8 else "bf16",
         "data": "synthetic (seeded N(0,1), generated on the host)",
         "config": add_mode(workload_config(w, None if args.fp8 else kernel_cfg, args.causal), args),
@@ -547,14 +560,18 @@ def run_bwd(args, w):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     e0.record(stream)
-    for _ in range(args.steps):
+    for i_ in range(args.steps):
+        marks[i_].record(stream)
         step()
+    marks[-1].record(stream)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     clocks = sampler.stop()
     ms = e0.elapsed_time(e1) / args.steps
+    step_stats = per_step_stats(marks)
     rc, info = fa.check_status()
     if rc != fa.FA_OK:
         raise SystemExit("device error in the timed region: %s %s" % (fa.strerror(rc), info))
@@ -580,7 +597,7 @@ def run_bwd(args, w):
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     line = {
         "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": ms_max, "step_ms": step_stats, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q, k, v, dO; o and lse from the forward)",
         "config": dict(workload_config(w, None, args.causal), launch="stream launches",
