@@ -160,7 +160,10 @@ class ClockSampler:
 
 
 # -------------------------------------------------------------- distributed
-def dist_setup(n_gpus: int):
+def dist_setup(n_gpus: int, backend: str = "nccl"):
+    """(rank, local rank, world size) from the launcher's environment; joins
+    the process group when there is more than one rank.  The benchmark's
+    ranks use NCCL, one GPU each; "gloo" serves the CPU tests of this logic."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if n_gpus > 1 and world != n_gpus:
         raise SystemExit("--gpus %d needs torchrun with %d processes (WORLD_SIZE=%d)" % (n_gpus, n_gpus, world))
@@ -169,8 +172,11 @@ def dist_setup(n_gpus: int):
     if world > 1:
         import torch.distributed as dist
         import torch
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
     return rank, local, world
 
 
@@ -181,11 +187,14 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest of the ranks' values (every rank gets it): a job is as
+    slow as its slowest rank."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 

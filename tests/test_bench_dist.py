@@ -1,0 +1,64 @@
+"""The benchmark's multi-rank host logic on CPU: two processes joined with the
+gloo backend (the GPU runs use NCCL, one rank per GPU, through the same
+functions), and the reference arm launched as two ranks by torchrun."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      LOCAL_RANK=str(rank), WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    import bench
+    import torch.distributed as dist
+    r, local, w = bench.dist_setup(world, backend="gloo")
+    bench.barrier(w)
+    m = bench.max_over_ranks(1.5 + r, w)
+    with open(os.path.join(out_dir, "rank%d.json" % r), "w") as f:
+        json.dump({"rank": r, "local": local, "world": w, "max": m}, f)
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_the_slowest_time(tmp_path):
+    import torch.multiprocessing as mp
+    port = _free_port()
+    mp.start_processes(_rank_main, args=(2, port, str(tmp_path)), nprocs=2, start_method="spawn", join=True)
+    got = [json.load(open(tmp_path / ("rank%d.json" % r))) for r in range(2)]
+    assert [g["rank"] for g in got] == [0, 1] and all(g["world"] == 2 for g in got)
+    assert all(g["max"] == 2.5 for g in got)
+
+
+def test_gpus_flag_must_match_the_launch(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    with pytest.raises(SystemExit):
+        bench.dist_setup(2)
+
+
+def test_reference_arm_under_torchrun_two_ranks():
+    """Rank 0 alone times the oracle and prints one JSON line; rank 1 exits 0."""
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference",
+           "--gpus", "2", "--steps", "1", "--warmup", "3", "--workload", "tiny"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
