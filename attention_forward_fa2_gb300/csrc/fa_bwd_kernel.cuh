@@ -23,10 +23,9 @@
 //   S^T  = K Q^T        M=128 keys, N=128 queries, K=d    tensor memory S
 //   dP^T = V dO^T       M=128 keys, N=128                 tensor memory dP
 //   P^T  = 2^(S^T * scale * log2 e - L * log2 e)           softmax warps, bf16 over S
-//   dS^T = P^T o (dP^T - D)                                bf16 over dP, and to
-//                                                          shared memory
+//   dS^T = P^T o (dP^T - D)                                bf16, to shared memory
 //   dV  += P^T dO       M=128 keys, N=d, K=128             P^T from tensor memory
-//   dK  += dS^T Q       M=128 keys, N=d, K=128             dS^T from tensor memory
+//   dK  += dS^T Q       M=128 keys, N=d, K=128             both from shared memory
 //   dQ^T = K^T dS^T     M=d, N=128 queries, K=128 keys     both from shared memory,
 //                                                          result over dP
 // Every product is N = 128 (the full tensor rate; N = 64 products are bound by
@@ -37,16 +36,17 @@
 // accumulator, so one reduction instruction per query adds a whole line and
 // nothing is staged in shared memory.
 // Tensor memory (512 columns): S [0,128) dP [128,256) dV [256,384)
-// dK [384,512); dQ^T(g) reuses dP's columns once dK(g) has read dS^T.  The
-// single MMA thread issues, per step g:
+// dK [384,512); dQ^T(g) reuses dP's columns once the softmax warps have read
+// dP(g).  The single MMA thread issues, per step g:
 //   dV(g) | S(g+1) | dK(g) dQ^T(g) | dP(g+1)   (dP(g+1) after the drain read dQ^T(g))
 // Softmax warpgroup c reads columns [64c, 64c + 64) of S and dP and writes
-// its packed bf16 words over the first 32 of them, 32 columns at a time.
+// its packed bf16 P^T words over the first 32 of S's, 32 columns at a time;
+// dS^T goes to shared memory only (the one copy both dK and dQ^T read).
 //
 // Roles (512 threads):
 //   warps 0-7   softmax: P, dS (warps 0-3 query columns 0-63, 4-7 columns 64-127)
 //   warps 8-11  dQ drain (TMEM -> registers -> L2 reductions) and the dK/dV epilogue
-//               (168 registers: all 128 accumulator columns are held at once, so
+//               (152 registers: all 128 accumulator columns are held at once, so
 //               the tensor memory is released before the reductions are issued)
 //   warp 12     MMA issue (one thread) + TMEM allocation
 //   warp 13     TMA loads (one thread)
@@ -396,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t vdesc = ptx::sw128_desc(base + L::kOffV, 16, 1024);
       const uint64_t kdesc_mn = ptx::sw128_desc(base + L::kOffK, L::kKVPanel, 1024);
       const uint64_t dsdesc_mn = ptx::sw128_desc(base + L::kOffDS, L::kDSPanel, 1024);
+      const uint64_t dsdesc_k = ptx::sw128_desc(base + L::kOffDS, 16, 1024);
       auto issue_s = [&](uint32_t t) {
         const uint64_t qdesc = ptx::sw128_desc(base + L::kOffQ + (t % STAGES) * L::kSlotBytes, 16, 1024);
 #pragma unroll
@@ -450,14 +451,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             issue_s(g + 1);
           }
-          // dK += dS^T Q, then dQ^T = K^T dS^T over dP (after dK has read dS^T).
+          // dK += dS^T Q, then dQ^T = K^T dS^T over dP.  Both read dS^T from shared
+          // memory: as dK's A operand it is K-major (key rows, queries along the
+          // 128-byte rows), as dQ^T's B operand MN-major.
           if (!wait(bar(L::kBarDSFull), g & 1u, kBSiteMmaDS)) break;
           ptx::tc_fence_after();
           const uint64_t qdesc_mn = ptx::sw128_desc(sq, L::kQPanel, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kBwdBQ / 16; ++kk)
-            ptx::mma_ts(tmem + kColDK, tmem + kColDP + (kk >> 2) * 64 + (kk & 3) * 8, qdesc_mn + kk * 128, id_acc,
-                        (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBwdBQ / 16; ++kk) {
+            const uint32_t oa = (kk / 4) * L::kDSPanel + (kk % 4) * 32;
+            ptx::mma_ss(tmem + kColDK, dsdesc_k + (oa >> 4), qdesc_mn + kk * 128, id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+          }
           ptx::mma_commit(bar(L::kBarQEmpty + slot));  // Q(g) and dO(g) read
 #pragma unroll
           for (int kk = 0; kk < kBwdBK / 16; ++kk)
@@ -485,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = ((warp & 3) << 5) + lane;     // key row of the block
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
     const uint32_t tSc = tmem + lane_off + kColS + c * 64;
-    const uint32_t tDc = tmem + lane_off + kColDP + c * 64;
+    const uint32_t tDc = tmem + lane_off + kColDP + c * 64;  // dP^T columns of this warpgroup
     const float c2 = p.scale_log2;
     uint32_t g = 0;
     bool ok = true;
@@ -576,7 +580,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               ds[k / 2] = ptx::pack_bf16x2(p0 * (__uint_as_float(dr[k]) - da), p1 * (__uint_as_float(dr[k + 1]) - db));
             }
           }
-          ptx::tmem_st16(tDc + hh * 16, ds);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             const int chunk = 4 * hh + q4;
@@ -585,8 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         ptx::fence_proxy_async_smem();
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
+        ptx::tc_fence_before();  // the dP loads above precede dQ^T overwriting those columns
         ptx::mbar_arrive(bar(L::kBarDSFull));
       }
     }
