@@ -400,7 +400,7 @@ def backward(q, k, v, o, lse, dout, scale=None, causal=False, workspace=None, dq
 
     q, o, dout: [B, Nq, H, d] bf16; k, v: [B, Nk, Hk, d] bf16 (H a multiple of
     Hk); lse: [B, H, Nq] fp32 from the forward with the same causal flag;
-    contiguous CUDA tensors on one device, d = 128.  workspace: optional uint8
+    contiguous CUDA tensors on one device, d = 64 or 128.  workspace: optional uint8
     tensor of at least bwd_workspace_bytes(B, Nq, H, d) bytes."""
     import torch
     B, Nq, H, d = q.shape

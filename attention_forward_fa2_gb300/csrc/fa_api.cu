@@ -452,7 +452,7 @@ int run_bwd(const BwdProblem& P) {
   if ((P.flags & ~FA_FLAG_CAUSAL) != 0) return FA_ERR_INVALID_ARG;
   if (P.H > 0 && (P.Hk == 0 || P.H % P.Hk != 0)) return FA_ERR_INVALID_ARG;
   if (!(std::isfinite(P.scale) && P.scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (P.d != 128) return FA_ERR_UNSUPPORTED;
+  if (P.d != 64 && P.d != 128) return FA_ERR_UNSUPPORTED;
   if (P.B == 0 || P.H == 0) return FA_OK;
   if (P.Nk == 0) return P.Nq == 0 ? FA_OK : FA_ERR_INVALID_ARG;  // as the forward: queries need keys
   if (!P.k || !P.v || !P.dk || !P.dv || !P.ws) return FA_ERR_INVALID_ARG;
@@ -528,7 +528,8 @@ int run_bwd(const BwdProblem& P) {
   if ((e = encode(&a.tm_v, P.v, 4, dk4, sk4, box_k)) != FA_OK) return e;
   a.grid = dim3(static_cast<unsigned>(p.num_items < st->num_sms ? p.num_items : st->num_sms), 1, 1);
   a.stream = P.stream;
-  const cudaError_t ce = p.causal ? fa::launch_bwd<128, true>(a) : fa::launch_bwd<128, false>(a);
+  const cudaError_t ce = D == 128 ? (p.causal ? fa::launch_bwd<128, true>(a) : fa::launch_bwd<128, false>(a))
+                                   : (p.causal ? fa::launch_bwd<64, true>(a) : fa::launch_bwd<64, false>(a));
   if (ce != cudaSuccess) return cuda_fail(ce);
   return FA_OK;
 }
@@ -725,7 +726,7 @@ int fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream) {
 
 long long fa_bwd_workspace_bytes(int B, int Nq, int H, int d) {
   if (B < 0 || Nq < 0 || H < 0) return FA_ERR_INVALID_ARG;
-  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   return static_cast<long long>(bwd_workspace_bytes(B, Nq, H, d));
 }
 

@@ -1,10 +1,13 @@
-// Instantiations and launchers of the backward pass (d_head = 128).
+// Instantiations and launchers of the backward pass (d_head = 64 and 128).
 #include "fa_launch.h"
 
 namespace fa {
 
 namespace {
-constexpr int kBwdStages = 2;
+// Q/dO ring depth: two 64 KB slots fit beside K, V and dS^T for d = 128; the
+// d = 64 slots are half the size, so four fit.
+template <int D>
+constexpr int kBwdStages = D == 128 ? 2 : 4;
 
 template <int D, bool CAUSAL>
 cudaError_t launch_bwd_impl(const BwdLaunchArgs& a) {
@@ -16,8 +19,8 @@ cudaError_t launch_bwd_impl(const BwdLaunchArgs& a) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  auto* kern = &fa_bwd_kernel<D, kBwdStages, CAUSAL>;
-  constexpr int smem = BwdSmem<D, kBwdStages>::kAlloc;
+  auto* kern = &fa_bwd_kernel<D, kBwdStages<D>, CAUSAL>;
+  constexpr int smem = BwdSmem<D, kBwdStages<D>>::kAlloc;
   static std::atomic<unsigned long long> done{0};
   e = set_smem_once(reinterpret_cast<const void*>(kern), smem, done);
   if (e != cudaSuccess) return e;
@@ -36,6 +39,14 @@ cudaError_t launch_bwd<128, false>(const BwdLaunchArgs& a) {
 template <>
 cudaError_t launch_bwd<128, true>(const BwdLaunchArgs& a) {
   return launch_bwd_impl<128, true>(a);
+}
+template <>
+cudaError_t launch_bwd<64, false>(const BwdLaunchArgs& a) {
+  return launch_bwd_impl<64, false>(a);
+}
+template <>
+cudaError_t launch_bwd<64, true>(const BwdLaunchArgs& a) {
+  return launch_bwd_impl<64, true>(a);
 }
 
 }  // namespace fa

@@ -150,7 +150,11 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdParams p) {
 // ---------------------------------------------------------------- main kernel
 template <int D, int STAGES>
 struct BwdSmem {
-  static constexpr int kKVBytes = kBwdBK * D * 2;        // one K or V block
+  static constexpr int kKVBytes = kBwdBK * D * 2;        // one K or V block as loaded
+  // K's shared tile always spans 128 features (two 64-feature panels): for
+  // d = 64 the second panel stays zero, so that dQ^T = K^T dS^T keeps M = 128
+  // (rows 64-127 of that product are zero and never drained).
+  static constexpr int kKBytes = kBwdBK * 128 * 2;
   static constexpr int kKVPanel = kBwdBK * 128;          // 64 features x 128 rows
   static constexpr int kQBytes = kBwdBQ * D * 2;         // one Q or dO block
   static constexpr int kQPanel = kBwdBQ * 128;           // 64 features x 128 queries
@@ -159,7 +163,7 @@ struct BwdSmem {
   static constexpr int kDSBytes = kBwdBK * kBwdBQ * 2;   // two query panels
   static constexpr int kLDBytes = 2 * kBwdBQ * 4;        // scaled LSE then D of a query block
   static constexpr int kOffK = 0;
-  static constexpr int kOffV = kOffK + kKVBytes;
+  static constexpr int kOffV = kOffK + kKBytes;
   static constexpr int kOffQ = kOffV + kKVBytes;
   static constexpr int kOffDS = kOffQ + STAGES * kSlotBytes;
   static constexpr int kOffLD = kOffDS + kDSBytes;       // one kLDBytes block per Q/dO slot
@@ -255,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const BwdParams p) {
-  static_assert(D == 128, "backward kernel: d = 128");
+  static_assert(D == 64 || D == 128, "backward kernel: d = 64 or 128");
   static_assert(STAGES >= 2, "backward ring depth");
   using L = BwdSmem<D, STAGES>;
   constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
@@ -309,6 +313,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_alloc(ptx::smem_u32(const_cast<uint32_t*>(s_tmem)), 512);
     ptx::tmem_relinquish();
   }
+  if constexpr (D < 128) {
+    // The K panels beyond d are never loaded: zero them once, visible to the
+    // tensor core (async proxy) before any MMA reads them.
+    for (uint32_t i = threadIdx.x; i < (L::kKBytes - L::kKVBytes) / 16; i += blockDim.x)
+      ptx::st_shared_v4(base + L::kOffK + L::kKVBytes + 16 * i, 0u, 0u, 0u, 0u);
+    ptx::fence_proxy_async_smem();
+  }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -333,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        ptx::mbar_arrive_expect_tx(bar(L::kBarKVFull), 2 * L::kKVBytes);
+        ptx::mbar_arrive_expect_tx(bar(L::kBarKVFull), 2 * L::kKVBytes);  // K and V, D features each
 #pragma unroll
         for (int pn = 0; pn < kDPanels; ++pn) {
           ptx::tma_load_4d(base + L::kOffK + pn * L::kKVPanel, &tm_k, bar(L::kBarKVFull), pn * 64, w.hk,
@@ -380,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ============================================================ MMA issue
       constexpr uint32_t id_s = ptx::idesc_bf16_f32(128, kBwdBQ, 0, 0);   // K Q^T, V dO^T
       constexpr uint32_t id_acc = ptx::idesc_bf16_f32(128, D, 0, 1);      // P^T dO, dS^T Q
-      constexpr uint32_t id_dq = ptx::idesc_bf16_f32(D, kBwdBQ, 1, 1);    // K^T dS^T
+      constexpr uint32_t id_dq = ptx::idesc_bf16_f32(128, kBwdBQ, 1, 1);  // K^T dS^T (K padded to 128 rows)
       uint32_t g = 0, uc = 0;
       bool ok = true;
       auto wait = [&](uint32_t b, uint32_t par, int site) -> bool {
@@ -624,17 +635,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        uint32_t v[128];
+        if ((wq << 5) < D) {
+          uint32_t v[128];
 #pragma unroll
-        for (int q32 = 0; q32 < 4; ++q32) ptx::tmem_ld32(tmem + lane_off + kColDP + q32 * 32, v + 32 * q32);
-        ptx::tmem_wait_ld();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(L::kBarDQEmpty));
-        // Query q of the block: the warp's 32 features are one 128-byte line.
-        float* const dst = p.dq_acc + (static_cast<size_t>(w.b * p.H + h) * p.nq_pad + static_cast<size_t>(qb) * kBwdBQ) * D +
-                           (wq << 5) + lane;
+          for (int q32 = 0; q32 < 4; ++q32) ptx::tmem_ld32(tmem + lane_off + kColDP + q32 * 32, v + 32 * q32);
+          ptx::tmem_wait_ld();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(L::kBarDQEmpty));
+          // Query q of the block: the warp's 32 features are one 128-byte line.
+          float* const dst = p.dq_acc +
+                             (static_cast<size_t>(w.b * p.H + h) * p.nq_pad + static_cast<size_t>(qb) * kBwdBQ) * D +
+                             (wq << 5) + lane;
 #pragma unroll
-        for (int q = 0; q < kBwdBQ; ++q) ptx::red_add(dst + static_cast<size_t>(q) * D, __uint_as_float(v[q]));
+          for (int q = 0; q < kBwdBQ; ++q) ptx::red_add(dst + static_cast<size_t>(q) * D, __uint_as_float(v[q]));
+        } else {
+          // Lanes (features) at or beyond d hold the zero rows of the padded product.
+          ptx::mbar_arrive(bar(L::kBarDQEmpty));
+        }
       }
       if (!ok) break;
       // Unit done: dK (times the scale) and dV to bf16, one key row per thread.

@@ -27,7 +27,7 @@ implementation; the oracle is the reference), printing the same JSON line.
 --fp8 times the e4m3 forward (fa_fwd_fp8) on the workload quantised once
 beforehand (block scales; the quantisation is not timed), against the fp8
 dense peak taken as twice the measured bf16 one (the nominal ratio).
---bwd times the backward pass instead (fa_bwd: preprocessing, key-block kernel,
+--bwd times the backward pass instead (fa_bwd, d = 64 or 128: preprocessing, key-block kernel,
 dQ conversion), FLOPs counted as 2.5x the forward's (five matrix products
 against two).  Rank 0 prints one JSON line on stdout.
 """
@@ -539,8 +539,8 @@ def run_bwd(args, w):
     from attention_forward_fa2_gb300 import build as fabuild
     from attention_forward_fa2_gb300 import inputs as I
 
-    if w.varlen or w.d != 128:
-        raise SystemExit("--bwd takes dense d = 128 workloads")
+    if w.varlen:
+        raise SystemExit("--bwd takes dense workloads")
     rank, local, world = dist_setup(args.gpus)
     torch.cuda.set_device(local)
     fabuild.build()
@@ -616,8 +616,8 @@ def run_bwd(args, w):
                      "frac": step_tflops / peak, "traffic": None,
                      "peak_source": "%s bf16 dense burst (MEASURED_PEAKS.json)" % src
                      if src == "measured" else "fallback 1.9 PFLOP/s bf16",
-                     "kernel": "fa_bwd step (prep + fa_bwd_kernel<128> + dq conversion); achieved is "
-                               "per step, a lower bound for the key-block kernel",
+                     "kernel": "fa_bwd step (prep + fa_bwd_kernel<%d> + dq conversion); achieved is "
+                               "per step, a lower bound for the key-block kernel" % w.d,
                      "algorithmic_flops_per_launch": flops},
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hosts),

@@ -170,11 +170,12 @@ def test_splitkv_workspace_arithmetic(L):
 
 def test_backward_workspace_and_argument_errors(L):
     """Backward sizes and the checks made before any device work."""
-    rows = 2 * 3 * 128  # B * H * Nq rounded up to 64-query blocks (100 -> 128)
+    rows = 2 * 3 * 128  # B * H * Nq rounded up to 128-query blocks (100 -> 128)
     assert fa.bwd_workspace_bytes(2, 100, 3, 128) == rows * (128 + 2) * 4
+    assert fa.bwd_workspace_bytes(2, 100, 3, 64) == rows * (64 + 2) * 4
     assert fa.bwd_workspace_bytes(1, 0, 1, 128) == 0
     with pytest.raises(fa.FaError) as e:
-        fa.bwd_workspace_bytes(1, 64, 1, 64)
+        fa.bwd_workspace_bytes(1, 64, 1, 32)
     assert e.value.code == fa.FA_ERR_UNSUPPORTED
     with pytest.raises(fa.FaError):
         fa.bwd_workspace_bytes(-1, 64, 1, 128)
@@ -185,7 +186,7 @@ def test_backward_workspace_and_argument_errors(L):
         a = dict(args, **kw)
         return fa.fa_bwd(*a.values())
 
-    assert call(d=64) == fa.FA_ERR_UNSUPPORTED
+    assert call(d=32) == fa.FA_ERR_UNSUPPORTED
     assert call(flags=4) == fa.FA_ERR_INVALID_ARG
     assert call(scale=0.0) == fa.FA_ERR_INVALID_ARG
     assert call(scale=float("nan")) == fa.FA_ERR_INVALID_ARG

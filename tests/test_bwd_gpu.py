@@ -76,6 +76,25 @@ def test_backward_matches_oracle(oracle_mod, B, Nq, Nk, H, Hk, causal):
     _assert_grads(got, ref, "B%d Nq%d Nk%d H%d Hk%d causal%d" % (B, Nq, Nk, H, Hk, causal))
 
 
+@pytest.mark.parametrize("B,Nq,Nk,H,Hk", [
+    (1, 256, 256, 2, 2),
+    (2, 200, 333, 4, 2),
+    (1, 1, 1, 1, 1),
+    (1, 300, 100, 2, 2),
+    (1, 1024, 1024, 2, 1),
+    (3, 130, 260, 6, 3),
+])
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_d64_matches_oracle(oracle_mod, B, Nq, Nk, H, Hk, causal):
+    """d = 64: the same kernel with one 64-feature panel per tile (K padded to
+    128 features for the transposed dQ product, whose extra rows are dropped)."""
+    q, k, v, do = _inputs(B, Nq, Nk, H, Hk, 64, 2000 + Nq + Nk + causal)
+    got = _gpu_grads(q, k, v, do, causal)
+    ref = oracle_mod.attn_bwd_dense(I.bf16_bits(q), I.bf16_bits(k), I.bf16_bits(v), I.bf16_bits(do),
+                                    causal=causal)[:3]
+    _assert_grads(got, ref, "B%d Nq%d Nk%d H%d Hk%d causal%d" % (B, Nq, Nk, H, Hk, causal))
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_backward_page_workload_sampled_heads(oracle_mod, causal):
     """The page workload (B16 N4096 H16 d128) in one call; two heads, the
@@ -115,10 +134,10 @@ def test_no_queries_gives_zero_key_gradients():
 
 
 def test_backward_errors():
-    q = torch.randn(1, 64, 2, 64, dtype=torch.bfloat16, device="cuda")
+    q = torch.randn(1, 64, 2, 32, dtype=torch.bfloat16, device="cuda")
     lse = torch.zeros(1, 2, 64, device="cuda")
     with pytest.raises(fa.FaError) as e:
-        fa.backward(q, q, q, q, lse, q)  # d = 64: not built
+        fa.backward(q, q, q, q, lse, q)  # d = 32: not built
     assert e.value.code == fa.FA_ERR_UNSUPPORTED
     q = torch.randn(1, 64, 2, 128, dtype=torch.bfloat16, device="cuda")
     ws = torch.empty(16, dtype=torch.uint8, device="cuda")
