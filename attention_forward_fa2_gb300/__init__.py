@@ -41,7 +41,7 @@ EXPORTS = (
     "fa_set_timeout_ns", "fa_set_config", "fa_get_config", "fa_autotune",
     "fa_selftest_wait_timeout", "fa_version", "fa_splitkv_num_splits",
     "fa_splitkv_workspace_bytes", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc",
-    "fa_bwd_workspace_bytes", "fa_bwd", "fa_fp8_sizes", "fa_quantize_fp8", "fa_fwd_fp8",
+    "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_varlen", "fa_fp8_sizes", "fa_quantize_fp8", "fa_fwd_fp8",
 )
 
 
@@ -90,6 +90,8 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci]
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp,
                              ctypes.c_longlong, vp]
+        L.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci,
+                                    vp, ctypes.c_longlong, vp]
         L.fa_fp8_sizes.argtypes = [ci, ci, ci, ci, ci, ci, ctypes.POINTER(ctypes.c_longlong)]
         L.fa_quantize_fp8.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, vp]
         L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp]
@@ -146,6 +148,12 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Nq, Nk, H, Hk, d, scale, flags,
            workspace_bytes, stream) -> int:
     return lib().fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Nq, Nk, H, Hk, d, scale, flags,
                         workspace, workspace_bytes, stream)
+
+
+def fa_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, cu_q, cu_k, B, max_q, max_k, H, Hk, d, scale, flags,
+                  workspace, workspace_bytes, stream) -> int:
+    return lib().fa_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, cu_q, cu_k, B, max_q, max_k, H, Hk, d, scale,
+                               flags, workspace, workspace_bytes, stream)
 
 
 def bwd_workspace_bytes(B, Nq, H, d) -> int:
@@ -427,6 +435,44 @@ def backward(q, k, v, o, lse, dout, scale=None, causal=False, workspace=None, dq
                     workspace.numel(), _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def backward_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                    scale=None, causal=False, workspace=None, dq=None, dk=None, dv=None, stream=None):
+    """Gradients (dq, dk, dv) for packed sequences (the variable-length forward's
+    layout): q, o, dout [total_q, H, d]; k, v [total_k, Hk, d]; cu_seqlens_q/k
+    int32 [B + 1] on the device; lse [B, H, max_seqlen_q] as the forward wrote it."""
+    import torch
+    total_q, H, d = q.shape
+    Hk = k.shape[1]
+    B = cu_seqlens_q.numel() - 1
+    for t in (q, k, v, o, dout):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v, o, dout must be contiguous bf16 CUDA tensors")
+    if o.shape != q.shape or dout.shape != q.shape or v.shape != k.shape or k.shape[2] != d:
+        raise ValueError("shape mismatch")
+    for c in (cu_seqlens_q, cu_seqlens_k):
+        if c.dtype != torch.int32 or not c.is_cuda or c.numel() != B + 1:
+            raise ValueError("cu_seqlens must be int32 CUDA tensors of B + 1 entries")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, max_seqlen_q) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [B, H, max_seqlen_q]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = bwd_workspace_bytes(B, max_seqlen_q, H, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    with _on_device(q.device):
+        rc = fa_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                           lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), cu_seqlens_q.data_ptr(),
+                           cu_seqlens_k.data_ptr(), B, int(max_seqlen_q), int(max_seqlen_k), H, Hk, d,
+                           float(scale), FA_FLAG_CAUSAL if causal else 0, workspace.data_ptr(),
+                           workspace.numel(), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd_varlen")
     return dq, dk, dv
 
 

@@ -439,6 +439,7 @@ struct BwdProblem {
   const void *q, *k, *v, *o, *dout;
   const float* lse;
   void *dq, *dk, *dv;
+  const int *cu_q, *cu_k;  // variable-length form (both or neither)
   int B, Nq, Nk, H, Hk, d;
   float scale;
   int flags;
@@ -453,8 +454,15 @@ int run_bwd(const BwdProblem& P) {
   if (P.H > 0 && (P.Hk == 0 || P.H % P.Hk != 0)) return FA_ERR_INVALID_ARG;
   if (!(std::isfinite(P.scale) && P.scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (P.d != 64 && P.d != 128) return FA_ERR_UNSUPPORTED;
+  const bool varlen = P.cu_q != nullptr;
+  if ((P.cu_q == nullptr) != (P.cu_k == nullptr)) return FA_ERR_INVALID_ARG;
+  if (varlen && ((reinterpret_cast<uintptr_t>(P.cu_q) & 3u) || (reinterpret_cast<uintptr_t>(P.cu_k) & 3u)))
+    return FA_ERR_ALIGN;
   if (P.B == 0 || P.H == 0) return FA_OK;
-  if (P.Nk == 0) return P.Nq == 0 ? FA_OK : FA_ERR_INVALID_ARG;  // as the forward: queries need keys
+  // Dense queries need keys (as the forward); packed sequences without keys
+  // are allowed and get dQ = 0.
+  if (!varlen && P.Nk == 0) return P.Nq == 0 ? FA_OK : FA_ERR_INVALID_ARG;
+  if (varlen && P.Nq == 0 && P.Nk == 0) return FA_OK;
   if (!P.k || !P.v || !P.dk || !P.dv || !P.ws) return FA_ERR_INVALID_ARG;
   if (P.Nq > 0 && (!P.q || !P.o || !P.dout || !P.lse || !P.dq)) return FA_ERR_INVALID_ARG;
   for (const void* ptr : {P.q, P.k, P.v, P.o, P.dout, static_cast<const void*>(P.dq), static_cast<const void*>(P.dk),
@@ -514,22 +522,49 @@ int run_bwd(const BwdProblem& P) {
   const void* qptr = P.Nq > 0 ? P.q : P.k;
   const void* doptr = P.Nq > 0 ? P.dout : P.k;
   const int nq_map = P.Nq > 0 ? P.Nq : 1;
+  const int nk_map = P.Nk > 0 ? P.Nk : 1;
+  const void* kptr = P.Nk > 0 ? P.k : qptr;
+  const void* vptr = P.Nk > 0 ? P.v : qptr;
   const int hq_map = P.Nq > 0 ? P.H : P.Hk;
-  cuuint64_t dq4[4] = {(cuuint64_t)D, (cuuint64_t)hq_map, (cuuint64_t)nq_map, (cuuint64_t)P.B};
-  cuuint64_t sq4[3] = {D * esz, (cuuint64_t)hq_map * D * esz, (cuuint64_t)nq_map * hq_map * D * esz};
-  cuuint64_t dk4[4] = {(cuuint64_t)D, (cuuint64_t)P.Hk, (cuuint64_t)P.Nk, (cuuint64_t)P.B};
-  cuuint64_t sk4[3] = {D * esz, (cuuint64_t)P.Hk * D * esz, (cuuint64_t)P.Nk * P.Hk * D * esz};
-  cuuint32_t box_q[4] = {64, 1, (cuuint32_t)fa::kBwdBQ, 1};
-  cuuint32_t box_k[4] = {64, 1, (cuuint32_t)fa::kBwdBK, 1};
+  const int hk_map = P.Nk > 0 ? P.Hk : hq_map;
   int e;
-  if ((e = encode(&a.tm_q, qptr, 4, dq4, sq4, box_q)) != FA_OK) return e;
-  if ((e = encode(&a.tm_do, doptr, 4, dq4, sq4, box_q)) != FA_OK) return e;
-  if ((e = encode(&a.tm_k, P.k, 4, dk4, sk4, box_k)) != FA_OK) return e;
-  if ((e = encode(&a.tm_v, P.v, 4, dk4, sk4, box_k)) != FA_OK) return e;
+  if (!varlen) {
+    cuuint64_t dq4[4] = {(cuuint64_t)D, (cuuint64_t)hq_map, (cuuint64_t)nq_map, (cuuint64_t)P.B};
+    cuuint64_t sq4[3] = {D * esz, (cuuint64_t)hq_map * D * esz, (cuuint64_t)nq_map * hq_map * D * esz};
+    cuuint64_t dk4[4] = {(cuuint64_t)D, (cuuint64_t)hk_map, (cuuint64_t)nk_map, (cuuint64_t)P.B};
+    cuuint64_t sk4[3] = {D * esz, (cuuint64_t)hk_map * D * esz, (cuuint64_t)nk_map * hk_map * D * esz};
+    cuuint32_t box_q[4] = {64, 1, (cuuint32_t)fa::kBwdBQ, 1};
+    cuuint32_t box_k[4] = {64, 1, (cuuint32_t)fa::kBwdBK, 1};
+    if ((e = encode(&a.tm_q, qptr, 4, dq4, sq4, box_q)) != FA_OK) return e;
+    if ((e = encode(&a.tm_do, doptr, 4, dq4, sq4, box_q)) != FA_OK) return e;
+    if ((e = encode(&a.tm_k, kptr, 4, dk4, sk4, box_k)) != FA_OK) return e;
+    if ((e = encode(&a.tm_v, vptr, 4, dk4, sk4, box_k)) != FA_OK) return e;
+  } else {
+    // Packed rows; the row extent is an upper bound (every length is at most
+    // the maximum), and the kernel never addresses a row past its sequence's
+    // end (a sequence's last tile is shifted back instead).
+    cuuint64_t dq3[3] = {(cuuint64_t)D, (cuuint64_t)hq_map, (cuuint64_t)P.B * nq_map};
+    cuuint64_t sq3[2] = {D * esz, (cuuint64_t)hq_map * D * esz};
+    cuuint64_t dk3[3] = {(cuuint64_t)D, (cuuint64_t)hk_map, (cuuint64_t)P.B * nk_map};
+    cuuint64_t sk3[2] = {D * esz, (cuuint64_t)hk_map * D * esz};
+    cuuint32_t box_q[3] = {64, 1, (cuuint32_t)fa::kBwdBQ};
+    cuuint32_t box_k[3] = {64, 1, (cuuint32_t)fa::kBwdBK};
+    if ((e = encode(&a.tm_q, qptr, 3, dq3, sq3, box_q)) != FA_OK) return e;
+    if ((e = encode(&a.tm_do, doptr, 3, dq3, sq3, box_q)) != FA_OK) return e;
+    if ((e = encode(&a.tm_k, kptr, 3, dk3, sk3, box_k)) != FA_OK) return e;
+    if ((e = encode(&a.tm_v, vptr, 3, dk3, sk3, box_k)) != FA_OK) return e;
+  }
+  p.cu_q = P.cu_q;
+  p.cu_k = P.cu_k;
   a.grid = dim3(static_cast<unsigned>(p.num_items < st->num_sms ? p.num_items : st->num_sms), 1, 1);
   a.stream = P.stream;
-  const cudaError_t ce = D == 128 ? (p.causal ? fa::launch_bwd<128, true>(a) : fa::launch_bwd<128, false>(a))
-                                   : (p.causal ? fa::launch_bwd<64, true>(a) : fa::launch_bwd<64, false>(a));
+  cudaError_t ce;
+  if (D == 128)
+    ce = varlen ? (p.causal ? fa::launch_bwd<128, true, true>(a) : fa::launch_bwd<128, false, true>(a))
+                : (p.causal ? fa::launch_bwd<128, true, false>(a) : fa::launch_bwd<128, false, false>(a));
+  else
+    ce = varlen ? (p.causal ? fa::launch_bwd<64, true, true>(a) : fa::launch_bwd<64, false, true>(a))
+                : (p.causal ? fa::launch_bwd<64, true, false>(a) : fa::launch_bwd<64, false, false>(a));
   if (ce != cudaSuccess) return cuda_fail(ce);
   return FA_OK;
 }
@@ -733,8 +768,18 @@ long long fa_bwd_workspace_bytes(int B, int Nq, int H, int d) {
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
            void* dq, void* dk, void* dv, int B, int Nq, int Nk, int H, int Hk, int d, float scale, int flags,
            void* workspace, long long workspace_bytes, void* stream) {
-  BwdProblem P{q, k, v, o, dout, lse, dq, dk, dv, B, Nq, Nk, H, Hk, d, scale, flags, workspace,
+  BwdProblem P{q, k, v, o, dout, lse, dq, dk, dv, nullptr, nullptr, B, Nq, Nk, H, Hk, d, scale, flags, workspace,
                workspace_bytes, static_cast<cudaStream_t>(stream)};
+  return run_bwd(P);
+}
+
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                  void* dq, void* dk, void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int B,
+                  int max_seqlen_q, int max_seqlen_k, int H, int Hk, int d, float scale, int flags,
+                  void* workspace, long long workspace_bytes, void* stream) {
+  if (!cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARG;
+  BwdProblem P{q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, B, max_seqlen_q, max_seqlen_k,
+               H, Hk, d, scale, flags, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
   return run_bwd(P);
 }
 

@@ -67,7 +67,7 @@ constexpr int kBwdBK = 128;  // keys per work unit (M of the key-row products)
 constexpr int kBwdBQ = 128;  // queries per step
 
 struct BwdParams {
-  int B, Nq, Nk, H, Hk, group;
+  int B, Nq, Nk, H, Hk, group;  // variable-length form: Nq / Nk are the maximum lengths
   int causal;           // bottom-right aligned: query i sees keys j <= i + Nk - Nq
   int nq_pad;           // Nq rounded up to kBwdBQ (row stride of lse2 / delta / dq_acc)
   int num_qb;           // query blocks per head
@@ -78,8 +78,15 @@ struct BwdParams {
   const __nv_bfloat16* o;     // [B, Nq, H, d]  (preprocessing)
   const __nv_bfloat16* dout;  // [B, Nq, H, d]  (preprocessing)
   const float* lse;           // [B, H, Nq] natural log, from the forward
+  const int* cu_q;            // variable-length form: int32 [B + 1] packed row offsets
+  const int* cu_k;
+  // The next three are in tile order: entry qb * 128 + c belongs to column c
+  // of query tile qb as the main kernel loads it (the same as query row
+  // qb * 128 + c, except for a variable-length sequence's last tile, which is
+  // shifted back to end at the sequence end; its columns that repeat the
+  // previous tile's rows carry lse2 = +inf, so they take no part).
   float* lse2;                // [B, H, nq_pad]  L * log2(e); +inf where no gradient flows
-  float* delta;               // [B, H, nq_pad]  D_i
+  float* delta;               // [B, H, nq_pad]  D_i (0 where no gradient flows)
   float* dq_acc;              // [B, H, nq_pad, d] fp32
   __nv_bfloat16* dq;          // [B, Nq, H, d]
   __nv_bfloat16* dk;          // [B, Nk, Hk, d]
@@ -91,24 +98,44 @@ struct BwdParams {
 };
 
 // ------------------------------------------------------------ preprocessing
-// One warp per (b, h, i < nq_pad): D_i = sum_c do_ic o_ic in fp32, lse2_i,
-// and a zeroed row of the dQ accumulator.  Padding rows (i >= Nq) and rows
-// without keys (L = -inf) get lse2 = +inf, so their P is exactly 0.
-template <int D>
+// Query rows of a sequence: its packed start and length (dense: 0 and Nq).
+template <bool VARLEN>
+__device__ __forceinline__ void bwd_seq_q(const BwdParams& p, int b, int& start, int& len) {
+  start = 0;
+  len = p.Nq;
+  if constexpr (VARLEN) {
+    start = p.cu_q[b];
+    len = p.cu_q[b + 1] - start;
+    if (len < 0 || len > p.Nq || start < 0) len = 0;  // reported by the main kernel
+  }
+}
+
+// One warp per (b, h, tile entry t < nq_pad): D_i = sum_c do_ic o_ic in fp32,
+// lse2_i for the query row i that column t % 128 of tile t / 128 holds, and a
+// zeroed row of the dQ accumulator.  Entries that hold no row of their own
+// (padding, or the repeated rows of a shifted last tile) and rows without
+// keys (L = -inf) get lse2 = +inf and D = 0, so their P and dS are exactly 0.
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdParams p) {
   const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const long long rows = static_cast<long long>(p.B) * p.H * p.nq_pad;
   if (row >= rows) return;
-  const int i = static_cast<int>(row % p.nq_pad);
+  const int t = static_cast<int>(row % p.nq_pad);
   const long long bh = row / p.nq_pad;
   const int h = static_cast<int>(bh % p.H);
   const int b = static_cast<int>(bh / p.H);
   constexpr int kPer = D / 32;  // elements per lane
+  int q_start, len_q;
+  bwd_seq_q<VARLEN>(p, b, q_start, len_q);
+  const int qb = t / kBwdBQ, c = t % kBwdBQ;
+  const RowWindow qw = make_window<VARLEN>(q_start, q_start + len_q, q_start + qb * kBwdBQ, kBwdBQ);
   float acc = 0.f;
   float l2 = INFINITY;
-  if (i < p.Nq) {
-    const size_t off = ((static_cast<size_t>(b) * p.Nq + i) * p.H + h) * D + lane * kPer;
+  if (qb * kBwdBQ < len_q && c >= qw.lo && c < qw.hi) {
+    const int i = qw.load_row - q_start + c;  // query row within the sequence
+    const size_t prow = VARLEN ? static_cast<size_t>(qw.load_row + c) : static_cast<size_t>(b) * p.Nq + i;
+    const size_t off = (prow * p.H + h) * D + lane * kPer;
 #pragma unroll
     for (int e = 0; e < kPer; ++e)
       acc += __bfloat162float(p.dout[off + e]) * __bfloat162float(p.o[off + e]);
@@ -126,8 +153,9 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdParams p) {
   for (int e = 0; e < kPer; ++e) dst[e] = 0.f;
 }
 
-// dq[b, i, h, :] = bf16(scale * dq_acc[b, h, i, :]); one warp per row.
-template <int D>
+// dq[b, i, h, :] = bf16(scale * dq_acc[b, h, t(i), :]) with t(i) the tile
+// entry that holds query row i; one warp per row.
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdParams p) {
   const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -138,8 +166,15 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdParams p) {
   const int h = static_cast<int>(bh % p.H);
   const int b = static_cast<int>(bh / p.H);
   constexpr int kPer = D / 32;
-  const float* src = p.dq_acc + (static_cast<size_t>(bh) * p.nq_pad + i) * D + lane * kPer;
-  __nv_bfloat16* dst = p.dq + ((static_cast<size_t>(b) * p.Nq + i) * p.H + h) * D + lane * kPer;
+  int q_start, len_q;
+  bwd_seq_q<VARLEN>(p, b, q_start, len_q);
+  if (i >= len_q) return;
+  const int qb = i / kBwdBQ;
+  const RowWindow qw = make_window<VARLEN>(q_start, q_start + len_q, q_start + qb * kBwdBQ, kBwdBQ);
+  const int t = qb * kBwdBQ + (q_start + i - qw.load_row);
+  const size_t prow = VARLEN ? static_cast<size_t>(q_start + i) : static_cast<size_t>(b) * p.Nq + i;
+  const float* src = p.dq_acc + (static_cast<size_t>(bh) * p.nq_pad + t) * D + lane * kPer;
+  __nv_bfloat16* dst = p.dq + (prow * p.H + h) * D + lane * kPer;
 #pragma unroll
   for (int e = 0; e < kPer; e += 2) {
     const float x0 = src[e] * p.scale, x1 = src[e + 1] * p.scale;
@@ -196,15 +231,21 @@ struct BwdSmem {
 };
 
 // One work unit: key block kb of key/value head hk in batch b, and the query
-// blocks [qb0, num_qb) of each of the group's query heads.
+// blocks [qb0, qb0 + nqb) of each of the group's query heads.  Rows are
+// sequence rows (packed rows = start + row in the variable-length form).
 struct BwdUnit {
   int b, hk, kb;
-  int qb0;     // first query block that sees any key of this block
-  int nqb;     // query blocks per head
-  int nsteps;  // group * nqb
+  int q_start, len_q;  // the sequence's queries (dense: 0, Nq)
+  int k_start, len_k;  // its keys
+  int off;             // causal: query i sees keys j <= i + off
+  RowWindow kw;        // the key tile as loaded (shifted back to end at the sequence end
+                       // in the variable-length form; keys [lo, hi) of it are this block's)
+  int qb0;             // first query block that sees any key of this block
+  int nqb;             // query blocks per head
+  int nsteps;          // group * nqb
 };
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool VARLEN>
 __device__ __forceinline__ BwdUnit bwd_decode(const BwdParams& p, int u) {
   BwdUnit w;
   int kb = u % p.num_kb;
@@ -218,15 +259,34 @@ __device__ __forceinline__ BwdUnit bwd_decode(const BwdParams& p, int u) {
   w.kb = kb;
   w.hk = r % p.Hk;
   w.b = r / p.Hk;
+  w.q_start = 0;
+  w.len_q = p.Nq;
+  w.k_start = 0;
+  w.len_k = p.Nk;
+  if constexpr (VARLEN) {
+    w.q_start = p.cu_q[w.b];
+    w.len_q = p.cu_q[w.b + 1] - w.q_start;
+    w.k_start = p.cu_k[w.b];
+    w.len_k = p.cu_k[w.b + 1] - w.k_start;
+    if (w.len_q < 0 || w.len_k < 0 || w.len_q > p.Nq || w.len_k > p.Nk || w.q_start < 0 || w.k_start < 0) {
+      if (kb == 0 && w.hk == 0 && (threadIdx.x & 31) == 0 && threadIdx.x < 32)
+        record_error(p.status, kErrBadSeqlens, 0);
+      w.len_q = 0;
+      w.len_k = 0;
+    }
+  }
+  w.off = w.len_k - w.len_q;
+  w.kw = make_window<VARLEN>(w.k_start, w.k_start + w.len_k, w.k_start + kb * kBwdBK, kBwdBK);
+  const int num_qb = (w.len_q + kBwdBQ - 1) / kBwdBQ;
   w.qb0 = 0;
   if constexpr (CAUSAL) {
     // Query i sees key j iff j <= i + off: the first query of interest is
-    // kb * 128 - off (never past the last query: every key j < Nk is seen by
-    // query Nq - 1).
-    const int first = kb * kBwdBK - (p.Nk - p.Nq);
+    // kb * 128 - off (never past the last query: every key j < len_k is seen
+    // by query len_q - 1).
+    const int first = kb * kBwdBK - w.off;
     w.qb0 = first <= 0 ? 0 : first / kBwdBQ;
   }
-  w.nqb = p.num_qb - w.qb0;
+  w.nqb = kb * kBwdBK < w.len_k ? num_qb - w.qb0 : 0;
   w.nsteps = w.nqb > 0 ? p.group * w.nqb : 0;
   return w;
 }
@@ -254,7 +314,7 @@ struct BwdRegSplit {
                 "register split exceeds the launch allocation");
 };
 
-template <int D, int STAGES, bool CAUSAL>
+template <int D, int STAGES, bool CAUSAL, bool VARLEN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -324,7 +384,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  const int off = p.Nk - p.Nq;
 
   // Handshake barriers are single: each one's next completion needs an action
   // of its own waiter first (S(g+1) is issued after P(g) is seen, dP(g+1)
@@ -337,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
 #pragma unroll 1
       FA_BWD_FOR_EACH_UNIT(u) {
-        const BwdUnit w = bwd_decode<CAUSAL>(p, u);
+        const BwdUnit w = bwd_decode<CAUSAL, VARLEN>(p, u);
         if (w.nsteps == 0) continue;
         if (uc > 0 && !ptx::mbar_wait(bar(L::kBarKVEmpty), (uc - 1) & 1u, s_abort, tmo)) {
           record_error(p.status, kErrTimeout, kBSiteLoadKV);
@@ -347,10 +406,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive_expect_tx(bar(L::kBarKVFull), 2 * L::kKVBytes);  // K and V, D features each
 #pragma unroll
         for (int pn = 0; pn < kDPanels; ++pn) {
-          ptx::tma_load_4d(base + L::kOffK + pn * L::kKVPanel, &tm_k, bar(L::kBarKVFull), pn * 64, w.hk,
-                           w.kb * kBwdBK, w.b);
-          ptx::tma_load_4d(base + L::kOffV + pn * L::kKVPanel, &tm_v, bar(L::kBarKVFull), pn * 64, w.hk,
-                           w.kb * kBwdBK, w.b);
+          if constexpr (VARLEN) {
+            // Packed rows; a tile shifted back below row 0 is zero-filled there.
+            ptx::tma_load_3d(base + L::kOffK + pn * L::kKVPanel, &tm_k, bar(L::kBarKVFull), pn * 64, w.hk,
+                             w.kw.load_row);
+            ptx::tma_load_3d(base + L::kOffV + pn * L::kKVPanel, &tm_v, bar(L::kBarKVFull), pn * 64, w.hk,
+                             w.kw.load_row);
+          } else {
+            ptx::tma_load_4d(base + L::kOffK + pn * L::kKVPanel, &tm_k, bar(L::kBarKVFull), pn * 64, w.hk,
+                             w.kb * kBwdBK, w.b);
+            ptx::tma_load_4d(base + L::kOffV + pn * L::kKVPanel, &tm_v, bar(L::kBarKVFull), pn * 64, w.hk,
+                             w.kb * kBwdBK, w.b);
+          }
         }
         ++uc;
 #pragma unroll 1
@@ -368,8 +435,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sq = base + L::kOffQ + slot * L::kSlotBytes;
 #pragma unroll
           for (int pn = 0; pn < kDPanels; ++pn) {
-            ptx::tma_load_4d(sq + pn * L::kQPanel, &tm_q, fb, pn * 64, h, qb * kBwdBQ, w.b);
-            ptx::tma_load_4d(sq + L::kQBytes + pn * L::kQPanel, &tm_do, fb, pn * 64, h, qb * kBwdBQ, w.b);
+            if constexpr (VARLEN) {
+              const int qrow = make_window<true>(w.q_start, w.q_start + w.len_q, w.q_start + qb * kBwdBQ, kBwdBQ).load_row;
+              ptx::tma_load_3d(sq + pn * L::kQPanel, &tm_q, fb, pn * 64, h, qrow);
+              ptx::tma_load_3d(sq + L::kQBytes + pn * L::kQPanel, &tm_do, fb, pn * 64, h, qrow);
+            } else {
+              ptx::tma_load_4d(sq + pn * L::kQPanel, &tm_q, fb, pn * 64, h, qb * kBwdBQ, w.b);
+              ptx::tma_load_4d(sq + L::kQBytes + pn * L::kQPanel, &tm_do, fb, pn * 64, h, qb * kBwdBQ, w.b);
+            }
           }
           // The block's scaled LSE and D rows (512 bytes each, 512-byte aligned:
           // nq_pad is a multiple of the block) for the softmax warps.
@@ -431,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
 #pragma unroll 1
       FA_BWD_FOR_EACH_UNIT(u) {
-        const BwdUnit w = bwd_decode<CAUSAL>(p, u);
+        const BwdUnit w = bwd_decode<CAUSAL, VARLEN>(p, u);
         if (w.nsteps == 0) continue;
         if (!wait(bar(L::kBarKVFull), uc & 1u, kBSiteMmaKV)) break;
         ptx::tc_fence_after();
@@ -506,15 +579,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
 #pragma unroll 1
     FA_BWD_FOR_EACH_UNIT(u) {
-      const BwdUnit w = bwd_decode<CAUSAL>(p, u);
+      const BwdUnit w = bwd_decode<CAUSAL, VARLEN>(p, u);
       if (w.nsteps == 0) continue;
-      const int kj = w.kb * kBwdBK + r;  // this thread's key
-      const bool key_ok = kj < p.Nk;
+      const int kj = w.kw.load_row - w.k_start + r;        // this thread's key (sequence index)
+      const bool key_ok = r >= w.kw.lo && r < w.kw.hi;  // a key of this block
 #pragma unroll 1
       for (int i = 0; i < w.nsteps && ok; ++i, ++g) {
         const int h = w.hk * p.group + i / w.nqb;
         const int qb = w.qb0 + i % w.nqb;
-        const int q0 = qb * kBwdBQ + c * 64;  // first query of this warpgroup's columns
+        // First query (sequence index) of this warpgroup's columns of the tile as loaded.
+        const int q0 = make_window<VARLEN>(w.q_start, w.q_start + w.len_q, w.q_start + qb * kBwdBQ, kBwdBQ).load_row -
+                       w.q_start + c * 64;
         // Scaled LSE and D of this warpgroup's 64 queries, staged with Q(g)
         // (shared-memory broadcasts instead of dependent global loads).
         const uint32_t slot = g % STAGES;
@@ -527,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        // P^T = 2^(S^T c2 - L log2 e), 32 columns at a time; keys past Nk and
+        // P^T = 2^(S^T c2 - L log2 e), 32 columns at a time; keys outside the block and
         // (causal) keys after a query's limit get 0; the bf16 pairs of half hh
         // go to columns 16 hh .. 16 hh + 15 (already read).  The packed pairs
         // stay in registers for dS: S(g + 1) overwrites these columns as soon
@@ -538,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t sr[32];
           ptx::tmem_ld32(tSc + hh * 32, sr);
           ptx::tmem_wait_ld();
-          const int lim = CAUSAL ? kj - off - (q0 + hh * 32) : -1;  // column k masked when k < lim
+          const int lim = CAUSAL ? kj - w.off - (q0 + hh * 32) : -1;  // column k masked when k < lim
 #pragma unroll
           for (int k4 = 0; k4 < 8; ++k4) {
             const float4 l = l2g[hh * 8 + k4];
@@ -612,12 +687,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
 #pragma unroll 1
     FA_BWD_FOR_EACH_UNIT(u) {
-      const BwdUnit w = bwd_decode<CAUSAL>(p, u);
-      const int kj = w.kb * kBwdBK + (wq << 5) + lane;
-      const size_t krow = ((static_cast<size_t>(w.b) * p.Nk + kj) * p.Hk + w.hk) * D;
+      const BwdUnit w = bwd_decode<CAUSAL, VARLEN>(p, u);
+      const int kr = (wq << 5) + lane;  // this thread's key row of the tile
+      const bool key_ok = kr >= w.kw.lo && kr < w.kw.hi;
+      const size_t prow = VARLEN ? static_cast<size_t>(w.kw.load_row + kr)
+                                 : static_cast<size_t>(w.b) * p.Nk + w.kw.load_row + kr;
+      const size_t krow = (prow * p.Hk + w.hk) * D;
       if (w.nsteps == 0) {
         // No query sees these keys: dK = dV = 0.
-        if (kj < p.Nk) {
+        if (key_ok) {
           for (int e = 0; e < D; e += 8) {
             ptx::st_global_v4(p.dk + krow + e, 0u, 0u, 0u, 0u);
             ptx::st_global_v4(p.dv + krow + e, 0u, 0u, 0u, 0u);
@@ -671,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t a[32];
           ptx::tmem_ld32(tmem + lane_off + col + c4 * 32, a);
           ptx::tmem_wait_ld();
-          if (kj < p.Nk) {
+          if (key_ok) {
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
               uint32_t wv[4];

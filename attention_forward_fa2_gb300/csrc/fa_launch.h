@@ -89,7 +89,8 @@ struct BwdLaunchArgs {
   cudaStream_t stream;
 };
 
-template <int D, bool CAUSAL>
+// VARLEN: packed [total, heads, d] tensors with cu_seqlens in a.p (3-D maps).
+template <int D, bool CAUSAL, bool VARLEN>
 cudaError_t launch_bwd(const BwdLaunchArgs& a);
 
 // FP8 path (fa_fp8.cu).

@@ -27,7 +27,7 @@ implementation; the oracle is the reference), printing the same JSON line.
 --fp8 times the e4m3 forward (fa_fwd_fp8) on the workload quantised once
 beforehand (block scales; the quantisation is not timed), against the fp8
 dense peak taken as twice the measured bf16 one (the nominal ratio).
---bwd times the backward pass instead (fa_bwd, d = 64 or 128: preprocessing, key-block kernel,
+--bwd times the backward pass instead (fa_bwd / fa_bwd_varlen, d = 64 or 128: preprocessing, key-block kernel,
 dQ conversion), FLOPs counted as 2.5x the forward's (five matrix products
 against two).  Rank 0 prints one JSON line on stdout.
 """
@@ -539,22 +539,33 @@ def run_bwd(args, w):
     from attention_forward_fa2_gb300 import build as fabuild
     from attention_forward_fa2_gb300 import inputs as I
 
-    if w.varlen:
-        raise SystemExit("--bwd takes dense workloads")
     rank, local, world = dist_setup(args.gpus)
     torch.cuda.set_device(local)
     fabuild.build()
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
-    q, k, v, _, _ = I.make(w)
+    q, k, v, cu_q, cu_k = I.make(w)
     dout = I.randn_bf16(tuple(q.shape), torch.Generator().manual_seed(w.seed + 1000))
     dq, dk, dv, ddo = q.to(dev), k.to(dev), v.to(dev), dout.to(dev)
-    o, lse = fa.forward_qk(dq, dk, dv, causal=args.causal)
-    ws = torch.empty(fa.bwd_workspace_bytes(w.B, w.Nq, w.H, w.d), dtype=torch.uint8, device=dev)
+    if w.varlen:
+        maxlen = max(w.lengths)
+        dcq, dck = cu_q.to(dev), cu_k.to(dev)
+        o, lse = fa.forward_qk(dq, dk, dv, None, dcq, dck, maxlen, maxlen, causal=args.causal)
+        ws = torch.empty(fa.bwd_workspace_bytes(w.B, maxlen, w.H, w.d), dtype=torch.uint8, device=dev)
+    else:
+        o, lse = fa.forward_qk(dq, dk, dv, causal=args.causal)
+        ws = torch.empty(fa.bwd_workspace_bytes(w.B, w.Nq, w.H, w.d), dtype=torch.uint8, device=dev)
     gq, gk, gv = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
 
+    def backward_on(bq, bk, bv, bo, bl, bdo, rq, rk, rv):
+        if w.varlen:
+            fa.backward_varlen(bq, bk, bv, bo, bl, bdo, dcq, dck, maxlen, maxlen, causal=args.causal, workspace=ws,
+                               dq=rq, dk=rk, dv=rv)
+        else:
+            fa.backward(bq, bk, bv, bo, bl, bdo, causal=args.causal, workspace=ws, dq=rq, dk=rk, dv=rv)
+
     def step():
-        fa.backward(dq, dk, dv, o, lse, ddo, causal=args.causal, workspace=ws, dq=gq, dk=gk, dv=gv)
+        backward_on(dq, dk, dv, o, lse, ddo, gq, gk, gv)
 
     for _ in range(args.warmup):
         step()
@@ -597,7 +608,7 @@ def run_bwd(args, w):
 
     def run_set(si):
         (bq, bk, bv, bo, bl, bdo), (rq, rk, rv) = sets[si]
-        fa.backward(bq, bk, bv, bo, bl, bdo, causal=args.causal, workspace=ws, dq=rq, dk=rk, dv=rv)
+        backward_on(bq, bk, bv, bo, bl, bdo, rq, rk, rv)
 
     e2e_ms = max_over_ranks(pipelined_e2e(torch, dev, stream, sets, hosts, outs, run_set, e2e_steps, world), world)
     if rank != 0:

@@ -204,6 +204,25 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            int d, float scale, int flags, void* workspace, long long workspace_bytes, void* stream);
 
 /*
+ * Variable-length backward: the same gradients for packed sequences, as the
+ * forward's variable-length form lays them out ([FMHA] §3.1): q, o, dout, dq
+ * are [total_q, H, d], k, v, dk, dv [total_k, Hk, d] (rows of sequence b at
+ * cu_seqlens[b] .. cu_seqlens[b + 1] - 1), lse [B, H, max_seqlen_q] as the
+ * variable-length forward writes it.  cu_seqlens_q / cu_seqlens_k: device
+ * int32 [B + 1], non-decreasing from 0, 4-byte aligned; every length at most
+ * the given maximum (a longer one is reported as FA_ERR_BAD_SEQLENS by
+ * fa_check_status and its units write nothing).  The workspace is
+ * fa_bwd_workspace_bytes(B, max_seqlen_q, H, d).  The causal mask is aligned
+ * bottom-right within each sequence.  Rows of dq, dk, dv past the last
+ * sequence are not written; a sequence without keys gets dq = 0.
+ */
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                  const float* lse, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int B, int max_seqlen_q, int max_seqlen_k, int H, int Hk,
+                  int d, float scale, int flags, void* workspace, long long workspace_bytes,
+                  void* stream);
+
+/*
  * FP8 forward ("GPU 内核与 FlashAttention" §15.5: e4m3 inputs with block
  * quantisation).  Quantisation: every block of values shares one fp32 scale
  * s = amax(block) / 448 (1 for an all-zero block) and a value x is stored as

@@ -155,3 +155,61 @@ def test_backward_is_repeatable():
     b = _gpu_grads(q, k, v, do, False)
     assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
     assert np.abs(a[0] - b[0]).max() <= 1e-2 * np.abs(a[0]).max()
+
+
+# ------------------------------------------------------------ variable length
+def _packed(lengths, H, d, gen):
+    total = int(sum(lengths))
+    return I.randn_bf16((total, H, d), gen)
+
+
+@pytest.mark.parametrize("lq,lk,H,Hk,d", [
+    ([129, 1, 384, 77], None, 2, 1, 128),       # ragged ends, one-row sequence, MQA
+    ([100, 260, 128], [300, 50, 128], 2, 2, 128),  # different query and key lengths
+    ([0, 200, 0, 33], [5, 200, 7, 40], 2, 2, 128),  # empty query sequences (keys still get dk = dv = 0)
+    ([129, 70, 256], None, 4, 2, 64),            # d = 64
+])
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_varlen_matches_oracle(oracle_mod, lq, lk, H, Hk, d, causal):
+    """Packed sequences: each sequence's gradients equal the dense oracle's
+    on that sequence alone (the causal mask is bottom-right per sequence)."""
+    lk = lq if lk is None else lk
+    g = torch.Generator().manual_seed(3000 + sum(lq) + causal)
+    q = _packed(lq, H, d, g)
+    k, v = _packed(lk, Hk, d, g), _packed(lk, Hk, d, g)
+    do = _packed(lq, H, d, g)
+    cu_q = torch.tensor(np.concatenate([[0], np.cumsum(lq)]), dtype=torch.int32)
+    cu_k = torch.tensor(np.concatenate([[0], np.cumsum(lk)]), dtype=torch.int32)
+    mq, mk = max(lq), max(lk)
+    dq_, dk_, dv_, ddo = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = fa.forward_qk(dq_, dk_, dv_, None, cu_q.cuda(), cu_k.cuda(), mq, mk, causal=causal)
+    dk_out = torch.full_like(dk_, 7.0)
+    dv_out = torch.full_like(dv_, 7.0)
+    gq, gk, gv = fa.backward_varlen(dq_, dk_, dv_, o, lse, ddo, cu_q.cuda(), cu_k.cuda(), mq, mk, causal=causal,
+                                    dk=dk_out, dv=dv_out)
+    rc, info = fa.check_status()
+    assert rc == fa.FA_OK, (fa.strerror(rc), info)
+    gq, gk, gv = (t.double().cpu().numpy() for t in (gq, gk, gv))
+    for b in range(len(lq)):
+        q0, q1, k0, k1 = int(cu_q[b]), int(cu_q[b + 1]), int(cu_k[b]), int(cu_k[b + 1])
+        what = "seq %d (lq %d lk %d) causal%d d%d" % (b, lq[b], lk[b], causal, d)
+        if k1 == k0:
+            continue
+        if q1 == q0:
+            assert np.all(gk[k0:k1] == 0) and np.all(gv[k0:k1] == 0), what
+            continue
+        sl = lambda t, a, z: I.bf16_bits(t[a:z].unsqueeze(0).contiguous())
+        ref = oracle_mod.attn_bwd_dense(sl(q, q0, q1), sl(k, k0, k1), sl(v, k0, k1), sl(do, q0, q1),
+                                        causal=causal)[:3]
+        mine = (gq[None, q0:q1], gk[None, k0:k1], gv[None, k0:k1])
+        _assert_grads(mine, ref, what)
+
+
+def test_backward_varlen_rejects_half_given_seqlens():
+    q = torch.randn(10, 2, 128, dtype=torch.bfloat16, device="cuda")
+    cu = torch.tensor([0, 10], dtype=torch.int32, device="cuda")
+    lse = torch.zeros(1, 2, 10, device="cuda")
+    rc = fa.fa_bwd_varlen(q.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(), lse.data_ptr(),
+                          q.data_ptr(), q.data_ptr(), q.data_ptr(), cu.data_ptr(), None, 1, 10, 10, 2, 2, 128,
+                          0.1, 0, q.data_ptr(), 1 << 20, None)
+    assert rc == fa.FA_ERR_INVALID_ARG
