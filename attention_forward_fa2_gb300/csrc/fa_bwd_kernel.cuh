@@ -19,6 +19,16 @@
 // registers, performed at L2).  A last kernel scales the accumulator into
 // bf16 dQ.
 //
+// Head dimension 64 or 128.  For d = 64 the K tile keeps a second, zeroed
+// 64-feature panel so that dQ^T = K^T dS^T stays an M = 128 product (its rows
+// 64-127 are zero and never drained).  Packed variable-length sequences
+// (VARLEN, "Flash Attention实现深度解析" §3.1 layout) use the forward's tile
+// rule: a tile that would run past its sequence's end is shifted back to end
+// there, keys of a shifted tile that belong to the previous block are masked,
+// and the preprocessing pass lays out the scaled LSE, D and the dQ
+// accumulator in tile order, so that the repeated query rows of a shifted
+// tile carry LSE = +inf (P = dS = 0) and drop out.
+//
 // Main kernel, per step (one block of 128 queries of one head):
 //   S^T  = K Q^T        M=128 keys, N=128 queries, K=d    tensor memory S
 //   dP^T = V dO^T       M=128 keys, N=128                 tensor memory dP
