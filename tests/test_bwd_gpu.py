@@ -213,3 +213,22 @@ def test_backward_varlen_rejects_half_given_seqlens():
                           q.data_ptr(), q.data_ptr(), q.data_ptr(), cu.data_ptr(), None, 1, 10, 10, 2, 2, 128,
                           0.1, 0, q.data_ptr(), 1 << 20, None)
     assert rc == fa.FA_ERR_INVALID_ARG
+
+
+def test_backward_varlen_reports_lengths_above_the_maximum():
+    """A sequence longer than the declared maximum is reported by the kernel
+    (FA_ERR_BAD_SEQLENS through fa_check_status) and its units write nothing."""
+    H, d = 2, 128
+    g = torch.Generator().manual_seed(71)
+    lens = [100, 200]
+    q = _packed(lens, H, d, g).cuda()
+    k, v, do = (_packed(lens, H, d, g).cuda() for _ in range(3))
+    cu = torch.tensor([0, 100, 300], dtype=torch.int32, device="cuda")
+    o, lse = fa.forward_qk(q, k, v, None, cu, cu, 200, 200)
+    assert fa.check_status()[0] == fa.FA_OK
+    fa.backward_varlen(q, k, v, o, lse[:, :, :150].contiguous(), do, cu, cu, 150, 150)
+    rc, info = fa.check_status()
+    assert rc == fa.FA_ERR_BAD_SEQLENS, (fa.strerror(rc), info)
+    # The context stays usable.
+    fa.backward_varlen(q, k, v, o, lse, do, cu, cu, 200, 200)
+    assert fa.check_status()[0] == fa.FA_OK
