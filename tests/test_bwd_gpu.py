@@ -232,3 +232,23 @@ def test_backward_varlen_reports_lengths_above_the_maximum():
     # The context stays usable.
     fa.backward_varlen(q, k, v, o, lse, do, cu, cu, 200, 200)
     assert fa.check_status()[0] == fa.FA_OK
+
+
+def test_backward_tensors_above_two_to_the_31_elements(oracle_mod):
+    """B128 N4096 H32 d128 (2^31 elements per tensor): the first and the last
+    (batch, head) gradients against the oracle."""
+    B, N, H, d = 128, 4096, 32, 128
+    gen = torch.Generator(device="cuda").manual_seed(6)
+    mk = lambda: torch.randn((B, N, H, d), generator=gen, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    q, k, v, do = mk(), mk(), mk(), mk()
+    o, lse = fa.forward_qk(q, k, v)
+    gq, gk, gv = fa.backward(q, k, v, o, lse, do)
+    rc, info = fa.check_status()
+    assert rc == fa.FA_OK, (fa.strerror(rc), info)
+    for b, h in ((0, 0), (B - 1, H - 1)):
+        sl = lambda t: I.bf16_bits(t[b:b + 1, :, h:h + 1].contiguous().cpu())
+        ref = oracle_mod.attn_bwd_dense(sl(q), sl(k), sl(v), sl(do))[:3]
+        mine = tuple(t[b:b + 1, :, h:h + 1].double().cpu().numpy() for t in (gq, gk, gv))
+        _assert_grads(mine, ref, "b%d h%d" % (b, h))
+    del q, k, v, do, o, lse, gq, gk, gv
+    torch.cuda.empty_cache()

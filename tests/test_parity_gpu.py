@@ -403,3 +403,28 @@ def test_splitkv_rejects_small_or_misaligned_workspace():
     assert fa.fa_fwd_splitkv(*args, ws.data_ptr() + 8, need, s) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_fwd_splitkv(*args, ws.data_ptr(), need, s) == fa.FA_OK
     assert fa.check_status()[0] == fa.FA_OK
+
+
+# ------------------------------------------------------------ maximum sizes
+def _device_bf16(shape, gen):
+    return torch.randn(shape, generator=gen, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+
+
+def test_tensors_above_two_to_the_31_elements(oracle_mod):
+    """B128 N4096 H32 d128: every input and the output hold 2^31 elements
+    (4.3 GB each), so the last heads sit past any 32-bit element offset.  The
+    first and the last (batch, head) are checked in full against the oracle."""
+    B, N, H, d = 128, 4096, 32, 128
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    q, k, v = (_device_bf16((B, N, H, d), gen) for _ in range(3))
+    assert q.numel() >= 2 ** 31
+    o, lse = fa.forward_qk(q, k, v)
+    rc, info = fa.check_status()
+    assert rc == fa.FA_OK, (fa.strerror(rc), info)
+    for b, h in ((0, 0), (B - 1, H - 1)):
+        sl = lambda t: bits(t[b:b + 1, :, h:h + 1].contiguous().cpu())
+        o_ref, lse_ref = oracle_mod.attn_dense(sl(q), sl(k), sl(v))
+        assert_close(o[b:b + 1, :, h:h + 1].double().cpu().numpy(), lse[b:b + 1, h:h + 1].double().cpu().numpy(),
+                     o_ref, lse_ref, "b%d h%d" % (b, h))
+    del q, k, v, o, lse
+    torch.cuda.empty_cache()
