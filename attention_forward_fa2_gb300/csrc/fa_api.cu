@@ -493,7 +493,6 @@ int run_bwd(const BwdProblem& P) {
   p.group = P.H / P.Hk;
   p.causal = (P.flags & FA_FLAG_CAUSAL) ? 1 : 0;
   p.nq_pad = bwd_nq_pad(P.Nq);
-  p.num_qb = p.nq_pad / fa::kBwdBQ;
   p.num_kb = (P.Nk + fa::kBwdBK - 1) / fa::kBwdBK;
   const long long units = static_cast<long long>(P.B) * P.Hk * p.num_kb;
   if (units > 0x7fffffffLL) return FA_ERR_INVALID_ARG;

@@ -78,9 +78,8 @@ constexpr int kBwdBQ = 128;  // queries per step
 
 struct BwdParams {
   int B, Nq, Nk, H, Hk, group;  // variable-length form: Nq / Nk are the maximum lengths
-  int causal;           // bottom-right aligned: query i sees keys j <= i + Nk - Nq
+  int causal;           // bottom-right aligned: query i sees keys j <= i + len_k - len_q (per sequence)
   int nq_pad;           // Nq rounded up to kBwdBQ (row stride of lse2 / delta / dq_acc)
-  int num_qb;           // query blocks per head
   int num_kb;           // key blocks per head
   int num_units;        // B * Hk * num_kb
   int units_per_item;   // 2 when causal (a balanced pair of key blocks)
