@@ -1,5 +1,6 @@
 /*
- * fa.h -- C ABI of the GB300 (sm_103a) FlashAttention-2 forward library.
+ * fa.h -- C ABI of the GB300 (sm_103a) FlashAttention-2 library: the forward
+ * pass (the hot path), its key-split form, the backward pass and an FP8 forward.
  *
  * The library computes, for bf16 tensors in [batch, seq, heads, d_head]
  * layout (the layout of the input generator on "Flash Attention 2 Chapter2",
@@ -38,7 +39,9 @@ extern "C" {
 
 #define FA_OK 0
 #define FA_ERR_INVALID_ARG (-1)  /* null pointer, negative size, bad scale, B*H too large */
-#define FA_ERR_UNSUPPORTED (-2)  /* d_head not in {64, 128}, or no sm_103a device       */
+#define FA_ERR_UNSUPPORTED (-2)  /* d_head not in {64, 128} (FP8: not 128), or no sm_103a
+                                    device, or the device's shared-memory window does not
+                                    fit the backward kernel's layout (fa_check_status)   */
 #define FA_ERR_ALIGN (-3)        /* a tensor pointer is not 16-byte aligned             */
 #define FA_ERR_CUDA (-4)         /* a CUDA call failed; fa_last_cuda_error() has it     */
 #define FA_ERR_TIMEOUT (-5)      /* a device-side wait gave up (fa_check_status)        */
