@@ -42,6 +42,7 @@ EXPORTS = (
     "fa_selftest_wait_timeout", "fa_version", "fa_splitkv_num_splits",
     "fa_splitkv_workspace_bytes", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc",
     "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_varlen", "fa_fp8_sizes", "fa_quantize_fp8", "fa_fwd_fp8",
+    "fa_fp8_varlen_sizes", "fa_quantize_fp8_varlen", "fa_fwd_fp8_varlen",
 )
 
 
@@ -95,6 +96,11 @@ def lib() -> ctypes.CDLL:
         L.fa_fp8_sizes.argtypes = [ci, ci, ci, ci, ci, ci, ctypes.POINTER(ctypes.c_longlong)]
         L.fa_quantize_fp8.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, vp]
         L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp]
+        L.fa_fp8_varlen_sizes.argtypes = [ci, ci, ci, ci, ci, ci, ci, ci, ctypes.POINTER(ctypes.c_longlong)]
+        L.fa_quantize_fp8_varlen.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp,
+                                             vp, vp]
+        L.fa_fwd_fp8_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf,
+                                        ci, vp]
         for name in EXPORTS:
             if name != "fa_strerror":
                 getattr(L, name).restype = ci
@@ -180,6 +186,27 @@ def fa_fwd_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, o, lse, B, Nq, Nk, H, Hk,
                stream) -> int:
     return lib().fa_fwd_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, o, lse, B, Nq, Nk, H, Hk, d, scale,
                             flags, stream)
+
+
+def fp8_varlen_sizes(B, total_q, total_k, max_seqlen_q, max_seqlen_k, H, Hk, d):
+    """fp8_sizes for packed sequences (the layouts of fa_quantize_fp8_varlen)."""
+    out = (ctypes.c_longlong * 6)()
+    rc = lib().fa_fp8_varlen_sizes(B, total_q, total_k, max_seqlen_q, max_seqlen_k, H, Hk, d, out)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fp8_varlen_sizes")
+    return tuple(int(x) for x in out)
+
+
+def fa_quantize_fp8_varlen(q, k, v, cu_q, cu_k, B, total_q, total_k, max_q, max_k, H, Hk, d, q8, k8, vt8,
+                           q_scale, k_scale, v_scale, stream) -> int:
+    return lib().fa_quantize_fp8_varlen(q, k, v, cu_q, cu_k, B, total_q, total_k, max_q, max_k, H, Hk, d, q8, k8,
+                                        vt8, q_scale, k_scale, v_scale, stream)
+
+
+def fa_fwd_fp8_varlen(q8, k8, vt8, q_scale, k_scale, v_scale, o, lse, cu_q, cu_k, B, total_q, total_k, max_q,
+                      max_k, H, Hk, d, scale, flags, stream) -> int:
+    return lib().fa_fwd_fp8_varlen(q8, k8, vt8, q_scale, k_scale, v_scale, o, lse, cu_q, cu_k, B, total_q,
+                                   total_k, max_q, max_k, H, Hk, d, scale, flags, stream)
 
 
 def fa_check_status(stream=None):
@@ -508,6 +535,70 @@ def quantize_fp8(q, k, v, stream=None):
     if rc != FA_OK:
         raise FaError(rc, "fa_quantize_fp8")
     return Fp8Tensors(q8, k8, vt8, qs, ks, vs, (B, Nq, Nk, H, Hk, d))
+
+
+class Fp8VarlenTensors:
+    """e4m3 codes and scales of packed sequences (see quantize_fp8_varlen)."""
+
+    def __init__(self, q8, k8, vt8, q_scale, k_scale, v_scale, cu_seqlens_q, cu_seqlens_k, shape):
+        self.q8, self.k8, self.vt8 = q8, k8, vt8
+        self.q_scale, self.k_scale, self.v_scale = q_scale, k_scale, v_scale
+        self.cu_seqlens_q, self.cu_seqlens_k = cu_seqlens_q, cu_seqlens_k
+        (self.B, self.total_q, self.total_k, self.max_seqlen_q, self.max_seqlen_k,
+         self.H, self.Hk, self.d) = shape
+
+
+def quantize_fp8_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, stream=None):
+    """Block-quantise packed bf16 q [total_q, H, d], k/v [total_k, Hk, d] per sequence (d = 128)."""
+    import torch
+    total_q, H, d = q.shape
+    total_k, Hk = k.shape[0], k.shape[1]
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+    _check_tensor("cu_seqlens_q", cu_seqlens_q, torch.int32, 1)
+    _check_tensor("cu_seqlens_k", cu_seqlens_k, torch.int32, 1)
+    B = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != B + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k differ in length")
+    shape = (B, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), H, Hk, d)
+    n_q8, n_k8, n_vt8, n_qs, n_ks, n_vs = fp8_varlen_sizes(*shape)
+    dev = q.device
+    q8 = torch.empty(max(n_q8, 16), dtype=torch.uint8, device=dev)
+    k8 = torch.empty(max(n_k8, 16), dtype=torch.uint8, device=dev)
+    vt8 = torch.empty(max(n_vt8, 16), dtype=torch.uint8, device=dev)
+    qs = torch.empty(max(n_qs, 1), dtype=torch.float32, device=dev)
+    ks = torch.empty(max(n_ks, 1), dtype=torch.float32, device=dev)
+    vs = torch.empty(max(n_vs, 1), dtype=torch.float32, device=dev)
+    with _on_device(dev):
+        rc = fa_quantize_fp8_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), cu_seqlens_q.data_ptr(),
+                                    cu_seqlens_k.data_ptr(), *shape, q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(),
+                                    qs.data_ptr(), ks.data_ptr(), vs.data_ptr(), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_quantize_fp8_varlen")
+    return Fp8VarlenTensors(q8, k8, vt8, qs, ks, vs, cu_seqlens_q, cu_seqlens_k, shape)
+
+
+def forward_fp8_varlen(t, scale=None, causal=False, out=None, lse=None, stream=None):
+    """FP8 forward on Fp8VarlenTensors t; returns (o bf16 [total_q, H, d], lse fp32 [B, H, max_seqlen_q])."""
+    import torch
+    dev = t.q8.device
+    if scale is None:
+        scale = 1.0 / math.sqrt(t.d)
+    out = torch.empty((t.total_q, t.H, t.d), dtype=torch.bfloat16, device=dev) if out is None else out
+    lse = torch.empty((t.B, t.H, t.max_seqlen_q), dtype=torch.float32, device=dev) if lse is None else lse
+    # Empty outputs (no query rows) still pass non-null pointers.
+    o_arg = out if out.numel() else torch.empty(16, dtype=torch.bfloat16, device=dev)
+    lse_arg = lse if lse.numel() else torch.empty(1, dtype=torch.float32, device=dev)
+    with _on_device(dev):
+        rc = fa_fwd_fp8_varlen(t.q8.data_ptr(), t.k8.data_ptr(), t.vt8.data_ptr(), t.q_scale.data_ptr(),
+                               t.k_scale.data_ptr(), t.v_scale.data_ptr(), o_arg.data_ptr(), lse_arg.data_ptr(),
+                               t.cu_seqlens_q.data_ptr(), t.cu_seqlens_k.data_ptr(), t.B, t.total_q, t.total_k,
+                               t.max_seqlen_q, t.max_seqlen_k, t.H, t.Hk, t.d, float(scale),
+                               FA_FLAG_CAUSAL if causal else 0, _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_fp8_varlen")
+    return out, lse
 
 
 def forward_fp8(t, scale=None, causal=False, out=None, lse=None, stream=None):

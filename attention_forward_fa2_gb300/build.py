@@ -21,7 +21,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfa_gb300.so")
 UNITS = ("fa_api.cu", "fa_fwd_d128.cu", "fa_fwd_d128_bc64.cu", "fa_fwd_d128_causal.cu",
          "fa_fwd_d64.cu", "fa_fwd_d64_bc64.cu", "fa_fwd_d64_causal.cu", "fa_fwd_quad.cu",
-         "fa_fwd_split.cu", "fa_static_scratch.cu", "fa_bwd.cu", "fa_fp8.cu")
+         "fa_fwd_split.cu", "fa_static_scratch.cu", "fa_bwd.cu", "fa_fp8.cu",
+         "fa_fp8_varlen.cu")
 HEADERS = ("ptx.cuh", "fa_fwd_kernel.cuh", "fa_launch.h", "fa_combine.cuh", "fa_bwd_kernel.cuh")
 
 NVCC_FLAGS = [

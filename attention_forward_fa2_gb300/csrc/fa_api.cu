@@ -326,6 +326,7 @@ int prepare(const Problem& P, const Config& cfg, DeviceState* st, fa::LaunchArgs
   p.status = st->status;
   p.num_splits = 1;
   p.split_tiles = 0;
+  p.total_q = p.total_k = 0x7fffffff;  // packed row counts are not passed to the bf16 forms
   a.stream = P.stream;
   return FA_OK;
 }
@@ -580,6 +581,24 @@ int fp8_check_shape(int B, int Nq, int Nk, int H, int Hk, int d) {
   return FA_OK;
 }
 
+// Variable-length FP8: columns of the transposed V codes (the start column of
+// a sequence b = B past the last one).
+long long fp8_vt_cols(int B, int total_k) { return fa::fp8_vt_col0(total_k, B); }
+
+int fp8_check_varlen(int B, int total_q, int total_k, int max_q, int max_k, int H, int Hk, int d) {
+  const int rc = fp8_check_shape(B, max_q, max_k, H, Hk, d);
+  if (rc != FA_OK) return rc;
+  if (total_q < 0 || total_k < 0) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(total_q) * H > 0x7fffffffLL || static_cast<long long>(total_k) * Hk > 0x7fffffffLL)
+    return FA_ERR_INVALID_ARG;
+  if (fp8_vt_cols(B, total_k) > 0x7fffffffLL - 256) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+bool misaligned4(const void* a, const void* b, const void* c) {
+  return ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b) | reinterpret_cast<uintptr_t>(c)) & 3u) != 0;
+}
+
 __global__ void wait_timeout_kernel(unsigned long long timeout_ns, int* status) {
   __shared__ __align__(8) unsigned long long bar;
   __shared__ int abort_flag;
@@ -812,7 +831,8 @@ int fa_quantize_fp8(const void* q, const void* k, const void* v, int B, int Nq, 
   if ((rc = device_state(&st)) != FA_OK) return rc;
   fa::Fp8QuantParams p{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
                        static_cast<const __nv_bfloat16*>(v), static_cast<uint8_t*>(q8), static_cast<uint8_t*>(k8),
-                       static_cast<uint8_t*>(vt8), q_scale, k_scale, v_scale, B, Nq, Nk, H, Hk, d, fp8_nk_pad(Nk)};
+                       static_cast<uint8_t*>(vt8), q_scale, k_scale, v_scale, B, Nq, Nk, H, Hk, d, fp8_nk_pad(Nk),
+                       nullptr, nullptr, 0, 0, 0};
   const cudaError_t e = fa::launch_fp8_quantize(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
@@ -857,6 +877,92 @@ int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_s
   a.p.k_blocks = (Nk + fa::kBR - 1) / fa::kBR;
   a.grid = dim3(static_cast<unsigned>(a.p.num_items < st->num_sms ? a.p.num_items : st->num_sms), 1, 1);
   const cudaError_t e = fa::launch_fwd_fp8((flags & FA_FLAG_CAUSAL) != 0, a);
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+int fa_fp8_varlen_sizes(int B, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int H, int Hk,
+                        int d, long long* sizes) {
+  if (!sizes) return FA_ERR_INVALID_ARG;
+  const int rc = fp8_check_varlen(B, total_q, total_k, max_seqlen_q, max_seqlen_k, H, Hk, d);
+  if (rc != FA_OK) return rc;
+  const long long qb = (max_seqlen_q + fa::kBR - 1) / fa::kBR, kb = (max_seqlen_k + fa::kBR - 1) / fa::kBR;
+  sizes[0] = static_cast<long long>(total_q) * H * d;
+  sizes[1] = static_cast<long long>(total_k) * Hk * d;
+  sizes[2] = static_cast<long long>(Hk) * d * fp8_vt_cols(B, total_k);
+  sizes[3] = static_cast<long long>(B) * H * qb;
+  sizes[4] = static_cast<long long>(B) * Hk * kb;
+  sizes[5] = static_cast<long long>(B) * Hk;
+  return FA_OK;
+}
+
+int fa_quantize_fp8_varlen(const void* q, const void* k, const void* v, const int* cu_seqlens_q,
+                           const int* cu_seqlens_k, int B, int total_q, int total_k, int max_seqlen_q,
+                           int max_seqlen_k, int H, int Hk, int d, void* q8, void* k8, void* vt8, float* q_scale,
+                           float* k_scale, float* v_scale, void* stream) {
+  int rc = fp8_check_varlen(B, total_q, total_k, max_seqlen_q, max_seqlen_k, H, Hk, d);
+  if (rc != FA_OK) return rc;
+  if (B == 0 || H == 0) return FA_OK;
+  if (!cu_seqlens_q || !cu_seqlens_k || !vt8 || !v_scale) return FA_ERR_INVALID_ARG;
+  if ((total_q > 0 && (!q || !q8)) || (max_seqlen_q > 0 && !q_scale) || (total_k > 0 && (!k || !v || !k8)) ||
+      (max_seqlen_k > 0 && !k_scale))
+    return FA_ERR_INVALID_ARG;
+  for (const void* ptr : {q, k, v, static_cast<const void*>(q8), static_cast<const void*>(k8), static_cast<const void*>(vt8)})
+    if (ptr && !aligned16(ptr)) return FA_ERR_ALIGN;
+  if (misaligned4(q_scale, k_scale, v_scale) || misaligned4(cu_seqlens_q, cu_seqlens_k, nullptr)) return FA_ERR_ALIGN;
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != FA_OK) return rc;
+  fa::Fp8QuantParams p{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+                       static_cast<const __nv_bfloat16*>(v), static_cast<uint8_t*>(q8), static_cast<uint8_t*>(k8),
+                       static_cast<uint8_t*>(vt8), q_scale, k_scale, v_scale, B, max_seqlen_q, max_seqlen_k, H, Hk,
+                       d, 0, cu_seqlens_q, cu_seqlens_k, total_q, total_k, fp8_vt_cols(B, total_k)};
+  const cudaError_t e = fa::launch_fp8_quantize(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+int fa_fwd_fp8_varlen(const void* q8, const void* k8, const void* vt8, const float* q_scale, const float* k_scale,
+                      const float* v_scale, void* o, float* lse, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                      int B, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int H, int Hk, int d,
+                      float scale, int flags, void* stream) {
+  int rc = fp8_check_varlen(B, total_q, total_k, max_seqlen_q, max_seqlen_k, H, Hk, d);
+  if (rc != FA_OK) return rc;
+  if (!cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARG;
+  Problem P{q8, k8, vt8, o, lse, B, max_seqlen_q, max_seqlen_k, H, Hk, d, scale, cu_seqlens_q, cu_seqlens_k, flags,
+            static_cast<cudaStream_t>(stream)};
+  rc = validate(P);
+  if (rc != FA_OK) return rc == 1 ? FA_OK : rc;
+  if (total_q == 0) return FA_OK;  // no query rows
+  if (!q_scale || !k_scale || !v_scale) return FA_ERR_INVALID_ARG;
+  if (misaligned4(q_scale, k_scale, v_scale)) return FA_ERR_ALIGN;
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != FA_OK) return rc;
+  fa::LaunchArgs a;
+  const Config cfg{128, 2, 2, 8.f, 0};
+  if ((rc = prepare(P, cfg, st, a)) != FA_OK) return rc;
+  // e4m3 maps over the packed rows (exact extents: a tile that runs past the
+  // last sequence reads the TMA zero fill) and over the V^T columns.
+  const long long kp = fp8_vt_cols(B, total_k);
+  const cuuint64_t tk = total_k > 0 ? (cuuint64_t)total_k : 1;  // no key is read when total_k == 0
+  cuuint64_t dq[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)total_q};
+  cuuint64_t sq[2] = {(cuuint64_t)d, (cuuint64_t)H * d};
+  cuuint64_t dk[3] = {(cuuint64_t)d, (cuuint64_t)Hk, tk};
+  cuuint64_t sk[2] = {(cuuint64_t)d, (cuuint64_t)Hk * d};
+  cuuint64_t dv[3] = {(cuuint64_t)kp, (cuuint64_t)d, (cuuint64_t)Hk};
+  cuuint64_t sv[2] = {(cuuint64_t)kp, (cuuint64_t)d * kp};
+  cuuint32_t box_q[3] = {128, 1, (cuuint32_t)fa::kBR};
+  cuuint32_t box_k[3] = {128, 1, (cuuint32_t)fa::kBC};
+  cuuint32_t box_v[3] = {(cuuint32_t)fa::kBC, 128, 1};
+  if ((rc = encode(&a.tm_q, q8, 3, dq, sq, box_q, CU_TENSOR_MAP_DATA_TYPE_UINT8)) != FA_OK) return rc;
+  if ((rc = encode(&a.tm_k, k8, 3, dk, sk, box_k, CU_TENSOR_MAP_DATA_TYPE_UINT8)) != FA_OK) return rc;
+  if ((rc = encode(&a.tm_v, vt8, 3, dv, sv, box_v, CU_TENSOR_MAP_DATA_TYPE_UINT8)) != FA_OK) return rc;
+  a.p.q_scale = q_scale;
+  a.p.k_scale = k_scale;
+  a.p.v_scale = v_scale;
+  a.p.q_blocks = (max_seqlen_q + fa::kBR - 1) / fa::kBR;
+  a.p.k_blocks = (max_seqlen_k + fa::kBR - 1) / fa::kBR;
+  a.p.total_q = total_q;
+  a.p.total_k = total_k;
+  a.grid = dim3(static_cast<unsigned>(a.p.num_items < st->num_sms ? a.p.num_items : st->num_sms), 1, 1);
+  const cudaError_t e = fa::launch_fwd_fp8_varlen((flags & FA_FLAG_CAUSAL) != 0, a);
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 

@@ -8,6 +8,15 @@
 // Q, 128 keys of one key/value head for K, one whole key/value head for V.
 // V is written transposed, [B, Hk, d, nk_pad] with nk_pad = Nk rounded up to
 // 16 (zero padding), so that it is a K-major operand of O += P V.
+//
+// Variable-length batches: Q and K codes keep the packed row layout, and the
+// blocks restart at every sequence (block j of sequence b covers its rows
+// 128j .. 128j + 127; scales [B, H, ceil(max_q / 128)] and [B, Hk,
+// ceil(max_k / 128)], scale 1 for blocks past a sequence's end; V scales
+// [B, Hk]).  The transposed V codes are [Hk, d, kp_total]: sequence b owns
+// columns [fp8_vt_col0(cu_k[b], b), fp8_vt_col0(cu_k[b + 1], b + 1)), its keys
+// first and zeros after them, so each sequence starts on a 16-byte boundary
+// (the TMA rule for the innermost coordinate) and every column is written.
 #include <cuda_bf16.h>
 
 #include "fa_launch.h"
@@ -53,7 +62,22 @@ __device__ __forceinline__ float amax8(uint4 u) {
 // block's scale.  K blocks also reduce the same rows of V and fold them into
 // the per-head V maximum (non-negative floats order like their bit patterns,
 // so an integer atomicMax on the bits is exact and order-independent).
-template <int D>
+// Rows of sequence b in the packed tensors (variable length; an inconsistent
+// entry counts as empty, so nothing outside the tensors is touched) or of
+// batch b (dense).
+template <bool VARLEN>
+__device__ __forceinline__ void fp8_seq(const int* cu, int max_len, int total, int b, int& row0, int& len) {
+  if constexpr (VARLEN) {
+    row0 = cu[b];
+    len = cu[b + 1] - row0;
+    if (len < 0 || len > max_len || row0 < 0 || row0 > total - len) len = 0;
+  } else {
+    row0 = b * max_len;
+    len = max_len;
+  }
+}
+
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(256) fp8_quant_qk_kernel(Fp8QuantParams p, unsigned int* v_amax_bits) {
   static_assert(D == 128, "16 chunks of 16 bytes per row");
   const int qb = (p.Nq + kBR - 1) / kBR, kb = (p.Nk + kBR - 1) / kBR;
@@ -62,11 +86,13 @@ __global__ void __launch_bounds__(256) fp8_quant_qk_kernel(Fp8QuantParams p, uns
   const bool isq = id < nq;
   if (!isq) id -= nq;
   const int blocks = isq ? qb : kb;
-  const int Hx = isq ? p.H : p.Hk, Nx = isq ? p.Nq : p.Nk;
+  const int Hx = isq ? p.H : p.Hk;
   const int blk = static_cast<int>(id % blocks);
   const long long bh = id / blocks;
   const int h = static_cast<int>(bh % Hx), b = static_cast<int>(bh / Hx);
-  const int r0 = blk * kBR, rows = min(Nx - r0, kBR);
+  int seq0, len;
+  fp8_seq<VARLEN>(isq ? p.cu_q : p.cu_k, isq ? p.Nq : p.Nk, isq ? p.total_q : p.total_k, b, seq0, len);
+  const int r0 = blk * kBR, rows = min(len - r0, kBR);  // <= 0: a block past the sequence (scale 1)
   const __nv_bfloat16* src = isq ? p.q : p.k;
   uint8_t* dst = isq ? p.q8 : p.k8;
   uint4 x[8];
@@ -77,7 +103,7 @@ __global__ void __launch_bounds__(256) fp8_quant_qk_kernel(Fp8QuantParams p, uns
     const int r = e >> 4, c = e & 15;
     x[i] = make_uint4(0u, 0u, 0u, 0u);
     if (r < rows) {
-      const size_t off = ((static_cast<size_t>(b) * Nx + r0 + r) * Hx + h) * D + c * 8;
+      const size_t off = ((static_cast<size_t>(seq0) + r0 + r) * Hx + h) * D + c * 8;
       x[i] = *reinterpret_cast<const uint4*>(src + off);
       m = fmaxf(m, amax8(x[i]));
       if (!isq) mv = fmaxf(mv, amax8(*reinterpret_cast<const uint4*>(p.v + off)));
@@ -104,7 +130,7 @@ __global__ void __launch_bounds__(256) fp8_quant_qk_kernel(Fp8QuantParams p, uns
                     a3 = __uint_as_float(w[2 * half + 1] & 0xffff0000u) / s;
         o[half] = to_e4m3x2(a0, a1) | (to_e4m3x2(a2, a3) << 16);
       }
-      const size_t off = ((static_cast<size_t>(b) * Nx + r0 + r) * Hx + h) * D + c * 8;
+      const size_t off = ((static_cast<size_t>(seq0) + r0 + r) * Hx + h) * D + c * 8;
       *reinterpret_cast<uint2*>(dst + off) = make_uint2(o[0], o[1]);
     }
   }
@@ -123,7 +149,7 @@ __global__ void fp8_v_scale_kernel(Fp8QuantParams p, const unsigned int* v_amax_
 // consecutive keys).  The words go through shared memory in feature-major
 // rows of 17 words (conflict-free for both phases) and leave as coalesced
 // 4-byte stores of the transposed rows.
-template <int D>
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(256) fp8_quant_vt_kernel(Fp8QuantParams p, const unsigned int* v_amax_bits) {
   static_assert(D == 128, "16 chunks of 8 features per key");
   constexpr int kRowWords = 17;  // 16 words of 4 keys, one word of padding
@@ -132,14 +158,25 @@ __global__ void __launch_bounds__(256) fp8_quant_vt_kernel(Fp8QuantParams p, con
   const int bh = blockIdx.y;  // b * Hk + hk
   const int h = bh % p.Hk, b = bh / p.Hk;
   const float s = scale_of(__uint_as_float(v_amax_bits[bh]));
+  int seq0, len;
+  fp8_seq<VARLEN>(p.cu_k, p.Nk, p.total_k, b, seq0, len);
+  // Columns this sequence owns (keys, then zeros).
+  long long col0 = 0;
+  int span = p.nk_pad;
+  if constexpr (VARLEN) {
+    col0 = fp8_vt_col0(p.cu_k[b], b);
+    const long long end = min(fp8_vt_col0(p.cu_k[b + 1], b + 1), p.kp_total);
+    span = col0 >= 0 && end > col0 ? static_cast<int>(min(end - col0, 64LL * gridDim.x)) : 0;
+  }
+  if (kt * 64 >= span) return;
   const int chunk = threadIdx.x & 15, kg = threadIdx.x >> 4;
   uint32_t q2[4][4];  // [key][feature pair]: e4m3 codes of features 2i (low byte) and 2i+1
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int key = kt * 64 + 4 * kg + k;
     uint4 u = make_uint4(0u, 0u, 0u, 0u);
-    if (key < p.Nk)
-      u = *reinterpret_cast<const uint4*>(p.v + ((static_cast<size_t>(b) * p.Nk + key) * p.Hk + h) * D + chunk * 8);
+    if (key < len)
+      u = *reinterpret_cast<const uint4*>(p.v + ((static_cast<size_t>(seq0) + key) * p.Hk + h) * D + chunk * 8);
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -157,13 +194,14 @@ __global__ void __launch_bounds__(256) fp8_quant_vt_kernel(Fp8QuantParams p, con
   for (int e = threadIdx.x; e < D * 16; e += 256) {
     const int c = e >> 4, wd = e & 15;
     const int key0 = kt * 64 + 4 * wd;
-    // nk_pad is a multiple of 16: a word is wholly inside or outside the padded row.
-    if (key0 < p.nk_pad)
-      *reinterpret_cast<uint32_t*>(p.vt8 + (static_cast<size_t>(bh) * D + c) * p.nk_pad + key0) = tile[c * kRowWords + wd];
+    // Spans are multiples of 16 keys: a word is wholly inside or outside.
+    if (key0 < span) {
+      const size_t row = VARLEN ? static_cast<size_t>(h) * D + c : static_cast<size_t>(bh) * D + c;
+      const size_t pitch = VARLEN ? static_cast<size_t>(p.kp_total) : static_cast<size_t>(p.nk_pad);
+      *reinterpret_cast<uint32_t*>(p.vt8 + row * pitch + col0 + key0) = tile[c * kRowWords + wd];
+    }
   }
 }
-
-constexpr int kFp8Stages = 4;
 
 template <bool CAUSAL>
 cudaError_t launch_fwd_fp8_impl(const LaunchArgs& a) {
@@ -186,15 +224,24 @@ cudaError_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream) {
   const long long bhk = static_cast<long long>(p.B) * p.Hk;
   cudaError_t e = cudaMemsetAsync(v_amax_bits, 0, static_cast<size_t>(bhk) * sizeof(unsigned int), stream);
   if (e != cudaSuccess) return e;
+  const bool varlen = p.cu_q != nullptr;
   const long long qb = (p.Nq + kBR - 1) / kBR, kb = (p.Nk + kBR - 1) / kBR;
   const long long nblocks = static_cast<long long>(p.B) * p.H * qb + bhk * kb;
   if (nblocks > 0) {
-    fp8_quant_qk_kernel<128><<<static_cast<unsigned>(nblocks), 256, 0, stream>>>(p, v_amax_bits);
+    if (varlen)
+      fp8_quant_qk_kernel<128, true><<<static_cast<unsigned>(nblocks), 256, 0, stream>>>(p, v_amax_bits);
+    else
+      fp8_quant_qk_kernel<128, false><<<static_cast<unsigned>(nblocks), 256, 0, stream>>>(p, v_amax_bits);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  const int kt = (p.nk_pad + 63) / 64;
-  if (kt > 0) {
-    fp8_quant_vt_kernel<128><<<dim3(static_cast<unsigned>(kt), static_cast<unsigned>(bhk)), 256, 0, stream>>>(p, v_amax_bits);
+  // Variable length: a sequence's span is at most its length + 31 columns.
+  const int kt = varlen ? (p.Nk + 31 + 63) / 64 : (p.nk_pad + 63) / 64;
+  if (kt > 0 && bhk > 0) {
+    const dim3 grid(static_cast<unsigned>(kt), static_cast<unsigned>(bhk));
+    if (varlen)
+      fp8_quant_vt_kernel<128, true><<<grid, 256, 0, stream>>>(p, v_amax_bits);
+    else
+      fp8_quant_vt_kernel<128, false><<<grid, 256, 0, stream>>>(p, v_amax_bits);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   fp8_v_scale_kernel<<<static_cast<unsigned>((bhk + 255) / 256), 256, 0, stream>>>(p, v_amax_bits);

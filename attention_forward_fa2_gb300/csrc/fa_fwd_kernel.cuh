@@ -70,7 +70,11 @@
 // (32 elements per instruction), the scales fold into the exp2 coefficient of
 // each key tile (the row maximum is then kept in scaled log2 units), P is
 // rounded to e4m3 (four per TMEM column) for O += P V, and the V scale joins
-// the final 1/l.
+// the final 1/l.  Variable-length FP8 batches keep every tile at a multiple of
+// 128 rows from its sequence's start (no shifted last tile), so that a tile is
+// exactly one quantisation block; rows read past a sequence's end belong to
+// the next sequence or to the TMA zero fill and are masked (keys) or never
+// stored (queries).
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -135,6 +139,7 @@ struct FwdParams {
   const float* k_scale;        // FP8: [B, Hk, k_blocks] of 128 keys
   const float* v_scale;        // FP8: [B, Hk] of a key/value head
   int q_blocks, k_blocks;
+  int total_q, total_k;        // variable-length form: packed rows (sequences past them are rejected)
   unsigned long long timeout_ns;
   int* status;                 // [4]: code, block, warp, site
 };
@@ -187,20 +192,29 @@ struct SmemLayout {
   static_assert(kAlloc <= 232448, "shared memory budget exceeded");
 };
 
+// First column of sequence b in the variable-length FP8 V^T codes: its packed
+// key offset rounded up to 16 plus 16 per earlier sequence.  Sequence b then
+// starts 16-byte aligned and its keys, rounded up to 16, end at or before the
+// start of sequence b + 1 (ceil((x + n) / 16) >= ceil(x / 16) + ceil(n / 16) - 1).
+__host__ __device__ __forceinline__ long long fp8_vt_col0(long long cu_b, int b) {
+  return (cu_b + 15) / 16 * 16 + 16LL * b;
+}
+
 // Geometry of one 128-row tile along the sequence axis.  `load_row` is the
 // first row the TMA box reads; rows [lo, hi) of the box are valid.  In the
-// variable-length form a tile that would run past the end of its sequence is
-// shifted back so that it ends exactly at the end, never touching memory past
-// the last row of the packed tensor (rows before the sequence are masked).
+// variable-length form (SHIFT) a tile that would run past the end of its
+// sequence is shifted back so that it ends exactly at the end, never touching
+// memory past the last row of the packed tensor (rows before the sequence are
+// masked).
 struct RowWindow {
   int load_row;
   int lo, hi;
 };
 
-template <bool VARLEN>
+template <bool SHIFT>
 __device__ __forceinline__ RowWindow make_window(int seq_start, int seq_end, int row0, int rows) {
   RowWindow w;
-  if (!VARLEN || row0 + rows <= seq_end) {
+  if (!SHIFT || row0 + rows <= seq_end) {
     w.load_row = row0;
     w.lo = 0;
     w.hi = min(rows, seq_end - row0);
@@ -232,7 +246,8 @@ struct Unit {
 };
 
 // Every role decodes the same unit identically (pure function of u and params).
-template <int BC, bool VARLEN, bool CAUSAL, bool SPLIT>
+// SHIFT: variable-length tiles at a sequence's end are shifted back (make_window).
+template <int BC, bool VARLEN, bool CAUSAL, bool SPLIT, bool SHIFT = VARLEN>
 __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   Unit w;
   w.split = 0;
@@ -263,7 +278,8 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
     w.k_start = p.cu_k[w.b];
     w.k_end = p.cu_k[w.b + 1];
     const int len_q = w.q_end - w.q_start, len_k = w.k_end - w.k_start;
-    bad = len_q < 0 || len_k < 0 || len_q > p.Nq || len_k > p.Nk || w.q_start < 0 || w.k_start < 0;
+    bad = len_q < 0 || len_k < 0 || len_q > p.Nq || len_k > p.Nk || w.q_start < 0 || w.k_start < 0 ||
+          w.q_start > p.total_q - len_q || w.k_start > p.total_k - len_k;
   }
   w.q_row0 = w.q_start + mb * (kBR * p.qtiles);
   w.off = (w.k_end - w.k_start) - (w.q_end - w.q_start);
@@ -277,7 +293,7 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
 #pragma unroll
   for (int t = 0; t < kQT; ++t) {
     const int r0 = w.q_row0 + t * kBR;
-    w.qwin[t] = make_window<VARLEN>(w.q_start, w.q_end, r0, kBR);
+    w.qwin[t] = make_window<SHIFT>(w.q_start, w.q_end, r0, kBR);
     const bool rows = has_rows && t < p.qtiles && r0 < w.q_end;
     int n = nkv_here;
     if (CAUSAL && rows) {
@@ -316,7 +332,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const FwdParams p) {
   using L = SmemLayout<D, BC, STAGES, FP8 ? 1 : 2>;
   static_assert(D == 64 || D == 128, "head dim");
-  static_assert(!FP8 || (D == 128 && BC == 128 && !VARLEN && !SPLIT && !QUAD), "FP8: d 128, dense");
+  static_assert(!FP8 || (D == 128 && BC == 128 && !SPLIT && !QUAD), "FP8: d 128, 128-key tiles");
+  // Variable-length tiles: shifted at a sequence's end, except FP8 ones (which
+  // must coincide with quantisation blocks).
+  constexpr bool kShift = VARLEN && !FP8;
   static_assert(BC == 64 || BC == 128, "key tile");
   static_assert(2 * BC + 2 * D <= 512, "TMEM columns");
   static_assert(!QUAD || (BC == 128 && !CAUSAL && !SPLIT), "quad reduction: 128-key tiles, no mask or split");
@@ -384,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
 #pragma unroll 1
       FA_FOR_EACH_UNIT(u) {
-        const Unit w = decode_unit<BC, VARLEN, CAUSAL, SPLIT>(p, u);
+        const Unit w = decode_unit<BC, VARLEN, CAUSAL, SPLIT, kShift>(p, u);
         if (!w.run) continue;
         // Q of this unit, once the previous unit's S MMAs no longer read it.
         if (!ptx::mbar_wait(bar(L::kBarQEmpty), (qcount & 1u) ^ 1u, s_abort, tmo)) {
@@ -422,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++g;
           const uint32_t sbase = base + L::kOffKV + slot * L::kSlotBytes;
           if (j < w.nkv) {
-            const RowWindow kw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + (w.j0 + j) * BC, BC);
+            const RowWindow kw = make_window<kShift>(w.k_start, w.k_end, w.k_start + (w.j0 + j) * BC, BC);
 #pragma unroll
             for (int pnl = 0; pnl < kDPanels; ++pnl) {
               const uint32_t dst = sbase + pnl * L::kKVPanelBytes;
@@ -433,9 +452,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (j >= 1) {
-            const RowWindow vw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + (w.j0 + j - 1) * BC, BC);
-            if constexpr (FP8) {
-              // V^T tile: d rows x 128 keys (one box, keys innermost).
+            const RowWindow vw = make_window<kShift>(w.k_start, w.k_end, w.k_start + (w.j0 + j - 1) * BC, BC);
+            if constexpr (FP8 && VARLEN) {
+              // V^T tile: d rows x 128 keys (one box, keys innermost) from the sequence's columns.
+              const int col = static_cast<int>(fp8_vt_col0(w.k_start, w.b)) + (vw.load_row - w.k_start);
+              ptx::tma_load_3d(sbase + L::kKVTileBytes, &tm_v, bar(L::kBarKVFull + slot), col, 0, w.hk);
+            } else if constexpr (FP8) {
               ptx::tma_load_4d(sbase + L::kKVTileBytes, &tm_v, bar(L::kBarKVFull + slot), vw.load_row, 0, w.hk, w.b);
             } else {
 #pragma unroll
@@ -469,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
 #pragma unroll 1
       FA_FOR_EACH_UNIT(u) {
-        const Unit w = decode_unit<BC, VARLEN, CAUSAL, SPLIT>(p, u);
+        const Unit w = decode_unit<BC, VARLEN, CAUSAL, SPLIT, kShift>(p, u);
         if (!w.run) continue;
         if (!ptx::mbar_wait(bar(L::kBarQFull), qcount & 1u, s_abort, tmo)) {
           record_error(p.status, kErrTimeout, kSiteMmaQ);
@@ -587,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
 #pragma unroll 1
     FA_FOR_EACH_UNIT(u) {
-      const Unit w = decode_unit<BC, VARLEN, CAUSAL, SPLIT>(p, u);
+      const Unit w = decode_unit<BC, VARLEN, CAUSAL, SPLIT, kShift>(p, u);
       const bool active = t == 0 ? w.active[0] : w.active[1];
       if (!active) continue;
       const RowWindow qw = t == 0 ? w.qwin[0] : w.qwin[1];
@@ -642,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 s[2 * h + 1][k + 1] = __uint_as_float(raw[2 * h + ch][4 * g + 3]);
               }
           if (w.j0 + j >= j_mask) {
-            const RowWindow kw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + (w.j0 + j) * BC, BC);
+            const RowWindow kw = make_window<kShift>(w.k_start, w.k_end, w.k_start + (w.j0 + j) * BC, BC);
 #pragma unroll
             for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -745,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // FP8: dequantisation scales of this query tile and key/value head.
         float cq = 0.f, vsc = 1.f;
         if constexpr (FP8) {
-          cq = c2 * p.q_scale[(w.b * p.H + w.h) * p.q_blocks + qw.load_row / kBR];
+          cq = c2 * p.q_scale[(w.b * p.H + w.h) * p.q_blocks + (qw.load_row - w.q_start) / kBR];
           vsc = p.v_scale[w.b * (p.H / p.group) + w.hk];
         }
   #pragma unroll 1
@@ -769,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   #pragma unroll
             for (int c = 0; c < BC; ++c) s[c] = __uint_as_float(sr[c]);
             if (w.j0 + j >= j_mask) {
-              const RowWindow kw = make_window<VARLEN>(w.k_start, w.k_end, w.k_start + (w.j0 + j) * BC, BC);
+              const RowWindow kw = make_window<kShift>(w.k_start, w.k_end, w.k_start + (w.j0 + j) * BC, BC);
               if (kw.lo != 0 || kw.hi != BC) {
                 // Keys outside [lo, hi) of this tile: past the end, or (variable
                 // length) before the sequence start / already seen by the previous tile.
@@ -928,7 +950,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
 #pragma unroll 1
     FA_FOR_EACH_UNIT(u) {
-      const Unit w = decode_unit<BC, VARLEN, CAUSAL, SPLIT>(p, u);
+      const Unit w = decode_unit<BC, VARLEN, CAUSAL, SPLIT, kShift>(p, u);
       if (w.nokeys) {
         // No keys: o = 0 and LSE = -inf (log of an empty sum).
         const int rows = min(kBR * p.qtiles, w.q_end - w.q_row0);
@@ -978,7 +1000,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inv_l = s_invl[t * kBR + row];
         const uint32_t tO = tmem + lane_off + static_cast<uint32_t>(2 * BC + t * D);
         const RowWindow qw = w.qwin[t];
-        const bool warp_full = (wq << 5) >= qw.lo;  // every row of this warp is valid
+        const bool warp_full = (wq << 5) >= qw.lo && (wq << 5) + 32 <= qw.hi;  // every row of this warp is valid
         const bool use_tma = !SPLIT && (!VARLEN || warp_full);
         const bool row_ok = row >= qw.lo && row < qw.hi;
         // Row pointer for the direct-store path (only formed for valid rows).

@@ -93,16 +93,24 @@ struct BwdLaunchArgs {
 template <int D, bool CAUSAL, bool VARLEN>
 cudaError_t launch_bwd(const BwdLaunchArgs& a);
 
-// FP8 path (fa_fp8.cu).
+// FP8 path (fa_fp8.cu; the variable-length kernels in fa_fp8_varlen.cu).
 struct Fp8QuantParams {
   const __nv_bfloat16 *q, *k, *v;  // bf16 inputs, [B, Nq, H, D] and [B, Nk, Hk, D]
+                                   // (variable length: packed [total_q, H, D] / [total_k, Hk, D])
   uint8_t *q8, *k8;                // e4m3 codes, same layouts
   uint8_t* vt8;                    // e4m3 codes of V, [B, Hk, D, nk_pad]
+                                   // (variable length: [Hk, D, kp_total], sequence b from
+                                   // column fp8_vt_col0(cu_k[b], b))
   float *q_scale, *k_scale, *v_scale;
-  int B, Nq, Nk, H, Hk, D, nk_pad;
+  int B, Nq, Nk, H, Hk, D, nk_pad;  // variable length: Nq / Nk are the maximum lengths
+  const int *cu_q, *cu_k;           // variable length: int32 [B + 1] (null when dense)
+  int total_q, total_k;             // variable length: packed rows of q / k
+  long long kp_total;               // variable length: columns of vt8
 };
+constexpr int kFp8Stages = 4;  // K/V ring slots of the FP8 kernels
 cudaError_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream);
 cudaError_t launch_fwd_fp8(bool causal, const LaunchArgs& a);
+cudaError_t launch_fwd_fp8_varlen(bool causal, const LaunchArgs& a);
 int fp8_smem_bytes();
 
 // Merge of the key splits (fa_combine.cuh); D in {64, 128}.

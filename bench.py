@@ -24,7 +24,8 @@ cpu_baseline  the fp64 CPU oracle (test infrastructure) timed on a bounded
 
 --impl reference times that oracle as the reference arm (the pages ship no
 implementation; the oracle is the reference), printing the same JSON line.
---fp8 times the e4m3 forward (fa_fwd_fp8) on the workload quantised once
+--fp8 times the e4m3 forward (fa_fwd_fp8, or fa_fwd_fp8_varlen on the packed
+workload) on the workload quantised once
 beforehand (block scales; the quantisation is not timed), against the fp8
 dense peak taken as twice the measured bf16 one (the nominal ratio).
 --bwd times the backward pass instead (fa_bwd / fa_bwd_varlen, d = 64 or 128: preprocessing, key-block kernel,
@@ -34,6 +35,7 @@ against two).  Rank 0 prints one JSON line on stdout.
 from __future__ import annotations
 
 import argparse
+import copy
 import hashlib
 import json
 import math
@@ -343,7 +345,7 @@ def add_mode(cfg, args):
     if args.split:
         cfg["form"] = "key-split (fa_fwd_splitkv)"
     if getattr(args, "fp8", False):
-        cfg["form"] = "fp8 e4m3, block-quantised (fa_fwd_fp8)"
+        cfg["form"] = "fp8 e4m3, block-quantised (fa_fwd_fp8%s)" % ("_varlen" if "sequences" in cfg else "")
     return cfg
 
 
@@ -369,14 +371,15 @@ def run_ours(args, w):
 
     t8 = None
     if args.fp8:
-        if w.varlen or w.d != 128 or args.split:
-            raise SystemExit("--fp8 takes dense d = 128 workloads")
-        t8 = fa.quantize_fp8(dq, dk, dv)
+        if w.d != 128 or args.split:
+            raise SystemExit("--fp8 takes d = 128 workloads without --split")
+        t8 = (fa.quantize_fp8_varlen(dq, dk, dv, dcu, dcu, maxlen, maxlen) if w.varlen
+              else fa.quantize_fp8(dq, dk, dv))
         torch.cuda.synchronize(dev)
 
     def step_on(bq, bk, bv, bcu, bt8, bo, bl):
         if args.fp8:
-            fa.forward_fp8(bt8, causal=args.causal, out=bo, lse=bl)
+            (fa.forward_fp8_varlen if w.varlen else fa.forward_fp8)(bt8, causal=args.causal, out=bo, lse=bl)
             return
         if args.split:
             fa.forward_splitkv(bq, bk, bv, out=bo, lse=bl, causal=args.causal, workspace=ws)
@@ -465,11 +468,16 @@ def run_ours(args, w):
             bt8, bo, bl = t8, o, lse
         else:
             ins = [torch.empty_like(t) for t in ((t8.q8, t8.k8, t8.vt8) if args.fp8 else (dq, dk, dv))]
-            bt8 = fa.Fp8Tensors(*ins, t8.q_scale, t8.k_scale, t8.v_scale,
-                                (t8.B, t8.Nq, t8.Nk, t8.H, t8.Hk, t8.d)) if args.fp8 else None
+            bt8 = None
+            if args.fp8:
+                # The same block scales with this set's code buffers.
+                bt8 = copy.copy(t8)
+                bt8.q8, bt8.k8, bt8.vt8 = ins
             bo, bl = torch.empty_like(o), torch.empty_like(lse)
         if w.varlen:
             ins = ins + [dcu if first else torch.empty_like(dcu)]
+            if bt8 is not None and not first:
+                bt8.cu_seqlens_q = bt8.cu_seqlens_k = ins[3]
         return ins, [bo, bl], bt8
 
     sets = [device_set(True), device_set(False)]
@@ -506,7 +514,8 @@ def run_ours(args, w):
         "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": UNIT,
                      "frac": kernel_tflops / peak, "traffic": traffic,
                      "peak_source": peak_note,
-                     "kernel": "fa_fwd_kernel<128,128,4,fp8>" if args.fp8 else "fa_fwd_kernel<%d,128,*>" % w.d,
+                     "kernel": ("fa_fwd_kernel<128,128,4,fp8%s>" % (",varlen" if w.varlen else "")) if args.fp8
+                     else "fa_fwd_kernel<%d,128,*>" % w.d,
                      "algorithmic_flops_per_launch": flops},
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,

@@ -249,7 +249,8 @@ int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, co
  *                     or FA_FLAG_CAUSAL.  S = Q K^T and O += P V run on the
  *                     tensor cores in e4m3 with fp32 accumulation; P is rounded
  *                     to e4m3 for the second product (the row sums use the
- *                     unrounded fp32 values).  Dense tensors, d = 128 only
+ *                     unrounded fp32 values).  Dense tensors (packed ones:
+ *                     fa_fwd_fp8_varlen below), d = 128 only
  *                     (FA_ERR_UNSUPPORTED otherwise).
  */
 int fa_fp8_sizes(int B, int Nq, int Nk, int H, int Hk, int d, long long* sizes);
@@ -258,6 +259,48 @@ int fa_quantize_fp8(const void* q, const void* k, const void* v, int B, int Nq, 
 int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_scale, const float* k_scale,
                const float* v_scale, void* o, float* lse, int B, int Nq, int Nk, int H, int Hk, int d, float scale,
                int flags, void* stream);
+
+/*
+ * Variable-length FP8 forward: packed sequences as in fa_fwd_ex's
+ * variable-length form ("Flash Attention实现深度解析" §3.1), quantised per
+ * sequence.
+ *   cu_seqlens_q / cu_seqlens_k : device int32 [B + 1], 4-byte aligned,
+ *       non-decreasing from 0; sequence b owns packed rows [cu[b], cu[b + 1]).
+ *   total_q / total_k : packed rows of q / k (= cu[B]); max_seqlen_q / _k
+ *       bound every length.  A sequence whose rows do not fit these bounds is
+ *       reported as FA_ERR_BAD_SEQLENS by fa_check_status() (fa_fwd_fp8_varlen)
+ *       and neither kernel touches memory for it.
+ *   Blocks restart at every sequence: block j of sequence b is its rows
+ *       128j .. 128j + 127 (Q: of one head; K: of one key/value head), and V has
+ *       one block per (sequence, key/value head).  Scales are fp32
+ *       q_scale [B, H, ceil(max_seqlen_q / 128)], k_scale [B, Hk,
+ *       ceil(max_seqlen_k / 128)], v_scale [B, Hk]; blocks past a sequence's
+ *       end get scale 1.
+ *   Codes: q8 [total_q, H, d] and k8 [total_k, Hk, d] (the packed row layout);
+ *       vt8 [Hk, d, kp] with kp = 16 * ceil(total_k / 16) + 16 * B: sequence b
+ *       owns columns [c(b), c(b + 1)), c(b) = 16 * ceil(cu_k[b] / 16) + 16 * b,
+ *       its keys in order and zeros after them.
+ * fa_fp8_varlen_sizes    -- sizes[0..5] as fa_fp8_sizes, for these layouts.
+ * fa_quantize_fp8_varlen -- fills them from packed bf16 q [total_q, H, d] and
+ *                           k, v [total_k, Hk, d]; pointer rules as
+ *                           fa_quantize_fp8.
+ * fa_fwd_fp8_varlen      -- the forward on them: o bf16 [total_q, H, d], lse
+ *                           fp32 [B, H, max_seqlen_q] (entries past a sequence's
+ *                           length not written), flags 0 or FA_FLAG_CAUSAL
+ *                           (bottom-right within each sequence); a sequence with
+ *                           no keys gets o = 0 and lse = -inf.  Every pointer
+ *                           non-NULL; d = 128 only.
+ */
+int fa_fp8_varlen_sizes(int B, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int H, int Hk,
+                        int d, long long* sizes);
+int fa_quantize_fp8_varlen(const void* q, const void* k, const void* v, const int* cu_seqlens_q,
+                           const int* cu_seqlens_k, int B, int total_q, int total_k, int max_seqlen_q,
+                           int max_seqlen_k, int H, int Hk, int d, void* q8, void* k8, void* vt8, float* q_scale,
+                           float* k_scale, float* v_scale, void* stream);
+int fa_fwd_fp8_varlen(const void* q8, const void* k8, const void* vt8, const float* q_scale, const float* k_scale,
+                      const float* v_scale, void* o, float* lse, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                      int B, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int H, int Hk, int d,
+                      float scale, int flags, void* stream);
 
 /*
  * fa_set_timeout_ns -- limit for every device-side wait (mbarrier waits) in

@@ -195,3 +195,42 @@ def test_backward_workspace_and_argument_errors(L):
     assert call(B=0) == fa.FA_OK   # nothing to do
     assert call(Nk=0) == fa.FA_ERR_INVALID_ARG  # queries without keys, as in the forward
     assert call(Nk=0, Nq=0) == fa.FA_OK
+
+
+def test_fp8_sizes_and_varlen_argument_errors(L):
+    """FP8 buffer sizes (dense and packed) and the checks made before any device work."""
+    assert fa.fp8_sizes(2, 200, 130, 4, 2, 128) == (2 * 200 * 4 * 128, 2 * 130 * 2 * 128, 2 * 2 * 128 * 144,
+                                                    2 * 4 * 2, 2 * 2 * 2, 2 * 2)
+    # Packed: V^T columns = 16 * ceil(total_k / 16) + 16 * B.
+    assert fa.fp8_varlen_sizes(3, 500, 333, 300, 200, 4, 2, 128) == (
+        500 * 4 * 128, 333 * 2 * 128, 2 * 128 * (336 + 48), 3 * 4 * 3, 3 * 2 * 2, 3 * 2)
+    assert fa.fp8_varlen_sizes(2, 0, 0, 0, 0, 1, 1, 128) == (0, 0, 128 * 32, 0, 0, 2)
+    for bad in ((1, 10, 10, 10, 10, 1, 1, 64), (1, -1, 10, 10, 10, 1, 1, 128), (1, 10, 10, 10, 10, 3, 2, 128),
+                (1, 1 << 24, 10, 10, 10, 256, 1, 128)):
+        with pytest.raises(fa.FaError):
+            fa.fp8_varlen_sizes(*bad)
+    args = dict(q8=A, k8=A, vt8=A, qs=A, ks=A, vs=A, o=A, lse=A, cu_q=A, cu_k=A, B=1, tq=64, tk=64, mq=64,
+                mk=64, H=1, Hk=1, d=128, scale=0.1, flags=0, stream=None)
+
+    def call(**kw):
+        return fa.fa_fwd_fp8_varlen(*dict(args, **kw).values())
+
+    assert call(d=64) == fa.FA_ERR_UNSUPPORTED
+    assert call(cu_q=None) == fa.FA_ERR_INVALID_ARG
+    assert call(flags=2) == fa.FA_ERR_INVALID_ARG
+    assert call(tq=-1) == fa.FA_ERR_INVALID_ARG
+    assert call(qs=A + 2) == fa.FA_ERR_ALIGN
+    assert call(q8=MIS) == fa.FA_ERR_ALIGN
+    assert call(cu_k=A + 2) == fa.FA_ERR_ALIGN
+    assert call(B=0) == fa.FA_OK
+    qargs = dict(q=A, k=A, v=A, cu_q=A, cu_k=A, B=1, tq=64, tk=64, mq=64, mk=64, H=1, Hk=1, d=128, q8=A, k8=A,
+                 vt8=A, qs=A, ks=A, vs=A, stream=None)
+
+    def qcall(**kw):
+        return fa.fa_quantize_fp8_varlen(*dict(qargs, **kw).values())
+
+    assert qcall(d=64) == fa.FA_ERR_UNSUPPORTED
+    assert qcall(cu_k=None) == fa.FA_ERR_INVALID_ARG
+    assert qcall(vt8=MIS) == fa.FA_ERR_ALIGN
+    assert qcall(cu_q=A + 1) == fa.FA_ERR_ALIGN
+    assert qcall(B=0) == fa.FA_OK

@@ -116,3 +116,150 @@ def test_fp8_errors():
     q = torch.randn(1, 64, 2, 64, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(fa.FaError):
         fa.quantize_fp8(q, q, q)
+
+
+# ------------------------------------------------------- packed sequences
+def _col0(cu_b, b):
+    """First V^T column of sequence b (the packed FP8 layout of include/fa.h)."""
+    return (int(cu_b) + 15) // 16 * 16 + 16 * b
+
+
+def _varlen_inputs(lens_q, lens_k, H, Hk, seed):
+    g = torch.Generator().manual_seed(seed)
+    cu_q = np.concatenate([[0], np.cumsum(lens_q)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lens_k)]).astype(np.int32)
+    q = I.randn_bf16((int(cu_q[-1]), H, 128), g)
+    k = I.randn_bf16((int(cu_k[-1]), Hk, 128), g)
+    v = I.randn_bf16((int(cu_k[-1]), Hk, 128), g)
+    return q, k, v, cu_q, cu_k
+
+
+def _gpu_quant_varlen(q, k, v, cu_q, cu_k):
+    t = fa.quantize_fp8_varlen(q.cuda(), k.cuda(), v.cuda(), torch.from_numpy(cu_q).cuda(),
+                               torch.from_numpy(cu_k).cuda(), int(np.diff(cu_q).max()), int(np.diff(cu_k).max()))
+    torch.cuda.synchronize()
+    n = fa.fp8_varlen_sizes(t.B, t.total_q, t.total_k, t.max_seqlen_q, t.max_seqlen_k, t.H, t.Hk, t.d)
+    kp = n[2] // (t.Hk * t.d)
+    cpu = lambda x, m: x[:m].cpu().numpy()
+    return t, (cpu(t.q8, n[0]).reshape(t.total_q, t.H, t.d), cpu(t.k8, n[1]).reshape(t.total_k, t.Hk, t.d),
+               cpu(t.vt8, n[2]).reshape(t.Hk, t.d, kp), cpu(t.q_scale, n[3]).reshape(t.B, t.H, -1),
+               cpu(t.k_scale, n[4]).reshape(t.B, t.Hk, -1), cpu(t.v_scale, n[5]).reshape(t.B, t.Hk))
+
+
+def _seq_codes(codes, cu_q, cu_k, b):
+    """Codes and scales of sequence b in the dense layouts of quantize_fp8 (batch of one)."""
+    q8, k8, vt8, qs, ks, vs = codes
+    lq, lk = int(cu_q[b + 1] - cu_q[b]), int(cu_k[b + 1] - cu_k[b])
+    c0 = _col0(cu_k[b], b)
+    return (q8[cu_q[b]:cu_q[b + 1]][None], k8[cu_k[b]:cu_k[b + 1]][None],
+            vt8[None, :, :, c0:c0 + (lk + 15) // 16 * 16], qs[b:b + 1, :, :(lq + 127) // 128],
+            ks[b:b + 1, :, :(lk + 127) // 128], vs[b:b + 1]), lq, lk
+
+
+LENS_Q = [1, 127, 128, 129, 300, 0, 513, 64, 17]
+LENS_K = [3, 130, 128, 1, 300, 40, 257, 0, 700]
+
+
+def test_varlen_quantiser_matches_oracle_per_sequence(oracle_mod):
+    """Packed codes and scales equal the oracle's quantisation of each sequence on its own."""
+    H, Hk = 4, 2
+    q, k, v, cu_q, cu_k = _varlen_inputs(LENS_Q, LENS_K, H, Hk, 501)
+    q = q * 3
+    t, codes = _gpu_quant_varlen(q, k, v, cu_q, cu_k)
+    vt8, qs, ks = codes[2], codes[3], codes[4]
+    bits = I.bf16_bits
+    for b in range(len(LENS_Q)):
+        got, lq, lk = _seq_codes(codes, cu_q, cu_k, b)
+        ref = oracle_mod.quantize_fp8(bits(q[cu_q[b]:cu_q[b + 1]][None]), bits(k[cu_k[b]:cu_k[b + 1]][None]),
+                                      bits(v[cu_k[b]:cu_k[b + 1]][None]))
+        for name, a, r in zip(("q8", "k8", "vt8", "q_scale", "k_scale", "v_scale"), got, ref):
+            assert a.shape == r.shape, (b, name)
+            assert np.array_equal(a, r), (b, name)
+        # Blocks past the sequence have scale 1; V^T columns after its keys are zero.
+        assert np.all(qs[b, :, (lq + 127) // 128:] == 1.0) and np.all(ks[b, :, (lk + 127) // 128:] == 1.0)
+        c0, c1 = _col0(cu_k[b], b), _col0(cu_k[b + 1], b + 1)
+        assert np.all(vt8[:, :, c0 + (lk + 15) // 16 * 16:c1] == 0), b
+    assert vt8.shape[2] == _col0(cu_k[-1], len(LENS_Q))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_varlen_forward_matches_oracle(oracle_mod, causal):
+    H, Hk = 4, 2
+    q, k, v, cu_q, cu_k = _varlen_inputs(LENS_Q, LENS_K, H, Hk, 502 + causal)
+    t, codes = _gpu_quant_varlen(q, k, v, cu_q, cu_k)
+    lse0 = torch.full((t.B, H, t.max_seqlen_q), 123.0, device="cuda")
+    o, lse = fa.forward_fp8_varlen(t, causal=causal, lse=lse0)
+    rc, info = fa.check_status()
+    assert rc == fa.FA_OK, (fa.strerror(rc), info)
+    o = o.double().cpu().numpy()
+    lse = lse.double().cpu().numpy()
+    for b in range(len(LENS_Q)):
+        (q8, k8, vt8, qs, ks, vs), lq, lk = _seq_codes(codes, cu_q, cu_k, b)
+        assert np.all(lse[b, :, lq:] == 123.0), b  # entries past the length untouched
+        if lq == 0:
+            continue
+        if lk == 0:
+            assert np.all(o[cu_q[b]:cu_q[b + 1]] == 0.0) and np.all(np.isneginf(lse[b, :, :lq])), b
+            continue
+        o_ref, lse_ref = oracle_mod.attn_fp8_dense(q8, k8, vt8, qs, ks, vs, lq, lk, causal=causal)
+        vmax = np.abs(oracle_mod.e4m3_decode(vt8) * vs[:, :, None, None]).max()
+        _check(torch.from_numpy(o[cu_q[b]:cu_q[b + 1]][None]), torch.from_numpy(lse[b:b + 1, :, :lq]),
+               o_ref, lse_ref, vmax, "seq %d (lq %d, lk %d, causal %d)" % (b, lq, lk, causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_varlen_equal_lengths_bitwise_equal_to_dense(causal):
+    """Sequences of one length run the same tiles as the dense form: identical codes and outputs."""
+    B, L, H, Hk = 3, 300, 4, 2
+    q, k, v, cu_q, cu_k = _varlen_inputs([L] * B, [L] * B, H, Hk, 503)
+    t, codes = _gpu_quant_varlen(q, k, v, cu_q, cu_k)
+    td, dense = _gpu_quant(q.reshape(B, L, H, 128), k.reshape(B, L, Hk, 128), v.reshape(B, L, Hk, 128))
+    assert np.array_equal(codes[0].reshape(B, L, H, 128), dense[0])
+    assert np.array_equal(codes[1].reshape(B, L, Hk, 128), dense[1])
+    for x, y in zip(codes[3:], dense[3:]):
+        assert np.array_equal(x, y)
+    for b in range(B):
+        c0 = _col0(cu_k[b], b)
+        assert np.array_equal(codes[2][:, :, c0:c0 + 304], dense[2][b])
+    o, lse = fa.forward_fp8_varlen(t, causal=causal)
+    od, lsed = fa.forward_fp8(td, causal=causal)
+    assert fa.check_status()[0] == fa.FA_OK
+    assert torch.equal(o.view(torch.int16).reshape(B, L, H, 128), od.view(torch.int16))
+    assert torch.equal(lse, lsed)
+
+
+def test_fp8_varlen_workload_sampled_heads(oracle_mod):
+    """The variable-length workload (32 sequences of 128..4096 tokens, H16 d128) in one call;
+    one head of four sequences (the shortest, the longest and two others) checked in full."""
+    w = I.VARLEN
+    q, k, v, cu_q, cu_k = I.make(w)
+    cu_q, cu_k = cu_q.numpy(), cu_k.numpy()
+    t, codes = _gpu_quant_varlen(q, k, v, cu_q, cu_k)
+    o, lse = fa.forward_fp8_varlen(t)
+    assert fa.check_status()[0] == fa.FA_OK
+    lens = np.diff(cu_q)
+    pick = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 0, w.B // 2})
+    for b in pick:
+        (q8, k8, vt8, qs, ks, vs), lq, lk = _seq_codes(codes, cu_q, cu_k, b)
+        h = b % w.H
+        o_ref, lse_ref = oracle_mod.attn_fp8_dense(q8[:, :, h:h + 1].copy(), k8[:, :, h:h + 1].copy(),
+                                                   vt8[:, h:h + 1].copy(), qs[:, h:h + 1].copy(),
+                                                   ks[:, h:h + 1].copy(), vs[:, h:h + 1].copy(), lq, lk)
+        vmax = np.abs(oracle_mod.e4m3_decode(vt8[0, h]) * vs[0, h]).max()
+        _check(o[cu_q[b]:cu_q[b + 1], h:h + 1][None], lse[b:b + 1, h:h + 1, :lq], o_ref, lse_ref, vmax,
+               "varlen seq %d (len %d) h%d" % (b, lq, h))
+
+
+def test_fp8_varlen_bad_seqlens_are_reported():
+    """A sequence longer than the stated maximum, or past the packed rows, is reported; nothing faults."""
+    H = 2
+    q, k, v, cu_q, cu_k = _varlen_inputs([100, 200], [100, 200], H, H, 504)
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    # Second sequence: 200 rows > maximum 150; then 220 rows ending at row 320 of 300.
+    for max_q, cq in ((150, cu_q), (250, np.array([0, 100, 320], np.int32))):
+        cqt = torch.from_numpy(cq).cuda()
+        t = fa.quantize_fp8_varlen(dq, dk, dv, cqt, torch.from_numpy(cu_k).cuda(), max_q, 200)
+        fa.forward_fp8_varlen(t)
+        rc, _ = fa.check_status()
+        assert rc == fa.FA_ERR_BAD_SEQLENS, (max_q, cq)
+    assert fa.check_status()[0] == fa.FA_OK
