@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) FlashAttention-2 forward (and backward).
+"""GB300 (sm_103a) FlashAttention-2 forward (plus the backward and an FP8 forward).
 
 Thin Python binding over the C ABI declared in ``include/fa.h``: the functions
 named ``fa_*`` here take plain integers (device addresses) and sizes exactly
@@ -11,7 +11,8 @@ stream).  Every step of the computation runs in the CUDA kernels of
 What is computed ("GPU 内核与 FlashAttention" §10, §11.3, §14.1):
 ``O = softmax(scale * Q K^T) V`` per (batch, head), plus the fp32 natural-log
 log-sum-exp of every score row; ``backward`` gives dQ, dK, dV from dO, O and the
-log-sum-exp (§13).
+log-sum-exp (§13); ``quantize_fp8`` / ``forward_fp8`` (and their ``_varlen``
+forms) run the forward on block-quantised e4m3 inputs (§15.5).
 """
 from __future__ import annotations
 

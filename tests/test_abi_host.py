@@ -234,3 +234,20 @@ def test_fp8_sizes_and_varlen_argument_errors(L):
     assert qcall(vt8=MIS) == fa.FA_ERR_ALIGN
     assert qcall(cu_q=A + 1) == fa.FA_ERR_ALIGN
     assert qcall(B=0) == fa.FA_OK
+
+
+def test_fp8_varlen_column_ranges_fit(L):
+    """The packed V^T layout: sequence b starts at c(b) = 16 ceil(cu[b] / 16) + 16 b, a multiple
+    of 16; its keys rounded up to 16 end at or before c(b + 1); c(B) is the column count."""
+    import numpy as np
+    rng = np.random.default_rng(11)
+    for _ in range(200):
+        B = int(rng.integers(1, 40))
+        lens = rng.integers(0, 300, size=B) * (rng.random(B) < 0.9)
+        cu = np.concatenate([[0], np.cumsum(lens)])
+        c = [(int(cu[b]) + 15) // 16 * 16 + 16 * b for b in range(B + 1)]
+        kp = fa.fp8_varlen_sizes(B, 1, int(cu[-1]), 1, int(lens.max()), 1, 1, 128)[2] // 128
+        assert kp == c[B]
+        for b in range(B):
+            assert c[b] % 16 == 0
+            assert c[b] + (int(lens[b]) + 15) // 16 * 16 <= c[b + 1]
