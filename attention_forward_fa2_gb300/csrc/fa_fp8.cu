@@ -42,7 +42,41 @@ __device__ __forceinline__ float block_amax(float v) {
 
 __device__ __forceinline__ float scale_of(float amax) { return amax > 0.f ? amax / kE4M3Max : 1.f; }
 
-__device__ __forceinline__ uint32_t to_e4m3x2(float lo, float hi) { return ptx::pack_e4m3x2(lo, hi); }
+// e4m3 codes of x / s for the bf16 values x of a block sharing the scale s > 0.
+// The quotient is the fp32 division's (x / s rounded to nearest) at two packed
+// multiplies and two packed FMAs per pair instead of two divisions: with
+// rs = RN(1 / s), q = RN(x rs) lies within an ulp of x / s, the residual
+// x - q s is exact in one FMA, and q + (x - q s) rs rounded once is the
+// correctly rounded quotient (Markstein, "Computation of elementary functions
+// on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990).  The
+// theorem wants x and the residual above the subnormal range: for scales below
+// 2^-60, x and s are first multiplied by 2^64 (exact, same quotient); for larger
+// scales a subnormal x has |x / s| < 2^-66, whose code is zero either way.  The
+// quotient takes the sign of x, as the division's does, also when it is zero.
+// An infinite scale (an infinite input) gives quotients 0 as the division does.
+struct BlockQuantizer {
+  uint64_t k2, rs2, nsk2;
+  __device__ explicit BlockQuantizer(float s) {
+    const float k = s < 0x1p-60f ? 0x1p64f : 1.f;
+    const float sk = s * k;
+    const float rs = __frcp_rn(sk);
+    const float nsk = isinf(sk) ? 0.f : -sk;
+    k2 = ptx::f2_pack(k, k);
+    rs2 = ptx::f2_pack(rs, rs);
+    nsk2 = ptx::f2_pack(nsk, nsk);
+  }
+  // Codes of the low and high bf16 halves of w (low code in the low byte).
+  __device__ __forceinline__ uint32_t codes2(uint32_t w) const {
+    const uint64_t x = ptx::f2_mul(ptx::f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)), k2);
+    const uint64_t q = ptx::f2_mul(x, rs2);
+    const uint64_t r = ptx::f2_fma(q, nsk2, x);
+    constexpr uint64_t kSign = 0x8000000080000000ull;
+    const uint64_t qq = (ptx::f2_fma(r, rs2, q) & ~kSign) | (x & kSign);
+    float lo, hi;
+    ptx::f2_unpack(qq, lo, hi);
+    return ptx::pack_e4m3x2(lo, hi);
+  }
+};
 
 __device__ __forceinline__ float amax8(uint4 u) {
   // Largest magnitude of eight bf16 values (the sign bit cleared).
@@ -87,9 +121,13 @@ __global__ void __launch_bounds__(256) fp8_quant_qk_kernel(Fp8QuantParams p, uns
   if (!isq) id -= nq;
   const int blocks = isq ? qb : kb;
   const int Hx = isq ? p.H : p.Hk;
-  const int blk = static_cast<int>(id % blocks);
-  const long long bh = id / blocks;
-  const int h = static_cast<int>(bh % Hx), b = static_cast<int>(bh / Hx);
+  // Heads vary fastest over consecutive blocks: blocks resident together read
+  // the same rows of every head, i.e. whole contiguous rows of the tensor,
+  // rather than slices of one head a row stride apart.
+  const int h = static_cast<int>(id % Hx);
+  const long long rest = id / Hx;
+  const int blk = static_cast<int>(rest % blocks), b = static_cast<int>(rest / blocks);
+  const long long bh = static_cast<long long>(b) * Hx + h;
   int seq0, len;
   fp8_seq<VARLEN>(isq ? p.cu_q : p.cu_k, isq ? p.Nq : p.Nk, isq ? p.total_q : p.total_k, b, seq0, len);
   const int r0 = blk * kBR, rows = min(len - r0, kBR);  // <= 0: a block past the sequence (scale 1)
@@ -111,7 +149,8 @@ __global__ void __launch_bounds__(256) fp8_quant_qk_kernel(Fp8QuantParams p, uns
   }
   m = block_amax(m);
   const float s = scale_of(m);
-  if (threadIdx.x == 0) (isq ? p.q_scale : p.k_scale)[id] = s;
+  const BlockQuantizer qz(s);
+  if (threadIdx.x == 0) (isq ? p.q_scale : p.k_scale)[bh * blocks + blk] = s;
   if (!isq) {
     mv = block_amax(mv);
     if (threadIdx.x == 0) atomicMax(v_amax_bits + bh, __float_as_uint(mv));
@@ -124,12 +163,7 @@ __global__ void __launch_bounds__(256) fp8_quant_qk_kernel(Fp8QuantParams p, uns
       const uint32_t w[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
       uint32_t o[2];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const float a0 = __uint_as_float(w[2 * half] << 16) / s, a1 = __uint_as_float(w[2 * half] & 0xffff0000u) / s;
-        const float a2 = __uint_as_float(w[2 * half + 1] << 16) / s,
-                    a3 = __uint_as_float(w[2 * half + 1] & 0xffff0000u) / s;
-        o[half] = to_e4m3x2(a0, a1) | (to_e4m3x2(a2, a3) << 16);
-      }
+      for (int half = 0; half < 2; ++half) o[half] = qz.codes2(w[2 * half]) | (qz.codes2(w[2 * half + 1]) << 16);
       const size_t off = ((static_cast<size_t>(seq0) + r0 + r) * Hx + h) * D + c * 8;
       *reinterpret_cast<uint2*>(dst + off) = make_uint2(o[0], o[1]);
     }
@@ -142,7 +176,8 @@ __global__ void fp8_v_scale_kernel(Fp8QuantParams p, const unsigned int* v_amax_
   if (i < p.B * p.Hk) p.v_scale[i] = scale_of(__uint_as_float(v_amax_bits[i]));
 }
 
-// V codes, transposed: one block per (64-key tile, b * Hk + hk).  Thread
+// V codes, transposed: one block per (b, 64-key tile, hk), hk fastest (as in
+// the kernel above, resident blocks read contiguous rows).  Thread
 // (chunk, kg) = (tid % 16, tid / 16) loads 8 features of keys 4kg .. 4kg+3
 // (16-byte loads; a warp reads two whole 256-byte key rows per instruction),
 // converts them and regroups the bytes into one 32-bit word per feature (four
@@ -150,14 +185,17 @@ __global__ void fp8_v_scale_kernel(Fp8QuantParams p, const unsigned int* v_amax_
 // rows of 17 words (conflict-free for both phases) and leave as coalesced
 // 4-byte stores of the transposed rows.
 template <int D, bool VARLEN>
-__global__ void __launch_bounds__(256) fp8_quant_vt_kernel(Fp8QuantParams p, const unsigned int* v_amax_bits) {
+__global__ void __launch_bounds__(256) fp8_quant_vt_kernel(Fp8QuantParams p, const unsigned int* v_amax_bits,
+                                                           int ktiles) {
   static_assert(D == 128, "16 chunks of 8 features per key");
   constexpr int kRowWords = 17;  // 16 words of 4 keys, one word of padding
   __shared__ uint32_t tile[D * kRowWords];
-  const int kt = blockIdx.x;  // 64-key tile
-  const int bh = blockIdx.y;  // b * Hk + hk
-  const int h = bh % p.Hk, b = bh / p.Hk;
-  const float s = scale_of(__uint_as_float(v_amax_bits[bh]));
+  const int h = static_cast<int>(blockIdx.x % p.Hk);
+  const long long rest = blockIdx.x / p.Hk;
+  const int kt = static_cast<int>(rest % ktiles);  // 64-key tile
+  const int b = static_cast<int>(rest / ktiles);
+  const int bh = b * p.Hk + h;
+  const BlockQuantizer qz(scale_of(__uint_as_float(v_amax_bits[bh])));
   int seq0, len;
   fp8_seq<VARLEN>(p.cu_k, p.Nk, p.total_k, b, seq0, len);
   // Columns this sequence owns (keys, then zeros).
@@ -166,7 +204,7 @@ __global__ void __launch_bounds__(256) fp8_quant_vt_kernel(Fp8QuantParams p, con
   if constexpr (VARLEN) {
     col0 = fp8_vt_col0(p.cu_k[b], b);
     const long long end = min(fp8_vt_col0(p.cu_k[b + 1], b + 1), p.kp_total);
-    span = col0 >= 0 && end > col0 ? static_cast<int>(min(end - col0, 64LL * gridDim.x)) : 0;
+    span = col0 >= 0 && end > col0 ? static_cast<int>(min(end - col0, 64LL * ktiles)) : 0;
   }
   if (kt * 64 >= span) return;
   const int chunk = threadIdx.x & 15, kg = threadIdx.x >> 4;
@@ -180,7 +218,7 @@ __global__ void __launch_bounds__(256) fp8_quant_vt_kernel(Fp8QuantParams p, con
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      q2[k][i] = to_e4m3x2(__uint_as_float(w[i] << 16) / s, __uint_as_float(w[i] & 0xffff0000u) / s);
+      q2[k][i] = qz.codes2(w[i]);
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -237,11 +275,13 @@ cudaError_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream) {
   // Variable length: a sequence's span is at most its length + 31 columns.
   const int kt = varlen ? (p.Nk + 31 + 63) / 64 : (p.nk_pad + 63) / 64;
   if (kt > 0 && bhk > 0) {
-    const dim3 grid(static_cast<unsigned>(kt), static_cast<unsigned>(bhk));
+    const long long nvt = bhk * kt;
+    if (nvt > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>(nvt));
     if (varlen)
-      fp8_quant_vt_kernel<128, true><<<grid, 256, 0, stream>>>(p, v_amax_bits);
+      fp8_quant_vt_kernel<128, true><<<grid, 256, 0, stream>>>(p, v_amax_bits, kt);
     else
-      fp8_quant_vt_kernel<128, false><<<grid, 256, 0, stream>>>(p, v_amax_bits);
+      fp8_quant_vt_kernel<128, false><<<grid, 256, 0, stream>>>(p, v_amax_bits, kt);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   fp8_v_scale_kernel<<<static_cast<unsigned>((bhk + 255) / 256), 256, 0, stream>>>(p, v_amax_bits);

@@ -60,6 +60,48 @@ def test_quantiser_matches_oracle_bit_for_bit(oracle_mod, B, Nq, Nk, H, Hk):
         assert np.array_equal(a, b), name
 
 
+def _regime_rows(kind, rows, heads, gen):
+    """bf16 [rows, heads, 128] values of one quantisation regime."""
+    shape = (rows, heads, 128)
+    z = torch.randn(shape, generator=gen)
+    if kind == "normal":
+        x = z * 3
+    elif kind == "tiny":        # scale below 2^-60: the quotients take the rescaled path
+        x = z * 1e-36
+    elif kind == "subnormal":   # bf16 subnormals only: a subnormal scale
+        x = z * 1e-39
+    elif kind == "spread":      # magnitudes 2^-140 .. 2^20 in one block, subnormals included
+        e = torch.randint(-140, 21, shape, generator=gen).double()
+        x = (torch.sign(z) * torch.exp2(e) * (1 + torch.rand(shape, generator=gen))).float()
+    elif kind == "signed_zeros":  # +0 and -0 with a few ordinary values
+        x = torch.where(torch.rand(shape, generator=gen) < 0.5, torch.tensor(0.0), torch.tensor(-0.0))
+        x[::17, :, ::5] = z[::17, :, ::5]
+    elif kind == "zeros":       # an all-zero block (scale 1), both signs
+        x = torch.where(torch.rand(shape, generator=gen) < 0.5, torch.tensor(0.0), torch.tensor(-0.0))
+    else:                       # "large"
+        x = z * 1e30
+    return x.to(torch.bfloat16)
+
+
+def test_quantiser_edge_regimes_bit_for_bit(oracle_mod):
+    """Blocks in every regime the quantiser's quotient distinguishes (ordinary values, scales
+    below 2^-60 and subnormal ones, bf16 subnormals, magnitudes over 160 binades, signed zeros,
+    all-zero blocks, huge values): codes and scales equal the oracle's bit for bit."""
+    kinds = ("normal", "tiny", "subnormal", "spread", "signed_zeros", "zeros", "large")
+    g = torch.Generator().manual_seed(606)
+    H, Hk = 2, 2
+    q = torch.cat([_regime_rows(k, 128, H, g) for k in kinds])[None]
+    k = torch.cat([_regime_rows(k, 128, Hk, g) for k in reversed(kinds)])[None]
+    v = torch.cat([_regime_rows(k, 128, Hk, g) for k in kinds[:3]])[None]
+    v = torch.cat([v, torch.zeros_like(k[:, 384:])], dim=1)  # V maxima: a subnormal-scale head...
+    v[:, :, 1] = k[:, :, 1]                                  # ...and one spanning every regime
+    _, got = _gpu_quant(q, k, v)
+    ref = oracle_mod.quantize_fp8(I.bf16_bits(q), I.bf16_bits(k), I.bf16_bits(v))
+    for name, a, b in zip(("q8", "k8", "vt8", "q_scale", "k_scale", "v_scale"), got, ref):
+        assert a.shape == b.shape, name
+        assert np.array_equal(a, b), (name, np.argwhere(a != b)[:5])
+
+
 def _check(o, lse, o_ref, lse_ref, vmax, what):
     o = o.double().cpu().numpy()
     lse = lse.double().cpu().numpy()
