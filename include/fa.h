@@ -192,7 +192,7 @@ int fa_last_cuda_error(void);
  *                    d) bytes, 16-byte aligned, owned by the caller; fully
  *                    overwritten (the fp32 dQ accumulator, D = rowsum(dO o O)
  *                    and the scaled log-sum-exp), nothing needs to persist.
- * d = 64 or 128 (FA_ERR_UNSUPPORTED otherwise); dense tensors only.  Three
+ * d = 64 or 128 (FA_ERR_UNSUPPORTED otherwise); dense tensors (packed ones: fa_bwd_varlen).  Three
  * kernels are enqueued on `stream`: preprocessing (D and a cleared
  * accumulator), the key-block kernel (writes dk, dv; adds dQ into the
  * accumulator) and the conversion of the accumulator to bf16 dq.  Errors as
