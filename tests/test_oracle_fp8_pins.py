@@ -44,6 +44,10 @@ def test_e4m3_encode_round_trip_and_rounding(oracle_mod):
     gap = np.abs(vals[None, :] - x[:, None]).min(axis=1)
     assert np.allclose(np.abs(e - x), gap)
     assert list(oracle_mod.e4m3_encode([448.0, 460.0, 1e6, -1e6])) == [0x7E, 0x7E, 0x7E, 0xFE]
+    # zeros and values that round to zero keep their sign (round to nearest is sign-symmetric)
+    assert list(oracle_mod.e4m3_encode([0.0, -0.0, 2.0 ** -11, -(2.0 ** -11), 2.0 ** -10, -(2.0 ** -10)])) == \
+        [0x00, 0x80, 0x00, 0x80, 0x00, 0x80]
+    assert list(oracle_mod.e4m3_encode([1.5 * 2.0 ** -10, -1.5 * 2.0 ** -10])) == [0x01, 0x81]
 
 
 def test_block_quantiser_bounds(oracle_mod):
