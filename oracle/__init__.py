@@ -22,7 +22,9 @@ in ``attn_ref.c``:
 * ``e4m3_decode`` / ``e4m3_encode`` / ``quantize_fp8``  the e4m3 format from its
                       definition and block quantisation (§15.5): the reference for
                       the quantiser
-* ``attn_fp8_dense``  the definition evaluated on dequantised e4m3 inputs
+* ``attn_fp8_dense``  the definition evaluated on dequantised e4m3 inputs (optionally
+                      also each row's largest score and sum_j P_ij |v_j|, the plain
+                      quantities the FP8 error bound is written in)
 
 Inputs are bf16 bit patterns (``numpy.uint16``); outputs are float64.
 """
@@ -87,7 +89,7 @@ def _load():
         lib.oracle_quantize_e4m3.argtypes = [f32p, ctypes.c_longlong, ctypes.c_float, u8p]
         lib.oracle_quantize_e4m3.restype = None
         lib.oracle_attn_fp8_dense.argtypes = [u8p, u8p, u8p, f32p, f32p, f32p, ci, ci, ci, ci, ci, ci, ci,
-                                              cd, ci, f64p, f64p]
+                                              cd, ci, f64p, f64p, f64p, f64p]
         for name in ("oracle_attn_dense", "oracle_attn_dense_rows", "oracle_attn_varlen",
                      "oracle_attn_online", "oracle_attn_bwd_dense", "oracle_attn_fp8_dense",
                      "oracle_num_threads"):
@@ -288,21 +290,32 @@ def quantize_fp8(q, k, v):
     return q8, k8, vt8, qs, ks, vs
 
 
-def attn_fp8_dense(q8, k8, vt8, q_scale, k_scale, v_scale, Nq, Nk, scale=None, causal=False):
+def attn_fp8_dense(q8, k8, vt8, q_scale, k_scale, v_scale, Nq, Nk, scale=None, causal=False,
+                   with_bound_terms=False):
     """The attention definition on dequantised e4m3 inputs (layouts of quantize_fp8).
 
-    Returns (o [B, Nq, H, d], lse [B, H, Nq]) in float64."""
+    Returns (o [B, Nq, H, d], lse [B, H, Nq]) in float64.  With
+    ``with_bound_terms`` also (rowmax [B, H, Nq], abs_o [B, Nq, H, d]): the
+    largest score each row sees and sum_j P_ij |v_j| (the weights of the
+    definition applied to the magnitudes of V)."""
     q8, k8, vt8 = (np.ascontiguousarray(x, np.uint8) for x in (q8, k8, vt8))
     qs, ks, vs = (np.ascontiguousarray(x, np.float32) for x in (q_scale, k_scale, v_scale))
     B, _, H, d = q8.shape
     Hk, nkp = vt8.shape[1], vt8.shape[3]
     o = np.zeros((B, Nq, H, d), np.float64)
     lse = np.zeros((B, H, Nq), np.float64)
+    rowmax = np.zeros((B, H, Nq), np.float64) if with_bound_terms else None
+    abs_o = np.zeros((B, Nq, H, d), np.float64) if with_bound_terms else None
+    null = ctypes.POINTER(ctypes.c_double)()
     rc = _load().oracle_attn_fp8_dense(_ptr(q8, ctypes.c_uint8), _ptr(k8, ctypes.c_uint8),
                                        _ptr(vt8, ctypes.c_uint8), _ptr(qs, ctypes.c_float),
                                        _ptr(ks, ctypes.c_float), _ptr(vs, ctypes.c_float), B, Nq, Nk, H,
                                        Hk, d, nkp, _default_scale(d, scale), int(bool(causal)),
-                                       _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double))
+                                       _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
+                                       _ptr(rowmax, ctypes.c_double) if with_bound_terms else null,
+                                       _ptr(abs_o, ctypes.c_double) if with_bound_terms else null)
     if rc != 0:
         raise MemoryError("oracle_attn_fp8_dense failed (%d)" % rc)
+    if with_bound_terms:
+        return o, lse, rowmax, abs_o
     return o, lse

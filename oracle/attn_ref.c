@@ -349,10 +349,13 @@ void oracle_quantize_e4m3(const float *x, long long n, float scale, uint8_t *cod
 }
 
 /* One head in double: nq query rows (q row i at q + i * d), nk keys (k row j
-   at k + j * d, v row j at v + j * d); o row i at o + i * o_rs. */
+   at k + j * d, v row j at v + j * d); o row i at o + i * o_rs.  Optional
+   outputs (NULL: not computed): mrow[i] = max_j s_ij over the keys row i sees
+   (-inf if none), and abs_o row i (at abs_o + i * o_rs) = sum_j P_ij |v_j|,
+   the same weights applied to the magnitudes of V. */
 static int head_attention_f64(const double *q, int nq, const double *k, const double *v, int nk, int d,
                               double scale, int causal, long offset, double *o, size_t o_rs,
-                              double *lse)
+                              double *lse, double *mrow, double *abs_o)
 {
     double *S = (double *)malloc((size_t)(nq > 0 ? nq : 1) * (size_t)(nk > 0 ? nk : 1) * sizeof(double));
     if (!S)
@@ -373,8 +376,14 @@ static int head_attention_f64(const double *q, int nq, const double *k, const do
                 m = row[j];
         }
         double *oi = o + (size_t)i * o_rs;
+        double *ai = abs_o ? abs_o + (size_t)i * o_rs : NULL;
         for (int c = 0; c < d; ++c)
             oi[c] = 0.0;
+        if (ai)
+            for (int c = 0; c < d; ++c)
+                ai[c] = 0.0;
+        if (mrow)
+            mrow[i] = m;
         if (m == -INFINITY) {
             lse[i] = -INFINITY;
             continue;
@@ -388,6 +397,9 @@ static int head_attention_f64(const double *q, int nq, const double *k, const do
             const double pj = row[j] / l;
             for (int c = 0; c < d; ++c)
                 oi[c] += pj * v[(size_t)j * d + c];
+            if (ai)
+                for (int c = 0; c < d; ++c)
+                    ai[c] += pj * fabs(v[(size_t)j * d + c]);
         }
         lse[i] = m + log(l);
     }
@@ -399,10 +411,14 @@ static int head_attention_f64(const double *q, int nq, const double *k, const do
  * FP8 dense form.  q8: [B, Nq, H, d] codes, k8: [B, Nk, Hk, d], vt8: [B, Hk, d,
  * nk_pad] (V transposed); q_scale [B, H, ceil(Nq/128)], k_scale [B, Hk,
  * ceil(Nk/128)], v_scale [B, Hk].  o: [B, Nq, H, d], lse: [B, H, Nq] (double).
+ * Optional (NULL: skipped): rowmax [B, H, Nq], the largest score each row sees,
+ * and abs_o [B, Nq, H, d], sum_j P_ij |v_j| -- the two plain quantities that
+ * bound the effect of rounding the weights P to e4m3 (tests only).
  */
 int oracle_attn_fp8_dense(const uint8_t *q8, const uint8_t *k8, const uint8_t *vt8, const float *q_scale,
                           const float *k_scale, const float *v_scale, int B, int Nq, int Nk, int H, int Hk,
-                          int d, int nk_pad, double scale, int causal, double *o, double *lse)
+                          int d, int nk_pad, double scale, int causal, double *o, double *lse,
+                          double *rowmax, double *abs_o)
 {
     if (Hk <= 0 || H % Hk != 0)
         return -1;
@@ -433,7 +449,9 @@ int oracle_attn_fp8_dense(const uint8_t *q8, const uint8_t *k8, const uint8_t *v
                 }
             err |= head_attention_f64(q, Nq, k, v, Nk, d, scale, causal, (long)Nk - Nq,
                                       o + (size_t)b * Nq * H * d + (size_t)h * d, (size_t)H * d,
-                                      lse + ((size_t)b * H + h) * Nq);
+                                      lse + ((size_t)b * H + h) * Nq,
+                                      rowmax ? rowmax + ((size_t)b * H + h) * Nq : NULL,
+                                      abs_o ? abs_o + (size_t)b * Nq * H * d + (size_t)h * d : NULL);
             free(q); free(k); free(v);
         }
     }

@@ -64,3 +64,36 @@ def sample_rows(B, Nq, H, n_random=48, seed=0):
 
 def bits(t):
     return I.bf16_bits(t)
+
+
+def fp8_bound(oracle_mod, q8, k8, vt8, qs, ks, vs, Nq, Nk, causal=False, scale=None):
+    """Oracle output of the FP8 forward and the per-element bar it must meet.
+
+    Returns (o_ref, lse_ref, bound) with bound [B, Nq, H, d].  The kernel
+    computes the definition on the dequantised codes except that each weight
+    p_j (relative to the kernel's reference maximum, which never exceeds the
+    row maximum m) is rounded to e4m3 before O += P V: off by at most 2^-4 of
+    itself (3 mantissa bits), or by 2^-10 absolute below the smallest normal
+    2^-6.  The row sum uses the unrounded weights, so with l = sum_j e^(s_j - m)
+    (the kernel's own sum is at least l):
+        |dO_ic| <= 2^-4 sum_j P_ij |v_jc| + 2^-10 sum_{j seen by i} |v_jc| / l
+    plus the bf16 rounding of the output (2^-9 of |O|, taken as 2^-8) and an
+    absolute 1e-3 for the fp32 sums.  l = e^(m - LSE) comes from the oracle's
+    row maximum and log-sum-exp."""
+    o, lse, m, a = oracle_mod.attn_fp8_dense(q8, k8, vt8, qs, ks, vs, Nq, Nk, scale=scale, causal=causal,
+                                             with_bound_terms=True)
+    B, _, H, d = o.shape
+    Hk = vt8.shape[1]
+    G = H // Hk
+    vabs = np.abs(oracle_mod.e4m3_decode(vt8[..., :Nk])) * np.asarray(vs, np.float64)[:, :, None, None]
+    csum = np.cumsum(vabs, axis=3)                      # [B, Hk, d, Nk]: sum over keys 0..j
+    fin = np.isfinite(lse)
+    inv_l = np.exp(np.where(fin, m, 0.0) - np.where(fin, lse, 0.0)) * fin  # [B, H, Nq]; 0 without keys
+    bound = 2.0 ** -4 * a + 2.0 ** -8 * np.abs(o) + 1e-3
+    i = np.arange(Nq)
+    last = np.minimum(Nk - 1, i + Nk - Nq) if causal else np.full(Nq, Nk - 1)
+    for h in range(H):
+        vsum = np.where(last[None, :, None] >= 0,
+                        np.transpose(csum[:, h // G][:, :, np.maximum(last, 0)], (0, 2, 1)), 0.0)  # [B, Nq, d]
+        bound[:, :, h, :] += 2.0 ** -10 * inv_l[:, h, :, None] * vsum
+    return o, lse, bound

@@ -112,3 +112,104 @@ def test_fp8_scales_act_as_multipliers(oracle_mod):
     o2, l2 = oracle_mod.attn_fp8_dense(q8, k8, vt8, one(B, H, 1), one(B, H, 1), one(B, H), Nq, Nk, scale=0.04)
     assert np.allclose(o1, 3 * o2, rtol=1e-12, atol=1e-12)
     assert np.allclose(l1, l2, rtol=1e-12, atol=1e-12)
+
+
+def _dequant(oracle_mod, q8, k8, vt8, qs, ks, vs, Nq, Nk):
+    """Dequantised q [B, Nq, H, d], k [B, Nk, Hk, d], v [B, Nk, Hk, d] in float64."""
+    dec = oracle_mod.e4m3_decode
+    q = dec(q8) * np.repeat(qs, 128, axis=2)[:, :, :Nq].transpose(0, 2, 1)[..., None]
+    k = dec(k8) * np.repeat(ks, 128, axis=2)[:, :, :Nk].transpose(0, 2, 1)[..., None]
+    v = dec(vt8[..., :Nk]).transpose(0, 3, 1, 2) * vs[:, None, :, None]
+    return q, k, v
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_bound_terms_brute_force(oracle_mod, causal):
+    """Row maximum and sum_j P_ij |v_j| against a direct numpy evaluation."""
+    B, Nq, Nk, H, Hk, d = 2, 9, 7, 4, 2, 128
+    g = torch.Generator().manual_seed(12)
+    q, k, v = (I.randn_bf16(s, g) for s in ((B, Nq, H, d), (B, Nk, Hk, d), (B, Nk, Hk, d)))
+    codes = oracle_mod.quantize_fp8(I.bf16_bits(q), I.bf16_bits(k), I.bf16_bits(v))
+    o, lse, m, a = oracle_mod.attn_fp8_dense(*codes, Nq, Nk, causal=causal, with_bound_terms=True)
+    qf, kf, vf = _dequant(oracle_mod, *codes, Nq, Nk)
+    sc = 1 / np.sqrt(d)
+    for b in range(B):
+        for h in range(H):
+            s = sc * qf[b, :, h] @ kf[b, :, h // 2].T
+            if causal:
+                s[np.arange(Nk)[None, :] > np.arange(Nq)[:, None] + Nk - Nq] = -np.inf
+            mx = s.max(axis=1)
+            assert np.allclose(m[b, h], mx, rtol=1e-13, atol=1e-13)
+            seen = np.isfinite(mx)
+            p = np.exp(s[seen] - mx[seen, None])
+            p /= p.sum(axis=1, keepdims=True)
+            assert np.allclose(a[b, seen, h], p @ np.abs(vf[b, :, h // 2]), rtol=1e-12, atol=1e-13)
+            assert np.allclose(o[b, seen, h], p @ vf[b, :, h // 2], rtol=1e-12, atol=1e-13)
+            assert np.all(a[b, ~seen, h] == 0) and np.all(np.isneginf(m[b, h][~seen]))
+    # the log-sum-exp lies between the row maximum and the maximum plus log(keys seen)
+    fin = np.isfinite(lse)
+    assert np.all(lse[fin] >= m[fin] - 1e-12) and np.all(lse[fin] <= m[fin] + np.log(Nk) + 1e-12)
+
+
+def test_fp8_bound_terms_invariants(oracle_mod):
+    """V with non-negative codes: sum_j P_ij |v_j| equals O; flipping the sign
+    of every V code negates O and leaves the magnitudes' sum alone."""
+    B, Nq, Nk, H, d = 1, 30, 70, 2, 128
+    q8 = _exact_codes((B, Nq, H, d), 7, oracle_mod)
+    k8 = _exact_codes((B, Nk, H, d), 8, oracle_mod)
+    vt8 = np.zeros((B, H, d, 80), np.uint8)
+    vt8[..., :Nk] = _exact_codes((B, H, d, Nk), 9, oracle_mod) & 0x7F
+    one = lambda *s: np.ones(s, np.float32)
+    args = (one(B, H, 1), one(B, H, 1), one(B, H), Nq, Nk)
+    o, _, _, a = oracle_mod.attn_fp8_dense(q8, k8, vt8, *args, scale=0.03, with_bound_terms=True)
+    assert np.allclose(a, o, rtol=1e-13, atol=0)
+    o2, _, _, a2 = oracle_mod.attn_fp8_dense(q8, k8, vt8 | 0x80, *args, scale=0.03, with_bound_terms=True)
+    assert np.array_equal(o2, -o) and np.array_equal(a2, a)
+
+
+def _blocky_codes(oracle_mod, seed, Nq=256, Nk=512, H=2, Hk=1):
+    """N(0,1) inputs whose 128-key blocks differ in amplitude (ratios up to 1.33)."""
+    g = torch.Generator().manual_seed(seed)
+    q = I.randn_bf16((1, Nq, H, 128), g)
+    k = I.randn_bf16((1, Nk, Hk, 128), g)
+    v = I.randn_bf16((1, Nk, Hk, 128), g)
+    amp = torch.tensor([1.0, 1.2, 0.9, 1.1]).repeat_interleave(128)[:Nk]
+    k = (k.float() * amp[None, :, None, None]).to(torch.bfloat16)
+    return oracle_mod.quantize_fp8(I.bf16_bits(q), I.bf16_bits(k), I.bf16_bits(v))
+
+
+def test_fp8_bar_holds_for_rounded_weights(oracle_mod):
+    """The bar covers what it claims: weights relative to a reference below the
+    row maximum (by up to the rescale threshold, 8 in log2 units), rounded to
+    e4m3, with the sum of the unrounded weights, stay within it."""
+    from fa_testutil import fp8_bound
+    Nq, Nk = 64, 512
+    codes = _blocky_codes(oracle_mod, 21, Nq=Nq, Nk=Nk, H=1)
+    o_ref, _, bound = fp8_bound(oracle_mod, *codes, Nq, Nk)
+    qf, kf, vf = _dequant(oracle_mod, *codes, Nq, Nk)
+    s = qf[0, :, 0] @ kf[0, :, 0].T / np.sqrt(128)
+    lag = np.random.default_rng(5).uniform(0, 8 * np.log(2), Nq)   # reference below the maximum
+    p = np.exp(s - (s.max(axis=1) - lag)[:, None])
+    assert p.max() <= 256.0 * (1 + 1e-12)
+    p8 = oracle_mod.e4m3_decode(oracle_mod.e4m3_encode(p))
+    o_emul = (p8 @ vf[0, :, 0]) / p.sum(axis=1, keepdims=True)
+    err = np.abs(o_emul - o_ref[0, :, 0])
+    assert np.all(err <= bound[0, :, 0]), float((err - bound[0, :, 0]).max())
+
+
+def test_fp8_bar_rejects_a_neighbouring_block_scale(oracle_mod):
+    """An output computed with one key block's scale taken from the next block
+    (what a kernel indexing the scales one block off would write) breaks the
+    per-element bar, while the earlier global bar 2^-4 max|v| + 2e-2 on O
+    would have let it through."""
+    from fa_testutil import fp8_bound
+    Nq, Nk = 256, 512
+    q8, k8, vt8, qs, ks, vs = _blocky_codes(oracle_mod, 1, Nq=Nq, Nk=Nk)
+    o_ref, _, bound = fp8_bound(oracle_mod, q8, k8, vt8, qs, ks, vs, Nq, Nk)
+    ks_bad = ks.copy()
+    ks_bad[0, 0, 1] = ks[0, 0, 2]
+    o_bad, _ = oracle_mod.attn_fp8_dense(q8, k8, vt8, qs, ks_bad, vs, Nq, Nk)
+    err = np.abs(o_bad - o_ref)
+    assert np.any(err > bound)
+    vmax = np.abs(oracle_mod.e4m3_decode(vt8) * vs[:, :, None, None]).max()
+    assert err.max() <= 2.0 ** -4 * vmax + 2e-2
