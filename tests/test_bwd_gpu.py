@@ -96,19 +96,28 @@ def test_backward_d64_matches_oracle(oracle_mod, B, Nq, Nk, H, Hk, causal):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_backward_page_workload_sampled_heads(oracle_mod, causal):
-    """The page workload (B16 N4096 H16 d128) in one call; two heads, the
-    first and the last, checked in full against the oracle."""
+def test_backward_page_workload_many_heads(oracle_mod, causal):
+    """The page workload (B16 N4096 H16 d128) in one call; checked in full
+    against the oracle: every head of the first and the last batch, and one
+    head of every other batch (head b of batch b), 46 of the 256 (batch, head)
+    pairs."""
     w = I.PAGE
     q, k, v, _, _ = I.make(w)
     do = I.randn_bf16(tuple(q.shape), torch.Generator().manual_seed(77))
     got = _gpu_grads(q, k, v, do, causal)
-    for b, h in ((0, 0), (w.B - 1, w.H - 1)):
-        sl = lambda t: t[b:b + 1, :, h:h + 1].contiguous()
+    # Whole batches: the oracle runs their heads in parallel.
+    for b in (0, w.B - 1):
+        sl = lambda t: t[b:b + 1].contiguous()
         ref = oracle_mod.attn_bwd_dense(I.bf16_bits(sl(q)), I.bf16_bits(sl(k)), I.bf16_bits(sl(v)),
                                         I.bf16_bits(sl(do)), causal=causal)[:3]
-        mine = tuple(g[b:b + 1, :, h:h + 1] for g in got)
-        _assert_grads(mine, ref, "page b%d h%d causal%d" % (b, h, causal))
+        _assert_grads(tuple(g[b:b + 1] for g in got), ref, "page b%d causal%d" % (b, causal))
+    # Head b of batch b, gathered as a batch of single-head problems.
+    pairs = [(b, b % w.H) for b in range(1, w.B - 1)]
+    pick = lambda t: torch.stack([t[b, :, h:h + 1] for b, h in pairs]).contiguous()
+    ref = oracle_mod.attn_bwd_dense(I.bf16_bits(pick(q)), I.bf16_bits(pick(k)), I.bf16_bits(pick(v)),
+                                    I.bf16_bits(pick(do)), causal=causal)[:3]
+    mine = tuple(np.stack([g[b, :, h:h + 1] for b, h in pairs]) for g in got)
+    _assert_grads(mine, ref, "page diagonal heads causal%d" % causal)
 
 
 def test_key_gradients_sum_to_zero_on_gpu():
