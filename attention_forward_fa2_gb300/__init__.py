@@ -23,6 +23,9 @@ import threading
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libfa_gb300.so")
+# The same library with the kernel's phase clocks compiled in (profiling only;
+# `python -m attention_forward_fa2_gb300.build --phase`).
+PHASE_LIB_PATH = os.path.join(PKG, "libfa_gb300_phase.so")
 
 FA_OK = 0
 FA_ERR_INVALID_ARG = -1
@@ -43,7 +46,7 @@ EXPORTS = (
     "fa_selftest_wait_timeout", "fa_version", "fa_splitkv_num_splits",
     "fa_splitkv_workspace_bytes", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc",
     "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_varlen", "fa_fp8_sizes", "fa_quantize_fp8", "fa_fwd_fp8",
-    "fa_fp8_varlen_sizes", "fa_quantize_fp8_varlen", "fa_fwd_fp8_varlen",
+    "fa_fp8_varlen_sizes", "fa_quantize_fp8_varlen", "fa_fwd_fp8_varlen", "fa_set_phase_buffer",
 )
 
 
@@ -66,49 +69,56 @@ def lib() -> ctypes.CDLL:
     with _lock:
         if _lib is not None:
             return _lib
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError("libfa_gb300.so is not built (%s); run "
-                               "`python -m attention_forward_fa2_gb300.build`" % LIB_PATH)
-        L = ctypes.CDLL(LIB_PATH)
-        vp, ci, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-        L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, vp, vp]
-        L.fa_fwd_qk.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp, vp, vp]
-        L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, vp, vp, ci, vp]
-        L.fa_check_status.argtypes = [vp, ctypes.POINTER(ci)]
-        L.fa_strerror.argtypes = [ci]
-        L.fa_strerror.restype = ctypes.c_char_p
-        L.fa_last_cuda_error.argtypes = []
-        L.fa_set_timeout_ns.argtypes = [ctypes.c_ulonglong]
-        L.fa_set_config.argtypes = [ctypes.c_char_p]
-        L.fa_get_config.argtypes = [ci, ci, ci, ctypes.c_char_p, ci]
-        L.fa_autotune.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, vp, vp]
-        L.fa_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, vp]
-        L.fa_version.argtypes = []
-        L.fa_splitkv_num_splits.argtypes = [ci, ci, ci, ci, ci, ci]
-        L.fa_splitkv_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
-        L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp,
-                                     ctypes.c_ulonglong, vp]
-        L.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
-        L.fa_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci]
-        L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp,
-                             ctypes.c_longlong, vp]
-        L.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci,
-                                    vp, ctypes.c_longlong, vp]
-        L.fa_fp8_sizes.argtypes = [ci, ci, ci, ci, ci, ci, ctypes.POINTER(ctypes.c_longlong)]
-        L.fa_quantize_fp8.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, vp]
-        L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp]
-        L.fa_fp8_varlen_sizes.argtypes = [ci, ci, ci, ci, ci, ci, ci, ci, ctypes.POINTER(ctypes.c_longlong)]
-        L.fa_quantize_fp8_varlen.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp,
-                                             vp, vp]
-        L.fa_fwd_fp8_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf,
-                                        ci, vp]
-        for name in EXPORTS:
-            if name != "fa_strerror":
-                getattr(L, name).restype = ci
-        L.fa_splitkv_workspace_bytes.restype = ctypes.c_longlong
-        L.fa_bwd_workspace_bytes.restype = ctypes.c_longlong
-        _lib = L
-        return L
+        _lib = load_library(LIB_PATH)
+        return _lib
+
+
+def load_library(path: str) -> ctypes.CDLL:
+    """Load a build of the library (the default one or the phase-clock one) and
+    declare the argument types of every C entry."""
+    if not os.path.exists(path):
+        raise RuntimeError("%s is not built; run `python -m attention_forward_fa2_gb300.build`"
+                           % os.path.basename(path))
+    L = ctypes.CDLL(path)
+    vp, ci, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, vp, vp]
+    L.fa_fwd_qk.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp, vp, vp]
+    L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, vp, vp, ci, vp]
+    L.fa_check_status.argtypes = [vp, ctypes.POINTER(ci)]
+    L.fa_strerror.argtypes = [ci]
+    L.fa_strerror.restype = ctypes.c_char_p
+    L.fa_last_cuda_error.argtypes = []
+    L.fa_set_timeout_ns.argtypes = [ctypes.c_ulonglong]
+    L.fa_set_config.argtypes = [ctypes.c_char_p]
+    L.fa_get_config.argtypes = [ci, ci, ci, ctypes.c_char_p, ci]
+    L.fa_autotune.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, vp, vp]
+    L.fa_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, vp]
+    L.fa_version.argtypes = []
+    L.fa_splitkv_num_splits.argtypes = [ci, ci, ci, ci, ci, ci]
+    L.fa_splitkv_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
+    L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp,
+                                 ctypes.c_ulonglong, vp]
+    L.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
+    L.fa_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci]
+    L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp,
+                         ctypes.c_longlong, vp]
+    L.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci,
+                                vp, ctypes.c_longlong, vp]
+    L.fa_fp8_sizes.argtypes = [ci, ci, ci, ci, ci, ci, ctypes.POINTER(ctypes.c_longlong)]
+    L.fa_quantize_fp8.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, vp]
+    L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp]
+    L.fa_fp8_varlen_sizes.argtypes = [ci, ci, ci, ci, ci, ci, ci, ci, ctypes.POINTER(ctypes.c_longlong)]
+    L.fa_quantize_fp8_varlen.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp,
+                                         vp, vp]
+    L.fa_fwd_fp8_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf,
+                                    ci, vp]
+    L.fa_set_phase_buffer.argtypes = [vp, ctypes.c_longlong]
+    for name in EXPORTS:
+        if name != "fa_strerror":
+            getattr(L, name).restype = ci
+    L.fa_splitkv_workspace_bytes.restype = ctypes.c_longlong
+    L.fa_bwd_workspace_bytes.restype = ctypes.c_longlong
+    return L
 
 
 # ------------------------------------------------------------ raw C-ABI calls

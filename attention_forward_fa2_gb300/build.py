@@ -3,7 +3,7 @@
 nvcc compiles each translation unit for sm_103a in parallel, then links a
 shared library with the C ABI of include/fa.h.  Usage:
 
-    python -m attention_forward_fa2_gb300.build [--force] [--verbose]
+    python -m attention_forward_fa2_gb300.build [--force] [--verbose] [--phase]
 """
 from __future__ import annotations
 
@@ -19,6 +19,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfa_gb300.so")
+# The same sources with the phase clocks compiled in (FA_PHASE_CLOCKS=1).
+BUILD_PHASE = os.path.join(PKG, "_build_phase")
+LIB_PHASE = os.path.join(PKG, "libfa_gb300_phase.so")
 UNITS = ("fa_api.cu", "fa_fwd_d128.cu", "fa_fwd_d128_bc64.cu", "fa_fwd_d128_causal.cu",
          "fa_fwd_d64.cu", "fa_fwd_d64_bc64.cu", "fa_fwd_d64_causal.cu", "fa_fwd_quad.cu",
          "fa_fwd_split.cu", "fa_static_scratch.cu", "fa_bwd.cu", "fa_fp8.cu",
@@ -50,17 +53,22 @@ def _newest_input() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile (if stale) and return the path of the shared library."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, phase: bool = False) -> str:
+    """Compile (if stale) and return the path of the shared library.
+
+    phase=True builds libfa_gb300_phase.so instead: the same sources with the
+    kernel's phase clocks compiled in (fa_set_phase_buffer), for profiling."""
+    lib, bdir = (LIB_PHASE, BUILD_PHASE) if phase else (LIB, BUILD)
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _newest_input():
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
+    defs = ["-DFA_PHASE_CLOCKS=1"] if phase else []
     procs = []
     for unit in UNITS:
-        obj = os.path.join(BUILD, unit.replace(".cu", ".o"))
-        log = open(os.path.join(BUILD, unit.replace(".cu", ".ptxas.log")), "w")
-        cmd = [cc] + NVCC_FLAGS + ["-I", INCLUDE, "-I", CSRC, "-c", os.path.join(CSRC, unit), "-o", obj]
+        obj = os.path.join(bdir, unit.replace(".cu", ".o"))
+        log = open(os.path.join(bdir, unit.replace(".cu", ".ptxas.log")), "w")
+        cmd = [cc] + NVCC_FLAGS + defs + ["-I", INCLUDE, "-I", CSRC, "-c", os.path.join(CSRC, unit), "-o", obj]
         procs.append((unit, obj, log, subprocess.Popen(cmd, stdout=log, stderr=subprocess.STDOUT)))
     failed = []
     for unit, obj, log, proc in procs:
@@ -73,20 +81,21 @@ def build(force: bool = False, verbose: bool = False) -> str:
                 sys.stderr.write(f.read())
     if failed:
         raise RuntimeError("nvcc failed for: %s" % ", ".join(failed))
-    tmp = LIB + ".tmp.%d" % os.getpid()
+    tmp = lib + ".tmp.%d" % os.getpid()
     link = [cc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-o", tmp]
     link += [obj for _, obj, _, _ in procs]
     subprocess.run(link, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
+    ap.add_argument("--phase", action="store_true", help="build libfa_gb300_phase.so (phase clocks)")
     args = ap.parse_args(argv)
-    print(build(force=args.force, verbose=args.verbose))
+    print(build(force=args.force, verbose=args.verbose, phase=args.phase))
 
 
 if __name__ == "__main__":

@@ -37,6 +37,11 @@ thread_local int t_last_cuda_error = 0;
 std::mutex g_mu;
 unsigned long long g_timeout_ns = 1000000000ull;
 
+// Phase-clock buffer of the instrumented build (FA_PHASE_CLOCKS=1): device
+// words, kPhaseWords per CTA; null = not attached.
+unsigned long long* g_phase_buf = nullptr;
+long long g_phase_words = 0;
+
 // Tile configuration ("Flash Attention 2 Chapter6", Kernel 7 searches B_r, B_c
 // and the pipeline depth per shape).
 struct Config {
@@ -107,6 +112,34 @@ int device_state(DeviceState** out) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Forward grid.  Packed variable-length batches launch one CTA per work item
+// and the running CTAs take over the items of CTAs not yet started (cluster
+// launch control: a dynamic schedule for units of unequal work); dense
+// problems launch one CTA per SM (at most the item count), each walking the
+// items blockIdx.x + k * gridDim.x.
+dim3 grid_for(int num_items, bool dynamic, int num_sms) {
+  return dim3(static_cast<unsigned>(dynamic || num_items < num_sms ? num_items : num_sms), 1, 1);
+}
+
+// Attaches the phase-clock buffer to a forward launch whose grid is set
+// (instrumented build only; the default build always leaves it null).
+int attach_phase(fa::LaunchArgs& a) {
+  a.p.phase = nullptr;
+  a.p.trace_off = 0;
+#if FA_PHASE_CLOCKS
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_phase_buf != nullptr) {
+    const long long need = static_cast<long long>(a.grid.x) * fa::kPhaseWords;
+    if (need > g_phase_words) return FA_ERR_INVALID_ARG;
+    a.p.phase = g_phase_buf;
+    // The event trace of CTA 0 follows the per-CTA words when there is room.
+    if (need + fa::kTraceWords <= g_phase_words && need <= 0x7fffffffLL - fa::kTraceWords)
+      a.p.trace_off = static_cast<int>(need);
+  }
+#endif
+  return FA_OK;
+}
 
 // Tiled tensor map (bf16 with 128-byte swizzle unless told otherwise).
 // dims/strides are innermost first; strides are in bytes for dims 1..rank-1.
@@ -345,7 +378,9 @@ int run(const Problem& P, const Config& cfg_in) {
   if (prc != FA_OK) return prc;
   fa::FwdParams& p = a.p;
   // Persistent grid: one CTA per SM (each walks items blockIdx.x + k * gridDim.x).
-  a.grid = dim3(static_cast<unsigned>(p.num_items < st->num_sms ? p.num_items : st->num_sms), 1, 1);
+  a.grid = grid_for(p.num_items, varlen, st->num_sms);
+  const int arc = attach_phase(a);
+  if (arc != FA_OK) return arc;
 
   cudaError_t e;
   if (p.causal)
@@ -414,7 +449,9 @@ int run_split(const Problem& P, const Config& cfg, int requested_splits, void* w
   const size_t rows = static_cast<size_t>(P.B) * P.H * P.Nq;
   p.ws_o = static_cast<float*>(ws);
   p.ws_lse = p.ws_o + static_cast<size_t>(splits) * rows * P.d;
-  a.grid = dim3(static_cast<unsigned>(p.num_items < st->num_sms ? p.num_items : st->num_sms), 1, 1);
+  a.grid = grid_for(p.num_items, false, st->num_sms);
+  const int arc = attach_phase(a);
+  if (arc != FA_OK) return arc;
   cudaError_t e;
   if (P.d == 128)
     e = p.causal ? fa::launch_fwd_split<128, 2, true>(a) : fa::launch_fwd_split<128, 2, false>(a);
@@ -617,6 +654,16 @@ __global__ void wait_timeout_kernel(unsigned long long timeout_ns, int* status) 
 }
 
 }  // namespace
+
+namespace fa {
+// Argument check of the key-split form, shared with the allocation-free entry
+// so that both return the same code for the same arguments.
+int check_split_problem(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Nq,
+                        int Nk, int H, int Hk, int d, float scale, int flags) {
+  Problem P{q, k, v, o, lse, B, Nq, Nk, H, Hk, d, scale, nullptr, nullptr, flags, nullptr};
+  return validate(P);
+}
+}  // namespace fa
 
 extern "C" {
 
@@ -875,7 +922,8 @@ int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_s
   a.p.v_scale = v_scale;
   a.p.q_blocks = (Nq + fa::kBR - 1) / fa::kBR;
   a.p.k_blocks = (Nk + fa::kBR - 1) / fa::kBR;
-  a.grid = dim3(static_cast<unsigned>(a.p.num_items < st->num_sms ? a.p.num_items : st->num_sms), 1, 1);
+  a.grid = grid_for(a.p.num_items, false, st->num_sms);
+  if ((rc = attach_phase(a)) != FA_OK) return rc;
   const cudaError_t e = fa::launch_fwd_fp8((flags & FA_FLAG_CAUSAL) != 0, a);
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
@@ -961,7 +1009,9 @@ int fa_fwd_fp8_varlen(const void* q8, const void* k8, const void* vt8, const flo
   a.p.k_blocks = (max_seqlen_k + fa::kBR - 1) / fa::kBR;
   a.p.total_q = total_q;
   a.p.total_k = total_k;
-  a.grid = dim3(static_cast<unsigned>(a.p.num_items < st->num_sms ? a.p.num_items : st->num_sms), 1, 1);
+  a.grid = grid_for(a.p.num_items, true, st->num_sms);
+  const int arc = attach_phase(a);
+  if (arc != FA_OK) return arc;
   const cudaError_t e = fa::launch_fwd_fp8_varlen((flags & FA_FLAG_CAUSAL) != 0, a);
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
@@ -986,6 +1036,21 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
   Problem P{q, k, v, o, lse, B, Nq, Nk, H, Hk, d, scale, nullptr, nullptr, flags,
             static_cast<cudaStream_t>(stream)};
   return run_split(P, pick_config(d, Nk, 0), num_splits, workspace, static_cast<size_t>(workspace_bytes));
+}
+
+int fa_set_phase_buffer(unsigned long long* buf, long long words) {
+#if FA_PHASE_CLOCKS
+  if (buf != nullptr && (words < fa::kPhaseWords || (reinterpret_cast<uintptr_t>(buf) & 7u) != 0))
+    return FA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_phase_buf = buf;
+  g_phase_words = buf ? words : 0;
+  return fa::kPhaseWords;
+#else
+  (void)buf;
+  (void)words;
+  return FA_ERR_UNSUPPORTED;
+#endif
 }
 
 int fa_version(void) { return 100; }

@@ -113,6 +113,107 @@ enum WaitSite : int {
   kSiteSoftS = 7,
   kSiteCorrFinal = 9,
   kSiteTeardown = 10,
+  kSiteItem = 11,
+};
+
+// Work items reach the roles through a ring of kItemSlots entries in shared
+// memory: the load thread writes item n (the x index of a CTA whose work this
+// CTA took over, or -1 at the end) and every consumer -- the MMA thread, the
+// eight softmax warps and the four epilogue warps -- releases the slot.
+constexpr int kItemSlots = 4;
+constexpr int kItemConsumers = 1 + 8 + 4;
+
+// Phase clocks: per-CTA cycle counts of where each role spends its time,
+// compiled in only when FA_PHASE_CLOCKS is 1 (a separate build of the
+// library; the default build has none of this code).  Each role keeps a few
+// accumulators in registers: `lap(i)` adds the cycles since the previous lap
+// to slot i, so a role's time is partitioned into its waits and its work; the
+// accumulators are stored once, at the end, to
+//   phase[blockIdx.x * kPhaseWords + role base + slot]  (unsigned 64-bit).
+#ifndef FA_PHASE_CLOCKS
+#define FA_PHASE_CLOCKS 0
+#endif
+
+constexpr int kPhaseWords = 48;   // per CTA
+constexpr int kPhaseRole = 8;     // slots per role
+enum PhaseBase : int {
+  kPhMma = 0,        // wait Q-full, wait K/V-full, wait P-full, wait O-empty, issue, steps, units
+  kPhLoad = 8,       // wait Q-empty, wait K/V-empty, issue, ring slots
+  kPhSoft0 = 16,     // tile 0 (warp 0, lane 0): wait S-full, store P and publish, steps, maximum
+                     // recomputed, final, load S, exponentials
+  kPhSoft1 = 24,     // tile 1 (warp 4, lane 0): same slots
+  kPhEpi = 32,       // warp 8, lane 0: wait l and O, read O, staging wait, store, tiles
+  kPhTimer = 40,     // %globaltimer (ns) at thread 0's start and end
+};
+enum PhaseSlot : int {
+  kPhMmaWaitQ = 0, kPhMmaWaitKV = 1, kPhMmaWaitP = 2, kPhMmaWaitO = 3, kPhMmaIssue = 4, kPhMmaSteps = 5,
+  kPhMmaUnits = 6,
+  kPhLoadWaitQ = 0, kPhLoadWaitKV = 1, kPhLoadIssue = 2, kPhLoadSlots = 3,
+  kPhSoftWait = 0, kPhSoftWork = 1, kPhSoftSteps = 2, kPhSoftSlow = 3, kPhSoftFinal = 4, kPhSoftLoad = 5,
+  kPhSoftExp = 6,
+  kPhEpiWait = 0, kPhEpiRead = 1, kPhEpiStage = 2, kPhEpiStore = 3, kPhEpiTiles = 4,
+};
+
+// Event trace (phase-clock builds): clock64 stamps of every hand-off of the
+// first kTraceUnits work units of CTA 0, at phase[trace_off + (unit *
+// kTraceSteps + step) * kTraceEvents + event], when the buffer has room.
+constexpr int kTraceUnits = 2;
+constexpr int kTraceSteps = 40;
+constexpr int kTraceEvents = 16;
+constexpr int kTraceWords = kTraceUnits * kTraceSteps * kTraceEvents;
+enum TraceEvent : int {
+  kTrMmaKV = 0,        // MMA thread: K/V slot of step j full
+  kTrMmaP0 = 1,        // MMA thread: P of tile 0 / 1 observed (step j covers P(j-1))
+  kTrMmaPV0 = 3,       // MMA thread: P V of tile 0 / 1 issued
+  kTrMmaS0 = 5,        // MMA thread: S of tile 0 / 1 issued and committed
+  kTrMmaOEmpty = 7,    // MMA thread: O-empty of tile 0 observed (first P V of the unit)
+  kTrSoftS0 = 8,       // softmax tile 0 / 1 (warp 0 / 4, lane 0): S(j) observed
+  kTrSoftP0 = 10,      // softmax tile 0 / 1: P(j) published
+  kTrSoftLoad0 = 12,   // softmax tile 0: S(j) in registers
+  kTrSoftExp0 = 13,    // softmax tile 0: exponentials done
+  kTrEpiO0 = 14,       // epilogue: O of tile 0 / 1 final observed
+};
+
+__device__ __forceinline__ void trace_event(unsigned long long* phase, int trace_off, int unit, int step, int ev) {
+#if FA_PHASE_CLOCKS
+  if (phase != nullptr && trace_off > 0 && blockIdx.x == 0 && unit < kTraceUnits && step < kTraceSteps)
+    phase[trace_off + (unit * kTraceSteps + step) * kTraceEvents + ev] = static_cast<unsigned long long>(clock64());
+#else
+  (void)phase;
+  (void)trace_off;
+  (void)unit;
+  (void)step;
+  (void)ev;
+#endif
+}
+#define FA_TRACE(unit, step, ev) trace_event(p.phase, p.trace_off, (unit), (step), (ev))
+
+struct PhaseClock {
+#if FA_PHASE_CLOCKS
+  unsigned long long acc[kPhaseRole];
+  long long t;
+  __device__ __forceinline__ void start() {
+#pragma unroll
+    for (int i = 0; i < kPhaseRole; ++i) acc[i] = 0;
+    t = clock64();
+  }
+  __device__ __forceinline__ void lap(int i) {
+    const long long n = clock64();
+    acc[i] += static_cast<unsigned long long>(n - t);
+    t = n;
+  }
+  __device__ __forceinline__ void count(int i, int n = 1) { acc[i] += static_cast<unsigned long long>(n); }
+  __device__ __forceinline__ void store(unsigned long long* phase, int base) const {
+    if (phase == nullptr) return;
+#pragma unroll
+    for (int i = 0; i < kPhaseRole; ++i) phase[static_cast<size_t>(blockIdx.x) * kPhaseWords + base + i] = acc[i];
+  }
+#else
+  __device__ __forceinline__ void start() {}
+  __device__ __forceinline__ void lap(int) {}
+  __device__ __forceinline__ void count(int, int = 1) {}
+  __device__ __forceinline__ void store(unsigned long long*, int) const {}
+#endif
 };
 
 struct FwdParams {
@@ -142,6 +243,8 @@ struct FwdParams {
   int total_q, total_k;        // variable-length form: packed rows (sequences past them are rejected)
   unsigned long long timeout_ns;
   int* status;                 // [4]: code, block, warp, site
+  unsigned long long* phase;   // phase clocks, [grid][kPhaseWords] (FA_PHASE_CLOCKS builds only; else null)
+  int trace_off;               // word offset of the event trace in `phase` (0: no trace)
 };
 
 // Error codes shared with the C-ABI header.
@@ -180,11 +283,16 @@ struct SmemLayout {
   static constexpr int kBarOFinal = kBarLReady + kQT;
   static constexpr int kBarOEmpty = kBarOFinal + kQT;
   static constexpr int kBarTeardown = kBarOEmpty + kQT;
-  static constexpr int kNumBars = kBarTeardown + 1;
+  static constexpr int kBarItemFull = kBarTeardown + 1;
+  static constexpr int kBarItemEmpty = kBarItemFull + kItemSlots;
+  static constexpr int kBarClc = kBarItemEmpty + kItemSlots;  // cancel response landed
+  static constexpr int kNumBars = kBarClc + 1;
   static constexpr int kOffInvL = kOffBar + ((kNumBars * 8 + 15) / 16) * 16;
   static constexpr int kOffTmem = kOffInvL + kQT * kBR * 4;
   static constexpr int kOffAbort = kOffTmem + 16;
-  static constexpr int kBytes = kOffAbort + 16;
+  static constexpr int kOffItems = kOffAbort + 16;  // kItemSlots ints
+  static constexpr int kOffClc = kOffItems + 16;    // 16-byte cancel response (16-byte aligned)
+  static constexpr int kBytes = kOffClc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
   static_assert(kOffKV % 1024 == 0 && kKVTileBytes % 1024 == 0 && kOffStage % 1024 == 0 &&
                     kStageWarpBytes % 1024 == 0,
@@ -316,12 +424,44 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   return w;
 }
 
-// Persistent walk over the work units of this CTA: items blockIdx.x,
-// blockIdx.x + gridDim.x, ...; each item is units_per_item consecutive units.
-// Every role runs the same walk, so all roles see the same unit sequence.
-#define FA_FOR_EACH_UNIT(u)                                                          \
-  for (int it_ = blockIdx.x; it_ < p.num_items && ok; it_ += gridDim.x)               \
-    for (int sub_ = 0, u = it_ * p.units_per_item;                                     \
+// Next entry of this CTA's work-item sequence (consumer side of the item
+// ring): the item, -1 at the end, -2 if a wait gave up.  `n` counts the items
+// read so far; `warp`: the whole warp reads and lane 0 releases the slot,
+// else a single thread does both.
+// The grid has one CTA per work item; a CTA starts with item blockIdx.x and
+// its load thread takes over the items of CTAs that have not started yet
+// (cluster launch control), so items are handed out in launch order to
+// whichever SM is free: CTAs never drift apart over unequal work (variable
+// lengths), which keeps the K/V of the heads in flight together in L2.
+__device__ __forceinline__ int item_next(uint32_t bar_full, uint32_t bar_empty, const volatile int* items,
+                                         volatile int* abort, uint64_t tmo, int* status, uint32_t& n, bool warp) {
+  const uint32_t slot = n % kItemSlots;
+  const uint32_t parity = (n / kItemSlots) & 1u;
+  const bool got = warp ? ptx::mbar_wait_warp(bar_full + 8u * slot, parity, abort, tmo)
+                        : ptx::mbar_wait(bar_full + 8u * slot, parity, abort, tmo);
+  if (!got) {
+    if (!warp || (threadIdx.x & 31) == 0) record_error(status, kErrTimeout, kSiteItem);
+    return -2;
+  }
+  const int item = items[slot];
+  if (warp) __syncwarp();
+  if (!warp || (threadIdx.x & 31) == 0) ptx::mbar_arrive(bar_empty + 8u * slot);
+  ++n;
+  return item;
+}
+
+// Walk over the work units of this CTA: each item is units_per_item
+// consecutive units.  Every role reads the same item sequence, so all roles
+// see the same unit sequence.
+// Dynamic (kDynamic: the item ring) or static (items blockIdx.x,
+// blockIdx.x + gridDim.x, ... on a grid of one CTA per SM) item sequence.
+#define FA_NEXT_ITEM(prev)                                                                        \
+  (kDynamic ? item_next(bar(L::kBarItemFull), bar(L::kBarItemEmpty), s_items, s_abort, tmo, p.status, \
+                        item_n_, warp != 12)                                                      \
+            : ((prev) < 0 ? static_cast<int>(blockIdx.x) : (prev) + static_cast<int>(gridDim.x)))
+#define FA_FOR_EACH_UNIT(u)                                                                       \
+  for (int it_ = FA_NEXT_ITEM(-1); it_ >= 0 && it_ < p.num_items && ok; it_ = FA_NEXT_ITEM(it_))  \
+    for (int sub_ = 0, u = it_ * p.units_per_item;                                                  \
          sub_ < p.units_per_item && u < p.num_units && ok; ++sub_, ++u)
 
 template <int D, int BC, int STAGES, bool VARLEN, bool CAUSAL, bool SPLIT = false, bool QUAD = false,
@@ -336,6 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Variable-length tiles: shifted at a sequence's end, except FP8 ones (which
   // must coincide with quantisation blocks).
   constexpr bool kShift = VARLEN && !FP8;
+  // Packed variable-length batches hand out work items dynamically (units of
+  // unequal work); dense problems, whose units are all alike, walk a static
+  // round-robin over a grid of one CTA per SM.
+  constexpr bool kDynamic = VARLEN;
   static_assert(BC == 64 || BC == 128, "key tile");
   static_assert(2 * BC + 2 * D <= 512, "TMEM columns");
   static_assert(!QUAD || (BC == 128 && !CAUSAL && !SPLIT), "quad reduction: 128-key tiles, no mask or split");
@@ -358,7 +502,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* const s_invl = reinterpret_cast<float*>(gbase + L::kOffInvL);
   volatile uint32_t* const s_tmem = reinterpret_cast<volatile uint32_t*>(gbase + L::kOffTmem);
   volatile int* const s_abort = reinterpret_cast<volatile int*>(gbase + L::kOffAbort);
+  volatile int* const s_items = reinterpret_cast<volatile int*>(gbase + L::kOffItems);
   const uint64_t tmo = p.timeout_ns;
+  // Items read from the work-item ring (the MMA thread reads alone, the
+  // softmax and epilogue warps read warp-wide; the load thread writes it).
+  uint32_t item_n_ = 0;
 
   // ------------------------------------------------------------------ setup
   if (warp == 13 && lane == 0) {
@@ -383,6 +531,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(L::kBarOEmpty + t), kBR);  // epilogue finished reading O_t
     }
     ptx::mbar_init(bar(L::kBarTeardown), 1);
+    for (int i = 0; i < kItemSlots; ++i) {
+      ptx::mbar_init(bar(L::kBarItemFull + i), 1);
+      ptx::mbar_init(bar(L::kBarItemEmpty + i), kItemConsumers);
+    }
+    ptx::mbar_init(bar(L::kBarClc), 1);
     ptx::fence_mbar_init();
   }
   if (warp == 12) {
@@ -393,6 +546,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *s_tmem;
+#if FA_PHASE_CLOCKS
+  if (threadIdx.x == 0 && p.phase) p.phase[static_cast<size_t>(blockIdx.x) * kPhaseWords + kPhTimer] = ptx::globaltimer_ns();
+#endif
 
   if (warp >= 12) {
     ptx::setmaxnreg_dec<RegSplit<VARLEN>::kOther>();
@@ -401,77 +557,140 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t qcount = 0;  // units whose Q was loaded
       uint32_t g = 0;       // ring slots handed to the TMA unit so far
       bool ok = true;
-#pragma unroll 1
-      FA_FOR_EACH_UNIT(u) {
-        const Unit w = decode_unit<BC, VARLEN, CAUSAL, SPLIT, kShift>(p, u);
-        if (!w.run) continue;
-        // Q of this unit, once the previous unit's S MMAs no longer read it.
-        if (!ptx::mbar_wait(bar(L::kBarQEmpty), (qcount & 1u) ^ 1u, s_abort, tmo)) {
-          record_error(p.status, kErrTimeout, kSiteLoadQ);
-          ok = false;
-          break;
+      PhaseClock ph;
+      ph.start();
+      // Dynamic schedule: the load thread produces the work-item ring, this
+      // CTA's own item first, then the items of CTAs whose launch the hardware
+      // cancelled on request.  The request for the next item is issued when an
+      // item starts, so its answer is back by the time the item's loads are
+      // all issued.  Static schedule: items blockIdx.x + k * gridDim.x.
+      uint32_t n_pub = 0, n_clc = 0;
+      bool clc_pending = false;
+      auto publish = [&](int item) -> bool {
+        const uint32_t slot = n_pub % kItemSlots;
+        if (!ptx::mbar_wait(bar(L::kBarItemEmpty + slot), ((n_pub / kItemSlots) & 1u) ^ 1u, s_abort, tmo)) {
+          record_error(p.status, kErrTimeout, kSiteItem);
+          return false;
         }
-        uint32_t q_bytes = 0;
-#pragma unroll
-        for (int t = 0; t < kQT; ++t) q_bytes += w.active[t] ? L::kQTileBytes : 0;
-        ptx::mbar_arrive_expect_tx(bar(L::kBarQFull), q_bytes);
-        ++qcount;
-#pragma unroll
-        for (int t = 0; t < kQT; ++t) {
-          if (!w.active[t]) continue;
-#pragma unroll
-          for (int pnl = 0; pnl < kDPanels; ++pnl) {
-            const uint32_t dst = base + L::kOffQ + t * L::kQTileBytes + pnl * L::kQPanelBytes;
-            if constexpr (VARLEN)
-              ptx::tma_load_3d(dst, &tm_q, bar(L::kBarQFull), pnl * kPanelElems, w.h, w.qwin[t].load_row);
-            else
-              ptx::tma_load_4d(dst, &tm_q, bar(L::kBarQFull), pnl * kPanelElems, w.h, w.qwin[t].load_row, w.b);
-          }
-        }
+        s_items[slot] = item;
+        ptx::mbar_arrive(bar(L::kBarItemFull + slot));
+        ++n_pub;
+        return true;
+      };
+      auto request = [&]() {
+        ptx::fence_proxy_async_smem();  // the previous answer was read before it is overwritten
+        ptx::mbar_arrive_expect_tx(bar(L::kBarClc), 16);
+        ptx::clc_try_cancel(base + L::kOffClc, bar(L::kBarClc));
+        clc_pending = true;
+      };
+      int cur = blockIdx.x;
+      if constexpr (kDynamic) {
+        ok = publish(cur);
+        if (ok) request();
+      }
 #pragma unroll 1
-        for (int j = 0; j <= w.nkv; ++j) {
-          const uint32_t slot = g % STAGES;
-          if (!ptx::mbar_wait(bar(L::kBarKVEmpty + slot), ((g / STAGES) & 1u) ^ 1u, s_abort, tmo)) {
-            record_error(p.status, kErrTimeout, kSiteLoadKV);
+      while (ok && cur >= 0 && cur < p.num_items) {
+#pragma unroll 1
+        for (int sub_ = 0, u = cur * p.units_per_item; sub_ < p.units_per_item && u < p.num_units && ok;
+             ++sub_, ++u) {
+          const Unit w = decode_unit<BC, VARLEN, CAUSAL, SPLIT, kShift>(p, u);
+          if (!w.run) continue;
+          // Q of this unit, once the previous unit's S MMAs no longer read it.
+          ph.lap(kPhLoadIssue);
+          if (!ptx::mbar_wait(bar(L::kBarQEmpty), (qcount & 1u) ^ 1u, s_abort, tmo)) {
+            record_error(p.status, kErrTimeout, kSiteLoadQ);
             ok = false;
             break;
           }
-          const uint32_t bytes = (j < w.nkv ? L::kKVTileBytes : 0) + (j >= 1 ? L::kKVTileBytes : 0);
-          ptx::mbar_arrive_expect_tx(bar(L::kBarKVFull + slot), bytes);
-          ++g;
-          const uint32_t sbase = base + L::kOffKV + slot * L::kSlotBytes;
-          if (j < w.nkv) {
-            const RowWindow kw = make_window<kShift>(w.k_start, w.k_end, w.k_start + (w.j0 + j) * BC, BC);
+          ph.lap(kPhLoadWaitQ);
+          uint32_t q_bytes = 0;
+#pragma unroll
+          for (int t = 0; t < kQT; ++t) q_bytes += w.active[t] ? L::kQTileBytes : 0;
+          ptx::mbar_arrive_expect_tx(bar(L::kBarQFull), q_bytes);
+          ++qcount;
+#pragma unroll
+          for (int t = 0; t < kQT; ++t) {
+            if (!w.active[t]) continue;
 #pragma unroll
             for (int pnl = 0; pnl < kDPanels; ++pnl) {
-              const uint32_t dst = sbase + pnl * L::kKVPanelBytes;
+              const uint32_t dst = base + L::kOffQ + t * L::kQTileBytes + pnl * L::kQPanelBytes;
               if constexpr (VARLEN)
-                ptx::tma_load_3d(dst, &tm_k, bar(L::kBarKVFull + slot), pnl * kPanelElems, w.hk, kw.load_row);
+                ptx::tma_load_3d(dst, &tm_q, bar(L::kBarQFull), pnl * kPanelElems, w.h, w.qwin[t].load_row);
               else
-                ptx::tma_load_4d(dst, &tm_k, bar(L::kBarKVFull + slot), pnl * kPanelElems, w.hk, kw.load_row, w.b);
+                ptx::tma_load_4d(dst, &tm_q, bar(L::kBarQFull), pnl * kPanelElems, w.h, w.qwin[t].load_row, w.b);
             }
           }
-          if (j >= 1) {
-            const RowWindow vw = make_window<kShift>(w.k_start, w.k_end, w.k_start + (w.j0 + j - 1) * BC, BC);
-            if constexpr (FP8 && VARLEN) {
-              // V^T tile: d rows x 128 keys (one box, keys innermost) from the sequence's columns.
-              const int col = static_cast<int>(fp8_vt_col0(w.k_start, w.b)) + (vw.load_row - w.k_start);
-              ptx::tma_load_3d(sbase + L::kKVTileBytes, &tm_v, bar(L::kBarKVFull + slot), col, 0, w.hk);
-            } else if constexpr (FP8) {
-              ptx::tma_load_4d(sbase + L::kKVTileBytes, &tm_v, bar(L::kBarKVFull + slot), vw.load_row, 0, w.hk, w.b);
-            } else {
+#pragma unroll 1
+          for (int j = 0; j <= w.nkv; ++j) {
+            const uint32_t slot = g % STAGES;
+            ph.lap(kPhLoadIssue);
+            if (!ptx::mbar_wait(bar(L::kBarKVEmpty + slot), ((g / STAGES) & 1u) ^ 1u, s_abort, tmo)) {
+              record_error(p.status, kErrTimeout, kSiteLoadKV);
+              ok = false;
+              break;
+            }
+            ph.lap(kPhLoadWaitKV);
+            ph.count(kPhLoadSlots);
+            const uint32_t bytes = (j < w.nkv ? L::kKVTileBytes : 0) + (j >= 1 ? L::kKVTileBytes : 0);
+            ptx::mbar_arrive_expect_tx(bar(L::kBarKVFull + slot), bytes);
+            ++g;
+            const uint32_t sbase = base + L::kOffKV + slot * L::kSlotBytes;
+            if (j < w.nkv) {
+              const RowWindow kw = make_window<kShift>(w.k_start, w.k_end, w.k_start + (w.j0 + j) * BC, BC);
 #pragma unroll
               for (int pnl = 0; pnl < kDPanels; ++pnl) {
-                const uint32_t dst = sbase + L::kKVTileBytes + pnl * L::kKVPanelBytes;
+                const uint32_t dst = sbase + pnl * L::kKVPanelBytes;
                 if constexpr (VARLEN)
-                  ptx::tma_load_3d(dst, &tm_v, bar(L::kBarKVFull + slot), pnl * kPanel, w.hk, vw.load_row);
+                  ptx::tma_load_3d(dst, &tm_k, bar(L::kBarKVFull + slot), pnl * kPanelElems, w.hk, kw.load_row);
                 else
-                  ptx::tma_load_4d(dst, &tm_v, bar(L::kBarKVFull + slot), pnl * kPanel, w.hk, vw.load_row, w.b);
+                  ptx::tma_load_4d(dst, &tm_k, bar(L::kBarKVFull + slot), pnl * kPanelElems, w.hk, kw.load_row, w.b);
+              }
+            }
+            if (j >= 1) {
+              const RowWindow vw = make_window<kShift>(w.k_start, w.k_end, w.k_start + (w.j0 + j - 1) * BC, BC);
+              if constexpr (FP8 && VARLEN) {
+                // V^T tile: d rows x 128 keys (one box, keys innermost) from the sequence's columns.
+                const int col = static_cast<int>(fp8_vt_col0(w.k_start, w.b)) + (vw.load_row - w.k_start);
+                ptx::tma_load_3d(sbase + L::kKVTileBytes, &tm_v, bar(L::kBarKVFull + slot), col, 0, w.hk);
+              } else if constexpr (FP8) {
+                ptx::tma_load_4d(sbase + L::kKVTileBytes, &tm_v, bar(L::kBarKVFull + slot), vw.load_row, 0, w.hk, w.b);
+              } else {
+#pragma unroll
+                for (int pnl = 0; pnl < kDPanels; ++pnl) {
+                  const uint32_t dst = sbase + L::kKVTileBytes + pnl * L::kKVPanelBytes;
+                  if constexpr (VARLEN)
+                    ptx::tma_load_3d(dst, &tm_v, bar(L::kBarKVFull + slot), pnl * kPanel, w.hk, vw.load_row);
+                  else
+                    ptx::tma_load_4d(dst, &tm_v, bar(L::kBarKVFull + slot), pnl * kPanel, w.hk, vw.load_row, w.b);
+                }
               }
             }
           }
         }
+        if (!ok) break;
+        if constexpr (kDynamic) {
+          // The next item: the cancelled CTA's index, or -1 when none is left.
+          if (!ptx::mbar_wait(bar(L::kBarClc), n_clc & 1u, s_abort, tmo)) {
+            record_error(p.status, kErrTimeout, kSiteItem);
+            ok = false;
+            break;
+          }
+          ++n_clc;
+          clc_pending = false;
+          cur = ptx::clc_cancelled_x(base + L::kOffClc);
+          if (!publish(cur)) {
+            ok = false;
+            break;
+          }
+          if (cur >= 0) request();
+        } else {
+          cur += gridDim.x;
+        }
       }
+      ph.lap(kPhLoadIssue);
+      ph.store(p.phase, kPhLoad);
+      // An answer still in flight is written by the async proxy: wait for it.
+      if (clc_pending) ptx::mbar_wait_drain(bar(L::kBarClc), n_clc & 1u, tmo);
       // Teardown: never leave a TMA write to shared memory in flight.  Slot s
       // last received ring index s + STAGES * (rounds - 1).
       if (qcount > 0) ptx::mbar_wait_drain(bar(L::kBarQFull), (qcount - 1) & 1u, tmo);
@@ -488,26 +707,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t qcount = 0, g = 0;
       uint32_t pc[kQT] = {0, 0};  // P-full completions consumed, per tile
       uint32_t uc[kQT] = {0, 0};  // units with the tile active, per tile
+      int tr_unit = 0;            // units issued (event trace)
       bool ok = true;
+      PhaseClock ph;
+      ph.start();
 #pragma unroll 1
       FA_FOR_EACH_UNIT(u) {
         const Unit w = decode_unit<BC, VARLEN, CAUSAL, SPLIT, kShift>(p, u);
         if (!w.run) continue;
+        ph.lap(kPhMmaIssue);
         if (!ptx::mbar_wait(bar(L::kBarQFull), qcount & 1u, s_abort, tmo)) {
           record_error(p.status, kErrTimeout, kSiteMmaQ);
           ok = false;
           break;
         }
+        ph.lap(kPhMmaWaitQ);
+        ph.count(kPhMmaUnits);
         ++qcount;
         ptx::tc_fence_after();
 #pragma unroll 1
         for (int j = 0; j <= w.nkv && ok; ++j) {
           const uint32_t slot = g % STAGES;
+          ph.lap(kPhMmaIssue);
           if (!ptx::mbar_wait(bar(L::kBarKVFull + slot), (g / STAGES) & 1u, s_abort, tmo)) {
             record_error(p.status, kErrTimeout, kSiteMmaK);
             ok = false;
             break;
           }
+          ph.lap(kPhMmaWaitKV);
+          ph.count(kPhMmaSteps);
+          FA_TRACE(tr_unit, j, kTrMmaKV);
           ptx::tc_fence_after();
           const uint32_t k_base = base + L::kOffKV + slot * L::kSlotBytes;
           const uint32_t v_base = k_base + L::kKVTileBytes;
@@ -520,11 +749,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tO = tmem + static_cast<uint32_t>(2 * BC + t * D);
             if (j >= 1 && j <= nt) {
               // O_t += P_t(j-1) V(j-1), once P is written and O rescaled.
+              ph.lap(kPhMmaIssue);
               if (!ptx::mbar_wait(bar(L::kBarPFull + t), pc[t] & 1u, s_abort, tmo)) {
                 record_error(p.status, kErrTimeout, kSiteMmaP);
                 ok = false;
                 break;
               }
+              ph.lap(kPhMmaWaitP);
+              FA_TRACE(tr_unit, j, kTrMmaP0 + t);
               ++pc[t];
               // The first P V of a unit overwrites O_t: the epilogue of the
               // previous unit must have finished reading it.
@@ -533,6 +765,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
               }
+              ph.lap(kPhMmaWaitO);
+              if (j == 1 && t == 0) FA_TRACE(tr_unit, j, kTrMmaOEmpty);
               ptx::tc_fence_after();
               // Descriptors advance by byte offset / 16 in their low word (the
               // address field cannot carry: shared addresses stay below 256 KiB);
@@ -556,6 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                               (j - 1 > 0 || kk > 0) ? 1u : 0u);
               }
               if (j == nt) ptx::mma_commit(bar(L::kBarOFinal + t));
+              FA_TRACE(tr_unit, j, kTrMmaPV0 + t);
             }
             if (j < nt) {
               // S_t = Q_t K(j)^T
@@ -578,6 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               }
               ptx::mma_commit(bar(L::kBarSFull + t));
+              FA_TRACE(tr_unit, j, kTrMmaS0 + t);
             }
           }
           if (!ok) break;
@@ -588,7 +824,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int t = 0; t < kQT; ++t) uc[t] += w.active[t] ? 1u : 0u;
+        ++tr_unit;
       }
+      ph.lap(kPhMmaIssue);
+      ph.store(p.phase, kPhMma);
       // Teardown: all MMAs must be complete before TMEM is released.
       ptx::mma_commit(bar(L::kBarTeardown));
       if (!ptx::mbar_wait_drain(bar(L::kBarTeardown), 0, tmo)) record_error(p.status, kErrTimeout, kSiteTeardown);
@@ -606,7 +845,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rescale threshold), with a margin for the rounding of the exponent.
     const float accept_sum = exp2f(p.rescale_threshold) * 0.9990234375f;
     uint32_t sc = 0;  // S-full completions consumed
+    int tr_unit = 0;  // units processed (event trace)
+    const bool tr_lead = lane == 0 && (warp & 3) == 0;
     bool ok = true;
+    PhaseClock ph;
+    ph.start();
 #pragma unroll 1
     FA_FOR_EACH_UNIT(u) {
       const Unit w = decode_unit<BC, VARLEN, CAUSAL, SPLIT, kShift>(p, u);
@@ -635,11 +878,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         float l_q[4] = {0.f, 0.f, 0.f, 0.f};  // this thread's share of each row sum
 #pragma unroll 1
         for (int j = 0; j < nt; ++j) {
+          ph.lap(kPhSoftWork);
           if (!ptx::mbar_wait_warp(bar(L::kBarSFull + t), sc & 1u, s_abort, tmo)) {
             record_error(p.status, kErrTimeout, kSiteSoftS);
             ok = false;
             break;
           }
+          ph.lap(kPhSoftWait);
+          ph.count(kPhSoftSteps);
           ++sc;
           ptx::tc_fence_after();
           uint32_t raw[4][32];
@@ -774,11 +1020,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < nt; ++j) {
           // FP8: exp2 coefficient of this key tile (query and key scales folded in).
           const float c2j = FP8 ? cq * p.k_scale[(w.b * (p.H / p.group) + w.hk) * p.k_blocks + w.j0 + j] : c2;
+          ph.lap(kPhSoftWork);
           if (!ptx::mbar_wait_warp(bar(L::kBarSFull + t), sc & 1u, s_abort, tmo)) {
             record_error(p.status, kErrTimeout, kSiteSoftS);
             ok = false;
             break;
           }
+          ph.lap(kPhSoftWait);
+          ph.count(kPhSoftSteps);
+          if (tr_lead) FA_TRACE(tr_unit, j, kTrSoftS0 + t);
           ++sc;
           ptx::tc_fence_after();
           // S row of this thread, with the keys outside the row's window at -inf.
@@ -841,6 +1091,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             return ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
           };
           load_scores();
+          ph.lap(kPhSoftLoad);
+          if (tr_lead && t == 0) FA_TRACE(tr_unit, j, kTrSoftLoad0);
           // The reference maximum m only moves when a block maximum exceeds it
           // by more than the threshold T (log2 units); the merge identity of
           // §11.2 holds for any common reference value, so results stay exact.
@@ -858,6 +1110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (slow) load_scores();  // the scores were consumed
           }
           if (slow) {
+            ph.count(kPhSoftSlow);
             // Row max: four independent chains of three-input maxima.
             float mx[4] = {s[0], s[1], s[2], s[3]};
   #pragma unroll
@@ -886,6 +1139,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             lblk = exponentiate(neg);
           }
+          ph.lap(kPhSoftExp);
+          if (tr_lead && t == 0) FA_TRACE(tr_unit, j, kTrSoftExp0);
   #pragma unroll
           for (int c0 = 0; c0 < BC; c0 += 32) {
             if constexpr (FP8)
@@ -918,9 +1173,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ptx::tmem_wait_st();  // P stores (and any O rescale) have landed
           ptx::tc_fence_before();
+          if (tr_lead) FA_TRACE(tr_unit, j, kTrSoftP0 + t);
           ptx::mbar_arrive(bar(L::kBarPFull + t));
         }
         if (!ok) break;
+        ph.lap(kPhSoftWork);
         // Final message for the epilogue: 1 / l, and the row's log-sum-exp.
         const bool has = l > 0.f;
         s_invl[t * kBR + row] = has ? vsc / l : 0.f;
@@ -936,7 +1193,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       ptx::mbar_arrive(bar(L::kBarLReady + t));
+      ph.lap(kPhSoftFinal);
+      ++tr_unit;
     }
+    if (lane == 0 && (warp & 3) == 0) ph.store(p.phase, t == 0 ? kPhSoft0 : kPhSoft1);
   } else {
     ptx::setmaxnreg_dec<RegSplit<VARLEN>::kCorrection>();
     // ================================================= correction + epilogue
@@ -946,8 +1206,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // This warp's 32 output rows are staged here for the TMA store.
     const uint32_t stage = base + L::kOffStage + wq * L::kStageWarpBytes;
     uint32_t uc[kQT] = {0, 0};
+    int tr_unit = 0;       // units processed (event trace)
     bool pending = false;  // a TMA store from the staging area may still be reading it
     bool ok = true;
+    PhaseClock ph;
+    ph.start();
 #pragma unroll 1
     FA_FOR_EACH_UNIT(u) {
       const Unit w = decode_unit<BC, VARLEN, CAUSAL, SPLIT, kShift>(p, u);
@@ -989,12 +1252,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (r >= zw.lo && r < zw.hi) p.lse[w.lse_base + (zw.load_row - w.q_start + r)] = -INFINITY;
         }
         if (!w.active[t]) continue;
+        ph.lap(kPhEpiStore);
         if (!ptx::mbar_wait_warp(bar(L::kBarLReady + t), uc[t] & 1u, s_abort, tmo) ||
             !ptx::mbar_wait_warp(bar(L::kBarOFinal + t), uc[t] & 1u, s_abort, tmo)) {
           record_error(p.status, kErrTimeout, kSiteCorrFinal);
           ok = false;
           break;
         }
+        ph.lap(kPhEpiWait);
+        ph.count(kPhEpiTiles);
+        if (lane == 0 && warp == 8) FA_TRACE(tr_unit, 0, kTrEpiO0 + t);
         ++uc[t];
         ptx::tc_fence_after();
         const float inv_l = s_invl[t * kBR + row];
@@ -1016,6 +1283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           pending = false;
         }
+        ph.lap(kPhEpiStage);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
@@ -1056,6 +1324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O_t has been read: the next unit's first P V may overwrite it.
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::kBarOEmpty + t));
+        ph.lap(kPhEpiRead);
         if (use_tma) {
           ptx::fence_proxy_async_smem();
           __syncwarp();
@@ -1072,14 +1341,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           pending = true;
         }
       }
+      ++tr_unit;
     }
     if (lane == 0 && pending) ptx::bulk_wait_group_read_0();
+    ph.lap(kPhEpiStore);
+    if (lane == 0 && warp == 8) ph.store(p.phase, kPhEpi);
   }
 
   // ---------------------------------------------------------------- teardown
   __syncwarp();  // single-lane roles rejoin their warp before the CTA barrier
   ptx::tc_fence_before();
   __syncthreads();
+#if FA_PHASE_CLOCKS
+  if (threadIdx.x == 0 && p.phase)
+    p.phase[static_cast<size_t>(blockIdx.x) * kPhaseWords + kPhTimer + 1] = ptx::globaltimer_ns();
+#endif
   if (warp == 12) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);

@@ -113,6 +113,12 @@ cudaError_t launch_fwd_fp8(bool causal, const LaunchArgs& a);
 cudaError_t launch_fwd_fp8_varlen(bool causal, const LaunchArgs& a);
 int fp8_smem_bytes();
 
+// Host-side argument check of the key-split form (the checks fa_fwd_splitkv
+// makes before sizing its workspace): FA_OK, 1 for a problem with nothing to
+// do, or a negative FA_ERR_* code.
+int check_split_problem(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Nq,
+                        int Nk, int H, int Hk, int d, float scale, int flags);
+
 // Merge of the key splits (fa_combine.cuh); D in {64, 128}.
 cudaError_t launch_combine(int D, const float* ws_o, const float* ws_lse, int S, long long rows, int H,
                            int Nq, __nv_bfloat16* o, float* lse, cudaStream_t stream);

@@ -20,6 +20,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_launch.h"
 
 namespace {
 
@@ -57,8 +58,20 @@ extern "C" {
 int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                            int Nq, int Nk, int H, int Hk, int d, float scale, int flags,
                            int num_splits, void* stream) {
-  if (B == 0 || Nq == 0 || H == 0) return fa_fwd_splitkv(q, k, v, o, lse, B, Nq, Nk, H, Hk, d, scale,
-                                                           flags, num_splits, nullptr, 0, stream);
+  // The same argument checks, in the same order, as fa_fwd_splitkv: both
+  // entries return the same code for the same arguments.
+  const int vrc = fa::check_split_problem(q, k, v, o, lse, B, Nq, Nk, H, Hk, d, scale, flags);
+  if (vrc == 1) return FA_OK;  // nothing to do
+  if (vrc != FA_OK) return vrc;
+  // The scratch address is the current device's: a stream of another device
+  // would run the kernels against memory that is not theirs.
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (st != nullptr && st != cudaStreamLegacy && st != cudaStreamPerThread) {
+    int cur = 0, sdev = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess) return FA_ERR_NO_DEVICE;
+    if (cudaStreamGetDevice(st, &sdev) != cudaSuccess) return FA_ERR_INVALID_ARG;
+    if (sdev != cur) return FA_ERR_INVALID_ARG;
+  }
   const int splits = fa_splitkv_num_splits(B, Nq, Nk, H, d, num_splits);
   if (splits < 0) return splits;
   const long long need = fa_splitkv_workspace_bytes(B, Nq, H, d, splits);

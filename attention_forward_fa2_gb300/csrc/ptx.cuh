@@ -109,6 +109,36 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
   return false;
 }
 
+// ------------------------------------------------- cluster launch control
+// Dynamic scheduling on Blackwell: a running CTA asks the hardware to cancel
+// the launch of a CTA that has not started yet and takes over its work.  The
+// 16-byte response is written to shared memory (16-byte aligned) by the async
+// proxy and completes `bar` with 16 transaction bytes.  After one failed
+// request no further request may be issued.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp_smem, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+          resp_smem),
+      "r"(bar)
+      : "memory");
+}
+
+// Decodes a response (after its barrier completed): the x index of the
+// cancelled CTA, or -1 when the request failed (no CTA left to take over).
+__device__ __forceinline__ int clc_cancelled_x(uint32_t resp_smem) {
+  int x;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 r, [%1];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "mov.s32 %0, -1;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, r;\n\t}"
+      : "=r"(x)
+      : "r"(resp_smem)
+      : "memory");
+  return x;
+}
+
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");

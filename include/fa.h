@@ -158,6 +158,14 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
  *   All calls on a device share the array: calls that overlap on the GPU (other
  *   streams or host threads) race and must be serialised by the caller.  No
  *   part of the array needs clearing: each call writes every entry it reads.
+ *   The array used is the one of the CURRENT device: `stream` must belong to
+ *   it (a stream of another device gives FA_ERR_INVALID_ARG).
+ *   Argument errors are those of fa_fwd_splitkv, checked in the same order
+ *   (for example d not in {64, 128} is FA_ERR_UNSUPPORTED).
+ *   If fa_check_status() then reports an error (a device wait gave up), o and
+ *   lse of that call are undefined: the merge may have combined partial
+ *   results that the aborted kernel never wrote with entries an earlier call
+ *   left in the shared array.
  */
 int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                            int Nq, int Nk, int H, int Hk, int d, float scale, int flags,
@@ -168,6 +176,8 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
  * device-side error recorded since the last call (FA_OK if none).  When
  * `info` is not NULL it receives {flat block index, warp, wait site} of that
  * error (zeros if none).  Returns FA_ERR_CUDA if synchronisation fails.
+ * After a non-OK status the outputs of the calls since the previous check are
+ * undefined (a kernel that gave up stops early and leaves rows unwritten).
  */
 int fa_check_status(void* stream, int* info);
 
@@ -346,6 +356,36 @@ int fa_autotune(const void* q, const void* k, const void* v, void* o, float* lse
  * device still usable.  Returns FA_OK when the launch was enqueued.
  */
 int fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
+
+/*
+ * fa_set_phase_buffer -- phase clocks for profiling the forward kernel's
+ * pipeline (where each role of a CTA waits and works: "GPU 内核与 FlashAttention"
+ * §8 asks where a kernel's time goes before tuning it).  Only the library
+ * built with FA_PHASE_CLOCKS=1 (libfa_gb300_phase.so, `build.py --phase`)
+ * records them; the default library returns FA_ERR_UNSUPPORTED and its
+ * kernels contain none of the instrumentation.
+ *   buf   : caller-owned DEVICE buffer of unsigned 64-bit words, 8-byte aligned,
+ *           or NULL to detach.  Every forward launch that follows (bf16, key
+ *           split, FP8) writes, for each CTA c, words [c * W, (c + 1) * W)
+ *           with W the value returned: cycle counts per role (MMA issue,
+ *           loads, the two softmax tiles, the epilogue) and the %globaltimer
+ *           of the CTA's start and end.  The slot map is the PhaseBase /
+ *           PhaseSlot enumeration of the kernel source.
+ *   words : size of buf in words; a launch whose grid needs more returns
+ *           FA_ERR_INVALID_ARG and launches nothing.  The grid has one CTA
+ *           per work item (B * H * ceil(Nq / 256) for the dense forward; half
+ *           as many items when causal, times the splits for the key split);
+ *           only the CTAs that run write their words (a CTA that takes over
+ *           another's items leaves that CTA's words untouched).  When the
+ *           buffer holds at least 1280 more words (2 units x 40 steps x 16
+ *           events), an event trace follows the per-CTA words: clock64 stamps
+ *           of each barrier hand-off of the first two work units of CTA 0
+ *           (TraceEvent enumeration of the kernel source).
+ * Returns W (> 0) on success, FA_ERR_INVALID_ARG for a too small or misaligned
+ * buffer, FA_ERR_UNSUPPORTED in the default library.  Process-wide setting,
+ * not thread-safe with respect to forward calls.
+ */
+int fa_set_phase_buffer(unsigned long long* buf, long long words);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int fa_version(void);

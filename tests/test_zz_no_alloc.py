@@ -5,8 +5,10 @@ runtime that reserved all of its memory at start-up, a real-time path, a C
 caller without a memory pool): they pass only inputs and outputs, and the
 library uses a fixed scratch array of its own.  Checked here through the C ABI
 against fa_fwd_splitkv with a caller-owned workspace, on two calls in a row
-(the second call finds the first call's leftovers in the shared scratch), and
-for the size limit.  This file is named so that pytest collects it last.
+(the second call finds the first call's leftovers in the shared scratch), after
+a larger call whose leftovers sit where a causal call's empty splits write, for
+device memory left unchanged by repeated calls, for the same error codes as the
+workspace entry, and for the size limit.  This file is named so that pytest collects it last.
 """
 import numpy as np
 import pytest
@@ -79,6 +81,54 @@ def test_matches_workspace_entry_on_two_calls(B, Nq, Nk, H, Hk, d, flags, splits
     _no_alloc(q2, k2, v2, 0, 3)
     o, lse = _no_alloc(q, k, v, flags, splits)
     assert_close(o, lse, o_ref, lse_ref, "no-alloc after another problem")
+
+
+def test_leftovers_of_a_larger_call_do_not_reach_empty_splits():
+    # A large non-causal call fills much of the shared scratch; then a causal
+    # call with more queries than keys, where the first query tile sees no key
+    # at all and the later splits of the second tile see none either (those
+    # splits write o = 0, LSE = -inf into the scratch for the merge).
+    q1, k1, v1 = _inputs(2, 256, 2048, 4, 4, 128, 901)  # 8 splits: 8.5 MB of the 16 MiB
+    _no_alloc(q1, k1, v1, 0, 8)
+    q, k, v = _inputs(1, 512, 384, 2, 2, 128, 902)
+    o_ref, lse_ref = _with_workspace(q, k, v, fa.FA_FLAG_CAUSAL, 3)
+    o, lse = _no_alloc(q, k, v, fa.FA_FLAG_CAUSAL, 3)
+    assert np.all(np.isneginf(lse[:, :, :128]))  # rows that see no key
+    assert_close(o, lse, o_ref, lse_ref, "no-alloc causal after a larger call")
+
+
+def test_allocates_nothing():
+    q, k, v = _inputs(2, 64, 4096, 4, 2, 128, 903)
+    o = torch.empty_like(q)
+    lse = torch.empty((2, 4, 64), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def call():
+        return fa.fa_fwd_splitkv_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), 2, 64, 4096, 4, 2, 128, 0.125, 0, 0, stream)
+
+    assert call() == fa.FA_OK  # first call: the one-time set-up (module load, address lookup)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        assert call() == fa.FA_OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, "device memory changed by %d bytes" % (free0 - free1)
+    assert fa.check_status()[0] == fa.FA_OK
+
+
+def test_same_error_codes_as_the_workspace_entry():
+    q = torch.zeros((1, 64, 2, 96), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((1, 2, 64), device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    args = (q.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(), lse.data_ptr(), 1, 64, 64, 2, 2, 96,
+            0.1, 0)
+    rc_ws = fa.fa_fwd_splitkv(*args, 0, None, 0, stream)
+    rc_na = fa.fa_fwd_splitkv_noalloc(*args, 0, stream)
+    assert rc_ws == rc_na == fa.FA_ERR_UNSUPPORTED  # d = 96
+    bad_scale = args[:10] + (128, -1.0, 0)
+    assert fa.fa_fwd_splitkv_noalloc(*bad_scale, 0, stream) == fa.FA_ERR_INVALID_ARG
 
 
 def test_rejects_problems_beyond_the_scratch():
