@@ -36,6 +36,7 @@ from __future__ import annotations
 
 import argparse
 import copy
+import ctypes
 import hashlib
 import json
 import math
@@ -235,6 +236,52 @@ class OracleSample:
         return time.perf_counter() - t0
 
 
+class OracleFull:
+    """The fp64 oracle over the whole workload once (every batch and head, the
+    full query and key lengths): the CPU baseline of the page workload."""
+
+    def __init__(self, w, threads: int, causal: bool = False):
+        import oracle
+        from attention_forward_fa2_gb300 import inputs as I
+        self.oracle = oracle
+        oracle.set_num_threads(threads)
+        self.w, self.causal = w, causal
+        q, k, v, cu_q, cu_k = I.make(w)
+        self.qb, self.kb, self.vb = I.bf16_bits(q), I.bf16_bits(k), I.bf16_bits(v)
+        self.cu = (cu_q.numpy(), cu_k.numpy()) if w.varlen else None
+        self.flops = w.flops(causal=causal)
+        self.desc = ("fp64 oracle (S and P materialised) on the whole %s workload (%s%s), timed once; "
+                     "%d threads" % (w.name, w.note, ", causal" if causal else "", threads))
+
+    def run(self) -> float:
+        t0 = time.perf_counter()
+        if self.cu is not None:
+            self.oracle.attn_varlen(self.qb, self.kb, self.vb, self.cu[0], self.cu[1], max(self.w.lengths),
+                                    causal=self.causal)
+        else:
+            self.oracle.attn_dense(self.qb, self.kb, self.vb, causal=self.causal)
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(args, w):
+    """The oracle timed on this host's cores: the whole workload once for the
+    page workload (about a minute on 16 cores), a bounded sample otherwise or
+    with --cpu-baseline sample."""
+    mode = args.cpu_baseline
+    if mode == "auto":
+        mode = "full" if w.name == "page" else "sample"
+    cores = host_cores()
+    if mode == "full":
+        ref = OracleFull(w, cores, causal=args.causal)
+        dt = ref.run()
+        return {"value": ref.flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+                "sample": ref.desc, "coverage": "full workload", "seconds": dt}
+    sample = OracleSample(w, args.cpu_seconds, cores)
+    dt = sample.run()
+    return {"value": sample.flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": sample.desc, "coverage": "sample", "seconds": dt}
+
+
 # --------------------------------------------------------------------- arms
 def run_reference(args, w):
     rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
@@ -252,7 +299,8 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded N(0,1), generated on the host)", "config": workload_config(w, None),
+        "data": "synthetic (seeded N(0,1), generated on the host)",
+        "config": workload_config(w, getattr(args, "causal", False)),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample.desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -314,6 +362,24 @@ def pipelined_e2e(torch, dev, stream, sets, host_in, host_out, run, steps, world
     return e0.elapsed_time(e1) / steps
 
 
+def copy_gbs(torch, dev, dsts, srcs):
+    """GB/s of copying srcs into dsts (one copy each, on a side stream), best of three."""
+    cs = torch.cuda.Stream(device=dev)
+    nbytes = sum(t.numel() * t.element_size() for t in srcs)
+    best = float("inf")
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(cs):
+            a.record(cs)
+            for d_, s_ in zip(dsts, srcs):
+                d_.copy_(s_, non_blocking=True)
+            b.record(cs)
+        torch.cuda.synchronize(dev)
+        best = min(best, a.elapsed_time(b))
+    return nbytes / (best * 1e-3) / 1e9 if best > 0 else None
+
+
 def per_step_stats(marks):
     """Median, minimum and maximum of the per-step device times (ms) from
     events recorded between the timed steps (empty for a graph replay)."""
@@ -323,7 +389,8 @@ def per_step_stats(marks):
     return {"median": statistics.median(t), "min": t[0], "max": t[-1]}
 
 
-def workload_config(w, kernel_cfg, causal=False):
+def workload_config(w, causal=False):
+    """The workload a line measures (the same dict on both arms)."""
     cfg = {"workload": "%s: %s" % (w.name, w.note or ""), "B": w.B, "H": w.H, "d": w.d,
            "layout": "[batch, seq, heads, d_head] bf16", "causal": bool(causal),
            "l2": "inputs and output larger than L2 (no flush needed)",
@@ -335,18 +402,19 @@ def workload_config(w, kernel_cfg, causal=False):
     else:
         cfg["Nq"] = w.Nq
         cfg["Nk"] = w.Nk
+    return cfg
+
+
+def kernel_info(w, args, kernel_cfg):
+    """How our arm ran the workload: entry point, launch mode, tile config."""
+    k = {"launch": "cuda graph replay" if args.graph else "stream launches", "form": "fa_fwd (bf16)"}
     if kernel_cfg:
-        cfg["kernel_config"] = kernel_cfg
-    return cfg
-
-
-def add_mode(cfg, args):
-    cfg["launch"] = "cuda graph replay" if args.graph else "stream launches"
+        k["config"] = kernel_cfg
     if args.split:
-        cfg["form"] = "key-split (fa_fwd_splitkv)"
+        k["form"] = "key-split (fa_fwd_splitkv)"
     if getattr(args, "fp8", False):
-        cfg["form"] = "fp8 e4m3, block-quantised (fa_fwd_fp8%s)" % ("_varlen" if "sequences" in cfg else "")
-    return cfg
+        k["form"] = "fp8 e4m3, block-quantised (fa_fwd_fp8%s)" % ("_varlen" if w.varlen else "")
+    return k
 
 
 def run_ours(args, w):
@@ -454,6 +522,31 @@ def run_ours(args, w):
     value = world * flops / (ms_max * 1e-3) / 1e12
     kernel_tflops = flops / (ms * 1e-3) / 1e12  # one launch per step, this rank
 
+    # ------------------------------------------------------------ sustained
+    # The same step back to back for a few seconds: the clocks settle under
+    # the power limit, so this is compared with the sustained GEMM peak.
+    sustained = None
+    if args.sustained_seconds > 0 and graph is None:
+        n_sus = max(args.steps, int(math.ceil(args.sustained_seconds * 1e3 / ms)))
+        sampler2 = ClockSampler("GPU-%s" % uuid if uuid is not None else str(local))
+        sampler2.start()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        s0.record(stream)
+        for _ in range(n_sus):
+            step()
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        clk_sus = sampler2.stop()
+        ms_sus = max_over_ranks(s0.elapsed_time(s1) / n_sus, world)
+        sustained = {"value": world * flops / (ms_sus * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms_sus,
+                     "steps": n_sus, "seconds": ms_sus * n_sus / 1e3, "clocks": clk_sus}
+        rc, info = fa.check_status()
+        if rc != fa.FA_OK:
+            raise SystemExit("device error in the sustained region: %s %s" % (fa.strerror(rc), info))
+
     # -------------------------------------------------------- end to end
     e2e_steps = max(3, min(args.steps, 20))
     # Every step copies its inputs from pinned host memory (the e4m3 codes for
@@ -491,6 +584,10 @@ def run_ours(args, w):
                                           run_set, e2e_steps, world), world)
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+    # The host link measured in the same run: one step's input bytes host ->
+    # device and its output bytes device -> host, alone (best of three).
+    h2d_gbs = copy_gbs(torch, dev, sets[1][0], host_in)
+    d2h_gbs = copy_gbs(torch, dev, host_out[0], sets[0][1])
     rc, info = fa.check_status()
     if rc != fa.FA_OK:
         raise SystemExit("device error in the e2e region: %s %s" % (fa.strerror(rc), info))
@@ -509,7 +606,8 @@ def run_ours(args, w):
         "warmup": args.warmup, "ms_per_step": ms_max, "step_ms": step_stats, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)" if args.fp8 else "bf16",
         "data": "synthetic (seeded N(0,1), generated on the host)",
-        "config": add_mode(workload_config(w, None if args.fp8 else kernel_cfg, args.causal), args),
+        "config": workload_config(w, args.causal),
+        "kernel": kernel_info(w, args, None if args.fp8 else kernel_cfg),
         "pct_of_peak": 100.0 * kernel_tflops / peak,
         "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": UNIT,
                      "frac": kernel_tflops / peak, "traffic": traffic,
@@ -519,16 +617,23 @@ def run_ours(args, w):
                      "algorithmic_flops_per_launch": flops},
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "steps": e2e_steps, "copies": E2E_COPIES},
+                "steps": e2e_steps, "copies": E2E_COPIES,
+                "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs,
+                "copy_bound_ms": 1e3 * h2d / (h2d_gbs * 1e9) if h2d_gbs else None},
         "gpu_launches": args.steps * (2 if args.split else 1),
         "clocks": clocks,
     }
-    if world == 1 and not args.no_cpu_baseline:
-        cores = host_cores()
-        sample = OracleSample(w, args.cpu_seconds, cores)
-        dt = sample.run()
-        line["cpu_baseline"] = {"value": sample.flops / dt / 1e12, "unit": UNIT, "cores": cores,
-                                "kind": "oracle", "sample": sample.desc, "seconds": dt}
+    if sustained is not None:
+        sus_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        if args.fp8:
+            sus_peak *= 2.0
+        sustained["peak"] = sus_peak
+        sustained["frac"] = sustained["value"] / world / sus_peak
+        sustained["peak_source"] = ("%s bf16 dense sustained (MEASURED_PEAKS.json)%s"
+                                    % (src, ", x2 for fp8" if args.fp8 else ""))
+        line["sustained"] = sustained
+    if world == 1 and args.cpu_baseline != "none":
+        line["cpu_baseline"] = cpu_baseline(args, w)
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -629,8 +734,8 @@ def run_bwd(args, w):
         "warmup": args.warmup, "ms_per_step": ms_max, "step_ms": step_stats, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q, k, v, dO; o and lse from the forward)",
-        "config": dict(workload_config(w, None, args.causal), launch="stream launches",
-                       form="backward (fa_bwd)"),
+        "config": workload_config(w, args.causal),
+        "kernel": {"launch": "stream launches", "form": "backward (fa_bwd%s)" % ("_varlen" if w.varlen else "")},
         "pct_of_peak": 100.0 * step_tflops / peak,
         "roofline": {"bound": "tensor", "achieved": step_tflops, "peak": peak, "unit": UNIT,
                      "frac": step_tflops / peak, "traffic": None,
@@ -653,6 +758,116 @@ def run_bwd(args, w):
     return 0
 
 
+PHASE_NAMES = {
+    "mma": (0, ("wait_q", "wait_kv", "wait_p", "wait_o_empty", "issue", "steps", "units")),
+    "load": (8, ("wait_q_empty", "wait_kv_empty", "issue", "ring_slots")),
+    "softmax_tile0": (16, ("wait_s", "store_publish", "steps", "max_recomputed", "final", "load_s", "exp")),
+    "softmax_tile1": (24, ("wait_s", "store_publish", "steps", "max_recomputed", "final", "load_s", "exp")),
+    "epilogue": (32, ("wait_l_and_o", "read_o", "staging_wait", "store", "tiles")),
+}
+
+
+def trace_summary(tr):
+    """Median hand-off latencies (cycles) from the event trace of CTA 0's first
+    unit: tr[unit, step, event] clock64 stamps (0 = not recorded)."""
+    import numpy as np
+    u = tr[0]
+    med = lambda a: round(float(np.median(a)), 1) if len(a) else None
+    res = {}
+    steps = [j for j in range(1, 39) if u[j, 0] > 0 and u[j + 1, 0] > 0]
+    for t in (0, 1):
+        s_issue = [u[j, 5 + t] for j in steps]
+        s_seen = [u[j, 8 + t] for j in steps]
+        p_pub = [u[j, 10 + t] for j in steps]
+        p_seen = [u[j + 1, 1 + t] for j in steps]  # P(j) is consumed at step j + 1
+        ok = [i for i in range(len(steps)) if min(s_issue[i], s_seen[i], p_pub[i], p_seen[i]) > 0]
+        res["tile%d_S_issued_to_softmax_sees_S" % t] = med([s_seen[i] - s_issue[i] for i in ok])
+        res["tile%d_softmax_S_to_P_published" % t] = med([p_pub[i] - s_seen[i] for i in ok])
+        res["tile%d_P_published_to_mma_sees_P" % t] = med([p_seen[i] - p_pub[i] for i in ok])
+        res["tile%d_cycle" % t] = med([u[j + 1, 5 + t] - u[j, 5 + t] for j in steps if u[j + 1, 5 + t] > 0])
+    ld = [u[j, 12] - u[j, 8] for j in steps if u[j, 12] > 0]
+    ex = [u[j, 13] - u[j, 12] for j in steps if u[j, 13] > 0]
+    res["tile0_softmax_load"] = med(ld)
+    res["tile0_softmax_exp"] = med(ex)
+    res["mma_pv0_issue"] = med([u[j, 3] - u[j, 1] for j in steps if u[j, 3] > 0 and u[j, 1] > 0])
+    res["mma_s0_issue_after_pv0"] = med([u[j, 5] - u[j, 3] for j in steps if u[j, 5] > 0 and u[j, 3] > 0])
+    res["raw_unit0_first_steps"] = [[int(x) for x in u[j]] for j in range(0, 4)]
+    return res
+
+
+def run_phase(args, w):
+    """--phase: one forward of the workload through the phase-clock build of
+    the library (libfa_gb300_phase.so); prints where each role of a CTA spends
+    its cycles, averaged over the CTAs.  The instrumented kernel is slightly
+    slower than the product one, so this line is a diagnostic, not a bench
+    value."""
+    import torch
+    import attention_forward_fa2_gb300 as fa
+    from attention_forward_fa2_gb300 import build as fabuild
+    from attention_forward_fa2_gb300 import inputs as I
+
+    fabuild.build(phase=True)
+    L = fa.load_library(fa.PHASE_LIB_PATH)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    q, k, v, cu_q, cu_k = I.make(w)
+    dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
+    maxlen = max(w.lengths) if w.varlen else w.Nq
+    dcu = cu_q.to(dev).contiguous() if w.varlen else None
+    o = torch.empty_like(dq)
+    lse = torch.empty((w.B, w.H, maxlen), dtype=torch.float32, device=dev)
+    # One record per CTA of the grid (one CTA per work item of 256 query rows).
+    items = w.B * w.H * ((maxlen + 255) // 256)
+    trace_words = 2 * 40 * 16  # event trace of CTA 0 (two units x 40 steps x 16 events)
+    buf = torch.zeros(items * 48 + trace_words, dtype=torch.int64, device=dev)
+    words = L.fa_set_phase_buffer(buf.data_ptr(), buf.numel())
+    if words <= 0:
+        raise SystemExit("fa_set_phase_buffer failed: %d" % words)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    cu = dcu.data_ptr() if dcu is not None else None
+    for _ in range(args.warmup + 1):
+        rc = L.fa_fwd_ex(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B, maxlen,
+                         maxlen if w.varlen else w.Nk, w.H, w.H, w.d, 1.0 / math.sqrt(w.d), cu, cu,
+                         fa.FA_FLAG_CAUSAL if args.causal else 0, stream)
+        if rc != 0:
+            raise SystemExit("forward failed: %d" % rc)
+    info = (ctypes.c_int * 3)()
+    rc = L.fa_check_status(stream, info)
+    L.fa_set_phase_buffer(None, 0)
+    if rc != 0:
+        raise SystemExit("device status %d" % rc)
+    allw = buf.cpu().numpy()
+    ph = allw[:items * words].reshape(-1, words).astype("float64")
+    grid = int((ph[:, 41] > 0).sum())
+    ph = ph[ph[:, 41] > 0]
+    # The trace follows the words of the grid (one CTA per item for packed
+    # batches, else min(items, SMs) CTAs).
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    launched = items if w.varlen else min(items, nsm)
+    tr = allw[launched * words:launched * words + trace_words].reshape(2, 40, 16).astype("float64")
+    trace = trace_summary(tr)
+    out = {}
+    for role, (base, names) in PHASE_NAMES.items():
+        out[role] = {n: round(float(ph[:, base + i].mean()), 1) for i, n in enumerate(names)}
+    ns = float((ph[:, 41] - ph[:, 40]).mean())
+    cycles = sum(out["mma"][n] for n in ("wait_q", "wait_kv", "wait_p", "wait_o_empty", "issue"))
+    steps = max(out["mma"]["steps"], 1.0)
+    per_step = {"mma_" + n: round(out["mma"][n] / steps, 1) for n in ("wait_q", "wait_kv", "wait_p",
+                                                                      "wait_o_empty", "issue")}
+    for t in ("softmax_tile0", "softmax_tile1"):
+        st = max(out[t]["steps"], 1.0)
+        for n in ("wait_s", "load_s", "exp", "store_publish"):
+            per_step[t + "_" + n] = round(out[t][n] / st, 1)
+    line = {"phase_clocks": out, "per_key_value_step_cycles": per_step, "ctas": grid, "trace": trace,
+            "cta_ns": round(ns, 1), "mma_role_cycles": round(cycles, 1),
+            "clock_ghz_estimate": round(cycles / ns, 3) if ns > 0 else None,
+            "workload": w.name, "causal": bool(args.causal),
+            "note": "instrumented build (FA_PHASE_CLOCKS=1), last of %d launches; not a bench value"
+                    % (args.warmup + 1)}
+    print(json.dumps(line))
+    return 0
+
+
 def main(argv=None):
     from attention_forward_fa2_gb300 import inputs as I
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -671,13 +886,24 @@ def main(argv=None):
     ap.add_argument("--bwd", action="store_true", help="time the backward pass instead")
     ap.add_argument("--fp8", action="store_true", help="time the e4m3 forward instead")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle sample budget")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline", choices=("auto", "full", "sample", "none"), default="auto",
+                    help="oracle timing: the whole workload once (default for the page workload), "
+                         "a bounded sample (default otherwise), or none")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="same as --cpu-baseline none")
+    ap.add_argument("--sustained-seconds", type=float, default=3.0,
+                    help="length of the back-to-back window for the sustained figure (0: skip)")
+    ap.add_argument("--phase", action="store_true",
+                    help="diagnostic: per-role phase clocks of one forward (instrumented build)")
     args = ap.parse_args(argv)
+    if args.no_cpu_baseline:
+        args.cpu_baseline = "none"
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     w = I.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.phase:
+        return run_phase(args, w)
     if args.bwd:
         return run_bwd(args, w)
     return run_ours(args, w)
