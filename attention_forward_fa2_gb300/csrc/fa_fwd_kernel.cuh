@@ -1063,12 +1063,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           // row sum in four packed accumulators (fixed order); P packed as bf16
           // pairs (FP8: e4m3, four per word).
           uint32_t pk[FP8 ? BC / 4 : BC / 2];
-          auto exponentiate = [&](float ng) -> float {
+          auto exp_range = [&](int c0, int c1, float ng, uint64_t (&acc)[4]) {
             const uint64_t c2x2 = ptx::f2_pack(c2j, c2j);
             const uint64_t negx2 = ptx::f2_pack(ng, ng);
-            uint64_t acc[4] = {0, 0, 0, 0};
   #pragma unroll
-            for (int c = 0; c < BC; c += 2) {
+            for (int c = c0; c < c1; c += 2) {
               float x0, x1;
               ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[c], s[c + 1]), c2x2, negx2), x0, x1);
               const float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1);
@@ -1083,6 +1082,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk[c >> 1] = ptx::pack_bf16x2(e0, e1);
               }
             }
+          };
+          auto sum_acc = [&](const uint64_t (&acc)[4]) -> float {
             float a0, a1, a2, a3, a4, a5, a6, a7;
             ptx::f2_unpack(acc[0], a0, a1);
             ptx::f2_unpack(acc[1], a2, a3);
@@ -1090,9 +1091,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::f2_unpack(acc[3], a6, a7);
             return ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
           };
-          load_scores();
-          ph.lap(kPhSoftLoad);
-          if (tr_lead && t == 0) FA_TRACE(tr_unit, j, kTrSoftLoad0);
+          auto exponentiate = [&](float ng) -> float {
+            uint64_t acc[4] = {0, 0, 0, 0};
+            exp_range(0, BC, ng, acc);
+            return sum_acc(acc);
+          };
           // The reference maximum m only moves when a block maximum exceeds it
           // by more than the threshold T (log2 units); the merge identity of
           // §11.2 holds for any common reference value, so results stay exact.
@@ -1104,10 +1107,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           // result is the one the maximum rule gives.
           float alpha = 1.f, lblk = 0.f;
           bool slow = __all_sync(0xffffffffu, m_ref == -INFINITY);
-          if (!slow) {
-            lblk = exponentiate(m_ref == -INFINITY ? 0.f : (FP8 ? -m_ref : -m_ref * c2));
+          const float ng_ref = m_ref == -INFINITY ? 0.f : (FP8 ? -m_ref : -m_ref * c2);
+          if (!FP8 && !slow && w.j0 + j < j_mask) {
+            // Unmasked tile, speculative path: the second half of the scores
+            // is loaded while the first half is exponentiated (the sums keep
+            // the order of the single pass, so results are identical).
+            // Measured on the page workload: 1.474 -> 1.453 ms; the FP8 form
+            // (2 % slower with it) keeps the single load.
+            uint32_t sr[BC];
+  #pragma unroll
+            for (int c = 0; c < BC / 64; ++c) ptx::tmem_ld32(tS + c * 32, &sr[c * 32]);
+            ptx::tmem_wait_ld();
+  #pragma unroll
+            for (int c = BC / 64; c < BC / 32; ++c) ptx::tmem_ld32(tS + c * 32, &sr[c * 32]);
+  #pragma unroll
+            for (int c = 0; c < BC / 2; ++c) s[c] = __uint_as_float(sr[c]);
+            ph.lap(kPhSoftLoad);
+            if (tr_lead && t == 0) FA_TRACE(tr_unit, j, kTrSoftLoad0);
+            uint64_t acc[4] = {0, 0, 0, 0};
+            exp_range(0, BC / 2, ng_ref, acc);
+            ptx::tmem_wait_ld();
+  #pragma unroll
+            for (int c = BC / 2; c < BC; ++c) s[c] = __uint_as_float(sr[c]);
+            exp_range(BC / 2, BC, ng_ref, acc);
+            lblk = sum_acc(acc);
             slow = __any_sync(0xffffffffu, m_ref == -INFINITY || !(lblk <= accept_sum));
             if (slow) load_scores();  // the scores were consumed
+          } else {
+            load_scores();
+            ph.lap(kPhSoftLoad);
+            if (tr_lead && t == 0) FA_TRACE(tr_unit, j, kTrSoftLoad0);
+            if (!slow) {
+              lblk = exponentiate(ng_ref);
+              slow = __any_sync(0xffffffffu, m_ref == -INFINITY || !(lblk <= accept_sum));
+              if (slow) load_scores();  // the scores were consumed
+            }
           }
           if (slow) {
             ph.count(kPhSoftSlow);
