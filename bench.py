@@ -837,13 +837,13 @@ def run_phase(args, w):
     if rc != 0:
         raise SystemExit("device status %d" % rc)
     allw = buf.cpu().numpy()
-    ph = allw[:items * words].reshape(-1, words).astype("float64")
-    grid = int((ph[:, 41] > 0).sum())
-    ph = ph[ph[:, 41] > 0]
     # The trace follows the words of the grid (one CTA per item for packed
     # batches, else min(items, SMs) CTAs).
     nsm = torch.cuda.get_device_properties(dev).multi_processor_count
     launched = items if w.varlen else min(items, nsm)
+    ph = allw[:launched * words].reshape(-1, words).astype("float64")
+    ph = ph[ph[:, 41] > 0]
+    grid = int(ph.shape[0])
     tr = allw[launched * words:launched * words + trace_words].reshape(2, 40, 16).astype("float64")
     trace = trace_summary(tr)
     out = {}
