@@ -600,7 +600,7 @@ def run_ours(args, w):
     if args.fp8:
         peak *= 2.0
         peak_note = "fp8 dense = 2 x " + peak_note + " (nominal fp8/bf16 ratio 4.5/2.25)"
-    traffic = load_traffic(w.name + ("_fp8" if args.fp8 else ""))
+    traffic = load_traffic(w.name + ("_fp8" if args.fp8 else "") + ("_causal" if args.causal else ""))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "step_ms": step_stats, "higher_is_better": True,
