@@ -114,6 +114,7 @@ enum WaitSite : int {
   kSiteCorrFinal = 9,
   kSiteTeardown = 10,
   kSiteItem = 11,
+  kSiteSoftFinal = 12,
 };
 
 // Work items reach the roles through a ring of kItemSlots entries in shared
@@ -157,9 +158,9 @@ enum PhaseSlot : int {
 // Event trace (phase-clock builds): clock64 stamps of every hand-off of the
 // first kTraceUnits work units of CTA 0, at phase[trace_off + (unit *
 // kTraceSteps + step) * kTraceEvents + event], when the buffer has room.
-constexpr int kTraceUnits = 2;
+constexpr int kTraceUnits = 3;
 constexpr int kTraceSteps = 40;
-constexpr int kTraceEvents = 16;
+constexpr int kTraceEvents = 24;
 constexpr int kTraceWords = kTraceUnits * kTraceSteps * kTraceEvents;
 enum TraceEvent : int {
   kTrMmaKV = 0,        // MMA thread: K/V slot of step j full
@@ -171,7 +172,17 @@ enum TraceEvent : int {
   kTrSoftP0 = 10,      // softmax tile 0 / 1: P(j) published
   kTrSoftLoad0 = 12,   // softmax tile 0: S(j) in registers
   kTrSoftExp0 = 13,    // softmax tile 0: exponentials done
-  kTrEpiO0 = 14,       // epilogue: O of tile 0 / 1 final observed
+  kTrEpiO0 = 14,       // epilogue (step 0 row): O of tile 0 / 1 final observed;
+                       // (step 1 row): O of tile 0 / 1 read, O-empty signalled;
+                       // (step 2 row): the staging wait of tile 0 / 1 done
+  kTrLoadKV = 16,      // load thread: K/V slot of step j free, its copies issued
+  kTrLoadQ = 17,       // load thread (step 0 row): Q-empty observed, Q copies issued
+  kTrMmaQ = 18,        // MMA thread (step 0 row): Q-full observed
+  kTrMmaQEmpty = 19,   // MMA thread: Q-empty committed (row of the step that commits it)
+  kTrMmaWaitQ = 20,    // MMA thread (step 0 row): starts waiting for Q-full
+  kTrMmaWaitKV = 21,   // MMA thread: starts waiting for the K/V slot of step j
+  kTrMmaStepEnd = 22,  // MMA thread: step j's last commit issued
+  kTrMmaDecoded = 23,  // MMA thread (step 0 row): unit decoded
 };
 
 __device__ __forceinline__ void trace_event(unsigned long long* phase, int trace_off, int unit, int step, int ev) {
@@ -556,6 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // =========================================================== TMA loads
       uint32_t qcount = 0;  // units whose Q was loaded
       uint32_t g = 0;       // ring slots handed to the TMA unit so far
+      int tr_unit = 0;      // units loaded (event trace)
       bool ok = true;
       PhaseClock ph;
       ph.start();
@@ -620,6 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tma_load_4d(dst, &tm_q, bar(L::kBarQFull), pnl * kPanelElems, w.h, w.qwin[t].load_row, w.b);
             }
           }
+          FA_TRACE(tr_unit, 0, kTrLoadQ);
 #pragma unroll 1
           for (int j = 0; j <= w.nkv; ++j) {
             const uint32_t slot = g % STAGES;
@@ -631,6 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ph.lap(kPhLoadWaitKV);
             ph.count(kPhLoadSlots);
+            FA_TRACE(tr_unit, j, kTrLoadKV);
             const uint32_t bytes = (j < w.nkv ? L::kKVTileBytes : 0) + (j >= 1 ? L::kKVTileBytes : 0);
             ptx::mbar_arrive_expect_tx(bar(L::kBarKVFull + slot), bytes);
             ++g;
@@ -666,6 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
+          ++tr_unit;
         }
         if (!ok) break;
         if constexpr (kDynamic) {
@@ -715,7 +730,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       FA_FOR_EACH_UNIT(u) {
         const Unit w = decode_unit<BC, VARLEN, CAUSAL, SPLIT, kShift>(p, u);
         if (!w.run) continue;
+        FA_TRACE(tr_unit, 0, kTrMmaDecoded);
         ph.lap(kPhMmaIssue);
+        FA_TRACE(tr_unit, 0, kTrMmaWaitQ);
         if (!ptx::mbar_wait(bar(L::kBarQFull), qcount & 1u, s_abort, tmo)) {
           record_error(p.status, kErrTimeout, kSiteMmaQ);
           ok = false;
@@ -723,12 +740,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ph.lap(kPhMmaWaitQ);
         ph.count(kPhMmaUnits);
+        FA_TRACE(tr_unit, 0, kTrMmaQ);
         ++qcount;
         ptx::tc_fence_after();
 #pragma unroll 1
         for (int j = 0; j <= w.nkv && ok; ++j) {
           const uint32_t slot = g % STAGES;
           ph.lap(kPhMmaIssue);
+          FA_TRACE(tr_unit, j, kTrMmaWaitKV);
           if (!ptx::mbar_wait(bar(L::kBarKVFull + slot), (g / STAGES) & 1u, s_abort, tmo)) {
             record_error(p.status, kErrTimeout, kSiteMmaK);
             ok = false;
@@ -818,8 +837,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!ok) break;
           // Q of this unit is free once its last S MMAs complete.
-          if (j == w.nkv - 1) ptx::mma_commit(bar(L::kBarQEmpty));
+          if (j == w.nkv - 1) {
+            ptx::mma_commit(bar(L::kBarQEmpty));
+            FA_TRACE(tr_unit, j, kTrMmaQEmpty);
+          }
           ptx::mma_commit(bar(L::kBarKVEmpty + slot));  // K(j) and V(j-1) no longer needed
+          FA_TRACE(tr_unit, j, kTrMmaStepEnd);
           ++g;
         }
 #pragma unroll
@@ -844,10 +867,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Largest block sum for which every p of the block is below 2^T (T the
     // rescale threshold), with a margin for the rounding of the exponent.
     const float accept_sum = exp2f(p.rescale_threshold) * 0.9990234375f;
-    uint32_t sc = 0;  // S-full completions consumed
+    // Bits 0-30: S-full completions consumed; bit 31: parity of the units
+    // this tile has finished (the epilogue's O-empty count).
+    uint32_t sc = 0;
     int tr_unit = 0;  // units processed (event trace)
     const bool tr_lead = lane == 0 && (warp & 3) == 0;
     bool ok = true;
+    // Before a unit's final message the epilogue must have taken the previous
+    // one (1 / l is one shared word per row, L-ready one barrier phase per
+    // unit).  With two or more key tiles the MMA thread's O-empty wait before
+    // the unit's first P V already orders the two; a unit of one key tile
+    // could otherwise finish while the epilogue still waits for the last.
+    auto wait_epilogue = [&]() -> bool {
+      if (!ptx::mbar_wait_warp(bar(L::kBarOEmpty + t), (sc >> 31) ^ 1u, s_abort, tmo)) {
+        if (lane == 0) record_error(p.status, kErrTimeout, kSiteSoftFinal);
+        return false;
+      }
+      return true;
+    };
     PhaseClock ph;
     ph.start();
 #pragma unroll 1
@@ -992,7 +1029,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_before();
           ptx::mbar_arrive(bar(L::kBarPFull + t));
         }
-        if (!ok) break;
+        if (!ok || (nt == 1 && !(ok = wait_epilogue()))) break;
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           float l = l_q[r] + __shfl_xor_sync(0xffffffffu, l_q[r], 1);
@@ -1212,6 +1249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         ph.lap(kPhSoftWork);
+        if (nt == 1 && !(ok = wait_epilogue())) break;
         // Final message for the epilogue: 1 / l, and the row's log-sum-exp.
         const bool has = l > 0.f;
         s_invl[t * kBR + row] = has ? vsc / l : 0.f;
@@ -1228,6 +1266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::mbar_arrive(bar(L::kBarLReady + t));
       ph.lap(kPhSoftFinal);
+      sc ^= 0x80000000u;
       ++tr_unit;
     }
     if (lane == 0 && (warp & 3) == 0) ph.store(p.phase, t == 0 ? kPhSoft0 : kPhSoft1);
@@ -1318,6 +1357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pending = false;
         }
         ph.lap(kPhEpiStage);
+        if (lane == 0 && warp == 8) FA_TRACE(tr_unit, 2, kTrEpiO0 + t);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
@@ -1359,6 +1399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::kBarOEmpty + t));
         ph.lap(kPhEpiRead);
+        if (lane == 0 && warp == 8) FA_TRACE(tr_unit, 1, kTrEpiO0 + t);
         if (use_tma) {
           ptx::fence_proxy_async_smem();
           __syncwarp();

@@ -792,6 +792,28 @@ def trace_summary(tr):
     res["mma_pv0_issue"] = med([u[j, 3] - u[j, 1] for j in steps if u[j, 3] > 0 and u[j, 1] > 0])
     res["mma_s0_issue_after_pv0"] = med([u[j, 5] - u[j, 3] for j in steps if u[j, 5] > 0 and u[j, 3] > 0])
     res["raw_unit0_first_steps"] = [[int(x) for x in u[j]] for j in range(0, 4)]
+    # Unit boundaries (unit n -> n + 1), relative to the MMA thread's last P V
+    # issue of unit n (cycles): epilogue O-final seen / staging free / O read,
+    # and the MMA thread's first S issue and O-empty observation in unit n + 1.
+    for n in range(tr.shape[0] - 1):
+        u, v = tr[n], tr[n + 1]
+        if not (u[:, 3] > 0).any() or v[0, 0] <= 0:
+            continue
+        last = max(j for j in range(tr.shape[1]) if u[j, 3] > 0)
+        t0 = u[last, 3]
+        rel = lambda x: int(x - t0) if x > 0 else None
+        res["boundary_%d_%d" % (n, n + 1)] = {
+            "epi_tile0_O_final_seen": rel(u[0, 14]), "epi_tile0_staging_free": rel(u[2, 14]),
+            "epi_tile0_O_read": rel(u[1, 14]), "epi_tile1_O_final_seen": rel(u[0, 15]),
+            "epi_tile1_staging_free": rel(u[2, 15]), "epi_tile1_O_read": rel(u[1, 15]),
+            "mma_next_kv0": rel(v[0, 0]), "mma_next_S0_issued": rel(v[0, 5]),
+            "mma_next_S1_issued": rel(v[0, 6]), "mma_next_P0_seen": rel(v[1, 1]),
+            "mma_next_O_empty_seen": rel(v[1, 7]), "mma_next_PV1_issued": rel(v[1, 4]),
+            "soft_last_P0": rel(u[last - 1, 10]) if last >= 1 else None,
+            "soft_next_S0_seen": rel(v[0, 8]), "soft_next_P0_published": rel(v[0, 10]),
+            "mma_Q_empty_committed": rel(max(u[:, 19])), "load_last_slot_issued": rel(u[last, 16]),
+            "load_next_Q_issued": rel(v[0, 17]), "load_next_kv0_issued": rel(v[0, 16]),
+            "load_next_kv1_issued": rel(v[1, 16]), "mma_next_Q_seen": rel(v[0, 18])}
     return res
 
 
@@ -818,7 +840,7 @@ def run_phase(args, w):
     lse = torch.empty((w.B, w.H, maxlen), dtype=torch.float32, device=dev)
     # One record per CTA of the grid (one CTA per work item of 256 query rows).
     items = w.B * w.H * ((maxlen + 255) // 256)
-    trace_words = 2 * 40 * 16  # event trace of CTA 0 (two units x 40 steps x 16 events)
+    trace_words = 3 * 40 * 24  # event trace of CTA 0 (three units x 40 steps x 24 events)
     buf = torch.zeros(items * 48 + trace_words, dtype=torch.int64, device=dev)
     words = L.fa_set_phase_buffer(buf.data_ptr(), buf.numel())
     if words <= 0:
@@ -844,8 +866,11 @@ def run_phase(args, w):
     ph = allw[:launched * words].reshape(-1, words).astype("float64")
     ph = ph[ph[:, 41] > 0]
     grid = int(ph.shape[0])
-    tr = allw[launched * words:launched * words + trace_words].reshape(2, 40, 16).astype("float64")
+    tr = allw[launched * words:launched * words + trace_words].reshape(3, 40, 24).astype("float64")
     trace = trace_summary(tr)
+    if args.trace_out:
+        with open(args.trace_out, "w") as f:
+            json.dump(tr.astype("int64").tolist(), f)
     out = {}
     for role, (base, names) in PHASE_NAMES.items():
         out[role] = {n: round(float(ph[:, base + i].mean()), 1) for i, n in enumerate(names)}
@@ -894,6 +919,8 @@ def main(argv=None):
                     help="length of the back-to-back window for the sustained figure (0: skip)")
     ap.add_argument("--phase", action="store_true",
                     help="diagnostic: per-role phase clocks of one forward (instrumented build)")
+    ap.add_argument("--trace-out", default=None,
+                    help="with --phase: write the raw event trace [unit][step][event] (JSON) to this file")
     args = ap.parse_args(argv)
     if args.no_cpu_baseline:
         args.cpu_baseline = "none"
