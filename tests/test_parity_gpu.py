@@ -1,7 +1,7 @@
 """Parity of the CUDA path (through the C ABI) with the fp64 oracle.
 
-Small cases compare every output element; the ten sweep workloads compare
-sampled rows that the oracle computes one by one, in the same launch
+Small cases compare every output element; the ten sweep workloads compare every
+element of four whole heads and sampled rows of the others, in the same launch
 configuration the benchmark times (the page and variable-length workloads are
 compared on every element in test_parity_full_gpu.py).  Bar: max|dO| <= 2e-2,
 max|dLSE| <= 1e-3.
@@ -52,19 +52,25 @@ def test_slice_full_parity(oracle_mod):
     assert_close(o, lse, o_ref, lse_ref, "slice 64x4096")
 
 
-def _sampled_dense(oracle_mod, w, n_random=48):
+@pytest.mark.parametrize("w", I.SWEEP, ids=[w.name for w in I.SWEEP])
+def test_sweep_heads_full_and_rows_sampled(oracle_mod, w):
+    """Each sweep workload in one launch (the benchmark's configuration): every element of
+    four whole (b, h) heads -- (0, 0), (B-1, H-1) and two seeded ones -- plus sampled rows
+    (corners, tile and CTA boundaries, random) over the other heads."""
     q, k, v, _, _ = I.make(w)
     o, lse = gpu_dense(q, k, v)
-    assert np.all(np.isfinite(lse))
-    rows = sample_rows(w.B, w.Nq, w.H, n_random=n_random, seed=w.seed)
-    o_ref, lse_ref = oracle_mod.attn_dense_rows(bits(q), bits(k), bits(v), rows)
-    b, h, i = rows[:, 0], rows[:, 1], rows[:, 2]
-    return assert_close(o[b, i, h, :], lse[b, h, i], o_ref, lse_ref, w.name)
-
-
-@pytest.mark.parametrize("w", I.SWEEP, ids=[w.name for w in I.SWEEP])
-def test_sweep_sampled(oracle_mod, w):
-    _sampled_dense(oracle_mod, w, n_random=24)
+    rng = np.random.default_rng(w.seed + 7)
+    heads = [(0, 0), (w.B - 1, w.H - 1)] + [(int(rng.integers(w.B)), int(rng.integers(w.H))) for _ in range(2)]
+    b = np.array([x[0] for x in heads])
+    h = np.array([x[1] for x in heads])
+    qb, kb, vb = bits(q), bits(k), bits(v)
+    sel = lambda t: np.ascontiguousarray(t[b, :, h, :][:, :, None, :])  # heads as a batch of one-head problems
+    o_ref, lse_ref = oracle_mod.attn_dense(sel(qb), sel(kb), sel(vb))
+    assert_close(o[b, :, h, :][:, :, None, :], lse[b, h, :][:, None, :], o_ref, lse_ref, w.name + " heads")
+    rows = sample_rows(w.B, w.Nq, w.H, n_random=24, seed=w.seed)
+    o_rows, lse_rows = oracle_mod.attn_dense_rows(qb, kb, vb, rows)
+    rb, rh, ri = rows[:, 0], rows[:, 1], rows[:, 2]
+    assert_close(o[rb, ri, rh, :], lse[rb, rh, ri], o_rows, lse_rows, w.name + " rows")
 
 
 # ----------------------------------------------------------------- edge cases
