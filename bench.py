@@ -767,53 +767,78 @@ PHASE_NAMES = {
 }
 
 
+# Event trace of the instrumented build: TRACE_SHAPE = (units, steps, events)
+# words after the per-CTA phase words, and the index of each event (the
+# TraceEvent enumeration of the kernel source; "...0" events of tile 1 are the
+# tile-0 index + 1).
+TRACE_SHAPE = (3, 40, 24)
+TRACE_EVENTS = {
+    "mma_kv": 0, "mma_p0": 1, "mma_pv0": 3, "mma_s0": 5, "mma_o_empty": 7, "soft_s0": 8,
+    "soft_p0": 10, "soft_load0": 12, "soft_exp0": 13, "epi_o0": 14, "load_kv": 16, "load_q": 17,
+    "mma_q": 18, "mma_q_empty": 19, "mma_wait_q": 20, "mma_wait_kv": 21, "mma_step_end": 22,
+    "mma_decoded": 23,
+}
+
+
 def trace_summary(tr):
     """Median hand-off latencies (cycles) from the event trace of CTA 0's first
-    unit: tr[unit, step, event] clock64 stamps (0 = not recorded)."""
+    unit, and the timeline of each unit boundary: tr[unit, step, event]
+    clock64 stamps (0 = not recorded)."""
     import numpy as np
+    E = TRACE_EVENTS
     u = tr[0]
+    nsteps = tr.shape[1]
     med = lambda a: round(float(np.median(a)), 1) if len(a) else None
     res = {}
-    steps = [j for j in range(1, 39) if u[j, 0] > 0 and u[j + 1, 0] > 0]
+    steps = [j for j in range(1, nsteps - 1) if u[j, E["mma_kv"]] > 0 and u[j + 1, E["mma_kv"]] > 0]
     for t in (0, 1):
-        s_issue = [u[j, 5 + t] for j in steps]
-        s_seen = [u[j, 8 + t] for j in steps]
-        p_pub = [u[j, 10 + t] for j in steps]
-        p_seen = [u[j + 1, 1 + t] for j in steps]  # P(j) is consumed at step j + 1
+        s_issue = [u[j, E["mma_s0"] + t] for j in steps]
+        s_seen = [u[j, E["soft_s0"] + t] for j in steps]
+        p_pub = [u[j, E["soft_p0"] + t] for j in steps]
+        p_seen = [u[j + 1, E["mma_p0"] + t] for j in steps]  # P(j) is consumed at step j + 1
         ok = [i for i in range(len(steps)) if min(s_issue[i], s_seen[i], p_pub[i], p_seen[i]) > 0]
         res["tile%d_S_issued_to_softmax_sees_S" % t] = med([s_seen[i] - s_issue[i] for i in ok])
         res["tile%d_softmax_S_to_P_published" % t] = med([p_pub[i] - s_seen[i] for i in ok])
         res["tile%d_P_published_to_mma_sees_P" % t] = med([p_seen[i] - p_pub[i] for i in ok])
-        res["tile%d_cycle" % t] = med([u[j + 1, 5 + t] - u[j, 5 + t] for j in steps if u[j + 1, 5 + t] > 0])
-    ld = [u[j, 12] - u[j, 8] for j in steps if u[j, 12] > 0]
-    ex = [u[j, 13] - u[j, 12] for j in steps if u[j, 13] > 0]
-    res["tile0_softmax_load"] = med(ld)
-    res["tile0_softmax_exp"] = med(ex)
-    res["mma_pv0_issue"] = med([u[j, 3] - u[j, 1] for j in steps if u[j, 3] > 0 and u[j, 1] > 0])
-    res["mma_s0_issue_after_pv0"] = med([u[j, 5] - u[j, 3] for j in steps if u[j, 5] > 0 and u[j, 3] > 0])
-    res["raw_unit0_first_steps"] = [[int(x) for x in u[j]] for j in range(0, 4)]
+        res["tile%d_cycle" % t] = med([u[j + 1, E["mma_s0"] + t] - u[j, E["mma_s0"] + t] for j in steps
+                                       if u[j + 1, E["mma_s0"] + t] > 0 and u[j, E["mma_s0"] + t] > 0])
+    res["tile0_softmax_load"] = med([u[j, E["soft_load0"]] - u[j, E["soft_s0"]] for j in steps
+                                     if u[j, E["soft_load0"]] > 0 and u[j, E["soft_s0"]] > 0])
+    res["tile0_softmax_exp"] = med([u[j, E["soft_exp0"]] - u[j, E["soft_load0"]] for j in steps
+                                    if u[j, E["soft_exp0"]] > 0 and u[j, E["soft_load0"]] > 0])
+    res["mma_pv0_issue"] = med([u[j, E["mma_pv0"]] - u[j, E["mma_p0"]] for j in steps
+                                if u[j, E["mma_pv0"]] > 0 and u[j, E["mma_p0"]] > 0])
+    res["mma_s0_issue_after_pv0"] = med([u[j, E["mma_s0"]] - u[j, E["mma_pv0"]] for j in steps
+                                         if u[j, E["mma_s0"]] > 0 and u[j, E["mma_pv0"]] > 0])
+    res["raw_unit0_first_steps"] = [[int(x) for x in u[j]] for j in range(0, min(4, nsteps))]
     # Unit boundaries (unit n -> n + 1), relative to the MMA thread's last P V
-    # issue of unit n (cycles): epilogue O-final seen / staging free / O read,
-    # and the MMA thread's first S issue and O-empty observation in unit n + 1.
+    # issue of tile 0 in unit n (cycles).  The epilogue's events of a unit sit
+    # in its step rows 0 (O final seen), 1 (O read, O-empty signalled) and 2
+    # (staging free).
     for n in range(tr.shape[0] - 1):
         u, v = tr[n], tr[n + 1]
-        if not (u[:, 3] > 0).any() or v[0, 0] <= 0:
+        pv0 = u[:, E["mma_pv0"]]
+        if not (pv0 > 0).any() or v[0, E["mma_kv"]] <= 0:
             continue
-        last = max(j for j in range(tr.shape[1]) if u[j, 3] > 0)
-        t0 = u[last, 3]
+        last = max(j for j in range(nsteps) if pv0[j] > 0)
+        t0 = pv0[last]
         rel = lambda x: int(x - t0) if x > 0 else None
+        eo = E["epi_o0"]
         res["boundary_%d_%d" % (n, n + 1)] = {
-            "epi_tile0_O_final_seen": rel(u[0, 14]), "epi_tile0_staging_free": rel(u[2, 14]),
-            "epi_tile0_O_read": rel(u[1, 14]), "epi_tile1_O_final_seen": rel(u[0, 15]),
-            "epi_tile1_staging_free": rel(u[2, 15]), "epi_tile1_O_read": rel(u[1, 15]),
-            "mma_next_kv0": rel(v[0, 0]), "mma_next_S0_issued": rel(v[0, 5]),
-            "mma_next_S1_issued": rel(v[0, 6]), "mma_next_P0_seen": rel(v[1, 1]),
-            "mma_next_O_empty_seen": rel(v[1, 7]), "mma_next_PV1_issued": rel(v[1, 4]),
-            "soft_last_P0": rel(u[last - 1, 10]) if last >= 1 else None,
-            "soft_next_S0_seen": rel(v[0, 8]), "soft_next_P0_published": rel(v[0, 10]),
-            "mma_Q_empty_committed": rel(max(u[:, 19])), "load_last_slot_issued": rel(u[last, 16]),
-            "load_next_Q_issued": rel(v[0, 17]), "load_next_kv0_issued": rel(v[0, 16]),
-            "load_next_kv1_issued": rel(v[1, 16]), "mma_next_Q_seen": rel(v[0, 18])}
+            "epi_tile0_O_final_seen": rel(u[0, eo]), "epi_tile0_staging_free": rel(u[2, eo]),
+            "epi_tile0_O_read": rel(u[1, eo]), "epi_tile1_O_final_seen": rel(u[0, eo + 1]),
+            "epi_tile1_staging_free": rel(u[2, eo + 1]), "epi_tile1_O_read": rel(u[1, eo + 1]),
+            "mma_next_decoded": rel(v[0, E["mma_decoded"]]), "mma_next_Q_wait": rel(v[0, E["mma_wait_q"]]),
+            "mma_next_Q_seen": rel(v[0, E["mma_q"]]), "mma_next_kv0": rel(v[0, E["mma_kv"]]),
+            "mma_next_S0_issued": rel(v[0, E["mma_s0"]]), "mma_next_S1_issued": rel(v[0, E["mma_s0"] + 1]),
+            "mma_next_P0_seen": rel(v[1, E["mma_p0"]]), "mma_next_O_empty_seen": rel(v[1, E["mma_o_empty"]]),
+            "mma_next_PV1_issued": rel(v[1, E["mma_pv0"] + 1]),
+            "soft_last_P0": rel(u[last - 1, E["soft_p0"]]) if last >= 1 else None,
+            "soft_next_S0_seen": rel(v[0, E["soft_s0"]]), "soft_next_P0_published": rel(v[0, E["soft_p0"]]),
+            "mma_Q_empty_committed": rel(max(u[:, E["mma_q_empty"]])),
+            "load_last_slot_issued": rel(u[last, E["load_kv"]]),
+            "load_next_Q_issued": rel(v[0, E["load_q"]]), "load_next_kv0_issued": rel(v[0, E["load_kv"]]),
+            "load_next_kv1_issued": rel(v[1, E["load_kv"]])}
     return res
 
 
@@ -840,7 +865,7 @@ def run_phase(args, w):
     lse = torch.empty((w.B, w.H, maxlen), dtype=torch.float32, device=dev)
     # One record per CTA of the grid (one CTA per work item of 256 query rows).
     items = w.B * w.H * ((maxlen + 255) // 256)
-    trace_words = 3 * 40 * 24  # event trace of CTA 0 (three units x 40 steps x 24 events)
+    trace_words = TRACE_SHAPE[0] * TRACE_SHAPE[1] * TRACE_SHAPE[2]  # event trace of CTA 0
     buf = torch.zeros(items * 48 + trace_words, dtype=torch.int64, device=dev)
     words = L.fa_set_phase_buffer(buf.data_ptr(), buf.numel())
     if words <= 0:
@@ -866,7 +891,7 @@ def run_phase(args, w):
     ph = allw[:launched * words].reshape(-1, words).astype("float64")
     ph = ph[ph[:, 41] > 0]
     grid = int(ph.shape[0])
-    tr = allw[launched * words:launched * words + trace_words].reshape(3, 40, 24).astype("float64")
+    tr = allw[launched * words:launched * words + trace_words].reshape(TRACE_SHAPE).astype("float64")
     trace = trace_summary(tr)
     if args.trace_out:
         with open(args.trace_out, "w") as f:
