@@ -160,7 +160,7 @@ enum PhaseSlot : int {
 // kTraceSteps + step) * kTraceEvents + event], when the buffer has room.
 constexpr int kTraceUnits = 3;
 constexpr int kTraceSteps = 40;
-constexpr int kTraceEvents = 24;
+constexpr int kTraceEvents = 32;
 constexpr int kTraceWords = kTraceUnits * kTraceSteps * kTraceEvents;
 enum TraceEvent : int {
   kTrMmaKV = 0,        // MMA thread: K/V slot of step j full
@@ -183,6 +183,7 @@ enum TraceEvent : int {
   kTrMmaWaitKV = 21,   // MMA thread: starts waiting for the K/V slot of step j
   kTrMmaStepEnd = 22,  // MMA thread: step j's last commit issued
   kTrMmaDecoded = 23,  // MMA thread (step 0 row): unit decoded
+  kTrSoftWarpP = 24,   // softmax warp w (0-7, lane 0): P(j) published (24 + w)
 };
 
 __device__ __forceinline__ void trace_event(unsigned long long* phase, int trace_off, int unit, int step, int ev) {
@@ -1245,6 +1246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_wait_st();  // P stores (and any O rescale) have landed
           ptx::tc_fence_before();
           if (tr_lead) FA_TRACE(tr_unit, j, kTrSoftP0 + t);
+          if (lane == 0) FA_TRACE(tr_unit, j, kTrSoftWarpP + warp);
           ptx::mbar_arrive(bar(L::kBarPFull + t));
         }
         if (!ok) break;

@@ -771,12 +771,12 @@ PHASE_NAMES = {
 # words after the per-CTA phase words, and the index of each event (the
 # TraceEvent enumeration of the kernel source; "...0" events of tile 1 are the
 # tile-0 index + 1).
-TRACE_SHAPE = (3, 40, 24)
+TRACE_SHAPE = (3, 40, 32)
 TRACE_EVENTS = {
     "mma_kv": 0, "mma_p0": 1, "mma_pv0": 3, "mma_s0": 5, "mma_o_empty": 7, "soft_s0": 8,
     "soft_p0": 10, "soft_load0": 12, "soft_exp0": 13, "epi_o0": 14, "load_kv": 16, "load_q": 17,
     "mma_q": 18, "mma_q_empty": 19, "mma_wait_q": 20, "mma_wait_kv": 21, "mma_step_end": 22,
-    "mma_decoded": 23,
+    "mma_decoded": 23, "soft_warp_p": 24,
 }
 
 
@@ -810,6 +810,16 @@ def trace_summary(tr):
                                 if u[j, E["mma_pv0"]] > 0 and u[j, E["mma_p0"]] > 0])
     res["mma_s0_issue_after_pv0"] = med([u[j, E["mma_s0"]] - u[j, E["mma_pv0"]] for j in steps
                                          if u[j, E["mma_s0"]] > 0 and u[j, E["mma_pv0"]] > 0])
+    # Spread of the P(j) publication over the four warps of each tile: the
+    # MMA thread sees P when the last of them has arrived.
+    wp = E["soft_warp_p"]
+    for t in (0, 1):
+        spread = [max(u[j, wp + 4 * t:wp + 4 * t + 4]) - min(u[j, wp + 4 * t:wp + 4 * t + 4]) for j in steps
+                  if min(u[j, wp + 4 * t:wp + 4 * t + 4]) > 0]
+        last_warp = [int(np.argmax(u[j, wp + 4 * t:wp + 4 * t + 4])) for j in steps
+                     if min(u[j, wp + 4 * t:wp + 4 * t + 4]) > 0]
+        res["tile%d_P_warp_spread" % t] = med(spread)
+        res["tile%d_P_last_warp_counts" % t] = [last_warp.count(i) for i in range(4)] if last_warp else None
     res["raw_unit0_first_steps"] = [[int(x) for x in u[j]] for j in range(0, min(4, nsteps))]
     # Unit boundaries (unit n -> n + 1), relative to the MMA thread's last P V
     # issue of tile 0 in unit n (cycles).  The epilogue's events of a unit sit

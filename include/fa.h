@@ -377,7 +377,7 @@ int fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
  *           as many items when causal, times the splits for the key split);
  *           only the CTAs that run write their words (a CTA that takes over
  *           another's items leaves that CTA's words untouched).  When the
- *           buffer holds at least 2880 more words (3 units x 40 steps x 24
+ *           buffer holds at least 3840 more words (3 units x 40 steps x 32
  *           events), an event trace follows the per-CTA words: clock64 stamps
  *           of each barrier hand-off of the first three work units of CTA 0
  *           (TraceEvent enumeration of the kernel source).
