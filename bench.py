@@ -882,10 +882,21 @@ def run_phase(args, w):
         raise SystemExit("fa_set_phase_buffer failed: %d" % words)
     stream = torch.cuda.current_stream(dev).cuda_stream
     cu = dcu.data_ptr() if dcu is not None else None
+    t8 = None
+    if args.fp8:
+        if w.varlen:
+            raise SystemExit("--phase --fp8 covers the dense workloads")
+        t8 = fa.quantize_fp8(dq, dk, dv)  # codes and scales (the quantiser is not instrumented)
+        torch.cuda.synchronize(dev)
     for _ in range(args.warmup + 1):
-        rc = L.fa_fwd_ex(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B, maxlen,
-                         maxlen if w.varlen else w.Nk, w.H, w.H, w.d, 1.0 / math.sqrt(w.d), cu, cu,
-                         fa.FA_FLAG_CAUSAL if args.causal else 0, stream)
+        if t8 is not None:
+            rc = L.fa_fwd_fp8(t8.q8.data_ptr(), t8.k8.data_ptr(), t8.vt8.data_ptr(), t8.q_scale.data_ptr(),
+                              t8.k_scale.data_ptr(), t8.v_scale.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B,
+                              w.Nq, w.Nk, w.H, w.H, w.d, 1.0 / math.sqrt(w.d), 1 if args.causal else 0, stream)
+        else:
+            rc = L.fa_fwd_ex(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B,
+                             maxlen, maxlen if w.varlen else w.Nk, w.H, w.H, w.d, 1.0 / math.sqrt(w.d), cu, cu,
+                             fa.FA_FLAG_CAUSAL if args.causal else 0, stream)
         if rc != 0:
             raise SystemExit("forward failed: %d" % rc)
     info = (ctypes.c_int * 3)()
@@ -921,7 +932,7 @@ def run_phase(args, w):
     line = {"phase_clocks": out, "per_key_value_step_cycles": per_step, "ctas": grid, "trace": trace,
             "cta_ns": round(ns, 1), "mma_role_cycles": round(cycles, 1),
             "clock_ghz_estimate": round(cycles / ns, 3) if ns > 0 else None,
-            "workload": w.name, "causal": bool(args.causal),
+            "workload": w.name, "causal": bool(args.causal), "fp8": bool(args.fp8),
             "note": "instrumented build (FA_PHASE_CLOCKS=1), last of %d launches; not a bench value"
                     % (args.warmup + 1)}
     print(json.dumps(line))
