@@ -251,3 +251,17 @@ def test_fp8_varlen_column_ranges_fit(L):
         for b in range(B):
             assert c[b] % 16 == 0
             assert c[b] + (int(lens[b]) + 15) // 16 * 16 <= c[b + 1]
+
+
+def test_phase_buffer_entry_without_a_device(L):
+    """The default library refuses the phase-clock buffer; the instrumented one
+    checks its arguments on the host (too small or misaligned buffers) and
+    detaches with a null buffer, all without touching a device."""
+    assert L.fa_set_phase_buffer(None, 0) == fa.FA_ERR_UNSUPPORTED
+    fabuild.build(phase=True)
+    P = fa.load_library(fa.PHASE_LIB_PATH)
+    words = P.fa_set_phase_buffer(None, 0)
+    assert words == 48  # per-CTA words (kPhaseWords of the kernel source)
+    assert P.fa_set_phase_buffer(8, 47) == fa.FA_ERR_INVALID_ARG   # fewer words than one CTA's record
+    assert P.fa_set_phase_buffer(12, 4096) == fa.FA_ERR_INVALID_ARG  # not 8-byte aligned
+    assert P.fa_set_phase_buffer(None, 0) == words
