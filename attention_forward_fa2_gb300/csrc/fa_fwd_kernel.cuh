@@ -12,9 +12,13 @@
 // Work split (§14.2, loop order with the query block outermost): a work unit
 // is two 128-row query tiles of one (b, h) against all key/value tiles of that
 // head (B_r = 256; with qtiles = 1 a unit is one tile, B_r = 128, and the
-// second softmax warpgroup idles).  The kernel is persistent: each CTA walks the units blockIdx.x,
-// blockIdx.x + gridDim.x, ...; units are numbered with the query block fastest,
-// so the CTAs that run at the same time share the K/V of a few heads in L2.
+// second softmax warpgroup idles).  Dense problems run a persistent grid: each
+// CTA walks the items blockIdx.x, blockIdx.x + gridDim.x, ...  Packed
+// variable-length batches launch one CTA per item, and a running CTA takes over
+// the items of CTAs not yet started (cluster launch control); its load thread
+// hands the item sequence to the other roles through a shared-memory ring.
+// Units are numbered with the query block fastest, so the CTAs that run at the
+// same time share the K/V of a few heads in L2.
 // Roles inside the CTA (§15.2-§15.4, re-expressed for tcgen05):
 //   warps 0-3   softmax warpgroup for query tile 0 (one thread per row)
 //   warps 4-7   softmax warpgroup for query tile 1

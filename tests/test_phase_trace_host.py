@@ -107,3 +107,14 @@ def test_trace_summary_of_an_empty_trace():
     r = bench.trace_summary(np.zeros(bench.TRACE_SHAPE))
     assert r["tile0_cycle"] is None and r["mma_pv0_issue"] is None
     assert not any(k.startswith("boundary") for k in r)
+
+
+def test_kernel_code_hash_ignores_comments_and_layout():
+    """profiles/traffic.json is keyed by the hash of the kernel's code: comments
+    and layout do not change it, code does, and string literals are kept."""
+    a = "int f(int x) {  // twice\n  return 2 * x; /* done */ }\n"
+    b = "int f(int x)\n{\n  return 2 * x;\n}\n"
+    c = "int f(int x) { return 3 * x; }"
+    assert bench.code_text(a) == bench.code_text(b) != bench.code_text(c)
+    assert bench.code_text('s = "a // b"; t = \'/\';') == 's = "a // b"; t = \'/\';'
+    assert len(bench.kernel_source_hash()) == 16
