@@ -372,11 +372,13 @@ int fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
  *           of the CTA's start and end.  The slot map is the PhaseBase /
  *           PhaseSlot enumeration of the kernel source.
  *   words : size of buf in words; a launch whose grid needs more returns
- *           FA_ERR_INVALID_ARG and launches nothing.  The grid has one CTA
- *           per work item (B * H * ceil(Nq / 256) for the dense forward; half
- *           as many items when causal, times the splits for the key split);
- *           only the CTAs that run write their words (a CTA that takes over
- *           another's items leaves that CTA's words untouched).  When the
+ *           FA_ERR_INVALID_ARG and launches nothing.  Work items: B * H *
+ *           ceil(Nq / 256) for the dense forward, half as many when causal,
+ *           times the splits for the key split.  Dense problems launch
+ *           min(items, SMs) CTAs, packed batches one CTA per item, so items
+ *           x W words always suffice; only the CTAs that run write their
+ *           words (a CTA that takes over another's items leaves that CTA's
+ *           words untouched).  When the
  *           buffer holds at least 3840 more words (3 units x 40 steps x 32
  *           events), an event trace follows the per-CTA words: clock64 stamps
  *           of each barrier hand-off of the first three work units of CTA 0
